@@ -1,0 +1,176 @@
+/*
+ * dsa.h -- C ABI of the GB300 (sm_103a) DSA "score, select, sparse read" path.
+ *
+ * The path has two steps:
+ *
+ *  1. dsa_index_topk: a lightweight indexer scores every causal history
+ *     position of every query from a paged index-key cache and keeps the Top-K
+ *     positions.  score(t, s) = sum_j w[t][j] * ReLU(q_idx[t][j] . k_idx[s]),
+ *     j over 64 index heads of dimension 128.  Scoring, head weighting and
+ *     selection run in one fused kernel that reads the paged cache directly and
+ *     writes back only the indices ("Optimizing Inference for Hybrid Attention
+ *     LLMs: A Practical Guide to Day-0 Adaptation", §3.1 Indexer Fusion; "Day-0
+ *     Inference Adaptation and Optimization for Hybrid Attention
+ *     Architectures", §3 Optimization 1; "Day0 Inference Support and
+ *     Performance Optimization for New-Architecture LLMs", §4 item 1).
+ *
+ *  2. dsa_sparse_mla: a sparse attention kernel gathers only the selected
+ *     576-wide latent KV rows (512 latent + 64 rope) and computes softmax
+ *     attention of every query head over them; values are the first 512 dims
+ *     ("Day0 Inference Support and Performance Optimization for
+ *     New-Architecture LLMs", §2 item 2 and §4 "Sparse attention reads by
+ *     index"; "Day0 Inference Optimization for a New Hybrid Attention
+ *     Architecture: A Full-Stack Deep Dive", operator fusion item 1).
+ *
+ * Conventions shared by every entry point
+ *  - All tensor arguments are caller-owned DEVICE pointers, row-major, densely
+ *    packed, 16-byte aligned.  Sizes are element counts.  The library never
+ *    allocates, frees or synchronises on these calls (dsa_get_error and the
+ *    *_sync helpers excepted); work is enqueued on `stream` (a cudaStream_t
+ *    passed as void*, NULL = legacy default stream).
+ *  - Paged caches: logical position s of sequence b lives in physical row
+ *    page_table[b * max_pages_per_seq + s / page_size] * page_size + s % page_size
+ *    of a cache shaped [num_pages, page_size, row_width].
+ *  - Queries: sequence b owns query rows cu_q[b] .. cu_q[b+1]-1, which are its
+ *    LAST (cu_q[b+1]-cu_q[b]) positions: query row t of sequence b sits at
+ *    position pos(t) = seq_lens[b] - (cu_q[b+1]-cu_q[b]) + (t - cu_q[b]) and may
+ *    attend to positions 0 .. pos(t) (causal, current token included).
+ *    Decode: one query per sequence at position seq_lens[b]-1.  Prefill of a
+ *    chunk: the chunk's tokens are the last positions of the cached sequence.
+ *  - Workspace: caller-owned device memory of at least the bytes reported by
+ *    the matching *_workspace_size() call.  Its first 16 bytes hold a sticky
+ *    device error word: call dsa_workspace_init() once after allocating it.
+ *    Kernels OR error bits into it; dsa_get_error() reads and clears it.
+ *  - Return value: DSA_OK if the work was enqueued.  Argument problems found
+ *    on the host return DSA_ERR_INVALID_ARG / DSA_ERR_UNSUPPORTED before any
+ *    launch; a failed launch returns DSA_ERR_CUDA.  Problems found on the
+ *    device (a page id outside [0, num_pages), an index outside 0..pos(t), a
+ *    pipeline wait that ran out) are reported later by dsa_get_error().  On
+ *    any error the outputs are unspecified.
+ */
+#ifndef DSA_H_
+#define DSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    DSA_OK = 0,
+    DSA_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, bad size or count       */
+    DSA_ERR_UNSUPPORTED = 2,  /* valid request this build does not implement      */
+    DSA_ERR_CUDA = 3,         /* a CUDA runtime/driver call or launch failed      */
+    DSA_ERR_BAD_PAGE = 4,     /* device: page-table entry outside [0, num_pages)  */
+    DSA_ERR_BAD_INDEX = 5,    /* device: selected index outside 0..pos(t)         */
+    DSA_ERR_TIMEOUT = 6       /* device: a bounded pipeline wait ran out          */
+} dsa_status;
+
+/* Index-path element type, shared by q_idx and k_idx.  MXFP8 is E4M3 with one
+ * E8M0 scale byte per 32 consecutive elements ("Day-0 Inference Adaptation and
+ * Optimization for Hybrid Attention Architectures", §4 Optimization 2). */
+typedef enum { DSA_IDX_BF16 = 0, DSA_IDX_MXFP8 = 1 } dsa_idx_dtype;
+
+/* Main KV cache element type.  FP8_ROWSCALE: the 512 latent dims are E4M3 with
+ * one fp32 scale per row, the 64 rope dims stay bf16. */
+typedef enum { DSA_KV_BF16 = 0, DSA_KV_FP8_ROWSCALE = 1 } dsa_kv_dtype;
+
+/* Fixed dimensions of this build. */
+#define DSA_INDEX_HEADS 64
+#define DSA_INDEX_DIM 128
+#define DSA_LATENT_DIM 576
+#define DSA_VALUE_DIM 512
+
+/* Short human-readable name of a status code (static storage). */
+const char *dsa_status_string(dsa_status s);
+
+/* Launch-shape tuning knobs, read on every call (0 = automatic).  Names:
+ * "indexer_cluster" (CTAs per cluster, power of two <= 16), "indexer_stages"
+ * (shared-memory ring depth 2..4), "indexer_group" (query rows per cluster:
+ * 1, 2 or 4), "mla_splits" (key splits per query row), "topk_cluster".
+ * Returns 0, or -1 for an unknown name.  Results do not depend on them. */
+int dsa_set_tuning(const char *name, int value);
+
+/* ---------------------------------------------------------------- workspace */
+
+/* Bytes of workspace dsa_index_topk / dsa_index_scores / dsa_topk_from_scores
+ * need (at least 16: the error word). */
+size_t dsa_index_topk_workspace_size(int32_t B, int32_t T, int32_t K, int32_t max_pages_per_seq,
+                                     int32_t page_size);
+
+/* Bytes of workspace dsa_sparse_mla needs for T query rows of H heads with K
+ * selected slots each: the error word plus split-K partial results. */
+size_t dsa_sparse_mla_workspace_size(int32_t T, int32_t H, int32_t K);
+
+/* Zero the error word of a workspace (enqueued on stream).  Call once after
+ * allocation; dsa_get_error() clears it again after each read. */
+dsa_status dsa_workspace_init(void *workspace, size_t workspace_bytes, void *stream);
+
+/* Synchronise `stream`, read the workspace's device error word, clear it and
+ * return the first error it records (DSA_OK if none).  Not for the hot path. */
+dsa_status dsa_get_error(void *workspace, void *stream);
+
+/* ---------------------------------------------------------------- indexer */
+
+/* Fused indexer + Top-K.
+ *   q_idx        [T, 64, 128]  bf16, or e4m3 codes for MXFP8
+ *   q_idx_scale  [T, 64, 4]    e8m0 bytes (MXFP8 only, else NULL)
+ *   head_w       [T, 64]       fp32 per-head weights
+ *   k_idx_cache  [num_pages, page_size, 128]  bf16, or e4m3 codes for MXFP8
+ *   k_idx_scale  [num_pages, page_size, 4]    e8m0 bytes (MXFP8 only)
+ *   page_table   [B, max_pages_per_seq] int32; seq_lens [B]; cu_q [B+1] int32
+ *   indices      [T, K] int32 OUT: for every query row, the min(K, pos(t)+1)
+ *                positions with the highest scores (ties: lower position
+ *                first), ascending, followed by -1 padding.
+ * page_size must be a multiple of 64; max_pages_per_seq * page_size bounds
+ * every seq_lens[b].  Scores never leave the chip. */
+dsa_status dsa_index_topk(const void *q_idx, const uint8_t *q_idx_scale, const float *head_w,
+                          const void *k_idx_cache, const uint8_t *k_idx_scale, int64_t num_pages,
+                          const int32_t *page_table, int32_t max_pages_per_seq, const int32_t *seq_lens,
+                          const int32_t *cu_q, int32_t B, int32_t T, int32_t K, int32_t page_size,
+                          dsa_idx_dtype dtype, int32_t *indices, void *workspace, size_t workspace_bytes,
+                          void *stream);
+
+/* Test hook with the same arguments as dsa_index_topk that also writes the
+ * fp32 scores: scores [T, ld_scores]; entry (t, s) for s <= pos(t) and
+ * s < ld_scores, other entries untouched.  Same kernel, same selection. */
+dsa_status dsa_index_scores(const void *q_idx, const uint8_t *q_idx_scale, const float *head_w,
+                            const void *k_idx_cache, const uint8_t *k_idx_scale, int64_t num_pages,
+                            const int32_t *page_table, int32_t max_pages_per_seq, const int32_t *seq_lens,
+                            const int32_t *cu_q, int32_t B, int32_t T, int32_t K, int32_t page_size,
+                            dsa_idx_dtype dtype, int32_t *indices, float *scores, int64_t ld_scores,
+                            void *workspace, size_t workspace_bytes, void *stream);
+
+/* Top-K of given fp32 score rows with the indexer's selection code: row r of
+ * scores [R, ld] is valid on entries 0..lens[r]-1 (lens <= ld); out [R, K]
+ * receives the selected positions as dsa_index_topk does.  Bit-exact
+ * selection: the result depends only on the score values (-0 == +0). */
+dsa_status dsa_topk_from_scores(const float *scores, int64_t ld, const int32_t *lens, int32_t R, int32_t K,
+                                int32_t *out, void *workspace, size_t workspace_bytes, void *stream);
+
+/* ---------------------------------------------------------------- sparse MLA */
+
+/* Sparse MLA attention over the selected rows.
+ *   q          [T, H, 576] bf16 query (latent 512 + rope 64)
+ *   kv_cache   BF16: [num_pages, page_size, 576] bf16 latent rows
+ *              FP8_ROWSCALE: [num_pages, page_size, 512] e4m3 latent dims
+ *   kv_rope    FP8_ROWSCALE only: [num_pages, page_size, 64] bf16 rope dims
+ *   kv_scale   FP8_ROWSCALE only: [num_pages, page_size] fp32 row scales
+ *   indices    [T, K] int32 logical positions; entries < 0 are skipped
+ *   out        [T, H, 512] bf16 OUT: sum_i softmax_i(scale * q_h . kv_i) kv_i[0:512]
+ *   lse        [T, H] fp32 OUT (natural-log log-sum-exp of the scaled logits)
+ *              or NULL.  A row with no valid index gets out = 0, lse = -inf.
+ * H must be a multiple of 16 (at most 128). */
+dsa_status dsa_sparse_mla(const void *q, const void *kv_cache, const void *kv_rope, const float *kv_scale,
+                          int64_t num_pages, const int32_t *page_table, int32_t max_pages_per_seq,
+                          const int32_t *seq_lens, const int32_t *cu_q, const int32_t *indices, int32_t B,
+                          int32_t T, int32_t H, int32_t K, float scale, int32_t page_size, dsa_kv_dtype dtype,
+                          void *out, float *lse, void *workspace, size_t workspace_bytes, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSA_H_ */

@@ -1,0 +1,336 @@
+// dsa_abi.cu -- the C ABI declared in include/dsa.h: argument validation,
+// TMA tensor-map encoding, launch-shape heuristics and the device error word.
+// Every compute step runs in the kernels of indexer_topk.cu and sparse_mla.cu.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/dsa.h"
+#include "kernels.h"
+
+namespace {
+
+using dsa::IndexerArgs;
+using dsa::MlaArgs;
+using dsa::TopkArgs;
+
+constexpr size_t kErrBytes = 256;  // error word block at the start of every workspace
+
+// ---------------------------------------------------------------- tuning knobs
+// 0 = automatic.  Set through dsa_set_tuning(); read on every call.
+std::atomic<int> g_idx_cluster{0}, g_idx_stages{0}, g_idx_group{0}, g_mla_splits{0}, g_topk_cluster{0};
+
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
+    return n;
+}
+
+size_t max_smem_optin() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 227 * 1024;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess || n <= 0)
+        return 227 * 1024;
+    return (size_t)n;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 2D bf16 tensor [rows, 128] with 64x64 boxes and the 128-byte swizzle.
+bool encode_rows128_bf16(CUtensorMap *m, const void *base, uint64_t rows) {
+    auto fn = encode_fn();
+    if (!fn || rows == 0 || rows > (1ull << 31)) return false;
+    cuuint64_t dims[2] = {128, rows};
+    cuuint64_t strides[1] = {256};
+    cuuint32_t box[2] = {64, 64};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
+
+struct IdxPlan {
+    int G, C, stages, tiles_cap, groups;
+    size_t smem;
+};
+
+bool plan_indexer(int B, int T, int max_len, IdxPlan *p) {
+    const int nsm = sm_count();
+    const size_t smax = max_smem_optin();
+    const int tiles_max = std::max(1, ceil_div(max_len, 128));
+    int G_list[3] = {4, 2, 1};
+    int g_force = g_idx_group.load();
+    for (int gi = 0; gi < 3; ++gi) {
+        int G = G_list[gi];
+        if (g_force ? G != g_force : (T <= B ? G != 1 : false)) continue;
+        const int groups = G == 1 ? T : ceil_div(T, G) + B;
+        int c_force = g_idx_cluster.load();
+        for (int C = 1; C <= 16; C <<= 1) {
+            if (c_force && C != c_force) continue;
+            const int tiles_cap = ceil_div(tiles_max, C);
+            // enough CTAs to cover the GPU twice, unless the history is too
+            // short to split further
+            if (!c_force && C < 16 && (long long)C * groups < 2LL * nsm && tiles_cap > 4) continue;
+            int s_force = g_idx_stages.load();
+            for (int stages = 4; stages >= 2; --stages) {
+                if (s_force && stages != s_force) continue;
+                size_t smem = dsa::indexer_smem_bytes(G, stages, tiles_cap);
+                // TMEM: 2*64*G columns per CTA; keep CTAs/SM * columns <= 512
+                const int cols = 2 * 64 * G <= 128 ? 128 : 2 * 64 * G;
+                const int max_ctas = 512 / cols;
+                const size_t floor_smem = (228u * 1024u) / (size_t)(max_ctas + 1) + 1;
+                smem = std::max(smem, floor_smem);
+                if (smem <= smax) {
+                    *p = IdxPlan{G, C, stages, tiles_cap, groups, smem};
+                    return true;
+                }
+            }
+        }
+    }
+    return false;
+}
+
+int mla_splits(int T, int H, int K) {
+    int forced = g_mla_splits.load();
+    const int tile = dsa::mla_key_tile();
+    const int max_splits = std::max(1, std::min(16, ceil_div(std::max(K, 1), tile)));
+    if (forced > 0) return std::min(forced, max_splits);
+    const long long pairs = (long long)T * ceil_div(H, 64);
+    const int nsm = sm_count();
+    if (pairs >= nsm) return 1;
+    return std::max(1, std::min<int>(max_splits, (int)(nsm / pairs)));
+}
+
+dsa_status cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return DSA_OK;
+    fprintf(stderr, "[dsa] CUDA error: %s\n", cudaGetErrorString(e));
+    return DSA_ERR_CUDA;
+}
+
+dsa_status index_common(const void *q_idx, const uint8_t *q_idx_scale, const float *head_w, const void *k_idx_cache,
+                        const uint8_t *k_idx_scale, int64_t num_pages, const int32_t *page_table,
+                        int32_t max_pages_per_seq, const int32_t *seq_lens, const int32_t *cu_q, int32_t B,
+                        int32_t T, int32_t K, int32_t page_size, dsa_idx_dtype dtype, int32_t *indices,
+                        float *scores, int64_t ld_scores, void *workspace, size_t workspace_bytes, void *stream) {
+    (void)q_idx_scale;
+    (void)k_idx_scale;
+    if (T < 0 || B < 1 || K < 1 || page_size < 1 || max_pages_per_seq < 1 || num_pages < 1) return DSA_ERR_INVALID_ARG;
+    if (!q_idx || !head_w || !k_idx_cache || !page_table || !seq_lens || !cu_q || !indices || !workspace)
+        return DSA_ERR_INVALID_ARG;
+    if (!aligned16(q_idx) || !aligned16(k_idx_cache) || !aligned16(workspace)) return DSA_ERR_INVALID_ARG;
+    if (workspace_bytes < dsa_index_topk_workspace_size(B, T, K, max_pages_per_seq, page_size))
+        return DSA_ERR_INVALID_ARG;
+    if (dtype != DSA_IDX_BF16) return DSA_ERR_UNSUPPORTED;
+    if (page_size % 64 != 0) return DSA_ERR_UNSUPPORTED;
+    if (T == 0) return DSA_OK;
+    const long long max_len = (long long)max_pages_per_seq * page_size;
+    if (max_len > (1LL << 30) || (long long)num_pages * page_size > (1LL << 31)) return DSA_ERR_UNSUPPORTED;
+    IdxPlan plan;
+    if (!plan_indexer(B, T, (int)max_len, &plan)) return DSA_ERR_UNSUPPORTED;
+    CUtensorMap tk, tq;
+    if (!encode_rows128_bf16(&tk, k_idx_cache, (uint64_t)num_pages * page_size)) return DSA_ERR_CUDA;
+    if (!encode_rows128_bf16(&tq, q_idx, (uint64_t)T * 64)) return DSA_ERR_CUDA;
+    IndexerArgs a{};
+    a.head_w = head_w;
+    a.page_table = page_table;
+    a.seq_lens = seq_lens;
+    a.cu_q = cu_q;
+    a.indices = indices;
+    a.scores = scores;
+    a.err = reinterpret_cast<uint32_t *>(workspace);
+    a.num_pages = num_pages;
+    a.ld_scores = ld_scores;
+    a.max_pages = max_pages_per_seq;
+    a.B = B;
+    a.T = T;
+    a.K = K;
+    a.page_size = page_size;
+    a.stages = plan.stages;
+    a.tiles_cap = plan.tiles_cap;
+    return cuda_status(dsa::launch_indexer_bf16(tk, tq, a, plan.G, plan.C, plan.groups, plan.smem,
+                                                scores != nullptr, static_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *dsa_status_string(dsa_status s) {
+    switch (s) {
+        case DSA_OK: return "ok";
+        case DSA_ERR_INVALID_ARG: return "invalid argument";
+        case DSA_ERR_UNSUPPORTED: return "unsupported";
+        case DSA_ERR_CUDA: return "CUDA error";
+        case DSA_ERR_BAD_PAGE: return "page id out of range";
+        case DSA_ERR_BAD_INDEX: return "selected index out of range";
+        case DSA_ERR_TIMEOUT: return "device wait timed out";
+    }
+    return "unknown";
+}
+
+int dsa_set_tuning(const char *name, int value) {
+    if (!name) return -1;
+    if (!strcmp(name, "indexer_cluster")) g_idx_cluster = value;
+    else if (!strcmp(name, "indexer_stages")) g_idx_stages = value;
+    else if (!strcmp(name, "indexer_group")) g_idx_group = value;
+    else if (!strcmp(name, "mla_splits")) g_mla_splits = value;
+    else if (!strcmp(name, "topk_cluster")) g_topk_cluster = value;
+    else return -1;
+    return 0;
+}
+
+size_t dsa_index_topk_workspace_size(int32_t B, int32_t T, int32_t K, int32_t max_pages_per_seq,
+                                     int32_t page_size) {
+    (void)B;
+    (void)T;
+    (void)K;
+    (void)max_pages_per_seq;
+    (void)page_size;
+    return kErrBytes;
+}
+
+size_t dsa_sparse_mla_workspace_size(int32_t T, int32_t H, int32_t K) {
+    if (T <= 0 || H <= 0 || K <= 0) return kErrBytes;
+    const int splits = mla_splits(T, H, K);
+    if (splits <= 1) return kErrBytes;
+    const size_t groups = (size_t)ceil_div(H, 64);
+    const size_t rows = (size_t)T * groups * splits * 64;
+    return kErrBytes + rows * 512 * sizeof(float) + rows * 2 * sizeof(float);
+}
+
+dsa_status dsa_workspace_init(void *workspace, size_t workspace_bytes, void *stream) {
+    if (!workspace || workspace_bytes < kErrBytes) return DSA_ERR_INVALID_ARG;
+    return cuda_status(cudaMemsetAsync(workspace, 0, kErrBytes, static_cast<cudaStream_t>(stream)));
+}
+
+dsa_status dsa_get_error(void *workspace, void *stream) {
+    if (!workspace) return DSA_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint32_t w[2] = {0, 0};
+    cudaError_t e = cudaMemcpyAsync(w, workspace, sizeof w, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(workspace, 0, sizeof w, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_status(e);
+    for (int code = 1; code < 32; ++code)
+        if (w[0] & (1u << code)) {
+            if (code == DSA_ERR_TIMEOUT) fprintf(stderr, "[dsa] device wait timed out at site 0x%x\n", w[1]);
+            return static_cast<dsa_status>(code);
+        }
+    return DSA_OK;
+}
+
+dsa_status dsa_index_topk(const void *q_idx, const uint8_t *q_idx_scale, const float *head_w,
+                          const void *k_idx_cache, const uint8_t *k_idx_scale, int64_t num_pages,
+                          const int32_t *page_table, int32_t max_pages_per_seq, const int32_t *seq_lens,
+                          const int32_t *cu_q, int32_t B, int32_t T, int32_t K, int32_t page_size,
+                          dsa_idx_dtype dtype, int32_t *indices, void *workspace, size_t workspace_bytes,
+                          void *stream) {
+    return index_common(q_idx, q_idx_scale, head_w, k_idx_cache, k_idx_scale, num_pages, page_table,
+                        max_pages_per_seq, seq_lens, cu_q, B, T, K, page_size, dtype, indices, nullptr, 0,
+                        workspace, workspace_bytes, stream);
+}
+
+dsa_status dsa_index_scores(const void *q_idx, const uint8_t *q_idx_scale, const float *head_w,
+                            const void *k_idx_cache, const uint8_t *k_idx_scale, int64_t num_pages,
+                            const int32_t *page_table, int32_t max_pages_per_seq, const int32_t *seq_lens,
+                            const int32_t *cu_q, int32_t B, int32_t T, int32_t K, int32_t page_size,
+                            dsa_idx_dtype dtype, int32_t *indices, float *scores, int64_t ld_scores,
+                            void *workspace, size_t workspace_bytes, void *stream) {
+    if (!scores || ld_scores < 1) return DSA_ERR_INVALID_ARG;
+    return index_common(q_idx, q_idx_scale, head_w, k_idx_cache, k_idx_scale, num_pages, page_table,
+                        max_pages_per_seq, seq_lens, cu_q, B, T, K, page_size, dtype, indices, scores, ld_scores,
+                        workspace, workspace_bytes, stream);
+}
+
+dsa_status dsa_topk_from_scores(const float *scores, int64_t ld, const int32_t *lens, int32_t R, int32_t K,
+                                int32_t *out, void *workspace, size_t workspace_bytes, void *stream) {
+    if (!scores || !lens || !out || !workspace || R < 0 || K < 1 || ld < 1 || workspace_bytes < kErrBytes)
+        return DSA_ERR_INVALID_ARG;
+    if (R == 0) return DSA_OK;
+    if (ld > (1LL << 30)) return DSA_ERR_UNSUPPORTED;
+    const size_t smax = max_smem_optin();
+    int forced = g_topk_cluster.load();
+    for (int C = 1; C <= 16; C <<= 1) {
+        if (forced && C != forced) continue;
+        const int cap = ceil_div(ld, C);
+        if (!forced && C < 16 && cap > 8192) continue;
+        const size_t smem = dsa::topk_smem_bytes(cap);
+        if (smem > smax) continue;
+        TopkArgs a{scores, lens, out, ld, R, K, cap};
+        return cuda_status(dsa::launch_topk_from_scores(a, C, smem, static_cast<cudaStream_t>(stream)));
+    }
+    return DSA_ERR_UNSUPPORTED;
+}
+
+dsa_status dsa_sparse_mla(const void *q, const void *kv_cache, const void *kv_rope, const float *kv_scale,
+                          int64_t num_pages, const int32_t *page_table, int32_t max_pages_per_seq,
+                          const int32_t *seq_lens, const int32_t *cu_q, const int32_t *indices, int32_t B,
+                          int32_t T, int32_t H, int32_t K, float scale, int32_t page_size, dsa_kv_dtype dtype,
+                          void *out, float *lse, void *workspace, size_t workspace_bytes, void *stream) {
+    (void)kv_rope;
+    (void)kv_scale;
+    if (T < 0 || B < 1 || K < 1 || H < 16 || H > 128 || H % 16 != 0 || page_size < 1 || num_pages < 1 ||
+        max_pages_per_seq < 1)
+        return DSA_ERR_INVALID_ARG;
+    if (!q || !kv_cache || !page_table || !seq_lens || !cu_q || !indices || !out || !workspace)
+        return DSA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(kv_cache) || !aligned16(out) || !aligned16(workspace))
+        return DSA_ERR_INVALID_ARG;
+    if (dtype != DSA_KV_BF16) return DSA_ERR_UNSUPPORTED;
+    if (workspace_bytes < dsa_sparse_mla_workspace_size(T, H, K)) return DSA_ERR_INVALID_ARG;
+    if (T == 0) return DSA_OK;
+    const int splits = mla_splits(T, H, K);
+    const int tile = dsa::mla_key_tile();
+    MlaArgs a{};
+    a.q = static_cast<const uint16_t *>(q);
+    a.kv = static_cast<const uint8_t *>(kv_cache);
+    a.page_table = page_table;
+    a.seq_lens = seq_lens;
+    a.cu_q = cu_q;
+    a.indices = indices;
+    a.out = static_cast<uint16_t *>(out);
+    a.lse = lse;
+    a.err = reinterpret_cast<uint32_t *>(workspace);
+    const size_t groups = (size_t)ceil_div(H, 64);
+    const size_t rows = (size_t)T * groups * splits * 64;
+    a.part_o = splits > 1 ? reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + kErrBytes) : nullptr;
+    a.part_ml = splits > 1 ? a.part_o + rows * 512 : nullptr;
+    a.num_pages = num_pages;
+    a.max_pages = max_pages_per_seq;
+    a.B = B;
+    a.T = T;
+    a.H = H;
+    a.K = K;
+    a.page_size = page_size;
+    a.splits = splits;
+    a.keys_per_split = ceil_div(ceil_div(K, splits), tile) * tile;
+    a.scale = scale;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    return cuda_status(dsa::launch_sparse_mla_bf16(a, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,563 @@
+// indexer_topk.cu -- fused lightweight indexer + Top-K for sm_103a.
+//
+// What it computes ("Optimizing Inference for Hybrid Attention LLMs: A
+// Practical Guide to Day-0 Adaptation", §3.1 Indexer Fusion; "Day0 Inference
+// Support and Performance Optimization for New-Architecture LLMs", §4 item 1):
+// for every query row t and causal position s <= pos(t)
+//     score(t, s) = sum_j w[t][j] * ReLU(q_idx[t][j] . k_idx[s])
+// then the top K positions by (score desc, position asc).  Scoring, head
+// weighting and selection are one kernel; the paged index-key cache is read
+// directly; scores stay in shared memory and only indices are written.
+//
+// Design (one thread-block cluster of C CTAs per group of G query rows of one
+// sequence; the group's causal history is split into C contiguous ranges of
+// 128-position tiles, one per CTA):
+//   warp 0      TMA producer: the group's Q rows once, then per tile two
+//               64-row page boxes x two 64-column halves, 128-byte swizzle,
+//               into a STAGES-deep ring.
+//   warp 1      tcgen05 issuer: D[128 pos x 64G] = K_tile[128 x 128] *
+//               Q[64G x 128]^T, eight K=16 steps, fp32 accumulators in TMEM
+//               (double-buffered), commits release the smem stage and hand the
+//               TMEM buffer to the epilogue.
+//   warps 2-5   epilogue: thread = TMEM lane = position; ReLU, weight by w and
+//               sum over the 64 heads in registers; store an order-preserving
+//               32-bit key per (query, position) in shared memory.
+//   all warps   cluster radix select (8-bit digits, histograms summed across
+//               the cluster through distributed shared memory), ties resolved
+//               to the lowest positions, indices written in ascending order.
+#include <cooperative_groups.h>
+
+#include "ptx.cuh"
+#include "kernels.h"
+
+namespace cg = cooperative_groups;
+
+namespace dsa {
+
+namespace {
+
+constexpr int kHI = 64;          // index heads
+constexpr int kDI = 128;         // index head dim
+constexpr int kTileM = 128;      // positions per tile (MMA M)
+constexpr int kBox = 64;         // rows / columns per TMA box
+constexpr int kBoxBytes = kBox * kBox * 2;           // 8 KB
+constexpr int kTileBytes = kTileM * kDI * 2;         // 32 KB
+constexpr int kRegionBytes = kTileM * 128;           // one 64-column half of a tile: 16 KB
+constexpr int kThreads = 192;
+constexpr int kHist = 256;
+
+// Order-preserving map from a finite float to uint32 (larger float -> larger
+// key); -0 is folded onto +0.  Every finite value maps above 0x007FFFFF, so 0
+// marks "not a candidate".
+__device__ __forceinline__ uint32_t score_key(float x) {
+    uint32_t u = __float_as_uint(x == 0.0f ? 0.0f : x);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+struct __align__(16) SelectSmem {
+    uint32_t hist[2][kHist];
+    uint32_t tot[kHist];
+    int32_t scan[2][8];
+    int32_t cnt[4];       // this CTA's (n_gt, n_eq) for the cluster exchange; [2] = abort flag
+    uint32_t bcast[4];    // digit, count-above
+};
+
+// Exclusive scan of one int per thread across the CTA (kThreads threads).
+__device__ __forceinline__ int block_exclusive_scan(int v, int32_t *warp_tot, int *total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_tot[warp] = x;
+    __syncthreads();
+    int before = 0, all = 0;
+#pragma unroll
+    for (int w = 0; w < kThreads / 32; ++w) {
+        int t = warp_tot[w];
+        if (w < warp) before += t;
+        all += t;
+    }
+    __syncthreads();
+    if (total) *total = all;
+    return before + x - v;
+}
+
+// Cluster-wide exact Top-K over keys held in shared memory.
+//   keys[0..n_local)   this CTA's keys, for positions pos0 + l (0 = invalid)
+//   n_valid            number of valid positions across the whole cluster
+// Writes min(K, n_valid) positions in ascending order to out[0..] and -1 to
+// the rest of out[0..K).  Every CTA of the cluster must call this with the
+// same n_valid and K (it contains cluster barriers).
+__device__ void cluster_topk(const uint32_t *keys, int n_local, int pos0, int n_valid, int K, int32_t *out,
+                             SelectSmem &ss) {
+    cg::cluster_group cluster = cg::this_cluster();
+    const unsigned C = cluster.num_blocks();
+    const unsigned my = cluster.block_rank();
+    const int tid = threadIdx.x;
+
+    if (n_valid <= K) {
+        // every valid position is selected; positions are contiguous from 0,
+        // so slot == position
+        for (int l = tid; l < n_local; l += kThreads) {
+            if (keys[l] != 0u) out[pos0 + l] = pos0 + l;
+        }
+        if (my == 0) {
+            for (int i = (n_valid > 0 ? n_valid : 0) + tid; i < K; i += kThreads) out[i] = -1;
+        }
+        cluster.sync();
+        return;
+    }
+
+    uint32_t prefix = 0, mask = 0;
+    int krem = K;
+    for (int pass = 0; pass < 4; ++pass) {
+        const int shift = 24 - 8 * pass;
+        uint32_t *h = ss.hist[pass & 1];
+        for (int d = tid; d < kHist; d += kThreads) h[d] = 0u;
+        __syncthreads();
+        for (int l = tid; l < n_local; l += kThreads) {
+            uint32_t k = keys[l];
+            if (k != 0u && (k & mask) == prefix) atomicAdd(&h[(k >> shift) & 0xFFu], 1u);
+        }
+        cluster.sync();
+        for (int d = tid; d < kHist; d += kThreads) {
+            uint32_t s = 0;
+            for (unsigned c = 0; c < C; ++c) s += cluster.map_shared_rank(h, c)[d];
+            ss.tot[d] = s;
+        }
+        __syncthreads();
+        if (tid < 32) {
+            // digits from high to low: lane L owns digits 255-8L .. 248-8L
+            uint32_t part = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) part += ss.tot[255 - 8 * tid - i];
+            uint32_t incl = part;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (tid >= o) incl += y;
+            }
+            uint32_t excl = incl - part;
+            bool mine = excl < (uint32_t)krem && (uint32_t)krem <= incl;
+            unsigned ball = __ballot_sync(0xffffffffu, mine);
+            int src = __ffs(ball) - 1;
+            if (tid == src) {
+                uint32_t above = excl;
+                int digit = 255 - 8 * tid;
+                for (int i = 0; i < 8; ++i, --digit) {
+                    uint32_t c = ss.tot[digit];
+                    if (above + c >= (uint32_t)krem) break;
+                    above += c;
+                }
+                ss.bcast[0] = (uint32_t)digit;
+                ss.bcast[1] = above;
+            }
+        }
+        __syncthreads();
+        const uint32_t digit = ss.bcast[0];
+        krem -= (int)ss.bcast[1];
+        prefix |= digit << shift;
+        mask |= 0xFFu << shift;
+        const bool done = ss.tot[digit] == (uint32_t)krem;
+        __syncthreads();
+        if (done) break;
+    }
+
+    // count (key > threshold) and (key == threshold) in this CTA, by contiguous
+    // segments so that output order follows position order
+    const int seg = (n_local + kThreads - 1) / kThreads;
+    const int l0 = min(n_local, tid * seg), l1 = min(n_local, l0 + seg);
+    int n_gt = 0, n_eq = 0;
+    for (int l = l0; l < l1; ++l) {
+        uint32_t k = keys[l];
+        if (k == 0u) continue;
+        uint32_t m = k & mask;
+        n_gt += m > prefix;
+        n_eq += m == prefix;
+    }
+    int cta_gt = 0, cta_eq = 0;
+    const int eq_before_seg = block_exclusive_scan(n_eq, ss.scan[0], &cta_eq);
+    const int gt_before_seg = block_exclusive_scan(n_gt, ss.scan[1], &cta_gt);
+    if (tid == 0) {
+        ss.cnt[0] = cta_gt;
+        ss.cnt[1] = cta_eq;
+    }
+    cluster.sync();
+    int eq_before_cta = 0, out_before_cta = 0;
+    for (unsigned c = 0; c < my; ++c) {
+        const int32_t *rc = cluster.map_shared_rank(ss.cnt, c);
+        int g = rc[0], e = rc[1];
+        int take = min(max(krem - eq_before_cta, 0), e);
+        out_before_cta += g + take;
+        eq_before_cta += e;
+    }
+    // per-segment selection counts, then their exclusive scan
+    const int eq_rank0 = eq_before_cta + eq_before_seg;
+    const int take_seg = min(max(krem - eq_rank0, 0), n_eq);
+    const int sel_before_seg = block_exclusive_scan(n_gt + take_seg, ss.scan[0], nullptr);
+    (void)gt_before_seg;
+    int slot = out_before_cta + sel_before_seg, eq_rank = eq_rank0;
+    for (int l = l0; l < l1; ++l) {
+        uint32_t k = keys[l];
+        if (k == 0u) continue;
+        uint32_t m = k & mask;
+        bool sel = m > prefix;
+        if (m == prefix) {
+            sel = eq_rank < krem;
+            ++eq_rank;
+        }
+        if (sel) out[slot++] = pos0 + l;
+    }
+    // nobody may reuse or leave shared memory another CTA still reads
+    cluster.sync();
+}
+
+template <int G>
+struct IdxLayout {
+    static constexpr int kQBytes = G * kHI * kDI * 2;  // both 64-column halves
+    static constexpr int kQRegion = G * kHI * 128;     // one half: G*64 rows x 128 B
+    static constexpr int kN = G * kHI;                 // MMA N
+    static constexpr int kTmemCols = 2 * kN <= 32 ? 32 : (2 * kN <= 64 ? 64 : (2 * kN <= 128 ? 128 : (2 * kN <= 256 ? 256 : 512)));
+};
+
+struct __align__(16) IdxBars {
+    uint64_t drain;
+    uint64_t full[8];
+    uint64_t empty[8];
+    uint64_t tfull[2];
+    uint64_t tempty[2];
+    uint64_t qbar;
+    uint32_t tmem_slot;
+    int abort;
+};
+
+__device__ __forceinline__ int find_seq(const int32_t *cu_q, int B, int t) {
+    int lo = 0, hi = B - 1;
+    while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if (__ldg(cu_q + mid) <= t) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
+}
+
+template <int G, bool kWriteScores>
+__global__ void __launch_bounds__(kThreads, 1)
+    indexer_topk_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
+                             IndexerArgs a) {
+    using L = IdxLayout<G>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int key_cap = a.tiles_cap * kTileM;
+    uint8_t *sQ = smem;
+    uint8_t *sK = sQ + L::kQBytes;
+    uint32_t *sKeys = reinterpret_cast<uint32_t *>(sK + (size_t)a.stages * kTileBytes);
+    float *sW = reinterpret_cast<float *>(sKeys + (size_t)G * key_cap);
+    SelectSmem *ss = reinterpret_cast<SelectSmem *>(sW + G * kHI);
+    IdxBars *bars = reinterpret_cast<IdxBars *>(ss + 1);
+    static_assert(sizeof(SelectSmem) % 16 == 0, "keep the barrier block 16-byte aligned");
+
+    cg::cluster_group cluster = cg::this_cluster();
+    const int C = (int)cluster.num_blocks();
+    const int crank = (int)cluster.block_rank();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // ---- which query rows this cluster serves
+    int b, t0, gn;
+    {
+        const int g = blockIdx.y;
+        if (G == 1) {
+            if (g >= a.T) return;
+            t0 = g;
+            b = find_seq(a.cu_q, a.B, t0);
+            gn = 1;
+        } else {
+            int acc = 0;
+            b = -1;
+            for (int s = 0; s < a.B; ++s) {
+                int nq = __ldg(a.cu_q + s + 1) - __ldg(a.cu_q + s);
+                int ng = (nq + G - 1) / G;
+                if (g < acc + ng) {
+                    b = s;
+                    break;
+                }
+                acc += ng;
+            }
+            if (b < 0) return;  // past the last group: the whole cluster leaves together
+            t0 = __ldg(a.cu_q + b) + (g - acc) * G;
+            gn = min(G, __ldg(a.cu_q + b + 1) - t0);
+        }
+    }
+    const int nq_b = __ldg(a.cu_q + b + 1) - __ldg(a.cu_q + b);
+    const int pos_first = __ldg(a.seq_lens + b) - nq_b + (t0 - __ldg(a.cu_q + b));
+    const int pos_last = pos_first + gn - 1;   // positions of rows t0 .. t0+gn-1
+    const int n_total = pos_last + 1;          // history the group needs
+    const int tiles_total = (n_total + kTileM - 1) / kTileM;
+    const int tpc = (tiles_total + C - 1) / C;
+    const int tile0 = min(tiles_total, crank * tpc);
+    int n_tiles = min(tiles_total, tile0 + tpc) - tile0;
+    if (n_tiles > a.tiles_cap) {  // a sequence longer than max_pages_per_seq * page_size
+        if (threadIdx.x == 0) report_error(a.err, kErrBadLen);
+        n_tiles = a.tiles_cap;
+    }
+    const int32_t *pt_row = a.page_table + (size_t)b * a.max_pages;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < a.stages; ++s) {
+            mbar_init(&bars->full[s], 1);
+            mbar_init(&bars->empty[s], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bars->tfull[i], 1);
+            mbar_init(&bars->tempty[i], 4);
+        }
+        mbar_init(&bars->qbar, 1);
+        mbar_init(&bars->drain, 1);
+        bars->abort = 0;
+        fence_mbar_init();
+    }
+    for (int i = threadIdx.x; i < G * kHI; i += kThreads) {
+        int gi = i / kHI;
+        sW[i] = gi < gn ? __ldg(a.head_w + (size_t)(t0 + gi) * kHI + (i % kHI)) : 0.0f;
+    }
+    if (warp == 1) tmem_alloc(&bars->tmem_slot, L::kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_slot;
+    volatile int *abort = &bars->abort;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- TMA producer
+            tma_prefetch_desc(&tm_k);
+            tma_prefetch_desc(&tm_q);
+            mbar_arrive_expect_tx(&bars->qbar, (uint32_t)(gn * 2 * kBoxBytes));
+            for (int gi = 0; gi < gn; ++gi) {
+                tma_load_2d(sQ + gi * kBoxBytes, &tm_q, &bars->qbar, 0, (t0 + gi) * kHI);
+                tma_load_2d(sQ + L::kQRegion + gi * kBoxBytes, &tm_q, &bars->qbar, kBox, (t0 + gi) * kHI);
+            }
+            int issued = 0;
+            for (int i = 0; i < n_tiles; ++i) {
+                const int s = i % a.stages;
+                if (i >= a.stages && !mbar_wait(&bars->empty[s], ((i / a.stages) & 1) ^ 1, a.err, 0x101, abort))
+                    break;
+                issued = i + 1;
+                uint8_t *dst = sK + (size_t)s * kTileBytes;
+                const int p_tile = (tile0 + i) * kTileM;
+                int rows[2];
+                uint32_t bytes = 0;
+                for (int h = 0; h < 2; ++h) {
+                    rows[h] = -1;
+                    const int p0 = p_tile + h * kBox;
+                    if (p0 > pos_last) continue;
+                    const int page = __ldg(pt_row + p0 / a.page_size);
+                    if (page < 0 || (int64_t)page >= a.num_pages) {
+                        report_error(a.err, kErrBadPage);
+                        continue;
+                    }
+                    rows[h] = page * a.page_size + p0 % a.page_size;
+                    bytes += 2 * kBoxBytes;
+                }
+                mbar_arrive_expect_tx(&bars->full[s], bytes);
+                for (int h = 0; h < 2; ++h) {
+                    if (rows[h] < 0) continue;
+                    tma_load_2d(dst + h * kBoxBytes, &tm_k, &bars->full[s], 0, rows[h]);
+                    tma_load_2d(dst + kRegionBytes + h * kBoxBytes, &tm_k, &bars->full[s], kBox, rows[h]);
+                }
+            }
+            if (*abort) {
+                // let copies still in flight land before shared memory is released
+                volatile int no_abort = 0;
+                mbar_wait(&bars->qbar, 0, nullptr, 0, &no_abort);
+                for (int i = max(0, issued - a.stages); i < issued; ++i)
+                    mbar_wait(&bars->full[i % a.stages], (i / a.stages) & 1, nullptr, 0, &no_abort);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---------------- tcgen05 issuer
+            constexpr uint32_t idesc = idesc_bf16_f32(kTileM, L::kN);
+            bool ok = mbar_wait(&bars->qbar, 0, a.err, 0x201, abort);
+            const uint32_t q_base = smem_u32(sQ);
+            for (int i = 0; ok && i < n_tiles; ++i) {
+                const int s = i % a.stages, buf = i & 1;
+                if (!mbar_wait(&bars->full[s], (i / a.stages) & 1, a.err, 0x202, abort)) break;
+                if (i >= 2 && !mbar_wait(&bars->tempty[buf], ((i >> 1) & 1) ^ 1, a.err, 0x203, abort)) break;
+                tc_fence_after();
+                const uint32_t k_base = smem_u32(sK + (size_t)s * kTileBytes);
+                const uint32_t d = tmem + (uint32_t)(buf * L::kN);
+#pragma unroll
+                for (int kk = 0; kk < kDI / 16; ++kk) {
+                    const uint32_t off = (uint32_t)((kk & 3) * 32);
+                    const uint64_t adesc = sdesc_kmajor_sw128(k_base + (kk >> 2) * kRegionBytes + off);
+                    const uint64_t bdesc = sdesc_kmajor_sw128(q_base + (kk >> 2) * L::kQRegion + off);
+                    mma_bf16_ss(d, adesc, bdesc, idesc, kk > 0 ? 1u : 0u);
+                }
+                mma_commit(&bars->empty[s]);
+                mma_commit(&bars->tfull[buf]);
+            }
+            if (*abort) {
+                // wait for every issued MMA before TMEM is released
+                volatile int no_abort = 0;
+                mma_commit(&bars->drain);
+                mbar_wait(&bars->drain, 0, nullptr, 0, &no_abort);
+            }
+        }
+    } else {
+        // ---------------- epilogue: warps 2..5, thread = position row
+        const int quad = warp & 3;
+        const int row = quad * 32 + lane;
+        for (int i = 0; i < n_tiles; ++i) {
+            const int buf = i & 1;
+            const bool ok = mbar_wait(&bars->tfull[buf], (i >> 1) & 1, a.err, 0x301, abort);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            tc_fence_after();
+            const int l = i * kTileM + row;          // local key slot
+            const int pos = (tile0 + i) * kTileM + row;
+#pragma unroll
+            for (int gi = 0; gi < G; ++gi) {
+                const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(buf * L::kN + gi * kHI);
+                uint32_t r0[32], r1[32];
+                tmem_ld32(taddr, r0);
+                tmem_ld32(taddr + 32, r1);
+                tmem_wait_ld();
+                const float *w = sW + gi * kHI;
+                float acc = 0.0f;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) acc = fmaf(w[j], fmaxf(__uint_as_float(r0[j]), 0.0f), acc);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) acc = fmaf(w[32 + j], fmaxf(__uint_as_float(r1[j]), 0.0f), acc);
+                const bool valid = gi < gn && pos <= pos_first + gi;
+                sKeys[(size_t)gi * key_cap + l] = valid ? score_key(acc) : 0u;
+                if (kWriteScores && valid && pos < a.ld_scores) a.scores[(size_t)(t0 + gi) * a.ld_scores + pos] = acc;
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->tempty[buf]);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, L::kTmemCols);
+    // If any CTA of the cluster gave up on a wait, the whole cluster skips
+    // selection (the decision must be uniform: selection has cluster barriers).
+    if (threadIdx.x == 0) ss->cnt[2] = bars->abort;
+    cluster.sync();
+    int any_abort = 0;
+    for (int c = 0; c < C; ++c) any_abort |= cluster.map_shared_rank(&ss->cnt[2], c)[0];
+    cluster.sync();
+    if (any_abort) return;
+
+    // ---------------- selection, one query row at a time
+    for (int gi = 0; gi < G; ++gi) {
+        if (gi >= gn) {
+            cluster.sync();
+            continue;
+        }
+        const int n_valid = pos_first + gi + 1;
+        int32_t *out = a.indices + (size_t)(t0 + gi) * a.K;
+        cluster_topk(sKeys + (size_t)gi * key_cap, n_tiles * kTileM, tile0 * kTileM, n_valid, a.K, out, *ss);
+    }
+}
+
+// Top-K of given score rows (test hook and standalone selection).
+__global__ void __launch_bounds__(kThreads, 1) topk_from_scores_kernel(TopkArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 15) & ~uintptr_t(15));
+    uint32_t *sKeys = reinterpret_cast<uint32_t *>(smem);
+    SelectSmem *ss = reinterpret_cast<SelectSmem *>(sKeys + a.chunk_cap);
+    cg::cluster_group cluster = cg::this_cluster();
+    const int C = (int)cluster.num_blocks();
+    const int crank = (int)cluster.block_rank();
+    const int r = blockIdx.y;
+    if (r >= a.R) return;
+    const int n = max(0, min(__ldg(a.lens + r), (int)a.ld));
+    const int chunk = (n + C - 1) / C;
+    const int p0 = min(n, crank * chunk);
+    const int nl = min(n, p0 + chunk) - p0;
+    const float *row = a.scores + (size_t)r * a.ld;
+    for (int l = threadIdx.x; l < nl; l += kThreads) sKeys[l] = score_key(__ldg(row + p0 + l));
+    __syncthreads();
+    cluster_topk(sKeys, nl, p0, n, a.K, a.out + (size_t)r * a.K, *ss);
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------ host side
+
+size_t indexer_smem_bytes(int G, int stages, int tiles_cap) {
+    size_t q = (size_t)G * kHI * kDI * 2;
+    size_t k = (size_t)stages * kTileBytes;
+    size_t keys = (size_t)G * tiles_cap * kTileM * 4;
+    size_t w = (size_t)G * kHI * 4;
+    return 1024 + q + k + keys + w + sizeof(SelectSmem) + sizeof(IdxBars);
+}
+
+size_t topk_smem_bytes(int chunk_cap) { return 16 + (size_t)chunk_cap * 4 + sizeof(SelectSmem); }
+
+template <int G, bool W>
+static cudaError_t launch_idx(const CUtensorMap &tk, const CUtensorMap &tq, const IndexerArgs &a, int C,
+                              int groups, size_t smem, cudaStream_t st) {
+    auto kern = indexer_topk_bf16_kernel<G, W>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    if (C > 8) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return e;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)C, (unsigned)groups, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, tk, tq, a);
+}
+
+cudaError_t launch_indexer_bf16(const CUtensorMap &tk, const CUtensorMap &tq, const IndexerArgs &a, int G, int C,
+                                int groups, size_t smem, bool write_scores, cudaStream_t st) {
+    if (G == 1) return write_scores ? launch_idx<1, true>(tk, tq, a, C, groups, smem, st)
+                                    : launch_idx<1, false>(tk, tq, a, C, groups, smem, st);
+    if (G == 2) return write_scores ? launch_idx<2, true>(tk, tq, a, C, groups, smem, st)
+                                    : launch_idx<2, false>(tk, tq, a, C, groups, smem, st);
+    if (G == 4) return write_scores ? launch_idx<4, true>(tk, tq, a, C, groups, smem, st)
+                                    : launch_idx<4, false>(tk, tq, a, C, groups, smem, st);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_topk_from_scores(const TopkArgs &a, int C, size_t smem, cudaStream_t st) {
+    auto kern = topk_from_scores_kernel;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    if (C > 8) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return e;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)C, (unsigned)a.R, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
+}  // namespace dsa

@@ -1,0 +1,70 @@
+// kernels.h -- internal interface between the C ABI (dsa_abi.cu) and the
+// kernel translation units.  Not installed; not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace dsa {
+
+// Fused indexer + Top-K (indexer_topk.cu).
+struct IndexerArgs {
+    const float *head_w;        // [T, 64]
+    const int32_t *page_table;  // [B, max_pages]
+    const int32_t *seq_lens;    // [B]
+    const int32_t *cu_q;        // [B+1]
+    int32_t *indices;           // [T, K]
+    float *scores;              // [T, ld_scores] (test hook) or null
+    uint32_t *err;              // device error word
+    int64_t num_pages;
+    int64_t ld_scores;
+    int32_t max_pages;
+    int32_t B, T, K, page_size;
+    int32_t stages;             // smem ring depth (<= 8)
+    int32_t tiles_cap;          // 128-position tiles one CTA can hold keys for
+};
+
+struct TopkArgs {
+    const float *scores;   // [R, ld]
+    const int32_t *lens;   // [R]
+    int32_t *out;          // [R, K]
+    int64_t ld;
+    int32_t R, K;
+    int32_t chunk_cap;     // keys one CTA holds
+};
+
+size_t indexer_smem_bytes(int G, int stages, int tiles_cap);
+size_t topk_smem_bytes(int chunk_cap);
+cudaError_t launch_indexer_bf16(const CUtensorMap &tm_k, const CUtensorMap &tm_q, const IndexerArgs &a, int G,
+                                int C, int groups, size_t smem, bool write_scores, cudaStream_t st);
+cudaError_t launch_topk_from_scores(const TopkArgs &a, int C, size_t smem, cudaStream_t st);
+
+// Sparse MLA (sparse_mla.cu).
+struct MlaArgs {
+    const uint16_t *q;          // [T, H, 576] bf16
+    const uint8_t *kv;          // [num_pages*page_size, 576] bf16 rows
+    const int32_t *page_table;  // [B, max_pages]
+    const int32_t *seq_lens;    // [B]
+    const int32_t *cu_q;        // [B+1]
+    const int32_t *indices;     // [T, K]
+    uint16_t *out;              // [T, H, 512] bf16
+    float *lse;                 // [T, H] or null
+    float *part_o;              // [T, H/64, splits, 64, 512] fp32 partial outputs (splits > 1)
+    float *part_ml;             // [T, H/64, splits, 64, 2] running max (log2 domain) and sum
+    uint32_t *err;
+    int64_t num_pages;
+    int32_t max_pages;
+    int32_t B, T, H, K, page_size;
+    int32_t splits;             // key splits per (query, head group)
+    int32_t keys_per_split;     // multiple of the key tile
+    float scale_log2;           // softmax scale * log2(e)
+    float scale;                // softmax scale
+};
+
+size_t mla_smem_bytes();
+int mla_key_tile();
+cudaError_t launch_sparse_mla_bf16(const MlaArgs &a, cudaStream_t st);
+
+}  // namespace dsa

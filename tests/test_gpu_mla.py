@@ -1,0 +1,92 @@
+"""GPU sparse MLA against the oracle on the same indices: outputs within
+2e-2 absolute / 1e-2 relative (bf16 path), lse within 1e-3; covers 16, 64 and
+128 heads, -1 padding, a single selected key, rows with no valid key, every
+split count, and the paged gather."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from _util import dev, dev_bf16, to_device
+from indexer_top_sparse_gb300.inputs import make_workload
+
+pytestmark = pytest.mark.gpu
+
+ATOL, RTOL = 2e-2, 1e-2
+
+
+def _random_indices(rng, wl, K, pad_frac=0.0):
+    pos = wl.query_pos()
+    idx = np.full((wl.T, K), -1, np.int32)
+    for t in range(wl.T):
+        n = int(pos[t]) + 1
+        m = min(K, n)
+        sel = np.sort(rng.choice(n, m, replace=False)).astype(np.int32)
+        if pad_frac:
+            sel[rng.random(m) < pad_frac] = -1
+        idx[t, :m] = sel
+    return idx
+
+
+def _run(wl, idx, want_lse=True):
+    import indexer_top_sparse_gb300 as d
+    t = to_device(wl)
+    lse = torch.empty((wl.T, wl.H), dtype=torch.float32, device="cuda") if want_lse else None
+    ws = d.Workspace(d.sparse_mla_workspace_size(wl.T, wl.H, idx.shape[1]))
+    out = d.dsa_sparse_mla(t["q"], t["kv"], t["page_table"], t["seq_lens"], t["cu_q"], dev(idx), wl.scale, lse=lse,
+                           workspace=ws)
+    ws.check()
+    return out.float().cpu().numpy(), (lse.cpu().numpy() if want_lse else None)
+
+
+def _compare(orc, wl, idx, rows=None):
+    out, lse = _run(wl, idx)
+    rows = np.arange(wl.T, dtype=np.int32) if rows is None else np.asarray(rows, np.int32)
+    ref, ref_lse = orc.sparse_mla(wl.q, wl.kv, wl.page_table, wl.cu_q, idx, wl.scale, wl.page_size, rows=rows)
+    np.testing.assert_allclose(out[rows], ref, atol=ATOL, rtol=RTOL)
+    fin = np.isfinite(ref_lse)
+    np.testing.assert_allclose(lse[rows][fin], ref_lse[fin], rtol=1e-3, atol=1e-3)
+    assert np.all(np.isneginf(lse[rows][~fin]))
+
+
+@pytest.mark.parametrize("H", [16, 64, 128])
+def test_decode_heads(orc, H):
+    rng = np.random.default_rng(H)
+    wl = make_workload("mla", [3000, 513, 70], [1, 1, 1], H=H, K=512, page_size=64, seed=H, with_idx=False)
+    _compare(orc, wl, _random_indices(rng, wl, 512))
+
+
+@pytest.mark.parametrize("splits", [1, 2, 3, 8])
+def test_every_split_count(orc, splits):
+    import indexer_top_sparse_gb300 as d
+    rng = np.random.default_rng(100 + splits)
+    wl = make_workload("mla", [4000, 900], [1, 1], H=64, K=1000, page_size=64, seed=splits, with_idx=False)
+    idx = _random_indices(rng, wl, 1000, pad_frac=0.1)
+    d.set_tuning("mla_splits", splits)
+    try:
+        _compare(orc, wl, idx)
+    finally:
+        d.set_tuning("mla_splits", 0)
+
+
+def test_padding_single_key_and_empty_rows(orc):
+    wl = make_workload("mla", [300, 300, 300, 50], [1, 1, 1, 1], H=16, K=64, page_size=32, seed=5, with_idx=False)
+    idx = np.full((4, 64), -1, np.int32)
+    idx[0, :40] = np.arange(0, 400, 10)[:40] % 300
+    idx[0] = np.where(np.arange(64) % 3 == 0, -1, idx[0])
+    idx[1, 17] = 123                      # a single selected key
+    # row 2: no valid key
+    idx[3, :50] = np.arange(50)           # every position of a short sequence
+    _compare(orc, wl, idx)
+    out, lse = _run(wl, idx)
+    v = wl.kv.reshape(-1, 576)[wl.page_table[1][123 // 32] * 32 + 123 % 32, :512]
+    from indexer_top_sparse_gb300.inputs import bf16_to_f32
+    np.testing.assert_allclose(out[1], np.broadcast_to(bf16_to_f32(v), (16, 512)), atol=1e-2, rtol=1e-2)
+    assert np.all(out[2] == 0) and np.all(np.isneginf(lse[2]))
+
+
+def test_prefill_rows(orc):
+    rng = np.random.default_rng(7)
+    wl = make_workload("mla_prefill", [400], [400], H=16, K=128, page_size=64, permute=False, seed=7, with_idx=False)
+    _compare(orc, wl, _random_indices(rng, wl, 128), rows=[0, 1, 2, 127, 128, 129, 255, 399])
