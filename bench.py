@@ -1,0 +1,352 @@
+"""Benchmark of the DSA "score, select, sparse read" path on GB300.
+
+One step = the whole hot path over one batch: dsa_index_topk (fused indexer +
+Top-K) then dsa_sparse_mla, on the decode workload of 32 sequences at 32768
+cached positions (K=2048, 64x128 index heads, 128 MLA heads, 576-wide bf16
+latent rows, 64-row pages in a seeded random permutation).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  Under torchrun (N>1) every rank runs its own
+batch (independent replicas, no collective on the data path): value is the
+sum of all ranks' tokens over the slowest rank's time.
+
+--impl reference times the CPU oracle (plain single-threaded C, fp64) on this
+machine's host cores, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode tokens/s + prefill tokens/s (index+TopK+sparse MLA), % HBM/tensor roofline"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+FALLBACK_HBM_GBS = 6800.0
+
+
+def peaks():
+    try:
+        p = json.load(open(PEAKS_FILE))
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash(name: str) -> str:
+    path = os.path.join(ROOT, "indexer_top_sparse_gb300", "csrc", name)
+    h = hashlib.sha256()
+    for f in (path, os.path.join(ROOT, "indexer_top_sparse_gb300", "csrc", "ptx.cuh")):
+        h.update(open(f, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, source: str):
+    """DRAM bytes per launch from a committed ncu summary, only if the kernel
+    source is unchanged since the capture."""
+    try:
+        t = json.load(open(TRAFFIC_FILE))[kernel]
+        if t["source_sha"] == kernel_source_hash(source):
+            return float(t["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+# ---------------------------------------------------------------- algorithmic bytes
+
+def indexer_bytes(wl) -> float:
+    """Bytes the indexer must move for the batch: every causal history key once
+    (128 bf16 = 256 B), the query's 64x128 bf16 index query and 64 fp32 head
+    weights, its page-table row and its K int32 indices."""
+    pos = wl.query_pos()
+    n = (pos + 1).astype(np.float64)
+    return float(np.sum(n * 256 + 64 * 128 * 2 + 64 * 4 + 4 * wl.K + 4 * np.ceil(n / wl.page_size)))
+
+
+def mla_bytes(wl) -> float:
+    """Bytes sparse MLA must move: min(K, n) selected 576-wide bf16 rows, the
+    H x 576 bf16 query, the H x 512 bf16 output, the K int32 indices and the
+    page-table row."""
+    pos = wl.query_pos()
+    n = (pos + 1).astype(np.float64)
+    sel = np.minimum(n, wl.K)
+    return float(np.sum(sel * 1152 + wl.H * 1152 + wl.H * 1024 + 4 * wl.K + 4 * np.ceil(n / wl.page_size)))
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                smax.append(float(f[1]))
+            except ValueError:
+                continue
+            for name, v in zip(names, f[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- oracle timing
+
+def oracle_rate(wl, budget_s, max_queries: int, frac: int = 1):
+    """Time the CPU oracle on whole decode queries (frac = 1) until budget_s
+    seconds of work (None: no time bound) or max_queries units; with frac > 1 each unit is 1/frac of a query
+    (the indexer over the first N/frac positions and Top-K of those, attention
+    for H/frac heads).  Returns (queries per second, units, seconds)."""
+    import oracle
+    oracle.build()
+    H = wl.H
+    hq = max(1, H // frac)
+    units, spent = 0, 0.0
+    t = 0
+    while units < max_queries and (budget_s is None or spent < budget_s or units == 0):
+        b = int(np.searchsorted(wl.cu_q, t, side="right") - 1)
+        n = int(wl.query_pos()[t]) + 1
+        n_part = max(1, n // frac)
+        t0 = time.perf_counter()
+        sc = oracle.index_scores_row(wl.q_idx[t], wl.head_w[t], wl.k_idx, wl.page_table[b], wl.page_size, n_part)
+        idx = oracle.topk_rows(sc[None, :], np.array([n_part], np.int32), wl.K)
+        q_part = np.ascontiguousarray(wl.q[t:t + 1, :hq])
+        cu = np.array([0, 1], np.int32)
+        oracle.sparse_mla(q_part, wl.kv, wl.page_table[b:b + 1], cu, idx, wl.scale, wl.page_size)
+        spent += time.perf_counter() - t0
+        units += 1
+        t = (t + 1) % wl.T
+    return (units / frac) / spent, units, spent
+
+
+# ---------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=32,
+                    help="sequences per rank (default 32, the benchmark workload; smaller only for profiling)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    from indexer_top_sparse_gb300.inputs import decode_b32_n32k, make_workload
+    if args.batch == 32:
+        wl = decode_b32_n32k(args.seed + rank)
+    else:
+        wl = make_workload(f"decode_b{args.batch}_n32768_k2048_h128_paged64", [32768] * args.batch,
+                           [1] * args.batch, H=128, K=2048, page_size=64, permute=True, seed=args.seed + rank)
+    cfg = {"workload": wl.name, "B": wl.B, "N": int(wl.seq_lens[0]), "K": wl.K, "H": wl.H, "H_I": 64, "d_I": 128,
+           "D": 576, "D_v": 512, "page_size": wl.page_size, "global_batch": wl.B * max(world, 1),
+           "l2": "flushed between steps (512 MiB device write)", "parallelism": f"replicas{max(world, 1)}"}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        # bounded sample: each step is 1/frac of one decode query, frac chosen
+        # so that the whole run takes about two minutes
+        probe, _, tprobe = oracle_rate(wl, None, 1)
+        per_query = 1.0 / probe
+        frac = 1
+        while frac < 256 and (args.steps + args.warmup) * per_query / frac > 120.0:
+            frac *= 2
+        oracle_rate(wl, None, args.warmup, frac)
+        rate, units, spent = oracle_rate(wl, None, args.steps, frac)
+        sample = (f"{units} steps, each 1/{frac} of a decode query (indexer over N/{frac} positions + Top-K, "
+                  f"attention for H/{frac} heads) of the same workload; tokens/s = queries / time")
+        line = {"impl": "reference", "metric": METRIC, "value": rate, "unit": "tokens/s", "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * spent / max(units, 1),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": cfg,
+                "cpu_baseline": {"value": rate, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample},
+                "e2e": {"value": rate, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
+
+    import torch
+    import indexer_top_sparse_gb300 as d
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+
+    def bf16(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    k_idx, kv = bf16(wl.k_idx), bf16(wl.kv)
+    q_idx, q = bf16(wl.q_idx), bf16(wl.q)
+    head_w = torch.from_numpy(wl.head_w).to(dev)
+    pt, sl, cq = (torch.from_numpy(a).to(dev) for a in (wl.page_table, wl.seq_lens, wl.cu_q))
+    idx = torch.empty((wl.T, wl.K), dtype=torch.int32, device=dev)
+    out = torch.empty((wl.T, wl.H, 512), dtype=torch.bfloat16, device=dev)
+    ws = d.Workspace(max(d.index_topk_workspace_size(wl.B, wl.T, wl.K, wl.max_pages, wl.page_size),
+                         d.sparse_mla_workspace_size(wl.T, wl.H, wl.K)), dev)
+    launches_per_step = 2 + (1 if d.sparse_mla_workspace_size(wl.T, wl.H, wl.K) > 256 else 0)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def run_step(qi, hw, qq, ptab, slen, cuq):
+        d.dsa_index_topk(qi, hw, k_idx, ptab, slen, cuq, wl.K, indices=idx, workspace=ws)
+        d.dsa_sparse_mla(qq, kv, ptab, slen, cuq, idx, wl.scale, out=out, workspace=ws)
+
+    def barrier():
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(dev)
+
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    t_soak = time.perf_counter()
+    while time.perf_counter() - t_soak < 1.0:           # bring clocks to their loaded state
+        run_step(q_idx, head_w, q, pt, sl, cq)
+        torch.cuda.synchronize(dev)
+    for _ in range(args.warmup):
+        flush.zero_()
+        run_step(q_idx, head_w, q, pt, sl, cq)
+    ws.check()
+
+    # ---- device-resident timing, per kernel, L2 flushed before every step
+    barrier()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        d.dsa_index_topk(q_idx, head_w, k_idx, pt, sl, cq, wl.K, indices=idx, workspace=ws)
+        ev[i][1].record(stream)
+        d.dsa_sparse_mla(q, kv, pt, sl, cq, idx, wl.scale, out=out, workspace=ws)
+        ev[i][2].record(stream)
+    barrier()
+    t_idx = [e[0].elapsed_time(e[1]) * 1e-3 for e in ev]
+    t_mla = [e[1].elapsed_time(e[2]) * 1e-3 for e in ev]
+    total = sum(t_idx) + sum(t_mla)
+    ws.check()
+
+    # ---- end to end through the public API: pinned host inputs -> device ->
+    # kernels -> output back to pinned host memory, every step
+    h_in = {k: v.pin_memory() for k, v in {"q_idx": q_idx.cpu(), "head_w": head_w.cpu(), "q": q.cpu(),
+                                           "pt": pt.cpu(), "sl": sl.cpu(), "cq": cq.cpu()}.items()}
+    d_in = {k: torch.empty_like(v, device=dev) for k, v in h_in.items()}
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in h_in.values())
+    d2h = h_out.numel() * h_out.element_size()
+    for _ in range(3):
+        for k in h_in:
+            d_in[k].copy_(h_in[k], non_blocking=True)
+        run_step(d_in["q_idx"], d_in["head_w"], d_in["q"], d_in["pt"], d_in["sl"], d_in["cq"])
+        h_out.copy_(out, non_blocking=True)
+    barrier()
+    e2e_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.zero_()
+        e2e_ev[i][0].record(stream)
+        for k in h_in:
+            d_in[k].copy_(h_in[k], non_blocking=True)
+        run_step(d_in["q_idx"], d_in["head_w"], d_in["q"], d_in["pt"], d_in["sl"], d_in["cq"])
+        h_out.copy_(out, non_blocking=True)
+        e2e_ev[i][1].record(stream)
+    barrier()
+    clk = clocks.stop()
+    e2e_total = sum(e[0].elapsed_time(e[1]) * 1e-3 for e in e2e_ev)
+    ws.check()
+
+    # ---- max over ranks
+    t_max, e2e_max = total, e2e_total
+    if world > 1:
+        tt = torch.tensor([total, e2e_total], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        t_max, e2e_max = float(tt[0]), float(tt[1])
+    tokens = wl.T * args.steps * max(world, 1)
+
+    if rank == 0:
+        hbm, peak_kind = peaks()
+        ib, mb = indexer_bytes(wl), mla_bytes(wl)
+        ti, tm = statistics.mean(t_idx), statistics.mean(t_mla)
+        kernels = {
+            "indexer_topk": {"seconds_per_launch": ti, "algorithmic_bytes": ib, "achieved_gbs": ib / ti / 1e9,
+                             "traffic": recorded_traffic("indexer_topk", "indexer_topk.cu")},
+            "sparse_mla": {"seconds_per_launch": tm, "algorithmic_bytes": mb, "achieved_gbs": mb / tm / 1e9,
+                           "traffic": recorded_traffic("sparse_mla", "sparse_mla.cu")},
+        }
+        dom = max(kernels, key=lambda k: kernels[k]["seconds_per_launch"])
+        k = kernels[dom]
+        line = {
+            "metric": METRIC, "value": tokens / t_max, "unit": "tokens/s", "n_gpus": max(world, 1),
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t_max / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) bf16, random page permutation)", "config": cfg,
+            "roofline": {"bound": "hbm", "kernel": dom, "achieved": k["achieved_gbs"], "peak": hbm,
+                         "peak_kind": peak_kind, "unit": "GB/s", "frac": k["achieved_gbs"] / hbm,
+                         "traffic": k["traffic"]},
+            "step_roofline": {"bytes": ib + mb, "achieved_gbs": (ib + mb) / (t_max / args.steps) / 1e9,
+                              "frac": (ib + mb) / (t_max / args.steps) / 1e9 / hbm},
+            "kernels": kernels,
+            "e2e": {"value": tokens / e2e_max, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clk,
+        }
+        if world <= 1 and not args.no_cpu_baseline:
+            rate, units, spent = oracle_rate(wl, 10.0, 16)
+            line["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                                    "sample": f"{units} whole decode queries of this workload ({spent:.1f} s, "
+                                              f"single-threaded C oracle, fp64)"}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

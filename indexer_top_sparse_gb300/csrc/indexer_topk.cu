@@ -471,7 +471,8 @@ __global__ void __launch_bounds__(kThreads, 1) topk_from_scores_kernel(TopkArgs 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 15) & ~uintptr_t(15));
     uint32_t *sKeys = reinterpret_cast<uint32_t *>(smem);
-    SelectSmem *ss = reinterpret_cast<SelectSmem *>(sKeys + a.chunk_cap);
+    // the selection block needs 16-byte alignment: round the key region up
+    SelectSmem *ss = reinterpret_cast<SelectSmem *>(sKeys + ((a.chunk_cap + 3) & ~3));
     cg::cluster_group cluster = cg::this_cluster();
     const int C = (int)cluster.num_blocks();
     const int crank = (int)cluster.block_rank();
@@ -499,7 +500,7 @@ size_t indexer_smem_bytes(int G, int stages, int tiles_cap) {
     return 1024 + q + k + keys + w + sizeof(SelectSmem) + sizeof(IdxBars);
 }
 
-size_t topk_smem_bytes(int chunk_cap) { return 16 + (size_t)chunk_cap * 4 + sizeof(SelectSmem); }
+size_t topk_smem_bytes(int chunk_cap) { return 16 + (size_t)((chunk_cap + 3) & ~3) * 4 + sizeof(SelectSmem); }
 
 template <int G, bool W>
 static cudaError_t launch_idx(const CUtensorMap &tk, const CUtensorMap &tq, const IndexerArgs &a, int C,
