@@ -160,6 +160,25 @@ def oracle_rate(wl, budget_s, max_queries: int, frac: int = 1):
     return (units / frac) / spent, units, spent
 
 
+# ---------------------------------------------------------------- multi-rank
+
+def max_over_ranks(values, device=None):
+    """Element-wise maximum of a list of floats across all ranks of the
+    default process group (identity without one)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.cpu()]
+
+
+def aggregate_rate(tokens_per_rank: int, world: int, seconds_max: float) -> float:
+    """Whole-job throughput: every rank's tokens over the slowest rank's time."""
+    return tokens_per_rank * max(world, 1) / seconds_max
+
+
 # ---------------------------------------------------------------- main
 
 def main():
@@ -303,12 +322,8 @@ def main():
     ws.check()
 
     # ---- max over ranks
-    t_max, e2e_max = total, e2e_total
-    if world > 1:
-        tt = torch.tensor([total, e2e_total], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        t_max, e2e_max = float(tt[0]), float(tt[1])
-    tokens = wl.T * args.steps * max(world, 1)
+    t_max, e2e_max = max_over_ranks([total, e2e_total], dev)
+    tokens = wl.T * args.steps
 
     if rank == 0:
         hbm, peak_kind = peaks()
@@ -323,7 +338,8 @@ def main():
         dom = max(kernels, key=lambda k: kernels[k]["seconds_per_launch"])
         k = kernels[dom]
         line = {
-            "metric": METRIC, "value": tokens / t_max, "unit": "tokens/s", "n_gpus": max(world, 1),
+            "metric": METRIC, "value": aggregate_rate(tokens, world, t_max), "unit": "tokens/s",
+            "n_gpus": max(world, 1),
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t_max / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded N(0,1) bf16, random page permutation)", "config": cfg,
@@ -333,7 +349,7 @@ def main():
             "step_roofline": {"bytes": ib + mb, "achieved_gbs": (ib + mb) / (t_max / args.steps) / 1e9,
                               "frac": (ib + mb) / (t_max / args.steps) / 1e9 / hbm},
             "kernels": kernels,
-            "e2e": {"value": tokens / e2e_max, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "e2e": {"value": aggregate_rate(tokens, world, e2e_max), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk,
