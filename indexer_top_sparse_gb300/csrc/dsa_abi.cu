@@ -55,17 +55,28 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// 2D bf16 tensor [rows, 128] with 64x64 boxes and the 128-byte swizzle.
-bool encode_rows128_bf16(CUtensorMap *m, const void *base, uint64_t rows) {
+// 2D bf16 tensor [rows, cols] (row-major, dense) with box_rows x 64-column
+// boxes and the 128-byte swizzle.
+bool encode_2d_bf16(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, uint32_t box_rows) {
     auto fn = encode_fn();
-    if (!fn || rows == 0 || rows > (1ull << 31)) return false;
-    cuuint64_t dims[2] = {128, rows};
-    cuuint64_t strides[1] = {256};
-    cuuint32_t box[2] = {64, 64};
+    if (!fn || rows == 0 || rows > (1ull << 31) || box_rows == 0 || box_rows > 256) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 2};
+    cuuint32_t box[2] = {64, box_rows};
     cuuint32_t estr[2] = {1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_rows128_bf16(CUtensorMap *m, const void *base, uint64_t rows) {
+    return encode_2d_bf16(m, base, 128, rows, 64);
+}
+
+int mla_heads_per_cta(int H) {
+    if (H == 16 || H == 32 || H == 64) return H;
+    if (H % 64 == 0) return 64;
+    return 0;
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -113,12 +124,17 @@ bool plan_indexer(int B, int T, int max_len, IdxPlan *p) {
     return false;
 }
 
+int mla_groups(int H) {
+    const int nh = mla_heads_per_cta(H);
+    return nh ? H / nh : 1;
+}
+
 int mla_splits(int T, int H, int K) {
     int forced = g_mla_splits.load();
     const int tile = dsa::mla_key_tile();
     const int max_splits = std::max(1, std::min(16, ceil_div(std::max(K, 1), tile)));
     if (forced > 0) return std::min(forced, max_splits);
-    const long long pairs = (long long)T * ceil_div(H, 64);
+    const long long pairs = (long long)T * mla_groups(H);
     const int nsm = sm_count();
     if (pairs >= nsm) return 1;
     return std::max(1, std::min<int>(max_splits, (int)(nsm / pairs)));
@@ -149,7 +165,7 @@ dsa_status index_common(const void *q_idx, const uint8_t *q_idx_scale, const flo
     const long long max_len = (long long)max_pages_per_seq * page_size;
     if (max_len > (1LL << 30) || (long long)num_pages * page_size > (1LL << 31)) return DSA_ERR_UNSUPPORTED;
     IdxPlan plan;
-    if (!plan_indexer(B, T, (int)max_len, &plan)) return DSA_ERR_UNSUPPORTED;
+    if (!plan_indexer(B, T, (int)max_len, &plan) || plan.groups > 65535) return DSA_ERR_UNSUPPORTED;
     CUtensorMap tk, tq;
     if (!encode_rows128_bf16(&tk, k_idx_cache, (uint64_t)num_pages * page_size)) return DSA_ERR_CUDA;
     if (!encode_rows128_bf16(&tq, q_idx, (uint64_t)T * 64)) return DSA_ERR_CUDA;
@@ -216,8 +232,7 @@ size_t dsa_sparse_mla_workspace_size(int32_t T, int32_t H, int32_t K) {
     if (T <= 0 || H <= 0 || K <= 0) return kErrBytes;
     const int splits = mla_splits(T, H, K);
     if (splits <= 1) return kErrBytes;
-    const size_t groups = (size_t)ceil_div(H, 64);
-    const size_t rows = (size_t)T * groups * splits * 64;
+    const size_t rows = (size_t)T * mla_groups(H) * splits * 64;
     return kErrBytes + rows * 512 * sizeof(float) + rows * 2 * sizeof(float);
 }
 
@@ -271,7 +286,7 @@ dsa_status dsa_topk_from_scores(const float *scores, int64_t ld, const int32_t *
     if (!scores || !lens || !out || !workspace || R < 0 || K < 1 || ld < 1 || workspace_bytes < kErrBytes)
         return DSA_ERR_INVALID_ARG;
     if (R == 0) return DSA_OK;
-    if (ld > (1LL << 30)) return DSA_ERR_UNSUPPORTED;
+    if (ld > (1LL << 30) || R > 65535) return DSA_ERR_UNSUPPORTED;
     const size_t smax = max_smem_optin();
     int forced = g_topk_cluster.load();
     for (int C = 1; C <= 16; C <<= 1) {
@@ -293,13 +308,15 @@ dsa_status dsa_sparse_mla(const void *q, const void *kv_cache, const void *kv_ro
                           void *out, float *lse, void *workspace, size_t workspace_bytes, void *stream) {
     (void)kv_rope;
     (void)kv_scale;
-    if (T < 0 || B < 1 || K < 1 || H < 16 || H > 128 || H % 16 != 0 || page_size < 1 || num_pages < 1 ||
-        max_pages_per_seq < 1)
+    if (T < 0 || B < 1 || K < 1 || H < 1 || page_size < 1 || num_pages < 1 || max_pages_per_seq < 1)
         return DSA_ERR_INVALID_ARG;
     if (!q || !kv_cache || !page_table || !seq_lens || !cu_q || !indices || !out || !workspace)
         return DSA_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(kv_cache) || !aligned16(out) || !aligned16(workspace))
         return DSA_ERR_INVALID_ARG;
+    const int NH = mla_heads_per_cta(H);
+    if (NH == 0 || H > 1024 || T > 65535) return DSA_ERR_UNSUPPORTED;
+    if ((long long)num_pages * page_size > (1LL << 31)) return DSA_ERR_UNSUPPORTED;
     if (dtype != DSA_KV_BF16) return DSA_ERR_UNSUPPORTED;
     if (workspace_bytes < dsa_sparse_mla_workspace_size(T, H, K)) return DSA_ERR_INVALID_ARG;
     if (T == 0) return DSA_OK;
@@ -315,8 +332,7 @@ dsa_status dsa_sparse_mla(const void *q, const void *kv_cache, const void *kv_ro
     a.out = static_cast<uint16_t *>(out);
     a.lse = lse;
     a.err = reinterpret_cast<uint32_t *>(workspace);
-    const size_t groups = (size_t)ceil_div(H, 64);
-    const size_t rows = (size_t)T * groups * splits * 64;
+    const size_t rows = (size_t)T * mla_groups(H) * splits * 64;
     a.part_o = splits > 1 ? reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + kErrBytes) : nullptr;
     a.part_ml = splits > 1 ? a.part_o + rows * 512 : nullptr;
     a.num_pages = num_pages;
@@ -330,7 +346,10 @@ dsa_status dsa_sparse_mla(const void *q, const void *kv_cache, const void *kv_ro
     a.keys_per_split = ceil_div(ceil_div(K, splits), tile) * tile;
     a.scale = scale;
     a.scale_log2 = scale * 1.4426950408889634f;
-    return cuda_status(dsa::launch_sparse_mla_bf16(a, static_cast<cudaStream_t>(stream)));
+    CUtensorMap tkv, tq;
+    if (!encode_2d_bf16(&tkv, kv_cache, 576, (uint64_t)num_pages * page_size, 1)) return DSA_ERR_CUDA;
+    if (!encode_2d_bf16(&tq, q, 576, (uint64_t)T * H, (uint32_t)NH)) return DSA_ERR_CUDA;
+    return cuda_status(dsa::launch_sparse_mla_bf16(tkv, tq, a, NH, static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

@@ -63,8 +63,12 @@ struct MlaArgs {
     float scale;                // softmax scale
 };
 
-size_t mla_smem_bytes();
+size_t mla_smem_bytes(int NH);
 int mla_key_tile();
-cudaError_t launch_sparse_mla_bf16(const MlaArgs &a, cudaStream_t st);
+// NH = heads per CTA (16, 32 or 64; H must be a multiple).  tm_kv: 2D map of
+// the latent cache [rows, 576] bf16, box 64 x 1 (gather4), 128-byte swizzle;
+// tm_q: 2D map of q [T*H, 576] bf16, box 64 x NH, 128-byte swizzle.
+cudaError_t launch_sparse_mla_bf16(const CUtensorMap &tm_kv, const CUtensorMap &tm_q, const MlaArgs &a, int NH,
+                                   cudaStream_t st);
 
 }  // namespace dsa

@@ -8,16 +8,27 @@
 // over the valid selected positions idx_i of row t only; the other cache rows
 // are never read.
 //
-// Design: CTA = (64-head group, key split, query row).  A producer warp
-// gathers the selected 576-wide bf16 rows (1152 B each, one bulk copy per row)
-// through the page table into a 4-deep ring of 32-row tiles, padded to a
-// 1168-byte row pitch so that ldmatrix is bank-conflict free.  Eight compute
-// warps: warp w owns heads 16*(w%4).. and value dims 256*(w/4)..; each
-// computes its 16x32 logit tile with mma.sync m16n8k16 (bf16 in, fp32 acc),
-// runs the online softmax in registers (exp2 with log2(e) folded into the
-// scale) and accumulates P*V for its 256 value dims.  With several key splits
-// per row, partial (O, max, sum) go to the workspace and a combine kernel
-// merges them.
+// Design (tcgen05, accumulators in TMEM).  CTA = (group of NH <= 64 heads,
+// key split, query row); heads are the MMA's N dimension so that the output
+// accumulator O^T [512 dims x NH heads] takes 4*NH TMEM columns and the logit
+// tile S^T [128 keys x NH heads] another NH.
+//   warp 0      gather producer: per tile of 128 selected keys, TMA
+//               tile::gather4 copies the 576-wide bf16 rows (resolved through
+//               the page table) into nine 64-column regions with the 128-byte
+//               swizzle; a region is refilled as soon as the MMAs of the
+//               previous tile are done with it.
+//   warp 1      tcgen05 issuer: S^T = K_tile * Q^T (K-major operands, 36 steps
+//               of K=16), then after the softmax O^T += V^T * P^T with V^T read
+//               MN-major from the same smem tile (4 chunks of 128 dims, 8 steps
+//               of 16 keys) and P^T K-major.
+//   warps 2-9   softmax: thread = key (TMEM lane), each warp half of the heads;
+//               per-head max and sum over the 128 keys by a warp transpose
+//               reduction plus a 4-way shared-memory combine; exp2 with log2(e)
+//               folded into the scale; the reference max moves only when a
+//               head's max grows by more than 2^8 (then O^T is rescaled in
+//               TMEM); P (bf16) is written over the tile's consumed rope region.
+// With several key splits per row, partial (O, max, sum) go to the workspace
+// and mla_combine_kernel merges them.
 #include <cuda_bf16.h>
 #include <math_constants.h>
 
@@ -28,45 +39,44 @@ namespace dsa {
 
 namespace {
 
-constexpr int kD = 576;
 constexpr int kDv = 512;
-constexpr int kRowBytes = kD * 2;            // 1152
-constexpr int kPitch = kRowBytes + 16;       // 1168: 4-bank shift per row
-constexpr int kHG = 64;                      // heads per CTA
-constexpr int kNT = 32;                      // keys per tile
-constexpr int kStages = 4;
-constexpr int kComputeWarps = 8;
-constexpr int kThreads = (kComputeWarps + 1) * 32;
-constexpr int kQBytes = kHG * kPitch;
-constexpr int kStageBytes = kNT * kPitch;
+constexpr int kHG = 64;                      // head-slot stride of the partial layout
+constexpr int kKeys = 128;                   // keys per tile (MMA M of S^T)
+constexpr int kRegions = 9;                  // 64-dim regions of a 576-wide row
+constexpr int kRegionBytes = kKeys * 128;    // 16 KB
+constexpr int kTileBytes = kRegions * kRegionBytes;
+constexpr int kThreads = 320;
+constexpr int kSmThreads = 256;              // softmax warps 2..9
+constexpr int kBarSm = 1;                    // named barrier of the softmax warps
 
-struct __align__(16) MlaBars {
-    uint64_t full[kStages];
-    uint64_t empty[kStages];
-    uint64_t qbar;
-    int abort;
-    int pad;
-    uint8_t valid[kStages][kNT];
+template <int NH>
+struct MlaLayout {
+    static constexpr int kQRegion = NH * 128;
+    static constexpr int kQBytes = kRegions * kQRegion;
+    static constexpr int kKVOff = kQBytes;
+    static constexpr int kPOff = kKVOff + 8 * kRegionBytes;  // the rope region doubles as P
+    static constexpr int kPHalf = NH * 128;                    // P^T rows for 64 keys
+    static constexpr int kMiscOff = kKVOff + kTileBytes;
+    static constexpr int kTmemCols = 5 * NH <= 128 ? 128 : (5 * NH <= 256 ? 256 : 512);
+    static_assert(kQBytes % 1024 == 0, "regions must stay 1024-byte aligned");
 };
 
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(addr));
-}
-__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                         uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
+struct __align__(16) MlaBars {
+    uint64_t reg_full[kRegions];
+    uint64_t reg_empty[kRegions];
+    uint64_t s_full, p_full, o_full, q_full, drain;
+    uint32_t tmem_slot;
+    int abort;
+};
+
+struct __align__(16) MlaStats {
+    float red[4][kHG];
+    float red2[4][kHG];
+    float m_ref[kHG];
+    float l_run[kHG];
+    float alpha[kHG];
+};
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&v);
@@ -82,233 +92,350 @@ __device__ __forceinline__ int find_seq(const int32_t *cu_q, int B, int t) {
     return lo;
 }
 
-__global__ void __launch_bounds__(kThreads, 1) sparse_mla_bf16_kernel(MlaArgs a) {
+template <int N>
+struct Log2 {
+    static constexpr int v = N <= 1 ? 0 : 1 + Log2<N / 2>::v;
+};
+template <>
+struct Log2<1> {
+    static constexpr int v = 0;
+};
+
+// Reduce N per-head values over the 32 lanes of a warp.  Halving exchanges
+// leave each lane with one head; the remaining offsets finish the reduction.
+// Returns the reduced value; *head receives which of the N heads it is.
+template <int N, bool kMax>
+__device__ __forceinline__ float warp_reduce_heads(float (&v)[N], int lane, int *head) {
+    constexpr int L = Log2<N>::v;
+    int h = 0;
+#pragma unroll
+    for (int s = 0; s < L; ++s) {
+        const int o = 16 >> s;
+        const int half = N >> (s + 1);
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < half; ++i) {
+            const float keep = up ? v[i + half] : v[i];
+            const float send = up ? v[i] : v[i + half];
+            const float recv = __shfl_xor_sync(0xffffffffu, send, o);
+            v[i] = kMax ? fmaxf(keep, recv) : keep + recv;
+        }
+        h += up ? half : 0;
+    }
+#pragma unroll
+    for (int o = 16 >> L; o >= 1; o >>= 1) {
+        const float r = __shfl_xor_sync(0xffffffffu, v[0], o);
+        v[0] = kMax ? fmaxf(v[0], r) : v[0] + r;
+    }
+    *head = h;
+    return v[0];
+}
+
+template <int NH>
+__global__ void __launch_bounds__(kThreads, 1)
+    sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_q,
+                         MlaArgs a) {
+    using L = MlaLayout<NH>;
+    constexpr int HW = NH / 2;  // heads per softmax warp
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sQ = smem;
-    uint8_t *sKV = sQ + kQBytes;
-    MlaBars *bars = reinterpret_cast<MlaBars *>(sKV + kStages * kStageBytes);
+    uint8_t *sKV = smem + L::kKVOff;
+    uint8_t *sP = smem + L::kPOff;
+    MlaBars *bars = reinterpret_cast<MlaBars *>(smem + L::kMiscOff);
+    MlaStats *st = reinterpret_cast<MlaStats *>(bars + 1);
 
     const int hg = blockIdx.x, split = blockIdx.y, t = blockIdx.z;
-    const int heads_here = min(kHG, a.H - hg * kHG);  // multiple of 16
-    const int n_hb = heads_here / 16;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int k_begin = split * a.keys_per_split;
     const int k_end = min(a.K, k_begin + a.keys_per_split);
-    const int n_tiles = k_end > k_begin ? (k_end - k_begin + kNT - 1) / kNT : 0;
-    const int active_warps = 2 * n_hb;
+    const int n_tiles = k_end > k_begin ? (k_end - k_begin + kKeys - 1) / kKeys : 0;
+    const int b = find_seq(a.cu_q, a.B, t);
+    const int pos = __ldg(a.seq_lens + b) - (__ldg(a.cu_q + b + 1) - __ldg(a.cu_q + b)) + (t - __ldg(a.cu_q + b));
+    const int32_t *idx_row = a.indices + (size_t)t * a.K;
 
-    // zero the ring once so that rows never loaded read as finite zeros
-    for (int i = threadIdx.x; i < kStages * kStageBytes / 16; i += kThreads)
-        reinterpret_cast<uint4 *>(sKV)[i] = make_uint4(0, 0, 0, 0);
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(&bars->full[s], 1);
-            mbar_init(&bars->empty[s], active_warps);
+        for (int r = 0; r < kRegions; ++r) {
+            mbar_init(&bars->reg_full[r], 1);
+            mbar_init(&bars->reg_empty[r], 1);
         }
-        mbar_init(&bars->qbar, 1);
+        mbar_init(&bars->s_full, 1);
+        mbar_init(&bars->p_full, kSmThreads / 32);
+        mbar_init(&bars->o_full, 1);
+        mbar_init(&bars->q_full, 1);
+        mbar_init(&bars->drain, 1);
         bars->abort = 0;
         fence_mbar_init();
     }
-    fence_proxy_async_smem();
+    if (threadIdx.x < NH) {
+        st->m_ref[threadIdx.x] = -CUDART_INF_F;
+        st->l_run[threadIdx.x] = 0.0f;
+    }
+    if (warp == 1) tmem_alloc(&bars->tmem_slot, L::kTmemCols);
+    tc_fence_before();
     __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_o = bars->tmem_slot;          // O^T: columns [0, 4*NH)
+    const uint32_t tmem_s = tmem_o + 4 * NH;          // S^T: columns [4*NH, 5*NH)
     volatile int *abort = &bars->abort;
 
-    if (warp == kComputeWarps) {
-        // ---------------- gather producer (whole warp; lane = key slot)
-        const int b = find_seq(a.cu_q, a.B, t);
-        const int nq = __ldg(a.cu_q + b + 1) - __ldg(a.cu_q + b);
-        const int pos = __ldg(a.seq_lens + b) - nq + (t - __ldg(a.cu_q + b));
+    if (warp == 0) {
+        // ---------------------------------------------------------------- gather producer
         const int32_t *pt_row = a.page_table + (size_t)b * a.max_pages;
-        const int32_t *idx_row = a.indices + (size_t)t * a.K;
-        const uint8_t *qsrc = reinterpret_cast<const uint8_t *>(a.q + ((size_t)t * a.H + hg * kHG) * kD);
-        if (lane == 0) mbar_arrive_expect_tx(&bars->qbar, (uint32_t)(heads_here * kRowBytes));
-        __syncwarp();
-        for (int h = lane; h < heads_here; h += 32)
-            bulk_load(sQ + h * kPitch, qsrc + (size_t)h * kRowBytes, kRowBytes, &bars->qbar);
-        int issued = 0;
+        if (lane == 0) {
+            tma_prefetch_desc(&tm_kv);
+            tma_prefetch_desc(&tm_q);
+            mbar_arrive_expect_tx(&bars->q_full, (uint32_t)(kRegions * L::kQRegion));
+            for (int r = 0; r < kRegions; ++r)
+                tma_load_2d(sQ + r * L::kQRegion, &tm_q, &bars->q_full, 64 * r, t * a.H + hg * NH);
+        }
+        int last_tile = -1, last_regions = 0;
         for (int i = 0; i < n_tiles; ++i) {
-            const int s = i % kStages;
-            bool ok = true;
-            if (i >= kStages) ok = mbar_wait(&bars->empty[s], ((i / kStages) & 1) ^ 1, a.err, 0x401, abort);
-            if (!__all_sync(0xffffffffu, ok)) break;
-            const int slot = k_begin + i * kNT + lane;
-            long long row = -1;
-            if (slot < k_end) {
-                const int idx = __ldg(idx_row + slot);
-                if (idx >= 0) {
+            int rows[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                rows[j] = 0;  // invalid slots read row 0 and are masked by the softmax
+                const int slot = k_begin + i * kKeys + 4 * lane + j;
+                if (slot < k_end) {
+                    const int idx = __ldg(idx_row + slot);
                     if (idx > pos) {
                         report_error(a.err, kErrBadIndex);
-                    } else {
+                    } else if (idx >= 0) {
                         const int page = __ldg(pt_row + idx / a.page_size);
                         if (page < 0 || (int64_t)page >= a.num_pages)
                             report_error(a.err, kErrBadPage);
                         else
-                            row = (long long)page * a.page_size + idx % a.page_size;
+                            rows[j] = page * a.page_size + idx % a.page_size;
                     }
                 }
             }
-            const bool v = row >= 0;
-            bars->valid[s][lane] = v ? 1 : 0;
-            const unsigned ball = __ballot_sync(0xffffffffu, v);
-            __syncwarp();
-            if (lane == 0) mbar_arrive_expect_tx(&bars->full[s], (uint32_t)(__popc(ball) * kRowBytes));
-            __syncwarp();
-            if (v) bulk_load(sKV + s * kStageBytes + lane * kPitch, a.kv + row * kRowBytes, kRowBytes, &bars->full[s]);
-            issued = i + 1;
+            bool stop = false;
+            for (int r = 0; r < kRegions; ++r) {
+                bool ok = true;
+                if (i > 0) ok = mbar_wait(&bars->reg_empty[r], (i - 1) & 1, a.err, 0x501, abort);
+                if (!__all_sync(0xffffffffu, ok)) {
+                    stop = true;
+                    break;
+                }
+                if (lane == 0) mbar_arrive_expect_tx(&bars->reg_full[r], (uint32_t)kRegionBytes);
+                __syncwarp();
+                tma_gather4(sKV + r * kRegionBytes + lane * 512, &tm_kv, &bars->reg_full[r], 64 * r, rows[0], rows[1],
+                            rows[2], rows[3]);
+                last_tile = i;
+                last_regions = r + 1;
+            }
+            if (stop) break;
         }
-        // keep the CTA alive until the copies it issued have landed, even if
-        // the compute warps stopped early
-        if (lane == 0) {
+        if (lane == 0 && *abort) {
+            // let the copies in flight land before shared memory is released
             volatile int no_abort = 0;
-            mbar_wait(&bars->qbar, 0, nullptr, 0, &no_abort);
-            for (int i = max(0, issued - kStages); i < issued; ++i)
-                mbar_wait(&bars->full[i % kStages], (i / kStages) & 1, nullptr, 0, &no_abort);
+            mbar_wait(&bars->q_full, 0, nullptr, 0, &no_abort);
+            for (int r = 0; r < last_regions; ++r)
+                mbar_wait(&bars->reg_full[r], last_tile & 1, nullptr, 0, &no_abort);
         }
-        return;
-    }
-    const int hb = warp & 3, dh = warp >> 2;
-    if (hb >= n_hb) return;
-
-    // ---------------- compute warps
-    const int g = lane >> 2, q4 = lane & 3;  // mma fragment coordinates
-    float o[32][4];
+    } else if (warp == 1) {
+        // ---------------------------------------------------------------- tcgen05 issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc_s = idesc_bf16_f32(kKeys, NH);
+            constexpr uint32_t idesc_o = idesc_bf16_f32_amn(128, NH);
+            const uint32_t q_base = smem_u32(sQ), kv_base = smem_u32(sKV), p_base = smem_u32(sP);
+            bool ok = mbar_wait(&bars->q_full, 0, a.err, 0x502, abort);
+            for (int i = 0; ok && i < n_tiles; ++i) {
+                // S^T[128 keys x NH] = K_tile[128 x 576] . Q[NH x 576]^T
+                for (int r = 0; r < kRegions && ok; ++r) {
+                    ok = mbar_wait(&bars->reg_full[r], i & 1, a.err, 0x503, abort);
+                    if (!ok) break;
+                    tc_fence_after();
 #pragma unroll
-    for (int n = 0; n < 32; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.0f;
-    float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F, l0 = 0.0f, l1 = 0.0f;
-
-    const bool qok = mbar_wait(&bars->qbar, 0, a.err, 0x402, abort);
-    const uint32_t q_addr = smem_u32(sQ) + (uint32_t)((hb * 16 + (lane & 15)) * kPitch + (lane >> 4) * 16);
-    for (int i = 0; qok && i < n_tiles; ++i) {
-        const int s = i % kStages;
-        const bool ok = mbar_wait(&bars->full[s], (i / kStages) & 1, a.err, 0x403, abort);
-        if (!__all_sync(0xffffffffu, ok)) break;
-        const uint32_t kv_base = smem_u32(sKV + s * kStageBytes);
-
-        // S[16 heads x 32 keys] = Q_hb . K^T over 576 dims
-        float sacc[4][4];
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t ad = sdesc_kmajor_sw128(kv_base + r * kRegionBytes + kk * 32);
+                        const uint64_t bd = sdesc_kmajor_sw128(q_base + r * L::kQRegion + kk * 32);
+                        mma_bf16_ss(tmem_s, ad, bd, idesc_s, (r | kk) ? 1u : 0u);
+                    }
+                }
+                if (!ok) break;
+                mma_commit(&bars->s_full);
+                ok = mbar_wait(&bars->p_full, i & 1, a.err, 0x504, abort);
+                if (!ok) break;
+                tc_fence_after();
+                // O^T[512 x NH] += V^T[512 x 128 keys] . P^T[NH x 128 keys]^T, by 128-dim chunks
+                for (int c = 0; c < 4; ++c) {
 #pragma unroll
-        for (int n = 0; n < 4; ++n) sacc[n][0] = sacc[n][1] = sacc[n][2] = sacc[n][3] = 0.0f;
-        // B (keys) addressing: lane -> key (lane/16)*8 + lane%8, dim offset ((lane/8)%2)*8
-        const uint32_t kb_addr = kv_base + (uint32_t)(((lane >> 4) * 8 + (lane & 7)) * kPitch + ((lane >> 3) & 1) * 16);
-#pragma unroll 4
-        for (int ks = 0; ks < kD / 16; ++ks) {
-            uint32_t a0, a1, a2, a3;
-            ldsm_x4(q_addr + ks * 32, a0, a1, a2, a3);
-            uint32_t b0, b1, b2, b3, b4, b5, b6, b7;
-            ldsm_x4(kb_addr + ks * 32, b0, b1, b2, b3);                 // keys 0-15
-            ldsm_x4(kb_addr + 16 * kPitch + ks * 32, b4, b5, b6, b7);   // keys 16-31
-            mma16816(sacc[0], a0, a1, a2, a3, b0, b1);
-            mma16816(sacc[1], a0, a1, a2, a3, b2, b3);
-            mma16816(sacc[2], a0, a1, a2, a3, b4, b5);
-            mma16816(sacc[3], a0, a1, a2, a3, b6, b7);
-        }
-        // mask invalid slots, scale into the log2 domain, online softmax
-        float tmax0 = -CUDART_INF_F, tmax1 = -CUDART_INF_F;
-#pragma unroll
-        for (int n = 0; n < 4; ++n) {
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                const int key = n * 8 + q4 * 2 + c;
-                const bool v = bars->valid[s][key] != 0;
-                sacc[n][c] = v ? sacc[n][c] * a.scale_log2 : -CUDART_INF_F;
-                sacc[n][2 + c] = v ? sacc[n][2 + c] * a.scale_log2 : -CUDART_INF_F;
-                tmax0 = fmaxf(tmax0, sacc[n][c]);
-                tmax1 = fmaxf(tmax1, sacc[n][2 + c]);
+                    for (int j = 0; j < 8; ++j) {
+                        const uint64_t ad =
+                            sdesc_mnmajor_sw128(kv_base + 2 * c * kRegionBytes + j * 2048, kRegionBytes, 1024);
+                        const uint64_t bd = sdesc_kmajor_sw128(p_base + (j >> 2) * L::kPHalf + (j & 3) * 32);
+                        mma_bf16_ss(tmem_o + c * NH, ad, bd, idesc_o, (i > 0 || j > 0) ? 1u : 0u);
+                    }
+                    mma_commit(&bars->reg_empty[2 * c]);
+                    mma_commit(&bars->reg_empty[2 * c + 1]);
+                }
+                mma_commit(&bars->reg_empty[8]);
             }
-        }
-        tmax0 = fmaxf(tmax0, __shfl_xor_sync(0xffffffffu, tmax0, 1));
-        tmax0 = fmaxf(tmax0, __shfl_xor_sync(0xffffffffu, tmax0, 2));
-        tmax1 = fmaxf(tmax1, __shfl_xor_sync(0xffffffffu, tmax1, 1));
-        tmax1 = fmaxf(tmax1, __shfl_xor_sync(0xffffffffu, tmax1, 2));
-        const float mn0 = fmaxf(m0, tmax0), mn1 = fmaxf(m1, tmax1);
-        const float ref0 = mn0 == -CUDART_INF_F ? 0.0f : mn0;
-        const float ref1 = mn1 == -CUDART_INF_F ? 0.0f : mn1;
-        const float al0 = exp2f(m0 - ref0), al1 = exp2f(m1 - ref1);
-        m0 = mn0;
-        m1 = mn1;
-        float ps0 = 0.0f, ps1 = 0.0f;
-        uint32_t pa[2][4];
-#pragma unroll
-        for (int n = 0; n < 4; ++n) {
-            const float p0 = exp2f(sacc[n][0] - ref0), p1 = exp2f(sacc[n][1] - ref0);
-            const float p2 = exp2f(sacc[n][2] - ref1), p3 = exp2f(sacc[n][3] - ref1);
-            ps0 += p0 + p1;
-            ps1 += p2 + p3;
-            // A fragment of P for k-step n/2: regs {r0 lo-k, r1 lo-k, r0 hi-k, r1 hi-k}
-            pa[n >> 1][(n & 1) * 2 + 0] = pack_bf16(p0, p1);
-            pa[n >> 1][(n & 1) * 2 + 1] = pack_bf16(p2, p3);
-        }
-        l0 = l0 * al0 + ps0;
-        l1 = l1 * al1 + ps1;
-#pragma unroll
-        for (int n = 0; n < 32; ++n) {
-            o[n][0] *= al0;
-            o[n][1] *= al0;
-            o[n][2] *= al1;
-            o[n][3] *= al1;
-        }
-        // O[16 x 256] += P[16 x 32] . V[32 x 256]
-#pragma unroll
-        for (int kk = 0; kk < 2; ++kk) {
-            // V (trans) addressing: lane -> key kk*16 + (lane%8) + ((lane/8)%2)*8, dims +(lane/16)*8
-            const uint32_t v_addr = kv_base +
-                                    (uint32_t)((kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8) * kPitch +
-                                               (dh * 256 + (lane >> 4) * 8) * 2);
-#pragma unroll
-            for (int np = 0; np < 16; ++np) {
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4_t(v_addr + np * 32, b0, b1, b2, b3);
-                mma16816(o[2 * np], pa[kk][0], pa[kk][1], pa[kk][2], pa[kk][3], b0, b1);
-                mma16816(o[2 * np + 1], pa[kk][0], pa[kk][1], pa[kk][2], pa[kk][3], b2, b3);
+            if (ok && n_tiles > 0) mma_commit(&bars->o_full);
+            if (*abort) {
+                volatile int no_abort = 0;
+                mma_commit(&bars->drain);
+                mbar_wait(&bars->drain, 0, nullptr, 0, &no_abort);
             }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->empty[s]);
-    }
-    // full row sums
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-
-    const int h0 = hg * kHG + hb * 16 + g, h1 = h0 + 8;
-    if (a.splits == 1) {
-        const float inv0 = l0 > 0.0f ? 1.0f / l0 : 0.0f, inv1 = l1 > 0.0f ? 1.0f / l1 : 0.0f;
-        uint32_t *out0 = reinterpret_cast<uint32_t *>(a.out + ((size_t)t * a.H + h0) * kDv + dh * 256);
-        uint32_t *out1 = reinterpret_cast<uint32_t *>(a.out + ((size_t)t * a.H + h1) * kDv + dh * 256);
-#pragma unroll
-        for (int n = 0; n < 32; ++n) {
-            out0[n * 4 + q4] = pack_bf16(o[n][0] * inv0, o[n][1] * inv0);
-            out1[n * 4 + q4] = pack_bf16(o[n][2] * inv1, o[n][3] * inv1);
-        }
-        if (a.lse && dh == 0 && q4 == 0) {
-            a.lse[(size_t)t * a.H + h0] = l0 > 0.0f ? m0 * 0.69314718055994531f + logf(l0) : -CUDART_INF_F;
-            a.lse[(size_t)t * a.H + h1] = l1 > 0.0f ? m1 * 0.69314718055994531f + logf(l1) : -CUDART_INF_F;
         }
     } else {
-        const size_t base = (((size_t)t * gridDim.x + hg) * a.splits + split) * kHG;
-        float *p0 = a.part_o + (base + hb * 16 + g) * kDv + dh * 256;
-        float *p1 = p0 + 8 * kDv;
+        // ---------------------------------------------------------------- softmax warps
+        const int sw = warp - 2, quad = warp & 3, ch = sw >> 2;
+        const int key_local = quad * 32 + lane;
+        const int tid_s = sw * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+        bool ok = true;
+        for (int i = 0; i < n_tiles; ++i) {
+            const int slot = k_begin + i * kKeys + key_local;
+            bool valid = false;
+            if (slot < k_end) {
+                const int idx = __ldg(idx_row + slot);
+                valid = idx >= 0 && idx <= pos;
+            }
+            ok = mbar_wait(&bars->s_full, i & 1, a.err, 0x505, abort);
+            ok = bar_and(kBarSm, kSmThreads, ok);
+            if (!ok) break;
+            tc_fence_after();
+            uint32_t raw[HW];
+            tmem_ld<HW>(tmem_s + lane_off + ch * HW, raw);
+            tmem_wait_ld();
+            float x[HW], y[HW];
 #pragma unroll
-        for (int n = 0; n < 32; ++n) {
-            reinterpret_cast<float2 *>(p0)[n * 4 + q4] = make_float2(o[n][0], o[n][1]);
-            reinterpret_cast<float2 *>(p1)[n * 4 + q4] = make_float2(o[n][2], o[n][3]);
+            for (int j = 0; j < HW; ++j) {
+                x[j] = valid ? __uint_as_float(raw[j]) * a.scale_log2 : -CUDART_INF_F;
+                y[j] = x[j];
+            }
+            int hl;
+            const float wmax = warp_reduce_heads<HW, true>(y, lane, &hl);
+            st->red[quad][ch * HW + hl] = wmax;
+            bar_sync(kBarSm, kSmThreads);
+            if (tid_s < NH) {
+                const int h = tid_s;
+                const float mt = fmaxf(fmaxf(st->red[0][h], st->red[1][h]), fmaxf(st->red[2][h], st->red[3][h]));
+                const float mo = st->m_ref[h];
+                float al = 1.0f;
+                if (mt != -CUDART_INF_F && (mo == -CUDART_INF_F || mt > mo + 8.0f)) {
+                    al = mo == -CUDART_INF_F ? 1.0f : exp2f(mo - mt);
+                    st->m_ref[h] = mt;
+                }
+                st->alpha[h] = al;
+            }
+            bar_sync(kBarSm, kSmThreads);
+            float p[HW];
+            bool rescale = false;
+#pragma unroll
+            for (int j = 0; j < HW; ++j) {
+                const float m = st->m_ref[ch * HW + j];
+                p[j] = exp2f(x[j] - (m == -CUDART_INF_F ? 0.0f : m));
+                y[j] = p[j];
+                rescale |= st->alpha[ch * HW + j] != 1.0f;
+            }
+            const float wsum = warp_reduce_heads<HW, false>(y, lane, &hl);
+            st->red2[quad][ch * HW + hl] = wsum;
+            // P^T (bf16), K-major with the 128-byte swizzle: row = head, column = key
+            {
+                const int sub = key_local >> 6, col = key_local & 63;
+                uint8_t *pbase = sP + sub * L::kPHalf + (col & 7) * 2;
+                const int chunk = col >> 3;
+#pragma unroll
+                for (int j = 0; j < HW; ++j) {
+                    const int h = ch * HW + j;
+                    __nv_bfloat16 v = __float2bfloat16_rn(p[j]);
+                    *reinterpret_cast<__nv_bfloat16 *>(pbase + h * 128 + ((chunk ^ (h & 7)) << 4)) = v;
+                }
+            }
+            if (rescale) {
+                // the reference max moved: O^T columns of this warp's heads *= alpha
+                float al[HW];
+#pragma unroll
+                for (int j = 0; j < HW; ++j) al[j] = st->alpha[ch * HW + j];
+#pragma unroll 1
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t o[HW];
+                    const uint32_t ta = tmem_o + lane_off + c * NH + ch * HW;
+                    tmem_ld<HW>(ta, o);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < HW; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * al[j]);
+                    tmem_st<HW>(ta, o);
+                }
+                tmem_wait_st();
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            bar_sync(kBarSm, kSmThreads);
+            if (tid_s < NH) {
+                const int h = tid_s;
+                st->l_run[h] = st->l_run[h] * st->alpha[h] + (st->red2[0][h] + st->red2[1][h]) +
+                               (st->red2[2][h] + st->red2[3][h]);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->p_full);
         }
-        if (dh == 0 && q4 == 0) {
-            a.part_ml[(base + hb * 16 + g) * 2 + 0] = m0;
-            a.part_ml[(base + hb * 16 + g) * 2 + 1] = l0;
-            a.part_ml[(base + hb * 16 + g + 8) * 2 + 0] = m1;
-            a.part_ml[(base + hb * 16 + g + 8) * 2 + 1] = l1;
+
+        // ---------------------------------------------------------------- epilogue
+        if (ok && n_tiles > 0) ok = mbar_wait(&bars->o_full, 0, a.err, 0x506, abort);
+        ok = bar_and(kBarSm, kSmThreads, ok);
+        if (ok) {
+            tc_fence_after();
+            const int groups = gridDim.x;
+            const int h_base = hg * NH + ch * HW;
+            float inv[HW];
+#pragma unroll
+            for (int j = 0; j < HW; ++j) {
+                const float l = st->l_run[ch * HW + j];
+                inv[j] = (a.splits == 1 && l > 0.0f) ? 1.0f / l : (a.splits == 1 ? 0.0f : 1.0f);
+            }
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                uint32_t o[HW];
+                if (n_tiles > 0) {
+                    tmem_ld<HW>(tmem_o + lane_off + c * NH + ch * HW, o);
+                    tmem_wait_ld();
+                } else {
+#pragma unroll
+                    for (int j = 0; j < HW; ++j) o[j] = 0u;
+                }
+                const int d = c * 128 + quad * 32 + lane;
+                if (a.splits == 1) {
+#pragma unroll
+                    for (int j = 0; j < HW; ++j)
+                        a.out[((size_t)t * a.H + h_base + j) * kDv + d] =
+                            __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(o[j]) * inv[j]));
+                } else {
+                    const size_t slot0 = (((size_t)t * groups + hg) * a.splits + split) * kHG + ch * HW;
+#pragma unroll
+                    for (int j = 0; j < HW; ++j) a.part_o[(slot0 + j) * kDv + d] = __uint_as_float(o[j]);
+                }
+            }
+            if (tid_s < NH) {
+                const int h = tid_s;
+                const float l = st->l_run[h], m = st->m_ref[h];
+                if (a.splits == 1) {
+                    if (a.lse)
+                        a.lse[(size_t)t * a.H + hg * NH + h] =
+                            l > 0.0f ? m * 0.69314718055994531f + logf(l) : -CUDART_INF_F;
+                } else {
+                    const size_t slot0 = (((size_t)t * groups + hg) * a.splits + split) * kHG + h;
+                    a.part_ml[slot0 * 2 + 0] = l > 0.0f ? m : -CUDART_INF_F;
+                    a.part_ml[slot0 * 2 + 1] = l;
+                }
+            }
         }
     }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem_o, L::kTmemCols);
 }
 
 // Merge split partials: block = (head, head group, query row), 128 threads x 4 dims.
-__global__ void __launch_bounds__(128) mla_combine_kernel(MlaArgs a) {
+__global__ void __launch_bounds__(128) mla_combine_kernel(MlaArgs a, int NH) {
     const int hl = blockIdx.x, hg = blockIdx.y, t = blockIdx.z;
-    const int h = hg * kHG + hl;
-    if (h >= a.H) return;
+    if (hl >= NH) return;
+    const int h = hg * NH + hl;
     const size_t base = ((size_t)t * gridDim.y + hg) * a.splits;
     float M = -CUDART_INF_F;
     for (int s = 0; s < a.splits; ++s) M = fmaxf(M, a.part_ml[((base + s) * kHG + hl) * 2]);
@@ -336,19 +463,31 @@ __global__ void __launch_bounds__(128) mla_combine_kernel(MlaArgs a) {
 
 }  // namespace
 
-size_t mla_smem_bytes() { return 128 + kQBytes + (size_t)kStages * kStageBytes + sizeof(MlaBars); }
-int mla_key_tile() { return kNT; }
+size_t mla_smem_bytes(int NH) {
+    const size_t q = (size_t)kRegions * NH * 128;
+    return 1024 + q + kTileBytes + sizeof(MlaBars) + sizeof(MlaStats);
+}
+int mla_key_tile() { return kKeys; }
 
-cudaError_t launch_sparse_mla_bf16(const MlaArgs &a, cudaStream_t st) {
-    const size_t smem = mla_smem_bytes();
-    cudaError_t e = cudaFuncSetAttribute(sparse_mla_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
+template <int NH>
+static cudaError_t launch_tc(const CUtensorMap &tkv, const CUtensorMap &tq, const MlaArgs &a, cudaStream_t st) {
+    const size_t smem = mla_smem_bytes(NH);
+    auto kern = sparse_mla_tc_kernel<NH>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    const int groups = (a.H + kHG - 1) / kHG;
-    sparse_mla_bf16_kernel<<<dim3(groups, a.splits, a.T), kThreads, smem, st>>>(a);
-    e = cudaGetLastError();
+    kern<<<dim3(a.H / NH, a.splits, a.T), kThreads, smem, st>>>(tkv, tq, a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_sparse_mla_bf16(const CUtensorMap &tkv, const CUtensorMap &tq, const MlaArgs &a, int NH,
+                                   cudaStream_t st) {
+    cudaError_t e;
+    if (NH == 64) e = launch_tc<64>(tkv, tq, a, st);
+    else if (NH == 32) e = launch_tc<32>(tkv, tq, a, st);
+    else if (NH == 16) e = launch_tc<16>(tkv, tq, a, st);
+    else return cudaErrorInvalidValue;
     if (e != cudaSuccess || a.splits == 1) return e;
-    mla_combine_kernel<<<dim3(kHG, groups, a.T), 128, 0, st>>>(a);
+    mla_combine_kernel<<<dim3(kHG, a.H / NH, a.T), 128, 0, st>>>(a, NH);
     return cudaGetLastError();
 }
 

@@ -90,3 +90,35 @@ def test_prefill_rows(orc):
     rng = np.random.default_rng(7)
     wl = make_workload("mla_prefill", [400], [400], H=16, K=128, page_size=64, permute=False, seed=7, with_idx=False)
     _compare(orc, wl, _random_indices(rng, wl, 128), rows=[0, 1, 2, 127, 128, 129, 255, 399])
+
+
+def test_heads_32(orc):
+    rng = np.random.default_rng(32)
+    wl = make_workload("mla32", [2000, 300], [1, 1], H=32, K=700, page_size=64, seed=32, with_idx=False)
+    _compare(orc, wl, _random_indices(rng, wl, 700, pad_frac=0.05))
+
+
+@pytest.mark.parametrize("order", ["rising", "falling"])
+def test_reference_max_moves_across_tiles(orc, order):
+    # logits that grow (or shrink) strongly from one 128-key tile to the next,
+    # so that the running maximum moves by far more than 2^8 between tiles
+    from indexer_top_sparse_gb300.inputs import bf16_bits, bf16_to_f32
+    n, K = 1024, 1024
+    wl = make_workload("mla_rescale", [n], [1], H=64, K=K, page_size=64, permute=True, seed=41, with_idx=False)
+    kv = bf16_to_f32(wl.kv).reshape(-1, 576)
+    q = bf16_to_f32(wl.q).reshape(64, 576)
+    qdir = q[0] / np.linalg.norm(q[0])
+    for s in range(n):
+        row = wl.page_table[0][s // 64] * 64 + s % 64
+        tile = s // 128
+        f = (tile + 1) if order == "rising" else (8 - tile)
+        kv[row, :] = 0.3 * kv[row, :] + 2.0 * f * qdir
+    wl.kv = bf16_bits(kv.reshape(wl.kv.shape).astype(np.float32))
+    wl.scale = 1.0
+    idx = np.arange(K, dtype=np.int32)[None, :]
+    import indexer_top_sparse_gb300 as d
+    d.set_tuning("mla_splits", 1)
+    try:
+        _compare(orc, wl, idx)
+    finally:
+        d.set_tuning("mla_splits", 0)
