@@ -9,9 +9,11 @@
 #include <atomic>
 #include <cstdio>
 #include <cstring>
+#include <map>
 #include <mutex>
+#include <tuple>
 
-#include "../../include/dsa.h"
+#include "dsa.h"
 #include "kernels.h"
 
 namespace {
@@ -88,40 +90,70 @@ struct IdxPlan {
     size_t smem;
 };
 
+// Resident clusters for a shape, cached per (device, G, C, smem).
+int cached_max_clusters(int G, int C, size_t smem) {
+    static std::mutex mu;
+    static std::map<std::tuple<int, int, int, size_t>, int> cache;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const auto key = std::make_tuple(dev, G, C, smem);
+    {
+        std::lock_guard<std::mutex> g(mu);
+        auto it = cache.find(key);
+        if (it != cache.end()) return it->second;
+    }
+    const int n = dsa::indexer_max_active_clusters(G, C, smem);
+    std::lock_guard<std::mutex> g(mu);
+    cache[key] = n;
+    return n;
+}
+
+// Launch shape of the fused indexer: G query rows per cluster, C CTAs per
+// cluster, ring depth.  Preference: the fewest waves (clusters / resident
+// clusters), then the most CTAs in flight, then the deepest ring; a CTA keeps
+// at least 4 tiles of history unless the shape is forced.
 bool plan_indexer(int B, int T, int max_len, IdxPlan *p) {
-    const int nsm = sm_count();
     const size_t smax = max_smem_optin();
     const int tiles_max = std::max(1, ceil_div(max_len, 128));
-    int G_list[3] = {4, 2, 1};
-    int g_force = g_idx_group.load();
-    for (int gi = 0; gi < 3; ++gi) {
-        int G = G_list[gi];
-        if (g_force ? G != g_force : (T <= B ? G != 1 : false)) continue;
+    const int g_force = g_idx_group.load(), c_force = g_idx_cluster.load(), s_force = g_idx_stages.load();
+    bool found = false;
+    long long best_waves = 0, best_used = 0;
+    int best_stages = 0;
+    for (int G : {4, 2, 1}) {
+        if (g_force ? G != g_force : (T <= B && G != 1)) continue;
         const int groups = G == 1 ? T : ceil_div(T, G) + B;
-        int c_force = g_idx_cluster.load();
         for (int C = 1; C <= 16; C <<= 1) {
             if (c_force && C != c_force) continue;
             const int tiles_cap = ceil_div(tiles_max, C);
-            // enough CTAs to cover the GPU twice, unless the history is too
-            // short to split further
-            if (!c_force && C < 16 && (long long)C * groups < 2LL * nsm && tiles_cap > 4) continue;
-            int s_force = g_idx_stages.load();
+            if (!c_force && C > 1 && tiles_cap < 4) continue;
             for (int stages = 4; stages >= 2; --stages) {
                 if (s_force && stages != s_force) continue;
                 size_t smem = dsa::indexer_smem_bytes(G, stages, tiles_cap);
-                // TMEM: 2*64*G columns per CTA; keep CTAs/SM * columns <= 512
-                const int cols = 2 * 64 * G <= 128 ? 128 : 2 * 64 * G;
-                const int max_ctas = 512 / cols;
-                const size_t floor_smem = (228u * 1024u) / (size_t)(max_ctas + 1) + 1;
+                // TMEM: 2*64*G columns per CTA; cap the CTAs per SM through
+                // shared memory so that allocations never wait on each other
+                const int cols = std::max(128, 2 * 64 * G);
+                const size_t floor_smem = (228u * 1024u) / (size_t)(512 / cols + 1) + 1;
                 smem = std::max(smem, floor_smem);
-                if (smem <= smax) {
+                if (smem > smax) continue;
+                const int resident = cached_max_clusters(G, C, smem);
+                if (resident <= 0) continue;
+                const long long waves = (groups + resident - 1) / resident;
+                const long long used = (long long)std::min(groups, resident) * C;
+                const bool better = !found || waves < best_waves ||
+                                    (waves == best_waves && (used > best_used ||
+                                                             (used == best_used && stages > best_stages)));
+                if (better) {
                     *p = IdxPlan{G, C, stages, tiles_cap, groups, smem};
-                    return true;
+                    found = true;
+                    best_waves = waves;
+                    best_used = used;
+                    best_stages = stages;
                 }
             }
         }
+        if (found) break;  // prefer the largest query group that fits
     }
-    return false;
+    return found;
 }
 
 int mla_groups(int H) {
@@ -346,10 +378,9 @@ dsa_status dsa_sparse_mla(const void *q, const void *kv_cache, const void *kv_ro
     a.keys_per_split = ceil_div(ceil_div(K, splits), tile) * tile;
     a.scale = scale;
     a.scale_log2 = scale * 1.4426950408889634f;
-    CUtensorMap tkv, tq;
-    if (!encode_2d_bf16(&tkv, kv_cache, 576, (uint64_t)num_pages * page_size, 1)) return DSA_ERR_CUDA;
+    CUtensorMap tq;
     if (!encode_2d_bf16(&tq, q, 576, (uint64_t)T * H, (uint32_t)NH)) return DSA_ERR_CUDA;
-    return cuda_status(dsa::launch_sparse_mla_bf16(tkv, tq, a, NH, static_cast<cudaStream_t>(stream)));
+    return cuda_status(dsa::launch_sparse_mla_bf16(tq, a, NH, static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

@@ -45,6 +45,7 @@ constexpr int kTileBytes = kTileM * kDI * 2;         // 32 KB
 constexpr int kRegionBytes = kTileM * 128;           // one 64-column half of a tile: 16 KB
 constexpr int kThreads = 192;
 constexpr int kHist = 256;
+constexpr int kMaxCluster = 16;
 
 // Order-preserving map from a finite float to uint32 (larger float -> larger
 // key); -0 is folded onto +0.  Every finite value maps above 0x007FFFFF, so 0
@@ -92,7 +93,7 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int32_t *warp_tot, in
 // the rest of out[0..K).  Every CTA of the cluster must call this with the
 // same n_valid and K (it contains cluster barriers).
 __device__ void cluster_topk(const uint32_t *keys, int n_local, int pos0, int n_valid, int K, int32_t *out,
-                             SelectSmem &ss) {
+                             SelectSmem &ss, const uint32_t *hist0 = nullptr) {
     cg::cluster_group cluster = cg::this_cluster();
     const unsigned C = cluster.num_blocks();
     const unsigned my = cluster.block_rank();
@@ -116,16 +117,26 @@ __device__ void cluster_topk(const uint32_t *keys, int n_local, int pos0, int n_
     for (int pass = 0; pass < 4; ++pass) {
         const int shift = 24 - 8 * pass;
         uint32_t *h = ss.hist[pass & 1];
-        for (int d = tid; d < kHist; d += kThreads) h[d] = 0u;
-        __syncthreads();
-        for (int l = tid; l < n_local; l += kThreads) {
-            uint32_t k = keys[l];
-            if (k != 0u && (k & mask) == prefix) atomicAdd(&h[(k >> shift) & 0xFFu], 1u);
+        if (pass == 0 && hist0 != nullptr) {
+            // the top-digit histogram was built while the scores were produced
+            for (int d = tid; d < kHist; d += kThreads) h[d] = hist0[d];
+        } else {
+            for (int d = tid; d < kHist; d += kThreads) h[d] = 0u;
+            __syncthreads();
+            for (int l = tid; l < n_local; l += kThreads) {
+                uint32_t k = keys[l];
+                if (k != 0u && (k & mask) == prefix) atomicAdd(&h[(k >> shift) & 0xFFu], 1u);
+            }
         }
         cluster.sync();
         for (int d = tid; d < kHist; d += kThreads) {
+            // issue every remote load before summing (they are independent)
+            uint32_t v[kMaxCluster];
+#pragma unroll
+            for (int c = 0; c < kMaxCluster; ++c) v[c] = c < (int)C ? cluster.map_shared_rank(h, c)[d] : 0u;
             uint32_t s = 0;
-            for (unsigned c = 0; c < C; ++c) s += cluster.map_shared_rank(h, c)[d];
+#pragma unroll
+            for (int c = 0; c < kMaxCluster; ++c) s += v[c];
             ss.tot[d] = s;
         }
         __syncthreads();
@@ -187,12 +198,17 @@ __device__ void cluster_topk(const uint32_t *keys, int n_local, int pos0, int n_
     }
     cluster.sync();
     int eq_before_cta = 0, out_before_cta = 0;
-    for (unsigned c = 0; c < my; ++c) {
-        const int32_t *rc = cluster.map_shared_rank(ss.cnt, c);
-        int g = rc[0], e = rc[1];
-        int take = min(max(krem - eq_before_cta, 0), e);
-        out_before_cta += g + take;
-        eq_before_cta += e;
+    {
+        int2 rc[kMaxCluster];
+#pragma unroll
+        for (int c = 0; c < kMaxCluster; ++c)
+            rc[c] = c < (int)my ? *reinterpret_cast<const int2 *>(cluster.map_shared_rank(ss.cnt, c)) : make_int2(0, 0);
+#pragma unroll
+        for (int c = 0; c < kMaxCluster; ++c) {
+            const int take = min(max(krem - eq_before_cta, 0), rc[c].y);
+            out_before_cta += rc[c].x + take;
+            eq_before_cta += rc[c].y;
+        }
     }
     // per-segment selection counts, then their exclusive scan
     const int eq_rank0 = eq_before_cta + eq_before_seg;
@@ -256,7 +272,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *sK = sQ + L::kQBytes;
     uint32_t *sKeys = reinterpret_cast<uint32_t *>(sK + (size_t)a.stages * kTileBytes);
     float *sW = reinterpret_cast<float *>(sKeys + (size_t)G * key_cap);
-    SelectSmem *ss = reinterpret_cast<SelectSmem *>(sW + G * kHI);
+    uint32_t *sHist0 = reinterpret_cast<uint32_t *>(sW + G * kHI);  // [G][256] top-digit histograms
+    SelectSmem *ss = reinterpret_cast<SelectSmem *>(sHist0 + G * kHist);
     IdxBars *bars = reinterpret_cast<IdxBars *>(ss + 1);
     static_assert(sizeof(SelectSmem) % 16 == 0, "keep the barrier block 16-byte aligned");
 
@@ -323,6 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int gi = i / kHI;
         sW[i] = gi < gn ? __ldg(a.head_w + (size_t)(t0 + gi) * kHI + (i % kHI)) : 0.0f;
     }
+    for (int i = threadIdx.x; i < G * kHist; i += kThreads) sHist0[i] = 0u;
     if (warp == 1) tmem_alloc(&bars->tmem_slot, L::kTmemCols);
     tc_fence_before();
     __syncthreads();
@@ -432,7 +450,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int j = 0; j < 32; ++j) acc = fmaf(w[32 + j], fmaxf(__uint_as_float(r1[j]), 0.0f), acc);
                 const bool valid = gi < gn && pos <= pos_first + gi;
-                sKeys[(size_t)gi * key_cap + l] = valid ? score_key(acc) : 0u;
+                const uint32_t key = valid ? score_key(acc) : 0u;
+                sKeys[(size_t)gi * key_cap + l] = key;
+                if (valid) atomicAdd(&sHist0[gi * kHist + (key >> 24)], 1u);
                 if (kWriteScores && valid && pos < a.ld_scores) a.scores[(size_t)(t0 + gi) * a.ld_scores + pos] = acc;
             }
             tc_fence_before();
@@ -445,14 +465,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tmem, L::kTmemCols);
-    // If any CTA of the cluster gave up on a wait, the whole cluster skips
-    // selection (the decision must be uniform: selection has cluster barriers).
-    if (threadIdx.x == 0) ss->cnt[2] = bars->abort;
-    cluster.sync();
-    int any_abort = 0;
-    for (int c = 0; c < C; ++c) any_abort |= cluster.map_shared_rank(&ss->cnt[2], c)[0];
-    cluster.sync();
-    if (any_abort) return;
+    // A CTA that gave up on a wait (its keys are then incomplete; the error is
+    // recorded) still runs the selection: every CTA of the cluster must pass
+    // the same sequence of cluster barriers, which depends only on
+    // cluster-wide totals.
 
     // ---------------- selection, one query row at a time
     for (int gi = 0; gi < G; ++gi) {
@@ -462,7 +478,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const int n_valid = pos_first + gi + 1;
         int32_t *out = a.indices + (size_t)(t0 + gi) * a.K;
-        cluster_topk(sKeys + (size_t)gi * key_cap, n_tiles * kTileM, tile0 * kTileM, n_valid, a.K, out, *ss);
+        cluster_topk(sKeys + (size_t)gi * key_cap, n_tiles * kTileM, tile0 * kTileM, n_valid, a.K, out, *ss,
+                     sHist0 + gi * kHist);
     }
 }
 
@@ -496,7 +513,7 @@ size_t indexer_smem_bytes(int G, int stages, int tiles_cap) {
     size_t q = (size_t)G * kHI * kDI * 2;
     size_t k = (size_t)stages * kTileBytes;
     size_t keys = (size_t)G * tiles_cap * kTileM * 4;
-    size_t w = (size_t)G * kHI * 4;
+    size_t w = (size_t)G * kHI * 4 + (size_t)G * kHist * 4;
     return 1024 + q + k + keys + w + sizeof(SelectSmem) + sizeof(IdxBars);
 }
 
@@ -536,6 +553,38 @@ cudaError_t launch_indexer_bf16(const CUtensorMap &tk, const CUtensorMap &tq, co
     if (G == 4) return write_scores ? launch_idx<4, true>(tk, tq, a, C, groups, smem, st)
                                     : launch_idx<4, false>(tk, tq, a, C, groups, smem, st);
     return cudaErrorInvalidValue;
+}
+
+template <int G>
+static int max_clusters_g(int C, size_t smem) {
+    auto kern = indexer_topk_bf16_kernel<G, false>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return 0;
+    if (C > 8 && cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+        return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)C, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
+int indexer_max_active_clusters(int G, int C, size_t smem) {
+    if (G == 1) return max_clusters_g<1>(C, smem);
+    if (G == 2) return max_clusters_g<2>(C, smem);
+    if (G == 4) return max_clusters_g<4>(C, smem);
+    return 0;
 }
 
 cudaError_t launch_topk_from_scores(const TopkArgs &a, int C, size_t smem, cudaStream_t st) {

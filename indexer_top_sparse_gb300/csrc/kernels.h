@@ -40,6 +40,9 @@ size_t topk_smem_bytes(int chunk_cap);
 cudaError_t launch_indexer_bf16(const CUtensorMap &tm_k, const CUtensorMap &tm_q, const IndexerArgs &a, int G,
                                 int C, int groups, size_t smem, bool write_scores, cudaStream_t st);
 cudaError_t launch_topk_from_scores(const TopkArgs &a, int C, size_t smem, cudaStream_t st);
+// Clusters of C CTAs of the G-query indexer kernel with `smem` bytes that can
+// be resident at once (0 if the shape cannot launch).
+int indexer_max_active_clusters(int G, int C, size_t smem);
 
 // Sparse MLA (sparse_mla.cu).
 struct MlaArgs {
@@ -65,10 +68,8 @@ struct MlaArgs {
 
 size_t mla_smem_bytes(int NH);
 int mla_key_tile();
-// NH = heads per CTA (16, 32 or 64; H must be a multiple).  tm_kv: 2D map of
-// the latent cache [rows, 576] bf16, box 64 x 1 (gather4), 128-byte swizzle;
-// tm_q: 2D map of q [T*H, 576] bf16, box 64 x NH, 128-byte swizzle.
-cudaError_t launch_sparse_mla_bf16(const CUtensorMap &tm_kv, const CUtensorMap &tm_q, const MlaArgs &a, int NH,
-                                   cudaStream_t st);
+// NH = heads per CTA (16, 32 or 64; H must be a multiple).  tm_q: 2D map of
+// q [T*H, 576] bf16, box 64 x NH, 128-byte swizzle.
+cudaError_t launch_sparse_mla_bf16(const CUtensorMap &tm_q, const MlaArgs &a, int NH, cudaStream_t st);
 
 }  // namespace dsa
