@@ -9,23 +9,25 @@
 // are never read.
 //
 // Design (tcgen05, accumulators in TMEM).  CTA = (group of NH <= 64 heads,
-// key split, query row); selected keys are processed in tiles of 64, two tiles
-// in flight (double-buffered shared memory).
-//   warps 0-7   gather: 16-byte cp.async copies (coalesced 128-byte row
+// key split, query row); selected keys are processed in tiles of 32, four
+// tiles in flight (a ring of shared-memory buffers).
+//   warps 0-7   gather (tiles of 32 keys, 4 in flight): 16-byte cp.async copies (coalesced 128-byte row
 //               segments) place each selected 576-wide bf16 row, resolved
 //               through the page table, into nine 64-column regions in the
 //               128-byte-swizzle layout; thousands of requests in flight.
-//   warp 8      tcgen05 issuer: S[64 heads x 64 keys] = Q . K_tile^T (M = 64,
+//   warp 8      tcgen05 issuer: S[64 heads x 32 keys] = Q . K_tile^T (M = 64,
 //               K-major operands, 36 steps of K = 16; double-buffered in
 //               TMEM, the next tile's S is issued before this tile's P*V),
 //               then O^T[512 dims x NH] += V^T . P^T with V^T read MN-major
-//               from the same tile (4 chunks of 128 dims, 4 steps of 16 keys).
+//               from the same tile and P^T MN-major (4 chunks of 128 dims,
+//               2 steps of 16 keys).
 //   warps 9-12  softmax: thread = head (M = 64 places rows 16q..16q+15 in the
 //               low 16 lanes of warp quadrant q), so max, exp2 and sum over
 //               the tile's keys stay in registers; the reference max moves
 //               only when a head's max grows by more than 2^8, and then the
 //               O^T columns are rescaled in TMEM; P (bf16) is written over the
-//               tile's consumed rope region.  The same warps run the epilogue.
+//               tile's consumed rope region as [key][head] rows.  The same
+//               warps run the epilogue.
 // With several key splits per row, partial (O, max, sum) go to the workspace
 // and mla_combine_kernel merges them.
 #include <cuda_bf16.h>
@@ -41,9 +43,10 @@ namespace {
 constexpr int kD = 576;
 constexpr int kDv = 512;
 constexpr int kHG = 64;                      // head-slot stride of the partial layout
-constexpr int kKeys = 64;                    // keys per tile (MMA N of S)
+constexpr int kKeys = 32;                    // keys per tile (MMA N of S)
+constexpr int kStages = 4;                   // tiles in flight
 constexpr int kRegions = 9;                  // 64-dim regions of a 576-wide row
-constexpr int kRegionBytes = kKeys * 128;    // 8 KB
+constexpr int kRegionBytes = kKeys * 128;    // 4 KB
 constexpr int kTileBytes = kRegions * kRegionBytes;
 constexpr int kQRegion = 64 * 128;           // Q rows padded to the MMA's M = 64
 #ifndef MLA_PRODUCER_WARPS
@@ -55,17 +58,17 @@ constexpr int kSmWarp0 = kProd + 1;          // 4 softmax / epilogue warps
 constexpr int kThreads = (kProd + 1 + 4) * 32;
 constexpr int kSmThreads = 128;
 constexpr int kBarSm = 1;
-static_assert(kKeys % kProd == 0 && (kKeys / kProd) * 8 % 32 == 0, "gather work splits evenly");
+static_assert(kKeys % kProd == 0, "gather work splits evenly");
 
 template <int NH>
 struct MlaLayout {
     static constexpr int kKVOff = kRegions * kQRegion;
-    static constexpr int kMiscOff = kKVOff + 2 * kTileBytes;
-    static constexpr int kTmemCols = 512;    // O^T: 4*NH columns at 0; S buffers at 256 and 320
+    static constexpr int kMiscOff = kKVOff + kStages * kTileBytes;
+    static constexpr int kTmemCols = 512;    // O^T: 4 chunks x 64 columns at 0; S buffers at 256 + 32 j
 };
 
 struct __align__(16) MlaBars {
-    uint64_t kv_full[2], kv_empty[2], s_full[2];
+    uint64_t kv_full[kStages], kv_empty[kStages], s_full[2];
     uint64_t p_full, o_done, o_full, q_full, drain;
     uint32_t tmem_slot;
     int abort;
@@ -73,7 +76,7 @@ struct __align__(16) MlaBars {
 
 struct __align__(16) MlaStats {
     int32_t rows[kKeys];
-    uint8_t valid[2][kKeys];
+    uint32_t valid[kStages];  // bit k: key k of the tile in that buffer is valid
     float alpha[2][kHG];
     float m_fin[kHG];
     float l_fin[kHG];
@@ -110,20 +113,20 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 // Issue S = Q . K_tile^T for tile i into S buffer i&1 once the tile landed.
 __device__ __forceinline__ bool issue_s_tile(int i, MlaBars *bars, uint32_t kv_base, uint32_t q_base, uint32_t tmem_s,
                                              uint32_t idesc_s, uint32_t *err, volatile int *abort) {
-    const int buf = i & 1;
-    if (!mbar_wait(&bars->kv_full[buf], (i >> 1) & 1, err, 0x503, abort)) return false;
+    const int st = i % kStages;
+    if (!mbar_wait(&bars->kv_full[st], (i / kStages) & 1, err, 0x503, abort)) return false;
     fence_proxy_async_smem();  // the tile was written through the generic proxy
     tc_fence_after();
-    const uint32_t kb = kv_base + buf * kTileBytes;
+    const uint32_t kb = kv_base + st * kTileBytes;
     for (int r = 0; r < kRegions; ++r) {
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
             const uint64_t ad = sdesc_kmajor_sw128(q_base + r * kQRegion + kk * 32);
             const uint64_t bd = sdesc_kmajor_sw128(kb + r * kRegionBytes + kk * 32);
-            mma_bf16_ss(tmem_s + 64 * buf, ad, bd, idesc_s, (r | kk) ? 1u : 0u);
+            mma_bf16_ss(tmem_s + kKeys * (i & 1), ad, bd, idesc_s, (r | kk) ? 1u : 0u);
         }
     }
-    mma_commit(&bars->s_full[buf]);
+    mma_commit(&bars->s_full[i & 1]);
     return true;
 }
 
@@ -147,11 +150,11 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
     const int32_t *idx_row = a.indices + (size_t)t * a.K;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kStages; ++i) {
             mbar_init(&bars->kv_full[i], 32 * kProd);  // one cp.async completion arrival per gather lane
             mbar_init(&bars->kv_empty[i], 1);
-            mbar_init(&bars->s_full[i], 1);
         }
+        for (int i = 0; i < 2; ++i) mbar_init(&bars->s_full[i], 1);
         mbar_init(&bars->p_full, kSmThreads / 32);
         mbar_init(&bars->o_done, 1);
         mbar_init(&bars->o_full, 1);
@@ -160,6 +163,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
         bars->abort = 0;
         fence_mbar_init();
     }
+    if (threadIdx.x < kStages) st->valid[threadIdx.x] = 0u;
     if (NH < 64) {
         // Q rows NH..63 feed MMA rows nobody reads; keep them finite
         for (int i = threadIdx.x; i < kRegions * (64 - NH) * 8; i += kThreads) {
@@ -172,14 +176,15 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem_o = bars->tmem_slot;      // O^T: columns [0, 4*NH)
-    const uint32_t tmem_s = tmem_o + 256;         // S buffer j at columns 256 + 64 j
+    const uint32_t tmem_o = bars->tmem_slot;      // O^T chunk c: columns [64 c, 64 c + NH)
+    const uint32_t tmem_s = tmem_o + 256;         // S buffer j at columns 256 + kKeys j
     volatile int *abort = &bars->abort;
 
     if (warp < kProd) {
         // ---------------------------------------------------------------- gather
         const int32_t *pt_row = a.page_table + (size_t)b * a.max_pages;
         constexpr int kKPW = kKeys / kProd;  // keys per gather warp
+        static_assert(kKPW * 8 % 32 == 0 && kKPW <= 32, "a warp instruction covers four keys");
         const int key0 = warp * kKPW;
         if (warp == 0 && lane == 0) {
             tma_prefetch_desc(&tm_q);
@@ -188,15 +193,15 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
                 tma_load_2d(sQ + r * kQRegion, &tm_q, &bars->q_full, 64 * r, t * a.H + hg * NH);
         }
         for (int i = 0; i < n_tiles; ++i) {
-            const int buf = i & 1;
+            const int stg = i % kStages;
             bool ok = true;
-            if (i >= 2) ok = mbar_wait(&bars->kv_empty[buf], ((i >> 1) & 1) ^ 1, a.err, 0x501, abort);
+            if (i >= kStages) ok = mbar_wait(&bars->kv_empty[stg], ((i / kStages) & 1) ^ 1, a.err, 0x501, abort);
             if (!__all_sync(0xffffffffu, ok)) break;
+            bool v = false;
             if (lane < kKPW) {
                 const int key = key0 + lane;
                 const int slot = k_begin + i * kKeys + key;
                 int row = 0;  // invalid slots read row 0 and are masked by the softmax
-                bool v = false;
                 if (slot < k_end) {
                     const int idx = __ldg(idx_row + slot);
                     if (idx > pos) {
@@ -212,10 +217,11 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
                     }
                 }
                 st->rows[key] = row;
-                st->valid[buf][key] = v ? 1 : 0;
             }
+            const uint32_t vb = __ballot_sync(0xffffffffu, v) & ((1u << kKPW) - 1u);
+            if (lane == 0) atomicOr(&st->valid[stg], vb << key0);
             __syncwarp();
-            uint8_t *dst = sKV + buf * kTileBytes;
+            uint8_t *dst = sKV + stg * kTileBytes;
 #pragma unroll 3
             for (int r = 0; r < kRegions; ++r) {
 #pragma unroll
@@ -225,7 +231,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
                     cp_async16(dst + r * kRegionBytes + key * 128 + ((cc ^ (key & 7)) << 4), src);
                 }
             }
-            cp_async_arrive(&bars->kv_full[buf]);
+            cp_async_arrive(&bars->kv_full[stg]);
             __syncwarp();
         }
         cp_async_wait_all();  // the CTA stays alive until every copy has landed
@@ -237,7 +243,9 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
         // ---------------------------------------------------------------- tcgen05 issuer
         if (lane == 0) {
             constexpr uint32_t idesc_s = idesc_bf16_f32(64, kKeys);
-            constexpr uint32_t idesc_o = idesc_bf16_f32_amn(128, NH);
+            // P*V always runs with N = 64 (a full 64-element swizzle atom of the
+            // MN-major P^T); columns NH..63 are unused when NH < 64
+            constexpr uint32_t idesc_o = idesc_bf16_f32_amn(128, 64) | (1u << 16);  // A and B MN-major
             const uint32_t q_base = smem_u32(sQ), kv_base = smem_u32(sKV);
             bool ok = mbar_wait(&bars->q_full, 0, a.err, 0x502, abort);
             uint32_t *const err = a.err;
@@ -249,18 +257,18 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
                     break;
                 if (!(ok = mbar_wait(&bars->p_full, i & 1, a.err, 0x504, abort))) break;
                 tc_fence_after();
-                const int buf = i & 1;
-                const uint32_t kb = kv_base + buf * kTileBytes;
-                const uint32_t pb = kb + 8 * kRegionBytes;  // P^T over the consumed rope region
+                const int stg = i % kStages;
+                const uint32_t kb = kv_base + stg * kTileBytes;
+                const uint32_t pb = kb + 8 * kRegionBytes;  // P^T [keys][heads] over the consumed rope region
                 for (int c = 0; c < 4; ++c) {
 #pragma unroll
                     for (int j = 0; j < kKeys / 16; ++j) {
                         const uint64_t ad = sdesc_mnmajor_sw128(kb + 2 * c * kRegionBytes + j * 2048, kRegionBytes, 1024);
-                        const uint64_t bd = sdesc_kmajor_sw128(pb + j * 32);
-                        mma_bf16_ss(tmem_o + c * NH, ad, bd, idesc_o, (i > 0 || j > 0) ? 1u : 0u);
+                        const uint64_t bd = sdesc_mnmajor_sw128(pb + j * 2048, kRegionBytes, 1024);
+                        mma_bf16_ss(tmem_o + c * 64, ad, bd, idesc_o, (i > 0 || j > 0) ? 1u : 0u);
                     }
                 }
-                mma_commit(&bars->kv_empty[buf]);
+                mma_commit(&bars->kv_empty[stg]);
                 mma_commit(&bars->o_done);
             }
             if (ok && n_tiles > 0) mma_commit(&bars->o_full);
@@ -280,55 +288,55 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
         float m_ref = -CUDART_INF_F, l_run = 0.0f;
         bool ok = true;
         for (int i = 0; i < n_tiles; ++i) {
-            const int buf = i & 1;
-            ok = mbar_wait(&bars->s_full[buf], (i >> 1) & 1, a.err, 0x505, abort);
-            if (ok) ok = mbar_wait(&bars->kv_full[buf], (i >> 1) & 1, a.err, 0x506, abort);  // valid flags
+            const int sb = i & 1, stg = i % kStages;
+            ok = mbar_wait(&bars->s_full[sb], (i >> 1) & 1, a.err, 0x505, abort);
+            if (ok) ok = mbar_wait(&bars->kv_full[stg], (i / kStages) & 1, a.err, 0x506, abort);  // valid mask
             ok = bar_and(kBarSm, kSmThreads, ok);
             if (!ok) break;
             tc_fence_after();
-            // va/vb: raw logits -> scaled/masked logits; va then holds packed bf16 P
-            uint32_t va[32], vb[32];
-            tmem_ld32(tmem_s + 64 * buf + lane_off, va);
-            tmem_ld32(tmem_s + 64 * buf + lane_off + 32, vb);
+            const uint32_t vmask = st->valid[stg];
+            uint32_t va[32];
+            tmem_ld32(tmem_s + kKeys * sb + lane_off, va);
             tmem_wait_ld();
-            float mt = -CUDART_INF_F;
+            float x[32];
 #pragma unroll
-            for (int k = 0; k < 32; ++k) {
-                const float xa = st->valid[buf][k] ? __uint_as_float(va[k]) * a.scale_log2 : -CUDART_INF_F;
-                const float xb = st->valid[buf][32 + k] ? __uint_as_float(vb[k]) * a.scale_log2 : -CUDART_INF_F;
-                va[k] = __float_as_uint(xa);
-                vb[k] = __float_as_uint(xb);
-                mt = fmaxf(mt, fmaxf(xa, xb));
-            }
+            for (int k = 0; k < 32; ++k) x[k] = ((vmask >> k) & 1u) ? __uint_as_float(va[k]) * a.scale_log2 : -CUDART_INF_F;
+            float m8[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) m8[k] = fmaxf(fmaxf(x[k], x[k + 8]), fmaxf(x[k + 16], x[k + 24]));
+            const float mt = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
             float al = 1.0f;
             if (mt != -CUDART_INF_F && (m_ref == -CUDART_INF_F || mt > m_ref + 8.0f)) {
                 al = m_ref == -CUDART_INF_F ? 1.0f : exp2f(m_ref - mt);
                 m_ref = mt;
             }
             const float ref = m_ref == -CUDART_INF_F ? 0.0f : m_ref;
-            float ps = 0.0f;
-            uint32_t pk[32];
+            float s8[8];
 #pragma unroll
-            for (int k = 0; k < 16; ++k) {
-                const float p0 = exp2f(__uint_as_float(va[2 * k]) - ref), p1 = exp2f(__uint_as_float(va[2 * k + 1]) - ref);
-                const float p2 = exp2f(__uint_as_float(vb[2 * k]) - ref), p3 = exp2f(__uint_as_float(vb[2 * k + 1]) - ref);
-                ps += (p0 + p1) + (p2 + p3);
-                pk[k] = pack_bf16(p0, p1);
-                pk[16 + k] = pack_bf16(p2, p3);
+            for (int k = 0; k < 8; ++k) s8[k] = 0.0f;
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+                x[k] = exp2f(x[k] - ref);
+                s8[k & 7] += x[k];
             }
-            l_run = l_run * al + ps;
-            if (owner) st->alpha[buf][h] = al;
+            l_run = l_run * al + (((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7])));
             if (owner) {
-                // P^T row h (tile i's buffer; the previous tile's P*V reads the other one): 64 keys = 128 bytes, K-major with the 128-byte swizzle
-                uint8_t *prow = sKV + buf * kTileBytes + 8 * kRegionBytes + h * 128;
+                st->alpha[sb][h] = al;
+                // P^T, MN-major [key][head] with the 128-byte swizzle, over the
+                // tile's consumed rope region (the previous tile's P*V reads
+                // another buffer)
+                uint8_t *pbase = sKV + stg * kTileBytes + 8 * kRegionBytes + (h & 7) * 2;
+                const int hc = h >> 3;
 #pragma unroll
-                for (int c8 = 0; c8 < 8; ++c8)
-                    *reinterpret_cast<uint4 *>(prow + ((c8 ^ (h & 7)) << 4)) =
-                        make_uint4(pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2], pk[4 * c8 + 3]);
+                for (int k = 0; k < 32; ++k)
+                    *reinterpret_cast<__nv_bfloat16 *>(pbase + k * 128 + ((hc ^ (k & 7)) << 4)) = __float2bfloat16_rn(x[k]);
             }
             // O^T of the previous tile must be complete before it is rescaled
             if (i > 0) ok = mbar_wait(&bars->o_done, (i - 1) & 1, a.err, 0x507, abort);
             const bool any = bar_or(kBarSm, kSmThreads, owner && al != 1.0f);
+            // every softmax thread read the mask before the barrier above; the
+            // gather refills it only after this tile's P*V (kv_empty)
+            if (threadIdx.x == kSmWarp0 * 32) st->valid[stg] = 0u;
             if (any && i > 0) {
                 // rescale the O^T columns (heads) of this warp's 32 value-dim lanes
                 constexpr int W = NH < 32 ? NH : 32;
@@ -337,11 +345,11 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
                     {
                         const int c = cc / (NH / W), h0 = (cc % (NH / W)) * W;
                         uint32_t o[W];
-                        const uint32_t ta = tmem_o + lane_off + c * NH + h0;
+                        const uint32_t ta = tmem_o + lane_off + c * 64 + h0;
                         tmem_ld<W>(ta, o);
                         tmem_wait_ld();
 #pragma unroll
-                        for (int j = 0; j < W; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * st->alpha[buf][h0 + j]);
+                        for (int j = 0; j < W; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * st->alpha[sb][h0 + j]);
                         tmem_st<W>(ta, o);
                     }
                 }
@@ -371,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
                 for (int h0 = 0; h0 < NH; h0 += W) {
                     uint32_t o[W];
                     if (n_tiles > 0) {
-                        tmem_ld<W>(tmem_o + lane_off + c * NH + h0, o);
+                        tmem_ld<W>(tmem_o + lane_off + c * 64 + h0, o);
                         tmem_wait_ld();
                     } else {
 #pragma unroll
@@ -445,7 +453,7 @@ __global__ void __launch_bounds__(128) mla_combine_kernel(MlaArgs a, int NH) {
 
 size_t mla_smem_bytes(int NH) {
     (void)NH;
-    return 1024 + (size_t)kRegions * kQRegion + 2 * (size_t)kTileBytes + sizeof(MlaBars) + sizeof(MlaStats);
+    return 1024 + (size_t)MlaLayout<64>::kMiscOff + sizeof(MlaBars) + sizeof(MlaStats);
 }
 int mla_key_tile() { return kKeys; }
 
