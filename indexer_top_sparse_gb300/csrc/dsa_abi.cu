@@ -165,11 +165,12 @@ int mla_splits(int T, int H, int K) {
     int forced = g_mla_splits.load();
     const int tile = dsa::mla_key_tile();
     const int max_splits = std::max(1, std::min(16, ceil_div(std::max(K, 1), tile)));
-    if (forced > 0) return std::min(forced, max_splits);
+    const int min_splits = ceil_div(std::max(K, 1), 2048);  // a CTA resolves at most 2048 keys
+    if (forced > 0) return std::max(min_splits, std::min(forced, max_splits));
     const long long pairs = (long long)T * mla_groups(H);
     const int nsm = sm_count();
-    if (pairs >= nsm) return 1;
-    return std::max(1, std::min<int>(max_splits, (int)(nsm / pairs)));
+    if (pairs >= nsm) return min_splits;
+    return std::max(min_splits, std::min<int>(max_splits, (int)(nsm / pairs)));
 }
 
 dsa_status cuda_status(cudaError_t e) {

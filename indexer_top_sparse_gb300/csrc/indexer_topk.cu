@@ -273,7 +273,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t *sKeys = reinterpret_cast<uint32_t *>(sK + (size_t)a.stages * kTileBytes);
     float *sW = reinterpret_cast<float *>(sKeys + (size_t)G * key_cap);
     uint32_t *sHist0 = reinterpret_cast<uint32_t *>(sW + G * kHI);  // [G][256] top-digit histograms
-    SelectSmem *ss = reinterpret_cast<SelectSmem *>(sHist0 + G * kHist);
+    int32_t *sRows = reinterpret_cast<int32_t *>(sHist0 + G * kHist);  // [2*tiles_cap] cache row per 64-row box
+    SelectSmem *ss = reinterpret_cast<SelectSmem *>(sRows + ((2 * a.tiles_cap + 3) & ~3));
     IdxBars *bars = reinterpret_cast<IdxBars *>(ss + 1);
     static_assert(sizeof(SelectSmem) % 16 == 0, "keep the barrier block 16-byte aligned");
 
@@ -341,6 +342,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         sW[i] = gi < gn ? __ldg(a.head_w + (size_t)(t0 + gi) * kHI + (i % kHI)) : 0.0f;
     }
     for (int i = threadIdx.x; i < G * kHist; i += kThreads) sHist0[i] = 0u;
+    // resolve the physical row of every 64-position box of this CTA's range up
+    // front, so that the TMA producer never waits on a page-table load
+    for (int j = threadIdx.x; j < 2 * n_tiles; j += kThreads) {
+        const int p0 = tile0 * kTileM + j * kBox;
+        int row = -1;
+        if (p0 <= pos_last) {
+            const int page = __ldg(pt_row + p0 / a.page_size);
+            if (page < 0 || (int64_t)page >= a.num_pages) report_error(a.err, kErrBadPage);
+            else row = page * a.page_size + p0 % a.page_size;
+        }
+        sRows[j] = row;
+    }
     if (warp == 1) tmem_alloc(&bars->tmem_slot, L::kTmemCols);
     tc_fence_before();
     __syncthreads();
@@ -365,20 +378,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 issued = i + 1;
                 uint8_t *dst = sK + (size_t)s * kTileBytes;
-                const int p_tile = (tile0 + i) * kTileM;
                 int rows[2];
                 uint32_t bytes = 0;
                 for (int h = 0; h < 2; ++h) {
-                    rows[h] = -1;
-                    const int p0 = p_tile + h * kBox;
-                    if (p0 > pos_last) continue;
-                    const int page = __ldg(pt_row + p0 / a.page_size);
-                    if (page < 0 || (int64_t)page >= a.num_pages) {
-                        report_error(a.err, kErrBadPage);
-                        continue;
-                    }
-                    rows[h] = page * a.page_size + p0 % a.page_size;
-                    bytes += 2 * kBoxBytes;
+                    rows[h] = sRows[2 * i + h];
+                    if (rows[h] >= 0) bytes += 2 * kBoxBytes;
                 }
                 mbar_arrive_expect_tx(&bars->full[s], bytes);
                 for (int h = 0; h < 2; ++h) {
@@ -513,7 +517,7 @@ size_t indexer_smem_bytes(int G, int stages, int tiles_cap) {
     size_t q = (size_t)G * kHI * kDI * 2;
     size_t k = (size_t)stages * kTileBytes;
     size_t keys = (size_t)G * tiles_cap * kTileM * 4;
-    size_t w = (size_t)G * kHI * 4 + (size_t)G * kHist * 4;
+    size_t w = (size_t)G * kHI * 4 + (size_t)G * kHist * 4 + (size_t)((2 * tiles_cap + 3) & ~3) * 4;
     return 1024 + q + k + keys + w + sizeof(SelectSmem) + sizeof(IdxBars);
 }
 

@@ -58,7 +58,9 @@ constexpr int kSmWarp0 = kProd + 1;          // 4 softmax / epilogue warps
 constexpr int kThreads = (kProd + 1 + 4) * 32;
 constexpr int kSmThreads = 128;
 constexpr int kBarSm = 1;
+constexpr int kBarProd = 2;
 static_assert(kKeys % kProd == 0, "gather work splits evenly");
+static_assert(kKeys == 32, "one validity word per tile");
 
 template <int NH>
 struct MlaLayout {
@@ -69,14 +71,16 @@ struct MlaLayout {
 
 struct __align__(16) MlaBars {
     uint64_t kv_full[kStages], kv_empty[kStages], s_full[2];
-    uint64_t p_full, o_done, o_full, q_full, drain;
+    uint64_t p_full, o_done, o_full, q_full, drain, table;
     uint32_t tmem_slot;
     int abort;
 };
 
+constexpr int kMaxKeysPerSplit = 2048;       // host keeps keys_per_split <= this
+
 struct __align__(16) MlaStats {
-    int32_t rows[kKeys];
-    uint32_t valid[kStages];  // bit k: key k of the tile in that buffer is valid
+    int32_t rows[kMaxKeysPerSplit];             // physical cache row of every key of the split
+    uint32_t valid[kMaxKeysPerSplit / 32];      // bit k%32 of word k/32: key k is valid
     float alpha[2][kHG];
     float m_fin[kHG];
     float l_fin[kHG];
@@ -160,11 +164,11 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
         mbar_init(&bars->o_full, 1);
         mbar_init(&bars->q_full, 1);
         mbar_init(&bars->drain, 1);
+        mbar_init(&bars->table, 1);
         bars->abort = 0;
         fence_mbar_init();
     }
-    if (threadIdx.x < kStages) st->valid[threadIdx.x] = 0u;
-    if (NH < 64) {
+    if constexpr (NH < 64) {
         // Q rows NH..63 feed MMA rows nobody reads; keep them finite
         for (int i = threadIdx.x; i < kRegions * (64 - NH) * 8; i += kThreads) {
             const int r = i / ((64 - NH) * 8), rem = i % ((64 - NH) * 8);
@@ -192,47 +196,51 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
             for (int r = 0; r < kRegions; ++r)
                 tma_load_2d(sQ + r * kQRegion, &tm_q, &bars->q_full, 64 * r, t * a.H + hg * NH);
         }
+        // resolve every selected key of the split to its physical row once,
+        // in parallel, so that the copy loop below never waits on the index
+        // or page-table loads
+        const int n_keys = n_tiles * kKeys;
+        for (int k = threadIdx.x; k < n_keys; k += kProd * 32) {
+            const int slot = k_begin + k;
+            int row = 0;  // invalid slots read row 0 and are masked by the softmax
+            bool v = false;
+            if (slot < k_end) {
+                const int idx = __ldg(idx_row + slot);
+                if (idx > pos) {
+                    report_error(a.err, kErrBadIndex);
+                } else if (idx >= 0) {
+                    const int page = __ldg(pt_row + idx / a.page_size);
+                    if (page < 0 || (int64_t)page >= a.num_pages) {
+                        report_error(a.err, kErrBadPage);
+                    } else {
+                        row = page * a.page_size + idx % a.page_size;
+                        v = true;
+                    }
+                }
+            }
+            st->rows[k] = row;
+            const uint32_t bits = __ballot_sync(0xffffffffu, v);
+            if (lane == 0) st->valid[k >> 5] = bits;
+        }
+        bar_sync(kBarProd, kProd * 32);  // gather warps only
+        if (threadIdx.x == 0) mbar_arrive(&bars->table);  // publishes the row / validity table
         for (int i = 0; i < n_tiles; ++i) {
             const int stg = i % kStages;
             bool ok = true;
             if (i >= kStages) ok = mbar_wait(&bars->kv_empty[stg], ((i / kStages) & 1) ^ 1, a.err, 0x501, abort);
             if (!__all_sync(0xffffffffu, ok)) break;
-            bool v = false;
-            if (lane < kKPW) {
-                const int key = key0 + lane;
-                const int slot = k_begin + i * kKeys + key;
-                int row = 0;  // invalid slots read row 0 and are masked by the softmax
-                if (slot < k_end) {
-                    const int idx = __ldg(idx_row + slot);
-                    if (idx > pos) {
-                        report_error(a.err, kErrBadIndex);
-                    } else if (idx >= 0) {
-                        const int page = __ldg(pt_row + idx / a.page_size);
-                        if (page < 0 || (int64_t)page >= a.num_pages) {
-                            report_error(a.err, kErrBadPage);
-                        } else {
-                            row = page * a.page_size + idx % a.page_size;
-                            v = true;
-                        }
-                    }
-                }
-                st->rows[key] = row;
-            }
-            const uint32_t vb = __ballot_sync(0xffffffffu, v) & ((1u << kKPW) - 1u);
-            if (lane == 0) atomicOr(&st->valid[stg], vb << key0);
-            __syncwarp();
             uint8_t *dst = sKV + stg * kTileBytes;
+            const int32_t *rows = st->rows + i * kKeys;
 #pragma unroll 3
             for (int r = 0; r < kRegions; ++r) {
 #pragma unroll
                 for (int m = 0; m < kKPW * 8 / 32; ++m) {
                     const int f = m * 32 + lane, key = key0 + (f >> 3), cc = f & 7;
-                    const uint8_t *src = a.kv + (size_t)st->rows[key] * (kD * 2) + r * 128 + cc * 16;
+                    const uint8_t *src = a.kv + (size_t)rows[key] * (kD * 2) + r * 128 + cc * 16;
                     cp_async16(dst + r * kRegionBytes + key * 128 + ((cc ^ (key & 7)) << 4), src);
                 }
             }
             cp_async_arrive(&bars->kv_full[stg]);
-            __syncwarp();
         }
         cp_async_wait_all();  // the CTA stays alive until every copy has landed
         if (warp == 0 && lane == 0 && *abort) {
@@ -286,15 +294,14 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
         const int h = quad * 16 + lane;           // head of this thread (lanes 0..15)
         const bool owner = lane < 16 && h < NH;
         float m_ref = -CUDART_INF_F, l_run = 0.0f;
-        bool ok = true;
+        bool ok = n_tiles == 0 || mbar_wait(&bars->table, 0, a.err, 0x509, abort);
         for (int i = 0; i < n_tiles; ++i) {
             const int sb = i & 1, stg = i % kStages;
             ok = mbar_wait(&bars->s_full[sb], (i >> 1) & 1, a.err, 0x505, abort);
-            if (ok) ok = mbar_wait(&bars->kv_full[stg], (i / kStages) & 1, a.err, 0x506, abort);  // valid mask
             ok = bar_and(kBarSm, kSmThreads, ok);
             if (!ok) break;
             tc_fence_after();
-            const uint32_t vmask = st->valid[stg];
+            const uint32_t vmask = st->valid[i];  // tile i = keys 32i..32i+31 of the split
             uint32_t va[32];
             tmem_ld32(tmem_s + kKeys * sb + lane_off, va);
             tmem_wait_ld();
@@ -334,9 +341,6 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
             // O^T of the previous tile must be complete before it is rescaled
             if (i > 0) ok = mbar_wait(&bars->o_done, (i - 1) & 1, a.err, 0x507, abort);
             const bool any = bar_or(kBarSm, kSmThreads, owner && al != 1.0f);
-            // every softmax thread read the mask before the barrier above; the
-            // gather refills it only after this tile's P*V (kv_empty)
-            if (threadIdx.x == kSmWarp0 * 32) st->valid[stg] = 0u;
             if (any && i > 0) {
                 // rescale the O^T columns (heads) of this warp's 32 value-dim lanes
                 constexpr int W = NH < 32 ? NH : 32;
