@@ -169,6 +169,28 @@ dsa_status dsa_sparse_mla(const void *q, const void *kv_cache, const void *kv_ro
                           int32_t T, int32_t H, int32_t K, float scale, int32_t page_size, dsa_kv_dtype dtype,
                           void *out, float *lse, void *workspace, size_t workspace_bytes, void *stream);
 
+/* ---------------------------------------------------------------- no-allocation variant */
+
+/* dsa_sparse_mla without a workspace, for callers that cannot allocate device
+ * memory around the call (a latency-critical step that must not take the
+ * synchronisation an allocation can imply, or a plug-in whose host framework
+ * owns all device memory).  The source pages have no counterpart to this
+ * call; it exists for such callers only.
+ *   Arguments and results are those of dsa_sparse_mla (without workspace).
+ *   Scratch: the split-K partials go to a fixed 32 MiB array in the library's
+ *   device image, held by every GPU that loads the library until exit.  A
+ *   request whose partials do not fit returns DSA_ERR_UNSUPPORTED.  The first
+ *   call on a device looks the array's address up (cudaGetSymbolAddress);
+ *   make it before any stream capture.  Every call on a device shares the
+ *   array: calls whose kernels overlap on the GPU race and must not be issued.
+ *   Device-side error bits go to the array's own error word, which each call
+ *   clears; they cannot be read back (use dsa_sparse_mla for that). */
+dsa_status dsa_sparse_mla_static(const void *q, const void *kv_cache, const void *kv_rope, const float *kv_scale,
+                                 int64_t num_pages, const int32_t *page_table, int32_t max_pages_per_seq,
+                                 const int32_t *seq_lens, const int32_t *cu_q, const int32_t *indices, int32_t B,
+                                 int32_t T, int32_t H, int32_t K, float scale, int32_t page_size, dsa_kv_dtype dtype,
+                                 void *out, float *lse, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -27,7 +27,7 @@ KV_DTYPES = {"bf16": 0, "fp8_rowscale": 1}
 # Every symbol include/dsa.h declares.
 EXPORTS = ("dsa_status_string", "dsa_set_tuning", "dsa_index_topk_workspace_size", "dsa_sparse_mla_workspace_size",
            "dsa_workspace_init", "dsa_get_error", "dsa_index_topk", "dsa_index_scores", "dsa_topk_from_scores",
-           "dsa_sparse_mla")
+           "dsa_sparse_mla", "dsa_sparse_mla_static")
 
 
 class DSAError(RuntimeError):
@@ -76,6 +76,9 @@ def load(build_if_missing: bool = True):
         lib.dsa_sparse_mla.argtypes = [P, P, P, P, i64, P, i32, P, P, P, i32, i32, i32, i32, ctypes.c_float, i32,
                                        c_int, P, P, P, sz, P]
         lib.dsa_sparse_mla.restype = c_int
+        lib.dsa_sparse_mla_static.argtypes = [P, P, P, P, i64, P, i32, P, P, P, i32, i32, i32, i32, ctypes.c_float,
+                                              i32, c_int, P, P, P]
+        lib.dsa_sparse_mla_static.restype = c_int
         _lib = lib
         return lib
 
