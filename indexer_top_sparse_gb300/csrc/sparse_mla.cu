@@ -43,10 +43,13 @@ namespace {
 constexpr int kD = 576;
 constexpr int kDv = 512;
 constexpr int kHG = 64;                      // head-slot stride of the partial layout
-constexpr int kKeys = 32;                    // keys per tile (MMA N of S)
-constexpr int kStages = 4;                   // tiles in flight
+#ifndef MLA_TILE_KEYS
+#define MLA_TILE_KEYS 64
+#endif
+constexpr int kKeys = MLA_TILE_KEYS;         // keys per tile (MMA N of S): 32 or 64
+constexpr int kStages = kKeys == 32 ? 4 : 2; // tiles in flight
 constexpr int kRegions = 9;                  // 64-dim regions of a 576-wide row
-constexpr int kRegionBytes = kKeys * 128;    // 4 KB
+constexpr int kRegionBytes = kKeys * 128;    // 4 or 8 KB
 constexpr int kTileBytes = kRegions * kRegionBytes;
 constexpr int kQRegion = 64 * 128;           // Q rows padded to the MMA's M = 64
 #ifndef MLA_PRODUCER_WARPS
@@ -60,7 +63,8 @@ constexpr int kSmThreads = 128;
 constexpr int kBarSm = 1;
 constexpr int kBarProd = 2;
 static_assert(kKeys % kProd == 0, "gather work splits evenly");
-static_assert(kKeys == 32, "one validity word per tile");
+static_assert(kKeys == 32 || kKeys == 64, "tiles of 32 or 64 keys");
+constexpr int kWords = kKeys / 32;           // validity words per tile
 
 template <int NH>
 struct MlaLayout {
@@ -181,7 +185,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_o = bars->tmem_slot;      // O^T chunk c: columns [64 c, 64 c + NH)
-    const uint32_t tmem_s = tmem_o + 256;         // S buffer j at columns 256 + kKeys j
+    const uint32_t tmem_s = tmem_o + 256;         // S buffer j at columns 256 + kKeys j (<= 384)
     volatile int *abort = &bars->abort;
 
     if (warp < kProd) {
@@ -259,9 +263,12 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
             uint32_t *const err = a.err;
             if (ok && n_tiles > 0) ok = issue_s_tile(0, bars, kv_base, q_base, tmem_s, idesc_s, err, abort);
             for (int i = 0; ok && i < n_tiles; ++i) {
-                // the next tile's logits overlap this tile's softmax; its S
-                // buffer was last read by the softmax of tile i-1 (p_full below)
-                if (i + 1 < n_tiles && !(ok = issue_s_tile(i + 1, bars, kv_base, q_base, tmem_s, idesc_s, err, abort)))
+                // With a ring of 3+ tiles the next tile's logits are issued
+                // first, so that they overlap this tile's softmax; with only
+                // 2 buffers the next tile is still loading, so this tile's
+                // P*V goes first (it frees the buffer the tile after needs).
+                if (kStages > 2 && i + 1 < n_tiles &&
+                    !(ok = issue_s_tile(i + 1, bars, kv_base, q_base, tmem_s, idesc_s, err, abort)))
                     break;
                 if (!(ok = mbar_wait(&bars->p_full, i & 1, a.err, 0x504, abort))) break;
                 tc_fence_after();
@@ -278,6 +285,9 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
                 }
                 mma_commit(&bars->kv_empty[stg]);
                 mma_commit(&bars->o_done);
+                if (kStages <= 2 && i + 1 < n_tiles &&
+                    !(ok = issue_s_tile(i + 1, bars, kv_base, q_base, tmem_s, idesc_s, err, abort)))
+                    break;
             }
             if (ok && n_tiles > 0) mma_commit(&bars->o_full);
             if (*abort) {
@@ -301,16 +311,24 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
             ok = bar_and(kBarSm, kSmThreads, ok);
             if (!ok) break;
             tc_fence_after();
-            const uint32_t vmask = st->valid[i];  // tile i = keys 32i..32i+31 of the split
-            uint32_t va[32];
-            tmem_ld32(tmem_s + kKeys * sb + lane_off, va);
-            tmem_wait_ld();
-            float x[32];
+            float x[kKeys];
 #pragma unroll
-            for (int k = 0; k < 32; ++k) x[k] = ((vmask >> k) & 1u) ? __uint_as_float(va[k]) * a.scale_log2 : -CUDART_INF_F;
+            for (int w = 0; w < kWords; ++w) {
+                const uint32_t vmask = st->valid[i * kWords + w];  // keys 32w..32w+31 of tile i
+                uint32_t va[32];
+                tmem_ld32(tmem_s + kKeys * sb + lane_off + 32 * w, va);
+                tmem_wait_ld();
+#pragma unroll
+                for (int k = 0; k < 32; ++k)
+                    x[32 * w + k] = ((vmask >> k) & 1u) ? __uint_as_float(va[k]) * a.scale_log2 : -CUDART_INF_F;
+            }
             float m8[8];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) m8[k] = fmaxf(fmaxf(x[k], x[k + 8]), fmaxf(x[k + 16], x[k + 24]));
+            for (int k = 0; k < 8; ++k) {
+                m8[k] = x[k];
+#pragma unroll
+                for (int j = 1; j < kKeys / 8; ++j) m8[k] = fmaxf(m8[k], x[k + 8 * j]);
+            }
             const float mt = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
             float al = 1.0f;
             if (mt != -CUDART_INF_F && (m_ref == -CUDART_INF_F || mt > m_ref + 8.0f)) {
@@ -322,7 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
 #pragma unroll
             for (int k = 0; k < 8; ++k) s8[k] = 0.0f;
 #pragma unroll
-            for (int k = 0; k < 32; ++k) {
+            for (int k = 0; k < kKeys; ++k) {
                 x[k] = exp2f(x[k] - ref);
                 s8[k & 7] += x[k];
             }
@@ -335,7 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
                 uint8_t *pbase = sKV + stg * kTileBytes + 8 * kRegionBytes + (h & 7) * 2;
                 const int hc = h >> 3;
 #pragma unroll
-                for (int k = 0; k < 32; ++k)
+                for (int k = 0; k < kKeys; ++k)
                     *reinterpret_cast<__nv_bfloat16 *>(pbase + k * 128 + ((hc ^ (k & 7)) << 4)) = __float2bfloat16_rn(x[k]);
             }
             // O^T of the previous tile must be complete before it is rescaled
