@@ -57,8 +57,9 @@ constexpr int kQRegion = 64 * 128;           // Q rows padded to the MMA's M = 6
 #endif
 constexpr int kProd = MLA_PRODUCER_WARPS;
 constexpr int kMmaWarp = kProd;
-constexpr int kSmWarp0 = kProd + 1;          // 4 softmax / epilogue warps
-constexpr int kThreads = (kProd + 1 + 4) * 32;
+constexpr int kSendWarp = kProd + 1;         // pairs only: forwards this CTA's half tiles to the peer
+constexpr int kSmWarp0 = kProd + 2;          // 4 softmax / epilogue warps
+constexpr int kThreads = (kProd + 2 + 4) * 32;
 constexpr int kSmThreads = 128;
 constexpr int kBarSm = 1;
 constexpr int kBarProd = 2;
@@ -75,6 +76,8 @@ struct MlaLayout {
 
 struct __align__(16) MlaBars {
     uint64_t kv_full[kStages], kv_empty[kStages], s_full[2];
+    uint64_t half_ready[kStages];  // pairs: this CTA's half of the tile landed
+    uint64_t peer_free[kStages];   // pairs: the peer's copy of this stage may be overwritten
     uint64_t p_full, o_done, o_full, q_full, drain, table;
     uint32_t tmem_slot;
     int abort;
@@ -138,7 +141,10 @@ __device__ __forceinline__ bool issue_s_tile(int i, MlaBars *bars, uint32_t kv_b
     return true;
 }
 
-template <int NH>
+// kPair: the two 64-head CTAs of a query row form a cluster; each gathers half
+// of every tile (from global memory) and forwards it to the other's shared
+// memory, so that each selected row is read from L2/HBM once.
+template <int NH, bool kPair>
 __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, MlaArgs a) {
     using L = MlaLayout<NH>;
     extern __shared__ uint8_t smem_raw[];
@@ -159,8 +165,12 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
-            mbar_init(&bars->kv_full[i], 32 * kProd);  // one cp.async completion arrival per gather lane
+            // unpaired: one cp.async completion arrival per gather lane; paired:
+            // the sender's arrival, plus the peer's half counted in bytes
+            mbar_init(&bars->kv_full[i], kPair ? 1 : 32 * kProd);
             mbar_init(&bars->kv_empty[i], 1);
+            mbar_init(&bars->half_ready[i], 32 * kProd);
+            mbar_init(&bars->peer_free[i], 1);
         }
         for (int i = 0; i < 2; ++i) mbar_init(&bars->s_full[i], 1);
         mbar_init(&bars->p_full, kSmThreads / 32);
@@ -184,6 +194,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    if constexpr (kPair) cluster_barrier();  // both CTAs' barriers are initialised before any remote arrive
+    const uint32_t peer = kPair ? (cluster_rank() ^ 1u) : 0u;
     const uint32_t tmem_o = bars->tmem_slot;      // O^T chunk c: columns [64 c, 64 c + NH)
     const uint32_t tmem_s = tmem_o + 256;         // S buffer j at columns 256 + kKeys j (<= 384)
     volatile int *abort = &bars->abort;
@@ -191,9 +203,11 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
     if (warp < kProd) {
         // ---------------------------------------------------------------- gather
         const int32_t *pt_row = a.page_table + (size_t)b * a.max_pages;
-        constexpr int kKPW = kKeys / kProd;  // keys per gather warp
+        // keys of a tile this CTA gathers: all of them, or its half when paired
+        constexpr int kMine = kPair ? kKeys / 2 : kKeys;
+        constexpr int kKPW = kMine / kProd;  // keys per gather warp
         static_assert(kKPW * 8 % 32 == 0 && kKPW <= 32, "a warp instruction covers four keys");
-        const int key0 = warp * kKPW;
+        const int key0 = (kPair ? (int)cluster_rank() * kMine : 0) + warp * kKPW;
         if (warp == 0 && lane == 0) {
             tma_prefetch_desc(&tm_q);
             mbar_arrive_expect_tx(&bars->q_full, (uint32_t)(kRegions * NH * 128));
@@ -233,6 +247,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
             bool ok = true;
             if (i >= kStages) ok = mbar_wait(&bars->kv_empty[stg], ((i / kStages) & 1) ^ 1, a.err, 0x501, abort);
             if (!__all_sync(0xffffffffu, ok)) break;
+            // this stage is free here: the peer may send its half of tile i
+            if (kPair && threadIdx.x == 0) mbar_arrive_remote(map_peer(smem_u32(&bars->peer_free[stg]), peer));
             uint8_t *dst = sKV + stg * kTileBytes;
             const int32_t *rows = st->rows + i * kKeys;
 #pragma unroll 3
@@ -244,12 +260,32 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
                     cp_async16(dst + r * kRegionBytes + key * 128 + ((cc ^ (key & 7)) << 4), src);
                 }
             }
-            cp_async_arrive(&bars->kv_full[stg]);
+            cp_async_arrive(kPair ? &bars->half_ready[stg] : &bars->kv_full[stg]);
         }
         cp_async_wait_all();  // the CTA stays alive until every copy has landed
         if (warp == 0 && lane == 0 && *abort) {
             volatile int no_abort = 0;
             mbar_wait(&bars->q_full, 0, nullptr, 0, &no_abort);
+        }
+    } else if (warp == kSendWarp) {
+        // ---------------------------------------------------------------- pair forwarding
+        if (kPair && lane == 0) {
+            constexpr uint32_t kHalfBytes = kKeys / 2 * 128;  // one region's half: 32 keys x 128 B
+            const uint32_t half_off = cluster_rank() * kHalfBytes;
+            for (int i = 0; i < n_tiles; ++i) {
+                const int stg = i % kStages;
+                const uint32_t par = (i / kStages) & 1;
+                if (!mbar_wait(&bars->half_ready[stg], par, a.err, 0x511, abort)) break;
+                fence_proxy_async_smem();  // own half was written through the generic proxy
+                if (!mbar_wait(&bars->peer_free[stg], par, a.err, 0x512, abort)) break;
+                const uint32_t rbar = map_peer(smem_u32(&bars->kv_full[stg]), peer);
+                uint8_t *src = sKV + stg * kTileBytes + half_off;
+                for (int r = 0; r < kRegions; ++r)
+                    bulk_copy_to_peer(map_peer(smem_u32(src + r * kRegionBytes), peer), src + r * kRegionBytes,
+                                      kHalfBytes, rbar);
+                // own tile is complete once the peer's half has arrived here
+                mbar_arrive_expect_tx(&bars->kv_full[stg], kRegions * kHalfBytes);
+            }
         }
     } else if (warp == kMmaWarp) {
         // ---------------------------------------------------------------- tcgen05 issuer
@@ -439,6 +475,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
     __syncthreads();
     tc_fence_after();
     if (warp == kMmaWarp) tmem_dealloc(tmem_o, L::kTmemCols);
+    // no CTA of a pair leaves while the other may still signal or copy into it
+    if constexpr (kPair) cluster_barrier();
 }
 
 // Merge split partials: block = (head, head group, query row), 128 threads x 4 dims.
@@ -479,21 +517,33 @@ size_t mla_smem_bytes(int NH) {
 }
 int mla_key_tile() { return kKeys; }
 
-template <int NH>
+template <int NH, bool kPair>
 static cudaError_t launch_tc(const CUtensorMap &tq, const MlaArgs &a, cudaStream_t st) {
     const size_t smem = mla_smem_bytes(NH);
-    auto kern = sparse_mla_tc_kernel<NH>;
+    auto kern = sparse_mla_tc_kernel<NH, kPair>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    kern<<<dim3(a.H / NH, a.splits, a.T), kThreads, smem, st>>>(tq, a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(a.H / NH), (unsigned)a.splits, (unsigned)a.T);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kPair ? 2 : 1;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, tq, a);
 }
 
 cudaError_t launch_sparse_mla_bf16(const CUtensorMap &tq, const MlaArgs &a, int NH, cudaStream_t st) {
     cudaError_t e;
-    if (NH == 64) e = launch_tc<64>(tq, a, st);
-    else if (NH == 32) e = launch_tc<32>(tq, a, st);
-    else if (NH == 16) e = launch_tc<16>(tq, a, st);
+    if (NH == 64 && a.H == 128) e = launch_tc<64, true>(tq, a, st);
+    else if (NH == 64) e = launch_tc<64, false>(tq, a, st);
+    else if (NH == 32) e = launch_tc<32, false>(tq, a, st);
+    else if (NH == 16) e = launch_tc<16, false>(tq, a, st);
     else return cudaErrorInvalidValue;
     if (e != cudaSuccess || a.splits == 1) return e;
     mla_combine_kernel<<<dim3(kHG, a.H / NH, a.T), 128, 0, st>>>(a, NH);

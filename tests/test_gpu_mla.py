@@ -57,11 +57,12 @@ def test_decode_heads(orc, H):
     _compare(orc, wl, _random_indices(rng, wl, 512))
 
 
+@pytest.mark.parametrize("H", [64, 128])
 @pytest.mark.parametrize("splits", [1, 2, 3, 8])
-def test_every_split_count(orc, splits):
+def test_every_split_count(orc, splits, H):
     import indexer_top_sparse_gb300 as d
     rng = np.random.default_rng(100 + splits)
-    wl = make_workload("mla", [4000, 900], [1, 1], H=64, K=1000, page_size=64, seed=splits, with_idx=False)
+    wl = make_workload("mla", [4000, 900], [1, 1], H=H, K=1000, page_size=64, seed=splits, with_idx=False)
     idx = _random_indices(rng, wl, 1000, pad_frac=0.1)
     d.set_tuning("mla_splits", splits)
     try:
@@ -98,15 +99,16 @@ def test_heads_32(orc):
     _compare(orc, wl, _random_indices(rng, wl, 700, pad_frac=0.05))
 
 
+@pytest.mark.parametrize("H", [64, 128])
 @pytest.mark.parametrize("order", ["rising", "falling"])
-def test_reference_max_moves_across_tiles(orc, order):
+def test_reference_max_moves_across_tiles(orc, order, H):
     # logits that grow (or shrink) strongly from one 128-key tile to the next,
     # so that the running maximum moves by far more than 2^8 between tiles
     from indexer_top_sparse_gb300.inputs import bf16_bits, bf16_to_f32
     n, K = 1024, 1024
-    wl = make_workload("mla_rescale", [n], [1], H=64, K=K, page_size=64, permute=True, seed=41, with_idx=False)
+    wl = make_workload("mla_rescale", [n], [1], H=H, K=K, page_size=64, permute=True, seed=41, with_idx=False)
     kv = bf16_to_f32(wl.kv).reshape(-1, 576)
-    q = bf16_to_f32(wl.q).reshape(64, 576)
+    q = bf16_to_f32(wl.q).reshape(H, 576)
     qdir = q[0] / np.linalg.norm(q[0])
     for s in range(n):
         row = wl.page_table[0][s // 64] * 64 + s % 64
