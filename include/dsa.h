@@ -169,6 +169,27 @@ dsa_status dsa_sparse_mla(const void *q, const void *kv_cache, const void *kv_ro
                           int32_t T, int32_t H, int32_t K, float scale, int32_t page_size, dsa_kv_dtype dtype,
                           void *out, float *lse, void *workspace, size_t workspace_bytes, void *stream);
 
+/* ---------------------------------------------------------------- quantisers */
+
+/* MXFP8 quantisation of n bf16 values (n a multiple of 32): every 32
+ * consecutive values share one E8M0 scale 2^X with X = floor(log2(amax)) - 8
+ * (clamped to [-127, 127]); elements are E4M3 of x / 2^X, round to nearest
+ * even, saturating at +-448; an all-zero block gets scale byte 127 and zero
+ * elements (OCP Microscaling v1.0; the index path's per-group-32 format of
+ * "Day-0 Inference Adaptation and Optimization for Hybrid Attention
+ * Architectures", §4 Optimization 2).
+ *   x [n] bf16 in; q [n] e4m3 codes out; e8m0 [n/32] scale bytes out. */
+dsa_status dsa_quant_mxfp8(const void *x, int64_t n, void *q, void *e8m0, void *stream);
+
+/* FP8 quantisation of 576-wide latent rows: the 512 latent dims share one fp32
+ * scale s = amax / 448 (1 when amax is 0), stored as E4M3(x / s) (round to
+ * nearest even, saturating); the 64 rope dims are copied as bf16 ("Day0
+ * Inference Adaptation and Performance Optimization for a Sparse Hybrid
+ * Architecture LLM", §3.1, with one scale per row).
+ *   kv [rows, 576] bf16 in; nope [rows, 512] e4m3, rope [rows, 64] bf16 and
+ *   scale [rows] fp32 out. */
+dsa_status dsa_quant_fp8_rows(const void *kv, int64_t rows, void *nope, void *rope, float *scale, void *stream);
+
 /* ---------------------------------------------------------------- no-allocation variant */
 
 /* dsa_sparse_mla without a workspace, for callers that cannot allocate device

@@ -27,7 +27,7 @@ KV_DTYPES = {"bf16": 0, "fp8_rowscale": 1}
 # Every symbol include/dsa.h declares.
 EXPORTS = ("dsa_status_string", "dsa_set_tuning", "dsa_index_topk_workspace_size", "dsa_sparse_mla_workspace_size",
            "dsa_workspace_init", "dsa_get_error", "dsa_index_topk", "dsa_index_scores", "dsa_topk_from_scores",
-           "dsa_sparse_mla", "dsa_sparse_mla_static")
+           "dsa_sparse_mla", "dsa_sparse_mla_static", "dsa_quant_mxfp8", "dsa_quant_fp8_rows")
 
 
 class DSAError(RuntimeError):
@@ -79,6 +79,10 @@ def load(build_if_missing: bool = True):
         lib.dsa_sparse_mla_static.argtypes = [P, P, P, P, i64, P, i32, P, P, P, i32, i32, i32, i32, ctypes.c_float,
                                               i32, c_int, P, P, P]
         lib.dsa_sparse_mla_static.restype = c_int
+        lib.dsa_quant_mxfp8.argtypes = [P, i64, P, P, P]
+        lib.dsa_quant_mxfp8.restype = c_int
+        lib.dsa_quant_fp8_rows.argtypes = [P, i64, P, P, P, P]
+        lib.dsa_quant_fp8_rows.restype = c_int
         _lib = lib
         return lib
 
@@ -166,6 +170,13 @@ def _index_call(scores_ld, q_idx, head_w, k_idx_cache, page_table, seq_lens, cu_
         raise ValueError("seq_lens [B], cu_q [B+1], page_table [B, max_pages] must agree")
     P, ps = k_idx_cache.shape[0], k_idx_cache.shape[1]
     maxp = page_table.shape[1]
+    if dt == 1:
+        _need(q_idx_scale, "q_idx_scale", torch.uint8, 3, dev)
+        _need(k_idx_scale, "k_idx_scale", torch.uint8, 3, dev)
+        if tuple(q_idx_scale.shape) != (T, 64, 4) or tuple(k_idx_scale.shape) != (P, ps, 4):
+            raise ValueError("MXFP8 scales must be q_idx_scale [T, 64, 4] and k_idx_scale [pages, page_size, 4]")
+    elif q_idx_scale is not None or k_idx_scale is not None:
+        raise ValueError("q_idx_scale / k_idx_scale are for dtype='mxfp8' only")
     if indices is None:
         indices = torch.empty((T, K), dtype=torch.int32, device=dev)
     _need(indices, "indices", torch.int32, 2, dev)
@@ -244,3 +255,37 @@ def dsa_sparse_mla(q, kv_cache, page_table, seq_lens, cu_q, indices, scale, *, o
                                                 _ptr(indices), B, T, H, K, float(scale), ps, dt, _ptr(out),
                                                 _ptr(lse), _ptr(workspace.buf), workspace.nbytes, _stream(stream)))
     return out
+
+
+def dsa_quant_mxfp8(x, *, q=None, scales=None, stream=None):
+    """MXFP8 quantisation of a bf16 tensor (last dim a multiple of 32).
+    Returns (e4m3 codes uint8, same shape; e8m0 scale bytes uint8, last dim / 32)."""
+    lib = load()
+    _need(x, "x", torch.bfloat16)
+    if x.shape[-1] % 32:
+        raise ValueError("last dim must be a multiple of 32")
+    if q is None:
+        q = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    if scales is None:
+        scales = torch.empty(x.shape[:-1] + (x.shape[-1] // 32,), dtype=torch.uint8, device=x.device)
+    _need(q, "q", torch.uint8, None, x.device)
+    _need(scales, "scales", torch.uint8, None, x.device)
+    _check("dsa_quant_mxfp8", lib.dsa_quant_mxfp8(_ptr(x), x.numel(), _ptr(q), _ptr(scales), _stream(stream)))
+    return q, scales
+
+
+def dsa_quant_fp8_rows(kv, *, nope=None, rope=None, scale=None, stream=None):
+    """FP8 row quantisation of [..., 576] bf16 latent rows.  Returns
+    (nope e4m3 [..., 512] uint8, rope [..., 64] bf16, scale [...] fp32)."""
+    lib = load()
+    _need(kv, "kv", torch.bfloat16)
+    if kv.shape[-1] != 576:
+        raise ValueError("last dim must be 576")
+    lead = kv.shape[:-1]
+    rows = kv.numel() // 576
+    nope = torch.empty(lead + (512,), dtype=torch.uint8, device=kv.device) if nope is None else nope
+    rope = torch.empty(lead + (64,), dtype=torch.bfloat16, device=kv.device) if rope is None else rope
+    scale = torch.empty(lead, dtype=torch.float32, device=kv.device) if scale is None else scale
+    _check("dsa_quant_fp8_rows", lib.dsa_quant_fp8_rows(_ptr(kv), rows, _ptr(nope), _ptr(rope), _ptr(scale),
+                                                        _stream(stream)))
+    return nope, rope, scale

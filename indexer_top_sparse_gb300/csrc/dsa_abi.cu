@@ -71,6 +71,19 @@ bool encode_2d_bf16(CUtensorMap *m, const void *base, uint64_t cols, uint64_t ro
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2D uint8 tensor [rows, 128] (E4M3 codes) with 64-row x 128-byte boxes and the 128-byte swizzle.
+bool encode_rows128_u8(CUtensorMap *m, const void *base, uint64_t rows) {
+    auto fn = encode_fn();
+    if (!fn || rows == 0 || rows > (1ull << 31)) return false;
+    cuuint64_t dims[2] = {128, rows};
+    cuuint64_t strides[1] = {128};
+    cuuint32_t box[2] = {128, 64};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool encode_rows128_bf16(CUtensorMap *m, const void *base, uint64_t rows) {
     return encode_2d_bf16(m, base, 128, rows, 64);
 }
@@ -156,6 +169,54 @@ bool plan_indexer(int B, int T, int max_len, IdxPlan *p) {
     return found;
 }
 
+// Launch shape of the MXFP8 indexer (one query row per cluster): fewest
+// waves, then most CTAs in flight, then the deepest ring.
+bool plan_indexer_mxfp8(int T, int max_len, int *C_out, int *stages_out, int *tiles_cap_out, size_t *smem_out) {
+    static std::mutex mu;
+    static std::map<std::tuple<int, int, size_t>, int> cache;
+    const size_t smax = max_smem_optin();
+    const int tiles_max = std::max(1, ceil_div(max_len, 128));
+    const int c_force = g_idx_cluster.load(), s_force = g_idx_stages.load();
+    bool found = false;
+    long long best_waves = 0, best_used = 0;
+    int best_stages = 0;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    for (int C = 1; C <= 16; C <<= 1) {
+        if (c_force && C != c_force) continue;
+        const int tiles_cap = ceil_div(tiles_max, C);
+        if (!c_force && C > 1 && tiles_cap < 4) continue;
+        for (int stages = 6; stages >= 2; --stages) {
+            if (s_force && stages != s_force) continue;
+            const size_t smem = std::max(dsa::indexer_mxfp8_smem_bytes(stages, tiles_cap), (size_t)116 * 1024);
+            if (smem > smax) continue;
+            int resident;
+            {
+                std::lock_guard<std::mutex> g(mu);
+                auto key = std::make_tuple(dev * 64 + C, stages, smem);
+                auto it = cache.find(key);
+                if (it == cache.end()) it = cache.emplace(key, dsa::indexer_mxfp8_max_active_clusters(C, smem)).first;
+                resident = it->second;
+            }
+            if (resident <= 0) continue;
+            const long long waves = (T + resident - 1) / resident;
+            const long long used = (long long)std::min(T, resident) * C;
+            if (!found || waves < best_waves || (waves == best_waves && (used > best_used ||
+                                                                         (used == best_used && stages > best_stages)))) {
+                *C_out = C;
+                *stages_out = stages;
+                *tiles_cap_out = tiles_cap;
+                *smem_out = smem;
+                found = true;
+                best_waves = waves;
+                best_used = used;
+                best_stages = stages;
+            }
+        }
+    }
+    return found;
+}
+
 int mla_groups(int H) {
     const int nh = mla_heads_per_cta(H);
     return nh ? H / nh : 1;
@@ -184,19 +245,49 @@ dsa_status index_common(const void *q_idx, const uint8_t *q_idx_scale, const flo
                         int32_t max_pages_per_seq, const int32_t *seq_lens, const int32_t *cu_q, int32_t B,
                         int32_t T, int32_t K, int32_t page_size, dsa_idx_dtype dtype, int32_t *indices,
                         float *scores, int64_t ld_scores, void *workspace, size_t workspace_bytes, void *stream) {
-    (void)q_idx_scale;
-    (void)k_idx_scale;
     if (T < 0 || B < 1 || K < 1 || page_size < 1 || max_pages_per_seq < 1 || num_pages < 1) return DSA_ERR_INVALID_ARG;
     if (!q_idx || !head_w || !k_idx_cache || !page_table || !seq_lens || !cu_q || !indices || !workspace)
         return DSA_ERR_INVALID_ARG;
     if (!aligned16(q_idx) || !aligned16(k_idx_cache) || !aligned16(workspace)) return DSA_ERR_INVALID_ARG;
     if (workspace_bytes < dsa_index_topk_workspace_size(B, T, K, max_pages_per_seq, page_size))
         return DSA_ERR_INVALID_ARG;
-    if (dtype != DSA_IDX_BF16) return DSA_ERR_UNSUPPORTED;
+    if (dtype != DSA_IDX_BF16 && dtype != DSA_IDX_MXFP8) return DSA_ERR_UNSUPPORTED;
+    if (dtype == DSA_IDX_MXFP8 && (!q_idx_scale || !k_idx_scale || !aligned16(k_idx_scale)))
+        return DSA_ERR_INVALID_ARG;
     if (page_size % 64 != 0) return DSA_ERR_UNSUPPORTED;
     if (T == 0) return DSA_OK;
     const long long max_len = (long long)max_pages_per_seq * page_size;
     if (max_len > (1LL << 30) || (long long)num_pages * page_size > (1LL << 31)) return DSA_ERR_UNSUPPORTED;
+    if (dtype == DSA_IDX_MXFP8) {
+        int C = 1, stages = 2, tiles_cap = 1;
+        size_t smem = 0;
+        if (T > 65535 || !plan_indexer_mxfp8(T, (int)max_len, &C, &stages, &tiles_cap, &smem))
+            return DSA_ERR_UNSUPPORTED;
+        CUtensorMap tk, tq;
+        if (!encode_rows128_u8(&tk, k_idx_cache, (uint64_t)num_pages * page_size)) return DSA_ERR_CUDA;
+        if (!encode_rows128_u8(&tq, q_idx, (uint64_t)T * 64)) return DSA_ERR_CUDA;
+        IndexerArgs a{};
+        a.head_w = head_w;
+        a.q_scale = q_idx_scale;
+        a.k_scale = k_idx_scale;
+        a.page_table = page_table;
+        a.seq_lens = seq_lens;
+        a.cu_q = cu_q;
+        a.indices = indices;
+        a.scores = scores;
+        a.err = reinterpret_cast<uint32_t *>(workspace);
+        a.num_pages = num_pages;
+        a.ld_scores = ld_scores;
+        a.max_pages = max_pages_per_seq;
+        a.B = B;
+        a.T = T;
+        a.K = K;
+        a.page_size = page_size;
+        a.stages = stages;
+        a.tiles_cap = tiles_cap;
+        return cuda_status(dsa::launch_indexer_mxfp8(tk, tq, a, C, smem, scores != nullptr,
+                                                     static_cast<cudaStream_t>(stream)));
+    }
     IdxPlan plan;
     if (!plan_indexer(B, T, (int)max_len, &plan) || plan.groups > 65535) return DSA_ERR_UNSUPPORTED;
     CUtensorMap tk, tq;
@@ -382,6 +473,22 @@ dsa_status dsa_sparse_mla(const void *q, const void *kv_cache, const void *kv_ro
     CUtensorMap tq;
     if (!encode_2d_bf16(&tq, q, 576, (uint64_t)T * H, (uint32_t)NH)) return DSA_ERR_CUDA;
     return cuda_status(dsa::launch_sparse_mla_bf16(tq, a, NH, static_cast<cudaStream_t>(stream)));
+}
+
+dsa_status dsa_quant_mxfp8(const void *x, int64_t n, void *q, void *e8m0, void *stream) {
+    if (n < 0 || n % 32 != 0 || (n > 0 && (!x || !q || !e8m0))) return DSA_ERR_INVALID_ARG;
+    if (n > 0 && (!aligned16(x) || !aligned16(q))) return DSA_ERR_INVALID_ARG;
+    return cuda_status(dsa::launch_quant_mxfp8(static_cast<const uint16_t *>(x), n, static_cast<uint8_t *>(q),
+                                               static_cast<uint8_t *>(e8m0), static_cast<cudaStream_t>(stream)));
+}
+
+dsa_status dsa_quant_fp8_rows(const void *kv, int64_t rows, void *nope, void *rope, float *scale, void *stream) {
+    if (rows < 0 || (rows > 0 && (!kv || !nope || !rope || !scale))) return DSA_ERR_INVALID_ARG;
+    if (rows > 0 && (!aligned16(kv) || !aligned16(nope) || (reinterpret_cast<uintptr_t>(rope) & 3u)))
+        return DSA_ERR_INVALID_ARG;
+    return cuda_status(dsa::launch_quant_fp8_rows(static_cast<const uint16_t *>(kv), rows,
+                                                  static_cast<uint8_t *>(nope), static_cast<uint16_t *>(rope), scale,
+                                                  static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

@@ -47,6 +47,11 @@ constexpr int kThreads = 192;
 constexpr int kHist = 256;
 constexpr int kMaxCluster = 16;
 
+// 2^(byte - 127) of an E8M0 scale byte (byte 0 is the subnormal 2^-127).
+__device__ __forceinline__ float e8m0_value(uint32_t byte) {
+    return byte ? __uint_as_float(byte << 23) : __uint_as_float(0x00400000u);
+}
+
 // Order-preserving map from a finite float to uint32 (larger float -> larger
 // key); -0 is folded onto +0.  Every finite value maps above 0x007FFFFF, so 0
 // marks "not a candidate".
@@ -58,12 +63,13 @@ __device__ __forceinline__ uint32_t score_key(float x) {
 struct __align__(16) SelectSmem {
     uint32_t hist[2][kHist];
     uint32_t tot[kHist];
-    int32_t scan[2][8];
+    int32_t scan[2][16];
     int32_t cnt[4];       // this CTA's (n_gt, n_eq) for the cluster exchange; [2] = abort flag
     uint32_t bcast[4];    // digit, count-above
 };
 
-// Exclusive scan of one int per thread across the CTA (kThreads threads).
+// Exclusive scan of one int per thread across the CTA (kT threads).
+template <int kT>
 __device__ __forceinline__ int block_exclusive_scan(int v, int32_t *warp_tot, int *total) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     int x = v;
@@ -76,7 +82,7 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int32_t *warp_tot, in
     __syncthreads();
     int before = 0, all = 0;
 #pragma unroll
-    for (int w = 0; w < kThreads / 32; ++w) {
+    for (int w = 0; w < kT / 32; ++w) {
         int t = warp_tot[w];
         if (w < warp) before += t;
         all += t;
@@ -92,6 +98,7 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int32_t *warp_tot, in
 // Writes min(K, n_valid) positions in ascending order to out[0..] and -1 to
 // the rest of out[0..K).  Every CTA of the cluster must call this with the
 // same n_valid and K (it contains cluster barriers).
+template <int kT>
 __device__ void cluster_topk(const uint32_t *keys, int n_local, int pos0, int n_valid, int K, int32_t *out,
                              SelectSmem &ss, const uint32_t *hist0 = nullptr) {
     cg::cluster_group cluster = cg::this_cluster();
@@ -102,11 +109,11 @@ __device__ void cluster_topk(const uint32_t *keys, int n_local, int pos0, int n_
     if (n_valid <= K) {
         // every valid position is selected; positions are contiguous from 0,
         // so slot == position
-        for (int l = tid; l < n_local; l += kThreads) {
-            if (keys[l] != 0u) out[pos0 + l] = pos0 + l;
+        for (int l = tid; l < n_local; l += kT) {
+            if (keys[l] != 0u && pos0 + l < n_valid) out[pos0 + l] = pos0 + l;
         }
         if (my == 0) {
-            for (int i = (n_valid > 0 ? n_valid : 0) + tid; i < K; i += kThreads) out[i] = -1;
+            for (int i = (n_valid > 0 ? n_valid : 0) + tid; i < K; i += kT) out[i] = -1;
         }
         cluster.sync();
         return;
@@ -119,17 +126,17 @@ __device__ void cluster_topk(const uint32_t *keys, int n_local, int pos0, int n_
         uint32_t *h = ss.hist[pass & 1];
         if (pass == 0 && hist0 != nullptr) {
             // the top-digit histogram was built while the scores were produced
-            for (int d = tid; d < kHist; d += kThreads) h[d] = hist0[d];
+            for (int d = tid; d < kHist; d += kT) h[d] = hist0[d];
         } else {
-            for (int d = tid; d < kHist; d += kThreads) h[d] = 0u;
+            for (int d = tid; d < kHist; d += kT) h[d] = 0u;
             __syncthreads();
-            for (int l = tid; l < n_local; l += kThreads) {
+            for (int l = tid; l < n_local; l += kT) {
                 uint32_t k = keys[l];
                 if (k != 0u && (k & mask) == prefix) atomicAdd(&h[(k >> shift) & 0xFFu], 1u);
             }
         }
         cluster.sync();
-        for (int d = tid; d < kHist; d += kThreads) {
+        for (int d = tid; d < kHist; d += kT) {
             // issue every remote load before summing (they are independent)
             uint32_t v[kMaxCluster];
 #pragma unroll
@@ -168,7 +175,8 @@ __device__ void cluster_topk(const uint32_t *keys, int n_local, int pos0, int n_
             }
         }
         __syncthreads();
-        const uint32_t digit = ss.bcast[0];
+        // (masked: after an aborted wait the counts may not add up)
+        const uint32_t digit = ss.bcast[0] & 0xFFu;
         krem -= (int)ss.bcast[1];
         prefix |= digit << shift;
         mask |= 0xFFu << shift;
@@ -179,7 +187,7 @@ __device__ void cluster_topk(const uint32_t *keys, int n_local, int pos0, int n_
 
     // count (key > threshold) and (key == threshold) in this CTA, by contiguous
     // segments so that output order follows position order
-    const int seg = (n_local + kThreads - 1) / kThreads;
+    const int seg = (n_local + kT - 1) / kT;
     const int l0 = min(n_local, tid * seg), l1 = min(n_local, l0 + seg);
     int n_gt = 0, n_eq = 0;
     for (int l = l0; l < l1; ++l) {
@@ -190,8 +198,8 @@ __device__ void cluster_topk(const uint32_t *keys, int n_local, int pos0, int n_
         n_eq += m == prefix;
     }
     int cta_gt = 0, cta_eq = 0;
-    const int eq_before_seg = block_exclusive_scan(n_eq, ss.scan[0], &cta_eq);
-    const int gt_before_seg = block_exclusive_scan(n_gt, ss.scan[1], &cta_gt);
+    const int eq_before_seg = block_exclusive_scan<kT>(n_eq, ss.scan[0], &cta_eq);
+    const int gt_before_seg = block_exclusive_scan<kT>(n_gt, ss.scan[1], &cta_gt);
     if (tid == 0) {
         ss.cnt[0] = cta_gt;
         ss.cnt[1] = cta_eq;
@@ -213,7 +221,7 @@ __device__ void cluster_topk(const uint32_t *keys, int n_local, int pos0, int n_
     // per-segment selection counts, then their exclusive scan
     const int eq_rank0 = eq_before_cta + eq_before_seg;
     const int take_seg = min(max(krem - eq_rank0, 0), n_eq);
-    const int sel_before_seg = block_exclusive_scan(n_gt + take_seg, ss.scan[0], nullptr);
+    const int sel_before_seg = block_exclusive_scan<kT>(n_gt + take_seg, ss.scan[0], nullptr);
     (void)gt_before_seg;
     int slot = out_before_cta + sel_before_seg, eq_rank = eq_rank0;
     for (int l = l0; l < l1; ++l) {
@@ -225,7 +233,7 @@ __device__ void cluster_topk(const uint32_t *keys, int n_local, int pos0, int n_
             sel = eq_rank < krem;
             ++eq_rank;
         }
-        if (sel) out[slot++] = pos0 + l;
+        if (sel && slot < K) out[slot++] = pos0 + l;
     }
     // nobody may reuse or leave shared memory another CTA still reads
     cluster.sync();
@@ -482,9 +490,220 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const int n_valid = pos_first + gi + 1;
         int32_t *out = a.indices + (size_t)(t0 + gi) * a.K;
-        cluster_topk(sKeys + (size_t)gi * key_cap, n_tiles * kTileM, tile0 * kTileM, n_valid, a.K, out, *ss,
-                     sHist0 + gi * kHist);
+        cluster_topk<kThreads>(sKeys + (size_t)gi * key_cap, n_tiles * kTileM, tile0 * kTileM, n_valid, a.K, out,
+                               *ss, sHist0 + gi * kHist);
     }
+}
+
+// ---------------------------------------------------------------------------
+// MXFP8 variant: q_idx and the index-key cache are E4M3 with one E8M0 scale per
+// 32 consecutive values ("Day-0 Inference Adaptation and Optimization for
+// Hybrid Attention Architectures", §4 Optimization 2).  A 128-byte K-major row
+// holds all 128 dims of a position, and one kind::f8f6f4 MMA (K = 32) covers
+// exactly one scale group, so each tile runs four MMAs into four accumulators
+// and the epilogue applies 2^(scale_q + scale_k) per group before the ReLU:
+//     score = sum_j w_j ReLU( sum_g 2^(sq_jg + sk_g) * (q_jg . k_g) ).
+// One query row per cluster (decode); warps: 0 TMA, 1 MMA, 2..9 epilogue
+// (two per TMEM lane quadrant, 32 heads each).
+constexpr int kF8Threads = 320;
+constexpr int kF8TileBytes = kTileM * kDI;      // 16 KB of E4M3 keys per tile
+constexpr int kF8BoxBytes = kBox * kDI;         // 8 KB per 64-row box
+
+struct __align__(16) F8Bars {
+    uint64_t full[8];
+    uint64_t empty[8];
+    uint64_t tfull[2];
+    uint64_t tempty[2];
+    uint64_t qbar;
+    uint64_t drain;
+    uint32_t tmem_slot;
+    int abort;
+};
+
+template <bool kWriteScores>
+__global__ void __launch_bounds__(kF8Threads, 1)
+    indexer_topk_mxfp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
+                              IndexerArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int key_cap = a.tiles_cap * kTileM;
+    uint8_t *sQ = smem;                                   // 64 heads x 128 B
+    uint8_t *sK = sQ + kHI * kDI;                         // stages x 16 KB
+    // Key scales get their own ring, two slots deeper than the key ring: the
+    // epilogue reads them after the MMA has released the key stage, but at
+    // most two tiles behind the MMA (the TMEM accumulators are double-buffered).
+    const int scale_slots = a.stages + 2;
+    uint8_t *sKs = sK + (size_t)a.stages * kF8TileBytes;  // scale_slots x 128 positions x 4 scale bytes
+    uint32_t *sKeys = reinterpret_cast<uint32_t *>(sKs + (size_t)scale_slots * kTileM * 4);
+    float *sW = reinterpret_cast<float *>(sKeys + key_cap);
+    float *sQs = sW + kHI;                                // [64][4] 2^(q scale)
+    float *sPart = sQs + kHI * 4;                         // [2][128] per-half partial scores
+    uint32_t *sHist0 = reinterpret_cast<uint32_t *>(sPart + 2 * kTileM);
+    int32_t *sRows = reinterpret_cast<int32_t *>(sHist0 + kHist);
+    SelectSmem *ss = reinterpret_cast<SelectSmem *>(sRows + ((2 * a.tiles_cap + 3) & ~3));
+    F8Bars *bars = reinterpret_cast<F8Bars *>(ss + 1);
+
+    cg::cluster_group cluster = cg::this_cluster();
+    const int C = (int)cluster.num_blocks();
+    const int crank = (int)cluster.block_rank();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t0 = blockIdx.y;
+    if (t0 >= a.T) return;
+    const int b = find_seq(a.cu_q, a.B, t0);
+    const int nq_b = __ldg(a.cu_q + b + 1) - __ldg(a.cu_q + b);
+    const int pos_last = __ldg(a.seq_lens + b) - nq_b + (t0 - __ldg(a.cu_q + b));
+    const int n_total = pos_last + 1;
+    const int tiles_total = (n_total + kTileM - 1) / kTileM;
+    const int tpc = (tiles_total + C - 1) / C;
+    const int tile0 = min(tiles_total, crank * tpc);
+    int n_tiles = min(tiles_total, tile0 + tpc) - tile0;
+    if (n_tiles > a.tiles_cap) {
+        if (threadIdx.x == 0) report_error(a.err, kErrBadLen);
+        n_tiles = a.tiles_cap;
+    }
+    const int32_t *pt_row = a.page_table + (size_t)b * a.max_pages;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < a.stages; ++s) {
+            mbar_init(&bars->full[s], 1);
+            mbar_init(&bars->empty[s], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bars->tfull[i], 1);
+            mbar_init(&bars->tempty[i], 8);
+        }
+        mbar_init(&bars->qbar, 1);
+        mbar_init(&bars->drain, 1);
+        bars->abort = 0;
+        fence_mbar_init();
+    }
+    for (int i = threadIdx.x; i < kHI; i += kF8Threads) sW[i] = __ldg(a.head_w + (size_t)t0 * kHI + i);
+    for (int i = threadIdx.x; i < kHI * 4; i += kF8Threads)
+        sQs[i] = e8m0_value(__ldg(a.q_scale + (size_t)t0 * kHI * 4 + i));
+    for (int i = threadIdx.x; i < kHist; i += kF8Threads) sHist0[i] = 0u;
+    for (int j = threadIdx.x; j < 2 * n_tiles; j += kF8Threads) {
+        const int p0 = tile0 * kTileM + j * kBox;
+        int row = -1;
+        if (p0 <= pos_last) {
+            const int page = __ldg(pt_row + p0 / a.page_size);
+            if (page < 0 || (int64_t)page >= a.num_pages) report_error(a.err, kErrBadPage);
+            else row = page * a.page_size + p0 % a.page_size;
+        }
+        sRows[j] = row;
+    }
+    if (warp == 1) tmem_alloc(&bars->tmem_slot, 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_slot;
+    volatile int *abort = &bars->abort;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            tma_prefetch_desc(&tm_k);
+            tma_prefetch_desc(&tm_q);
+            mbar_arrive_expect_tx(&bars->qbar, (uint32_t)(kHI * kDI));
+            tma_load_2d(sQ, &tm_q, &bars->qbar, 0, t0 * kHI);
+            int issued = 0;
+            for (int i = 0; i < n_tiles; ++i) {
+                const int s = i % a.stages;
+                if (i >= a.stages && !mbar_wait(&bars->empty[s], ((i / a.stages) & 1) ^ 1, a.err, 0x121, abort))
+                    break;
+                issued = i + 1;
+                uint32_t bytes = 0;
+                for (int h = 0; h < 2; ++h)
+                    if (sRows[2 * i + h] >= 0) bytes += kF8BoxBytes + kBox * 4;
+                mbar_arrive_expect_tx(&bars->full[s], bytes);
+                for (int h = 0; h < 2; ++h) {
+                    const int row = sRows[2 * i + h];
+                    if (row < 0) continue;
+                    tma_load_2d(sK + (size_t)s * kF8TileBytes + h * kF8BoxBytes, &tm_k, &bars->full[s], 0, row);
+                    uint8_t *dst = sKs + (size_t)(i % scale_slots) * kTileM * 4 + h * kBox * 4;
+                    bulk_load(dst, a.k_scale + (size_t)row * 4, kBox * 4, &bars->full[s]);
+                }
+            }
+            if (*abort) {
+                volatile int no_abort = 0;
+                mbar_wait(&bars->qbar, 0, nullptr, 0, &no_abort);
+                for (int i = max(0, issued - a.stages); i < issued; ++i)
+                    mbar_wait(&bars->full[i % a.stages], (i / a.stages) & 1, nullptr, 0, &no_abort);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_e4m3_f32(kTileM, kHI);
+            bool ok = mbar_wait(&bars->qbar, 0, a.err, 0x221, abort);
+            const uint32_t q_base = smem_u32(sQ);
+            for (int i = 0; ok && i < n_tiles; ++i) {
+                const int s = i % a.stages, buf = i & 1;
+                if (!mbar_wait(&bars->full[s], (i / a.stages) & 1, a.err, 0x222, abort)) break;
+                if (i >= 2 && !mbar_wait(&bars->tempty[buf], ((i >> 1) & 1) ^ 1, a.err, 0x223, abort)) break;
+                tc_fence_after();
+                const uint32_t k_base = smem_u32(sK + (size_t)s * kF8TileBytes);
+#pragma unroll
+                for (int g = 0; g < 4; ++g)  // one scale group of 32 dims per MMA
+                    mma_f8_ss(tmem + (uint32_t)(buf * 256 + g * kHI), sdesc_kmajor_sw128(k_base + g * 32),
+                              sdesc_kmajor_sw128(q_base + g * 32), idesc, 0u);
+                mma_commit(&bars->empty[s]);
+                mma_commit(&bars->tfull[buf]);
+            }
+            if (*abort) {
+                volatile int no_abort = 0;
+                mma_commit(&bars->drain);
+                mbar_wait(&bars->drain, 0, nullptr, 0, &no_abort);
+            }
+        }
+    } else {
+        // epilogue: warp -> (TMEM lane quadrant, half of the heads)
+        const int quad = warp & 3, hh = (warp - 2) >> 2;
+        const int row = quad * 32 + lane;
+        bool ok = true;
+        for (int i = 0; i < n_tiles; ++i) {
+            const int buf = i & 1, slot = i % scale_slots;
+            ok = mbar_wait(&bars->tfull[buf], (i >> 1) & 1, a.err, 0x321, abort);
+            ok = bar_and(2, 256, ok);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t ks = *reinterpret_cast<const uint32_t *>(sKs + (size_t)slot * kTileM * 4 + row * 4);
+            float acc[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) acc[j] = 0.0f;
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                uint32_t r[32];
+                tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(buf * 256 + g * kHI + hh * 32), r);
+                tmem_wait_ld();
+                const float skg = e8m0_value((ks >> (8 * g)) & 0xFFu);
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    acc[j] = fmaf(__uint_as_float(r[j]), sQs[(hh * 32 + j) * 4 + g] * skg, acc[j]);
+            }
+            float part = 0.0f;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) part = fmaf(sW[hh * 32 + j], fmaxf(acc[j], 0.0f), part);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->tempty[buf]);
+            sPart[hh * kTileM + row] = part;
+            bar_sync(2, 256);
+            if (hh == 0) {
+                const float sc = sPart[row] + sPart[kTileM + row];
+                const int pos = (tile0 + i) * kTileM + row;
+                const bool valid = pos <= pos_last;
+                const uint32_t key = valid ? score_key(sc) : 0u;
+                sKeys[i * kTileM + row] = key;
+                if (valid) atomicAdd(&sHist0[key >> 24], 1u);
+                if (kWriteScores && valid && pos < a.ld_scores) a.scores[(size_t)t0 * a.ld_scores + pos] = sc;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, 512);
+    int32_t *out = a.indices + (size_t)t0 * a.K;
+    cluster_topk<kF8Threads>(sKeys, n_tiles * kTileM, tile0 * kTileM, n_total, a.K, out, *ss, sHist0);
 }
 
 // Top-K of given score rows (test hook and standalone selection).
@@ -506,7 +725,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_from_scores_kernel(TopkArgs 
     const float *row = a.scores + (size_t)r * a.ld;
     for (int l = threadIdx.x; l < nl; l += kThreads) sKeys[l] = score_key(__ldg(row + p0 + l));
     __syncthreads();
-    cluster_topk(sKeys, nl, p0, n, a.K, a.out + (size_t)r * a.K, *ss);
+    cluster_topk<kThreads>(sKeys, nl, p0, n, a.K, a.out + (size_t)r * a.K, *ss);
 }
 
 }  // namespace
@@ -519,6 +738,67 @@ size_t indexer_smem_bytes(int G, int stages, int tiles_cap) {
     size_t keys = (size_t)G * tiles_cap * kTileM * 4;
     size_t w = (size_t)G * kHI * 4 + (size_t)G * kHist * 4 + (size_t)((2 * tiles_cap + 3) & ~3) * 4;
     return 1024 + q + k + keys + w + sizeof(SelectSmem) + sizeof(IdxBars);
+}
+
+size_t indexer_mxfp8_smem_bytes(int stages, int tiles_cap) {
+    return 1024 + (size_t)kHI * kDI + (size_t)stages * kF8TileBytes + (size_t)(stages + 2) * kTileM * 4 +
+           (size_t)tiles_cap * kTileM * 4 +
+           (size_t)(kHI + kHI * 4 + 2 * kTileM + kHist) * 4 + (size_t)((2 * tiles_cap + 3) & ~3) * 4 +
+           sizeof(SelectSmem) + sizeof(F8Bars);
+}
+
+template <bool W>
+static cudaError_t launch_f8(const CUtensorMap &tk, const CUtensorMap &tq, const IndexerArgs &a, int C, size_t smem,
+                             cudaStream_t st) {
+    auto kern = indexer_topk_mxfp8_kernel<W>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    if (C > 8) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return e;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)C, (unsigned)a.T, 1);
+    cfg.blockDim = dim3(kF8Threads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, tk, tq, a);
+}
+
+cudaError_t launch_indexer_mxfp8(const CUtensorMap &tm_k, const CUtensorMap &tm_q, const IndexerArgs &a, int C,
+                                 size_t smem, bool write_scores, cudaStream_t st) {
+    return write_scores ? launch_f8<true>(tm_k, tm_q, a, C, smem, st) : launch_f8<false>(tm_k, tm_q, a, C, smem, st);
+}
+
+int indexer_mxfp8_max_active_clusters(int C, size_t smem) {
+    auto kern = indexer_topk_mxfp8_kernel<false>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return 0;
+    if (C > 8 && cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+        return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)C, 1, 1);
+    cfg.blockDim = dim3(kF8Threads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return n;
 }
 
 size_t topk_smem_bytes(int chunk_cap) { return 16 + (size_t)((chunk_cap + 3) & ~3) * 4 + sizeof(SelectSmem); }

@@ -12,6 +12,8 @@ namespace dsa {
 // Fused indexer + Top-K (indexer_topk.cu).
 struct IndexerArgs {
     const float *head_w;        // [T, 64]
+    const uint8_t *q_scale;     // MXFP8: [T, 64, 4] e8m0
+    const uint8_t *k_scale;     // MXFP8: [rows, 4] e8m0
     const int32_t *page_table;  // [B, max_pages]
     const int32_t *seq_lens;    // [B]
     const int32_t *cu_q;        // [B+1]
@@ -43,6 +45,11 @@ cudaError_t launch_topk_from_scores(const TopkArgs &a, int C, size_t smem, cudaS
 // Clusters of C CTAs of the G-query indexer kernel with `smem` bytes that can
 // be resident at once (0 if the shape cannot launch).
 int indexer_max_active_clusters(int G, int C, size_t smem);
+// MXFP8 variant (one query row per cluster).
+size_t indexer_mxfp8_smem_bytes(int stages, int tiles_cap);
+cudaError_t launch_indexer_mxfp8(const CUtensorMap &tm_k, const CUtensorMap &tm_q, const IndexerArgs &a, int C,
+                                 size_t smem, bool write_scores, cudaStream_t st);
+int indexer_mxfp8_max_active_clusters(int C, size_t smem);
 
 // Sparse MLA (sparse_mla.cu).
 struct MlaArgs {
@@ -71,5 +78,10 @@ int mla_key_tile();
 // NH = heads per CTA (16, 32 or 64; H must be a multiple).  tm_q: 2D map of
 // q [T*H, 576] bf16, box 64 x NH, 128-byte swizzle.
 cudaError_t launch_sparse_mla_bf16(const CUtensorMap &tm_q, const MlaArgs &a, int NH, cudaStream_t st);
+
+// Quantisers (quant.cu).
+cudaError_t launch_quant_mxfp8(const uint16_t *x, int64_t n, uint8_t *q, uint8_t *e8m0, cudaStream_t st);
+cudaError_t launch_quant_fp8_rows(const uint16_t *kv, int64_t rows, uint8_t *nope, uint16_t *rope, float *scale,
+                                  cudaStream_t st);
 
 }  // namespace dsa
