@@ -236,6 +236,18 @@ def dsa_sparse_mla(q, kv_cache, page_table, seq_lens, cu_q, indices, scale, *, o
     if D != 576:
         raise ValueError("q must be [T, H, 576]")
     _need(kv_cache, "kv_cache", torch.bfloat16 if dt == 0 else torch.uint8, 3, dev)
+    if dt == 1:
+        _need(kv_rope, "kv_rope", torch.bfloat16, 3, dev)
+        _need(kv_scale, "kv_scale", torch.float32, 2, dev)
+        pp, pps = kv_cache.shape[0], kv_cache.shape[1]
+        if (kv_cache.shape[2] != 512 or tuple(kv_rope.shape) != (pp, pps, 64)
+                or tuple(kv_scale.shape) != (pp, pps)):
+            raise ValueError("FP8 cache: kv_cache [pages, page_size, 512] e4m3, kv_rope [.., 64] bf16, "
+                             "kv_scale [pages, page_size] fp32")
+    elif kv_rope is not None or kv_scale is not None:
+        raise ValueError("kv_rope / kv_scale are for dtype='fp8_rowscale' only")
+    elif kv_cache.shape[2] != 576:
+        raise ValueError("kv_cache must be [pages, page_size, 576] bf16")
     _need(page_table, "page_table", torch.int32, 2, dev)
     _need(seq_lens, "seq_lens", torch.int32, 1, dev)
     _need(cu_q, "cu_q", torch.int32, 1, dev)

@@ -430,8 +430,6 @@ dsa_status dsa_sparse_mla(const void *q, const void *kv_cache, const void *kv_ro
                           const int32_t *seq_lens, const int32_t *cu_q, const int32_t *indices, int32_t B,
                           int32_t T, int32_t H, int32_t K, float scale, int32_t page_size, dsa_kv_dtype dtype,
                           void *out, float *lse, void *workspace, size_t workspace_bytes, void *stream) {
-    (void)kv_rope;
-    (void)kv_scale;
     if (T < 0 || B < 1 || K < 1 || H < 1 || page_size < 1 || num_pages < 1 || max_pages_per_seq < 1)
         return DSA_ERR_INVALID_ARG;
     if (!q || !kv_cache || !page_table || !seq_lens || !cu_q || !indices || !out || !workspace)
@@ -441,7 +439,10 @@ dsa_status dsa_sparse_mla(const void *q, const void *kv_cache, const void *kv_ro
     const int NH = mla_heads_per_cta(H);
     if (NH == 0 || H > 1024 || T > 65535) return DSA_ERR_UNSUPPORTED;
     if ((long long)num_pages * page_size > (1LL << 31)) return DSA_ERR_UNSUPPORTED;
-    if (dtype != DSA_KV_BF16) return DSA_ERR_UNSUPPORTED;
+    if (dtype != DSA_KV_BF16 && dtype != DSA_KV_FP8_ROWSCALE) return DSA_ERR_UNSUPPORTED;
+    const bool fp8 = dtype == DSA_KV_FP8_ROWSCALE;
+    if (fp8 && (!kv_rope || !kv_scale || !aligned16(kv_rope) || (reinterpret_cast<uintptr_t>(kv_scale) & 3u)))
+        return DSA_ERR_INVALID_ARG;
     if (workspace_bytes < dsa_sparse_mla_workspace_size(T, H, K)) return DSA_ERR_INVALID_ARG;
     if (T == 0) return DSA_OK;
     const int splits = mla_splits(T, H, K);
@@ -449,6 +450,8 @@ dsa_status dsa_sparse_mla(const void *q, const void *kv_cache, const void *kv_ro
     MlaArgs a{};
     a.q = static_cast<const uint16_t *>(q);
     a.kv = static_cast<const uint8_t *>(kv_cache);
+    a.kv_rope = fp8 ? static_cast<const uint8_t *>(kv_rope) : nullptr;
+    a.kv_scale = fp8 ? kv_scale : nullptr;
     a.page_table = page_table;
     a.seq_lens = seq_lens;
     a.cu_q = cu_q;
@@ -472,7 +475,7 @@ dsa_status dsa_sparse_mla(const void *q, const void *kv_cache, const void *kv_ro
     a.scale_log2 = scale * 1.4426950408889634f;
     CUtensorMap tq;
     if (!encode_2d_bf16(&tq, q, 576, (uint64_t)T * H, (uint32_t)NH)) return DSA_ERR_CUDA;
-    return cuda_status(dsa::launch_sparse_mla_bf16(tq, a, NH, static_cast<cudaStream_t>(stream)));
+    return cuda_status(dsa::launch_sparse_mla(tq, a, NH, fp8, static_cast<cudaStream_t>(stream)));
 }
 
 dsa_status dsa_quant_mxfp8(const void *x, int64_t n, void *q, void *e8m0, void *stream) {

@@ -54,7 +54,9 @@ int indexer_mxfp8_max_active_clusters(int C, size_t smem);
 // Sparse MLA (sparse_mla.cu).
 struct MlaArgs {
     const uint16_t *q;          // [T, H, 576] bf16
-    const uint8_t *kv;          // [num_pages*page_size, 576] bf16 rows
+    const uint8_t *kv;          // [num_pages*page_size, 576] bf16 rows, or [.., 512] E4M3 (FP8 rows)
+    const uint8_t *kv_rope;     // FP8 rows: [num_pages*page_size, 64] bf16 rope dims
+    const float *kv_scale;      // FP8 rows: [num_pages*page_size] fp32 row scales
     const int32_t *page_table;  // [B, max_pages]
     const int32_t *seq_lens;    // [B]
     const int32_t *cu_q;        // [B+1]
@@ -77,7 +79,9 @@ size_t mla_smem_bytes(int NH);
 int mla_key_tile();
 // NH = heads per CTA (16, 32 or 64; H must be a multiple).  tm_q: 2D map of
 // q [T*H, 576] bf16, box 64 x NH, 128-byte swizzle.
-cudaError_t launch_sparse_mla_bf16(const CUtensorMap &tm_q, const MlaArgs &a, int NH, cudaStream_t st);
+// fp8: the cache holds E4M3 latent dims with one fp32 scale per row (kv,
+// kv_rope, kv_scale), dequantised to bf16 on the way into shared memory.
+cudaError_t launch_sparse_mla(const CUtensorMap &tm_q, const MlaArgs &a, int NH, bool fp8, cudaStream_t st);
 
 // Quantisers (quant.cu).
 cudaError_t launch_quant_mxfp8(const uint16_t *x, int64_t n, uint8_t *q, uint8_t *e8m0, cudaStream_t st);

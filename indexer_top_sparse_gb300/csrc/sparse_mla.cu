@@ -9,19 +9,25 @@
 // are never read.
 //
 // Design (tcgen05, accumulators in TMEM).  CTA = (group of NH <= 64 heads,
-// key split, query row); selected keys are processed in tiles of 32, four
-// tiles in flight (a ring of shared-memory buffers).
-//   warps 0-7   gather (tiles of 32 keys, 4 in flight): 16-byte cp.async copies (coalesced 128-byte row
-//               segments) place each selected 576-wide bf16 row, resolved
-//               through the page table, into nine 64-column regions in the
-//               128-byte-swizzle layout; thousands of requests in flight.
-//   warp 8      tcgen05 issuer: S[64 heads x 32 keys] = Q . K_tile^T (M = 64,
-//               K-major operands, 36 steps of K = 16; double-buffered in
-//               TMEM, the next tile's S is issued before this tile's P*V),
-//               then O^T[512 dims x NH] += V^T . P^T with V^T read MN-major
-//               from the same tile and P^T MN-major (4 chunks of 128 dims,
-//               2 steps of 16 keys).
-//   warps 9-12  softmax: thread = head (M = 64 places rows 16q..16q+15 in the
+// key split, query row); selected keys are processed in tiles of 64, two
+// tiles in flight (a ring of shared-memory buffers).  With 128 heads the two
+// 64-head CTAs of a query row form a cluster: each gathers half of every tile
+// and forwards it to the other over distributed shared memory, so that every
+// selected row is read from memory once.
+//   warps 0-7   gather: every selected key of the split is first resolved to
+//               its physical cache row (one table, built up front); then
+//               16-byte cp.async copies place each 576-wide bf16 row into nine
+//               64-column regions in the 128-byte-swizzle layout.  For the FP8
+//               cache the 512 E4M3 latent dims go through registers (loaded a
+//               tile ahead), are multiplied by the row scale and stored as
+//               bf16; the rope dims are copied as they are.
+//   warp 8      tcgen05 issuer: S[64 heads x 64 keys] = Q . K_tile^T (M = 64,
+//               K-major operands, 36 steps of K = 16, double-buffered in
+//               TMEM), then O^T[512 dims x 64] += V^T . P^T with V^T read
+//               MN-major from the same tile and P^T MN-major (4 chunks of 128
+//               dims, 4 steps of 16 keys).
+//   warp 9      (pairs) forwards this CTA's half tiles to the peer.
+//   warps 10-13 softmax: thread = head (M = 64 places rows 16q..16q+15 in the
 //               low 16 lanes of warp quadrant q), so max, exp2 and sum over
 //               the tile's keys stay in registers; the reference max moves
 //               only when a head's max grows by more than 2^8, and then the
@@ -31,6 +37,8 @@
 // With several key splits per row, partial (O, max, sum) go to the workspace
 // and mla_combine_kernel merges them.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <math_constants.h>
 
 #include "ptx.cuh"
@@ -121,6 +129,22 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
+// 16 E4M3 latent values (one lane's 16 bytes of a row) times the row scale,
+// as 8 words of bf16 pairs (low half = lower dim).  E4M3 -> f16 -> f32 is
+// exact; the product is rounded once, to bf16.
+__device__ __forceinline__ void dequant16(const uint4 v, const float s, uint32_t out[8]) {
+    const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const __half2_raw r = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(in[i] >> (16 * h)), __NV_E4M3);
+            const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&r));
+            out[2 * i + h] = pack_bf16(f.x * s, f.y * s);
+        }
+    }
+}
+
 // Issue S = Q . K_tile^T for tile i into S buffer i&1 once the tile landed.
 __device__ __forceinline__ bool issue_s_tile(int i, MlaBars *bars, uint32_t kv_base, uint32_t q_base, uint32_t tmem_s,
                                              uint32_t idesc_s, uint32_t *err, volatile int *abort) {
@@ -144,7 +168,9 @@ __device__ __forceinline__ bool issue_s_tile(int i, MlaBars *bars, uint32_t kv_b
 // kPair: the two 64-head CTAs of a query row form a cluster; each gathers half
 // of every tile (from global memory) and forwards it to the other's shared
 // memory, so that each selected row is read from L2/HBM once.
-template <int NH, bool kPair>
+// kF8: the cache holds E4M3 latent dims + an fp32 scale per row + bf16 rope
+// dims; the gather warps dequantise the latent dims to bf16 through registers.
+template <int NH, bool kPair, bool kF8>
 __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, MlaArgs a) {
     using L = MlaLayout<NH>;
     extern __shared__ uint8_t smem_raw[];
@@ -164,12 +190,15 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
     const int32_t *idx_row = a.indices + (size_t)t * a.K;
 
     if (threadIdx.x == 0) {
+        // a gather warp's part of a tile: one cp.async completion arrival per
+        // lane, plus (FP8) one arrival per warp after its dequantised stores
+        constexpr int kGatherArrivals = 32 * kProd + (kF8 ? kProd : 0);
         for (int i = 0; i < kStages; ++i) {
-            // unpaired: one cp.async completion arrival per gather lane; paired:
-            // the sender's arrival, plus the peer's half counted in bytes
-            mbar_init(&bars->kv_full[i], kPair ? 1 : 32 * kProd);
+            // unpaired: the gather arrivals; paired: the sender's arrival, plus
+            // the peer's half counted in bytes
+            mbar_init(&bars->kv_full[i], kPair ? 1 : kGatherArrivals);
             mbar_init(&bars->kv_empty[i], 1);
-            mbar_init(&bars->half_ready[i], 32 * kProd);
+            mbar_init(&bars->half_ready[i], kGatherArrivals);
             mbar_init(&bars->peer_free[i], 1);
         }
         for (int i = 0; i < 2; ++i) mbar_init(&bars->s_full[i], 1);
@@ -242,6 +271,21 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
         }
         bar_sync(kBarProd, kProd * 32);  // gather warps only
         if (threadIdx.x == 0) mbar_arrive(&bars->table);  // publishes the row / validity table
+        // FP8: lane l holds bytes 16l..16l+15 (dims 16l..16l+15) of each of
+        // the warp's keys, loaded one tile ahead so that the loads overlap the
+        // wait for a free stage
+        uint4 f8v[kF8 ? kKPW : 1];
+        float f8s[kF8 ? kKPW : 1];
+        if constexpr (kF8) {
+            if (n_tiles > 0) {
+#pragma unroll
+                for (int j = 0; j < kKPW; ++j) {
+                    const int row = st->rows[key0 + j];
+                    f8v[j] = __ldg(reinterpret_cast<const uint4 *>(a.kv + (size_t)row * kDv) + lane);
+                    f8s[j] = __ldg(a.kv_scale + row);
+                }
+            }
+        }
         for (int i = 0; i < n_tiles; ++i) {
             const int stg = i % kStages;
             bool ok = true;
@@ -251,16 +295,54 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
             if (kPair && threadIdx.x == 0) mbar_arrive_remote(map_peer(smem_u32(&bars->peer_free[stg]), peer));
             uint8_t *dst = sKV + stg * kTileBytes;
             const int32_t *rows = st->rows + i * kKeys;
+            uint64_t *done = kPair ? &bars->half_ready[stg] : &bars->kv_full[stg];
+            if constexpr (!kF8) {
 #pragma unroll 3
-            for (int r = 0; r < kRegions; ++r) {
+                for (int r = 0; r < kRegions; ++r) {
+#pragma unroll
+                    for (int m = 0; m < kKPW * 8 / 32; ++m) {
+                        const int f = m * 32 + lane, key = key0 + (f >> 3), cc = f & 7;
+                        const uint8_t *src = a.kv + (size_t)rows[key] * (kD * 2) + r * 128 + cc * 16;
+                        cp_async16(dst + r * kRegionBytes + key * 128 + ((cc ^ (key & 7)) << 4), src);
+                    }
+                }
+                cp_async_arrive(done);
+            } else {
+                // rope dims (bf16) straight into region 8
 #pragma unroll
                 for (int m = 0; m < kKPW * 8 / 32; ++m) {
                     const int f = m * 32 + lane, key = key0 + (f >> 3), cc = f & 7;
-                    const uint8_t *src = a.kv + (size_t)rows[key] * (kD * 2) + r * 128 + cc * 16;
-                    cp_async16(dst + r * kRegionBytes + key * 128 + ((cc ^ (key & 7)) << 4), src);
+                    cp_async16(dst + 8 * kRegionBytes + key * 128 + ((cc ^ (key & 7)) << 4),
+                               a.kv_rope + (size_t)rows[key] * 128 + cc * 16);
+                }
+                cp_async_arrive(done);
+                // latent dims: lane l fills 16-byte chunks 2(l%4), 2(l%4)+1 of
+                // region l/4; odd regions store the odd chunk first, so each
+                // store instruction covers all eight chunk positions (banks)
+                const int r = lane >> 2, c0 = (lane & 3) * 2, flip = r & 1;
+#pragma unroll
+                for (int j = 0; j < kKPW; ++j) {
+                    const int key = key0 + j;
+                    uint32_t w[8];
+                    dequant16(f8v[j], f8s[j], w);
+                    uint8_t *base = dst + r * kRegionBytes + key * 128;
+                    const uint4 lo = make_uint4(w[0], w[1], w[2], w[3]), hi = make_uint4(w[4], w[5], w[6], w[7]);
+                    *reinterpret_cast<uint4 *>(base + (((c0 + flip) ^ (key & 7)) << 4)) = flip ? hi : lo;
+                    *reinterpret_cast<uint4 *>(base + (((c0 + 1 - flip) ^ (key & 7)) << 4)) = flip ? lo : hi;
+                }
+                fence_proxy_async_smem();  // the tensor cores (or the pair copy) read these stores
+                __syncwarp();
+                if (lane == 0) mbar_arrive(done);
+                if (i + 1 < n_tiles) {
+                    const int32_t *nrows = rows + kKeys;
+#pragma unroll
+                    for (int j = 0; j < kKPW; ++j) {
+                        const int row = nrows[key0 + j];
+                        f8v[j] = __ldg(reinterpret_cast<const uint4 *>(a.kv + (size_t)row * kDv) + lane);
+                        f8s[j] = __ldg(a.kv_scale + row);
+                    }
                 }
             }
-            cp_async_arrive(kPair ? &bars->half_ready[stg] : &bars->kv_full[stg]);
         }
         cp_async_wait_all();  // the CTA stays alive until every copy has landed
         if (warp == 0 && lane == 0 && *abort) {
@@ -517,10 +599,10 @@ size_t mla_smem_bytes(int NH) {
 }
 int mla_key_tile() { return kKeys; }
 
-template <int NH, bool kPair>
+template <int NH, bool kPair, bool kF8>
 static cudaError_t launch_tc(const CUtensorMap &tq, const MlaArgs &a, cudaStream_t st) {
     const size_t smem = mla_smem_bytes(NH);
-    auto kern = sparse_mla_tc_kernel<NH, kPair>;
+    auto kern = sparse_mla_tc_kernel<NH, kPair, kF8>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -538,13 +620,17 @@ static cudaError_t launch_tc(const CUtensorMap &tq, const MlaArgs &a, cudaStream
     return cudaLaunchKernelEx(&cfg, kern, tq, a);
 }
 
-cudaError_t launch_sparse_mla_bf16(const CUtensorMap &tq, const MlaArgs &a, int NH, cudaStream_t st) {
-    cudaError_t e;
-    if (NH == 64 && a.H == 128) e = launch_tc<64, true>(tq, a, st);
-    else if (NH == 64) e = launch_tc<64, false>(tq, a, st);
-    else if (NH == 32) e = launch_tc<32, false>(tq, a, st);
-    else if (NH == 16) e = launch_tc<16, false>(tq, a, st);
-    else return cudaErrorInvalidValue;
+template <bool kF8>
+static cudaError_t launch_heads(const CUtensorMap &tq, const MlaArgs &a, int NH, cudaStream_t st) {
+    if (NH == 64 && a.H == 128) return launch_tc<64, true, kF8>(tq, a, st);
+    if (NH == 64) return launch_tc<64, false, kF8>(tq, a, st);
+    if (NH == 32) return launch_tc<32, false, kF8>(tq, a, st);
+    if (NH == 16) return launch_tc<16, false, kF8>(tq, a, st);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_sparse_mla(const CUtensorMap &tq, const MlaArgs &a, int NH, bool fp8, cudaStream_t st) {
+    const cudaError_t e = fp8 ? launch_heads<true>(tq, a, NH, st) : launch_heads<false>(tq, a, NH, st);
     if (e != cudaSuccess || a.splits == 1) return e;
     mla_combine_kernel<<<dim3(kHG, a.H / NH, a.T), 128, 0, st>>>(a, NH);
     return cudaGetLastError();

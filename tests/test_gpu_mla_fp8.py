@@ -1,0 +1,88 @@
+"""GPU sparse MLA on the FP8 latent cache (E4M3 latent dims with one fp32
+scale per row, bf16 rope dims) against the oracle fed the same FP8 codes.
+The bar is the bf16 path's 2e-2 absolute / 1e-2 relative, tighter than the
+6e-2 / 3e-2 allowed for FP8: the kernel's only extra rounding is the bf16 of
+each dequantised value.  (The E4M3 rounding itself, FP8 cache against the
+unquantised cache, is not a kernel error and is not tested here.)"""
+import numpy as np
+import pytest
+import torch
+
+from _util import dev, dev_bf16
+from indexer_top_sparse_gb300.inputs import make_workload
+
+pytestmark = pytest.mark.gpu
+
+
+def _random_indices(rng, wl, K, pad_frac=0.0):
+    pos = wl.query_pos()
+    idx = np.full((wl.T, K), -1, np.int32)
+    for t in range(wl.T):
+        n = int(pos[t]) + 1
+        m = min(K, n)
+        sel = np.sort(rng.choice(n, m, replace=False)).astype(np.int32)
+        if pad_frac:
+            sel[rng.random(m) < pad_frac] = -1
+        idx[t, :m] = sel
+    return idx
+
+
+def _run(wl, nope, rope, sc, idx):
+    import indexer_top_sparse_gb300 as d
+    lse = torch.empty((wl.T, wl.H), dtype=torch.float32, device="cuda")
+    ws = d.Workspace(d.sparse_mla_workspace_size(wl.T, wl.H, idx.shape[1]))
+    out = d.dsa_sparse_mla(dev_bf16(wl.q), dev(nope), dev(wl.page_table), dev(wl.seq_lens), dev(wl.cu_q), dev(idx),
+                           wl.scale, lse=lse, workspace=ws, kv_rope=dev_bf16(rope), kv_scale=dev(sc),
+                           dtype="fp8_rowscale")
+    ws.check()
+    return out.float().cpu().numpy(), lse.cpu().numpy()
+
+
+def _compare(orc, wl, idx):
+    nope, rope, sc = orc.quant_fp8_rows(wl.kv)
+    out, lse = _run(wl, nope, rope, sc, idx)
+    ref, ref_lse = orc.sparse_mla(wl.q, nope, wl.page_table, wl.cu_q, idx, wl.scale, wl.page_size,
+                                  dtype=orc.KV_FP8_ROWSCALE, kv_rope=rope, kv_scale=sc)
+    np.testing.assert_allclose(out, ref, atol=2e-2, rtol=1e-2)
+    fin = np.isfinite(ref_lse)
+    np.testing.assert_allclose(lse[fin], ref_lse[fin], rtol=1e-3, atol=1e-3)
+    assert np.all(np.isneginf(lse[~fin]))
+
+
+@pytest.mark.parametrize("H", [16, 64, 128])
+def test_fp8_decode_heads(orc, H):
+    rng = np.random.default_rng(200 + H)
+    wl = make_workload("mla8", [3000, 513, 70], [1, 1, 1], H=H, K=512, page_size=64, seed=200 + H, with_idx=False)
+    _compare(orc, wl, _random_indices(rng, wl, 512))
+
+
+@pytest.mark.parametrize("H", [64, 128])
+@pytest.mark.parametrize("splits", [1, 3])
+def test_fp8_splits_and_padding(orc, splits, H):
+    import indexer_top_sparse_gb300 as d
+    rng = np.random.default_rng(300 + splits)
+    wl = make_workload("mla8", [4000, 900], [1, 1], H=H, K=1000, page_size=64, seed=300 + splits, with_idx=False)
+    idx = _random_indices(rng, wl, 1000, pad_frac=0.1)
+    d.set_tuning("mla_splits", splits)
+    try:
+        _compare(orc, wl, idx)
+    finally:
+        d.set_tuning("mla_splits", 0)
+
+
+def test_fp8_zero_rows_and_wide_scales(orc):
+    # all-zero latent rows (scale 1) and rows whose magnitudes span 2^-8..2^8
+    from indexer_top_sparse_gb300.inputs import bf16_bits, bf16_to_f32
+    rng = np.random.default_rng(9)
+    wl = make_workload("mla8", [1500], [1], H=32, K=600, page_size=64, seed=9, with_idx=False)
+    kv = bf16_to_f32(wl.kv).reshape(-1, 576)
+    kv[::7, :512] = 0.0
+    kv[3::7, :512] *= np.float32(2.0) ** rng.integers(-8, 9, (kv[3::7].shape[0], 1)).astype(np.float32)
+    wl.kv = bf16_bits(kv.reshape(wl.kv.shape).astype(np.float32))
+    wl.scale = 0.002
+    nope, rope, sc = orc.quant_fp8_rows(wl.kv)
+    idx = _random_indices(rng, wl, 600)
+    out, _ = _run(wl, nope, rope, sc, idx)
+    ref, _ = orc.sparse_mla(wl.q, nope, wl.page_table, wl.cu_q, idx, wl.scale, wl.page_size,
+                            dtype=orc.KV_FP8_ROWSCALE, kv_rope=rope, kv_scale=sc)
+    np.testing.assert_allclose(out, ref, atol=2e-2 * max(1.0, np.abs(ref).max()), rtol=1e-2)
