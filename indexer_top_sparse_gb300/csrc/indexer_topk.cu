@@ -290,6 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int C = (int)cluster.num_blocks();
     const int crank = (int)cluster.block_rank();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    grid_dep_wait();  // inputs written by the kernel launched just before are visible
 
     // ---- which query rows this cluster serves
     int b, t0, gn;
@@ -477,6 +478,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tmem, L::kTmemCols);
+    if (threadIdx.x == 0) grid_dep_launch();  // scoring is done: the next kernel may begin launching
     // A CTA that gave up on a wait (its keys are then incomplete; the error is
     // recorded) still runs the selection: every CTA of the cluster must pass
     // the same sequence of cluster barriers, which depends only on
@@ -549,6 +551,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t0 = blockIdx.y;
     if (t0 >= a.T) return;
+    grid_dep_wait();  // inputs written by the kernel launched just before are visible
     const int b = find_seq(a.cu_q, a.B, t0);
     const int nq_b = __ldg(a.cu_q + b + 1) - __ldg(a.cu_q + b);
     const int pos_last = __ldg(a.seq_lens + b) - nq_b + (t0 - __ldg(a.cu_q + b));
@@ -702,6 +705,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
     __syncthreads();
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tmem, 512);
+    if (threadIdx.x == 0) grid_dep_launch();  // scoring is done: the next kernel may begin launching
     int32_t *out = a.indices + (size_t)t0 * a.K;
     cluster_topk<kF8Threads>(sKeys, n_tiles * kTileM, tile0 * kTileM, n_total, a.K, out, *ss, sHist0);
 }
@@ -762,13 +766,15 @@ static cudaError_t launch_f8(const CUtensorMap &tk, const CUtensorMap &tq, const
     cfg.blockDim = dim3(kF8Threads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = (unsigned)C;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, kern, tk, tq, a);
 }
 
@@ -818,13 +824,15 @@ static cudaError_t launch_idx(const CUtensorMap &tk, const CUtensorMap &tq, cons
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = (unsigned)C;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, kern, tk, tq, a);
 }
 

@@ -26,8 +26,9 @@
 //               TMEM), then O^T[512 dims x 64] += V^T . P^T with V^T read
 //               MN-major from the same tile and P^T MN-major (4 chunks of 128
 //               dims, 4 steps of 16 keys).
-//   warp 9      (pairs) forwards this CTA's half tiles to the peer.
-//   warps 10-13 softmax: thread = head (M = 64 places rows 16q..16q+15 in the
+//               With pairs, each gather warp forwards its rows to the peer
+//               (bulk shared-to-shared copies) as soon as they have landed.
+//   warps 9-12  softmax: thread = head (M = 64 places rows 16q..16q+15 in the
 //               low 16 lanes of warp quadrant q), so max, exp2 and sum over
 //               the tile's keys stay in registers; the reference max moves
 //               only when a head's max grows by more than 2^8, and then the
@@ -51,11 +52,8 @@ namespace {
 constexpr int kD = 576;
 constexpr int kDv = 512;
 constexpr int kHG = 64;                      // head-slot stride of the partial layout
-#ifndef MLA_TILE_KEYS
-#define MLA_TILE_KEYS 64
-#endif
-constexpr int kKeys = MLA_TILE_KEYS;         // keys per tile (MMA N of S): 32 or 64
-constexpr int kStages = kKeys == 32 ? 4 : 2; // tiles in flight
+constexpr int kKeys = 64;                    // keys per tile (MMA N of S; P rows are 128 bytes)
+constexpr int kStages = 2;                   // tiles in flight
 constexpr int kRegions = 9;                  // 64-dim regions of a 576-wide row
 constexpr int kRegionBytes = kKeys * 128;    // 4 or 8 KB
 constexpr int kTileBytes = kRegions * kRegionBytes;
@@ -65,14 +63,12 @@ constexpr int kQRegion = 64 * 128;           // Q rows padded to the MMA's M = 6
 #endif
 constexpr int kProd = MLA_PRODUCER_WARPS;
 constexpr int kMmaWarp = kProd;
-constexpr int kSendWarp = kProd + 1;         // pairs only: forwards this CTA's half tiles to the peer
-constexpr int kSmWarp0 = kProd + 2;          // 4 softmax / epilogue warps
-constexpr int kThreads = (kProd + 2 + 4) * 32;
+constexpr int kSmWarp0 = kProd + 1;          // 4 softmax / epilogue warps
+constexpr int kThreads = (kProd + 1 + 4) * 32;
 constexpr int kSmThreads = 128;
 constexpr int kBarSm = 1;
 constexpr int kBarProd = 2;
 static_assert(kKeys % kProd == 0, "gather work splits evenly");
-static_assert(kKeys == 32 || kKeys == 64, "tiles of 32 or 64 keys");
 constexpr int kWords = kKeys / 32;           // validity words per tile
 
 template <int NH>
@@ -84,7 +80,6 @@ struct MlaLayout {
 
 struct __align__(16) MlaBars {
     uint64_t kv_full[kStages], kv_empty[kStages], s_full[2];
-    uint64_t half_ready[kStages];  // pairs: this CTA's half of the tile landed
     uint64_t peer_free[kStages];   // pairs: the peer's copy of this stage may be overwritten
     uint64_t p_full, o_done, o_full, q_full, drain, table;
     uint32_t tmem_slot;
@@ -152,14 +147,16 @@ __device__ __forceinline__ bool issue_s_tile(int i, MlaBars *bars, uint32_t kv_b
     if (!mbar_wait(&bars->kv_full[st], (i / kStages) & 1, err, 0x503, abort)) return false;
     fence_proxy_async_smem();  // the tile was written through the generic proxy
     tc_fence_after();
-    const uint32_t kb = kv_base + st * kTileBytes;
+    // descriptors advance by (byte offset >> 4) in their start-address field
+    const uint64_t ad0 = sdesc_kmajor_sw128(q_base);
+    const uint64_t bd0 = sdesc_kmajor_sw128(kv_base + st * kTileBytes);
+    const uint32_t d = tmem_s + kKeys * (i & 1);
+#pragma unroll
     for (int r = 0; r < kRegions; ++r) {
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t ad = sdesc_kmajor_sw128(q_base + r * kQRegion + kk * 32);
-            const uint64_t bd = sdesc_kmajor_sw128(kb + r * kRegionBytes + kk * 32);
-            mma_bf16_ss(tmem_s + kKeys * (i & 1), ad, bd, idesc_s, (r | kk) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < 4; ++kk)
+            mma_bf16_ss(d, ad0 + (uint64_t)((r * kQRegion + kk * 32) >> 4),
+                        bd0 + (uint64_t)((r * kRegionBytes + kk * 32) >> 4), idesc_s, (r | kk) ? 1u : 0u);
     }
     mma_commit(&bars->s_full[i & 1]);
     return true;
@@ -185,20 +182,22 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
     const int k_begin = split * a.keys_per_split;
     const int k_end = min(a.K, k_begin + a.keys_per_split);
     const int n_tiles = k_end > k_begin ? (k_end - k_begin + kKeys - 1) / kKeys : 0;
+    // Inputs may come from the kernel launched just before this one (the
+    // indexer's indices, or a caller's kernel); with programmatic dependent
+    // launch this kernel starts early and waits here until they are visible.
+    grid_dep_wait();
     const int b = find_seq(a.cu_q, a.B, t);
     const int pos = __ldg(a.seq_lens + b) - (__ldg(a.cu_q + b + 1) - __ldg(a.cu_q + b)) + (t - __ldg(a.cu_q + b));
     const int32_t *idx_row = a.indices + (size_t)t * a.K;
 
     if (threadIdx.x == 0) {
-        // a gather warp's part of a tile: one cp.async completion arrival per
-        // lane, plus (FP8) one arrival per warp after its dequantised stores
-        constexpr int kGatherArrivals = 32 * kProd + (kF8 ? kProd : 0);
+        // a tile is complete after one cp.async completion arrival per gather
+        // lane, (FP8) one arrival per gather warp after its dequantised
+        // stores, and (pairs) one arrival that expects the peer's half in bytes
+        constexpr int kFullArrivals = 32 * kProd + (kF8 ? kProd : 0) + (kPair ? 1 : 0);
         for (int i = 0; i < kStages; ++i) {
-            // unpaired: the gather arrivals; paired: the sender's arrival, plus
-            // the peer's half counted in bytes
-            mbar_init(&bars->kv_full[i], kPair ? 1 : kGatherArrivals);
+            mbar_init(&bars->kv_full[i], kFullArrivals);
             mbar_init(&bars->kv_empty[i], 1);
-            mbar_init(&bars->half_ready[i], kGatherArrivals);
             mbar_init(&bars->peer_free[i], 1);
         }
         for (int i = 0; i < 2; ++i) mbar_init(&bars->s_full[i], 1);
@@ -271,6 +270,22 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
         }
         bar_sync(kBarProd, kProd * 32);  // gather warps only
         if (threadIdx.x == 0) mbar_arrive(&bars->table);  // publishes the row / validity table
+        // Prefetch this warp's rows of every tile past the first kStages into
+        // L2, in tile order, so that the copies into a freed buffer wait for
+        // L2 rather than for the memory.
+        for (int k = lane; k < n_tiles * kKPW; k += 32) {
+            const int tile = k / kKPW;
+            if (tile < kStages) continue;
+            const int key = tile * kKeys + key0 + k % kKPW;
+            if (!((st->valid[key >> 5] >> (key & 31)) & 1u)) continue;
+            const size_t row = (size_t)st->rows[key];
+            if constexpr (kF8) {
+                prefetch_l2_bulk(a.kv + row * kDv, kDv);
+                prefetch_l2_bulk(a.kv_rope + row * 128, 128);
+            } else {
+                prefetch_l2_bulk(a.kv + row * (kD * 2), kD * 2);
+            }
+        }
         // FP8: lane l holds bytes 16l..16l+15 (dims 16l..16l+15) of each of
         // the warp's keys, loaded one tile ahead so that the loads overlap the
         // wait for a free stage
@@ -291,11 +306,14 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
             bool ok = true;
             if (i >= kStages) ok = mbar_wait(&bars->kv_empty[stg], ((i / kStages) & 1) ^ 1, a.err, 0x501, abort);
             if (!__all_sync(0xffffffffu, ok)) break;
-            // this stage is free here: the peer may send its half of tile i
-            if (kPair && threadIdx.x == 0) mbar_arrive_remote(map_peer(smem_u32(&bars->peer_free[stg]), peer));
+            if (kPair && threadIdx.x == 0) {
+                // this stage is free here: the peer may send its half of tile i
+                mbar_arrive_remote(map_peer(smem_u32(&bars->peer_free[stg]), peer));
+                mbar_arrive_expect_tx(&bars->kv_full[stg], kRegions * kMine * 128);
+            }
             uint8_t *dst = sKV + stg * kTileBytes;
             const int32_t *rows = st->rows + i * kKeys;
-            uint64_t *done = kPair ? &bars->half_ready[stg] : &bars->kv_full[stg];
+            uint64_t *done = &bars->kv_full[stg];
             if constexpr (!kF8) {
 #pragma unroll 3
                 for (int r = 0; r < kRegions; ++r) {
@@ -343,39 +361,37 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
                     }
                 }
             }
+            if constexpr (kPair) {
+                // forward this warp's keys (kKPW rows of every region) to the
+                // peer as soon as they have landed here
+                cp_async_wait_all();
+                fence_proxy_async_smem();  // written through the generic proxy, read by the bulk copy
+                __syncwarp();
+                if (lane == 0) {
+                    ok = mbar_wait(&bars->peer_free[stg], (i / kStages) & 1, a.err, 0x512, abort);
+                    if (ok) {
+                        const uint32_t rbar = map_peer(smem_u32(&bars->kv_full[stg]), peer);
+                        for (int r = 0; r < kRegions; ++r) {
+                            uint8_t *src = dst + r * kRegionBytes + key0 * 128;
+                            bulk_copy_to_peer(map_peer(smem_u32(src), peer), src, kKPW * 128, rbar);
+                        }
+                    }
+                }
+                if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+            }
         }
         cp_async_wait_all();  // the CTA stays alive until every copy has landed
         if (warp == 0 && lane == 0 && *abort) {
             volatile int no_abort = 0;
             mbar_wait(&bars->q_full, 0, nullptr, 0, &no_abort);
         }
-    } else if (warp == kSendWarp) {
-        // ---------------------------------------------------------------- pair forwarding
-        if (kPair && lane == 0) {
-            constexpr uint32_t kHalfBytes = kKeys / 2 * 128;  // one region's half: 32 keys x 128 B
-            const uint32_t half_off = cluster_rank() * kHalfBytes;
-            for (int i = 0; i < n_tiles; ++i) {
-                const int stg = i % kStages;
-                const uint32_t par = (i / kStages) & 1;
-                if (!mbar_wait(&bars->half_ready[stg], par, a.err, 0x511, abort)) break;
-                fence_proxy_async_smem();  // own half was written through the generic proxy
-                if (!mbar_wait(&bars->peer_free[stg], par, a.err, 0x512, abort)) break;
-                const uint32_t rbar = map_peer(smem_u32(&bars->kv_full[stg]), peer);
-                uint8_t *src = sKV + stg * kTileBytes + half_off;
-                for (int r = 0; r < kRegions; ++r)
-                    bulk_copy_to_peer(map_peer(smem_u32(src + r * kRegionBytes), peer), src + r * kRegionBytes,
-                                      kHalfBytes, rbar);
-                // own tile is complete once the peer's half has arrived here
-                mbar_arrive_expect_tx(&bars->kv_full[stg], kRegions * kHalfBytes);
-            }
-        }
     } else if (warp == kMmaWarp) {
         // ---------------------------------------------------------------- tcgen05 issuer
         if (lane == 0) {
             constexpr uint32_t idesc_s = idesc_bf16_f32(64, kKeys);
-            // P*V always runs with N = 64 (a full 64-element swizzle atom of the
-            // MN-major P^T); columns NH..63 are unused when NH < 64
-            constexpr uint32_t idesc_o = idesc_bf16_f32_amn(128, 64) | (1u << 16);  // A and B MN-major
+            // P*V always runs with N = 64 (all 64 rows of P); columns NH..63
+            // are unused when NH < 64
+            constexpr uint32_t idesc_o = idesc_bf16_f32_amn(128, 64);  // A (V^T) MN-major, B (P) K-major
             const uint32_t q_base = smem_u32(sQ), kv_base = smem_u32(sKV);
             bool ok = mbar_wait(&bars->q_full, 0, a.err, 0x502, abort);
             uint32_t *const err = a.err;
@@ -392,14 +408,15 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
                 tc_fence_after();
                 const int stg = i % kStages;
                 const uint32_t kb = kv_base + stg * kTileBytes;
-                const uint32_t pb = kb + 8 * kRegionBytes;  // P^T [keys][heads] over the consumed rope region
+                // P [heads][keys] (K-major) over the consumed rope region
+                const uint64_t ad0 = sdesc_mnmajor_sw128(kb, kRegionBytes, 1024);
+                const uint64_t bd0 = sdesc_kmajor_sw128(kb + 8 * kRegionBytes);
+#pragma unroll
                 for (int c = 0; c < 4; ++c) {
 #pragma unroll
-                    for (int j = 0; j < kKeys / 16; ++j) {
-                        const uint64_t ad = sdesc_mnmajor_sw128(kb + 2 * c * kRegionBytes + j * 2048, kRegionBytes, 1024);
-                        const uint64_t bd = sdesc_mnmajor_sw128(pb + j * 2048, kRegionBytes, 1024);
-                        mma_bf16_ss(tmem_o + c * 64, ad, bd, idesc_o, (i > 0 || j > 0) ? 1u : 0u);
-                    }
+                    for (int j = 0; j < kKeys / 16; ++j)
+                        mma_bf16_ss(tmem_o + c * 64, ad0 + (uint64_t)((2 * c * kRegionBytes + j * 2048) >> 4),
+                                    bd0 + (uint64_t)((j * 32) >> 4), idesc_o, (i > 0 || j > 0) ? 1u : 0u);
                 }
                 mma_commit(&bars->kv_empty[stg]);
                 mma_commit(&bars->o_done);
@@ -419,9 +436,13 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
         const int sw = warp - kSmWarp0, quad = warp & 3;
         const int tid_s = sw * 32 + lane;
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-        const int h = quad * 16 + lane;           // head of this thread (lanes 0..15)
-        const bool owner = lane < 16 && h < NH;
-        float m_ref = -CUDART_INF_F, l_run = 0.0f;
+        // With M = 64, S rows (heads) 16q..16q+15 sit in the first 16 lanes of
+        // quadrant q; the 16x256b load spreads them over the whole warp:
+        // thread = heads hA, hB (= hA + 8) x keys 8j + kc + {0, 1}.
+        const int hA = quad * 16 + (lane >> 2), hB = hA + 8;
+        const int kc = 2 * (lane & 3);
+        const bool lead = (lane & 3) == 0;  // writes the per-head values
+        float m_ref[2] = {-CUDART_INF_F, -CUDART_INF_F}, l_run[2] = {0.0f, 0.0f};
         bool ok = n_tiles == 0 || mbar_wait(&bars->table, 0, a.err, 0x509, abort);
         for (int i = 0; i < n_tiles; ++i) {
             const int sb = i & 1, stg = i % kStages;
@@ -429,57 +450,76 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
             ok = bar_and(kBarSm, kSmThreads, ok);
             if (!ok) break;
             tc_fence_after();
-            float x[kKeys];
-#pragma unroll
-            for (int w = 0; w < kWords; ++w) {
-                const uint32_t vmask = st->valid[i * kWords + w];  // keys 32w..32w+31 of tile i
-                uint32_t va[32];
-                tmem_ld32(tmem_s + kKeys * sb + lane_off + 32 * w, va);
+            constexpr int kJ = kKeys / 8;  // 8-column chunks
+            float x[2][2 * kJ];
+            {
+                uint32_t r[4 * kJ];
+                tmem_ld16x256b_x8(tmem_s + kKeys * sb + lane_off, r);
                 tmem_wait_ld();
+                const uint32_t v0 = st->valid[i * kWords], v1 = st->valid[i * kWords + 1];
 #pragma unroll
-                for (int k = 0; k < 32; ++k)
-                    x[32 * w + k] = ((vmask >> k) & 1u) ? __uint_as_float(va[k]) * a.scale_log2 : -CUDART_INF_F;
+                for (int j = 0; j < kJ; ++j) {
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int key = 8 * j + kc + e;
+                        const bool valid = (((j < 4 ? v0 : v1) >> (key & 31)) & 1u) != 0;
+                        x[0][2 * j + e] = valid ? __uint_as_float(r[4 * j + e]) * a.scale_log2 : -CUDART_INF_F;
+                        x[1][2 * j + e] = valid ? __uint_as_float(r[4 * j + 2 + e]) * a.scale_log2 : -CUDART_INF_F;
+                    }
+                }
             }
-            float m8[8];
+            float al[2];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                m8[k] = x[k];
+            for (int u = 0; u < 2; ++u) {
+                float m4[4] = {x[u][0], x[u][1], x[u][2], x[u][3]};
 #pragma unroll
-                for (int j = 1; j < kKeys / 8; ++j) m8[k] = fmaxf(m8[k], x[k + 8 * j]);
+                for (int k = 4; k < 2 * kJ; ++k) m4[k & 3] = fmaxf(m4[k & 3], x[u][k]);
+                float mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+                mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 1));
+                mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 2));
+                al[u] = 1.0f;
+                if (mt != -CUDART_INF_F && (m_ref[u] == -CUDART_INF_F || mt > m_ref[u] + 8.0f)) {
+                    al[u] = m_ref[u] == -CUDART_INF_F ? 1.0f : exp2f(m_ref[u] - mt);
+                    m_ref[u] = mt;
+                }
+                const float ref = m_ref[u] == -CUDART_INF_F ? 0.0f : m_ref[u];
+                float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+                for (int k = 0; k < 2 * kJ; ++k) {
+                    x[u][k] = exp2f(x[u][k] - ref);
+                    s4[k & 3] += x[u][k];
+                }
+                float sum = (s4[0] + s4[1]) + (s4[2] + s4[3]);
+                sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+                sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+                l_run[u] = l_run[u] * al[u] + sum;
             }
-            const float mt = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
-            float al = 1.0f;
-            if (mt != -CUDART_INF_F && (m_ref == -CUDART_INF_F || mt > m_ref + 8.0f)) {
-                al = m_ref == -CUDART_INF_F ? 1.0f : exp2f(m_ref - mt);
-                m_ref = mt;
+            if (lead) {
+                if (hA < NH) st->alpha[sb][hA] = al[0];
+                if (hB < NH) st->alpha[sb][hB] = al[1];
             }
-            const float ref = m_ref == -CUDART_INF_F ? 0.0f : m_ref;
-            float s8[8];
+            {
+                // P (bf16) as K-major [head][key] rows of 128 bytes with the
+                // 128-byte swizzle, over the tile's consumed rope region (the
+                // previous tile's P*V reads the other buffer)
+                uint8_t *pb = sKV + stg * kTileBytes + 8 * kRegionBytes;
 #pragma unroll
-            for (int k = 0; k < 8; ++k) s8[k] = 0.0f;
+                for (int u = 0; u < 2; ++u) {
+                    const int h = u ? hB : hA;
+                    uint8_t *row = pb + h * 128 + 2 * kc;
 #pragma unroll
-            for (int k = 0; k < kKeys; ++k) {
-                x[k] = exp2f(x[k] - ref);
-                s8[k & 7] += x[k];
-            }
-            l_run = l_run * al + (((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7])));
-            if (owner) {
-                st->alpha[sb][h] = al;
-                // P^T, MN-major [key][head] with the 128-byte swizzle, over the
-                // tile's consumed rope region (the previous tile's P*V reads
-                // another buffer)
-                uint8_t *pbase = sKV + stg * kTileBytes + 8 * kRegionBytes + (h & 7) * 2;
-                const int hc = h >> 3;
-#pragma unroll
-                for (int k = 0; k < kKeys; ++k)
-                    *reinterpret_cast<__nv_bfloat16 *>(pbase + k * 128 + ((hc ^ (k & 7)) << 4)) = __float2bfloat16_rn(x[k]);
+                    for (int j = 0; j < kJ; ++j)
+                        *reinterpret_cast<uint32_t *>(row + ((j ^ (h & 7)) << 4)) = pack_bf16(x[u][2 * j], x[u][2 * j + 1]);
+                }
             }
             // O^T of the previous tile must be complete before it is rescaled
             if (i > 0) ok = mbar_wait(&bars->o_done, (i - 1) & 1, a.err, 0x507, abort);
-            const bool any = bar_or(kBarSm, kSmThreads, owner && al != 1.0f);
+            const bool any = bar_or(kBarSm, kSmThreads,
+                                    lead && ((hA < NH && al[0] != 1.0f) || (hB < NH && al[1] != 1.0f)));
             if (any && i > 0) {
                 // rescale the O^T columns (heads) of this warp's 32 value-dim lanes
-                constexpr int W = NH < 32 ? NH : 32;
+                // (a rare path: 16 columns at a time keeps registers free)
+                constexpr int W = 16;
 #pragma unroll 1
                 for (int cc = 0; cc < 4 * (NH / W); ++cc) {
                     {
@@ -500,11 +540,18 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars->p_full);
         }
-        if (owner) {
-            st->m_fin[h] = m_ref;
-            st->l_fin[h] = l_run;
+        if (lead) {
+            if (hA < NH) {
+                st->m_fin[hA] = m_ref[0];
+                st->l_fin[hA] = l_run[0];
+            }
+            if (hB < NH) {
+                st->m_fin[hB] = m_ref[1];
+                st->l_fin[hB] = l_run[1];
+            }
         }
         // ---------------------------------------------------------------- epilogue
+        if (tid_s == 0) grid_dep_launch();  // the split combine may start launching
         if (ok && n_tiles > 0) ok = mbar_wait(&bars->o_full, 0, a.err, 0x508, abort);
         ok = bar_and(kBarSm, kSmThreads, ok);
         if (ok) {
@@ -564,6 +611,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
 // Merge split partials: block = (head, head group, query row), 128 threads x 4 dims.
 __global__ void __launch_bounds__(128) mla_combine_kernel(MlaArgs a, int NH) {
     const int hl = blockIdx.x, hg = blockIdx.y, t = blockIdx.z;
+    grid_dep_wait();  // the partials of the attention kernel launched just before
     if (hl >= NH) return;
     const int h = hg * NH + hl;
     const size_t base = ((size_t)t * gridDim.y + hg) * a.splits;
@@ -610,13 +658,15 @@ static cudaError_t launch_tc(const CUtensorMap &tq, const MlaArgs &a, cudaStream
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = kPair ? 2 : 1;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, kern, tq, a);
 }
 
@@ -632,8 +682,16 @@ static cudaError_t launch_heads(const CUtensorMap &tq, const MlaArgs &a, int NH,
 cudaError_t launch_sparse_mla(const CUtensorMap &tq, const MlaArgs &a, int NH, bool fp8, cudaStream_t st) {
     const cudaError_t e = fp8 ? launch_heads<true>(tq, a, NH, st) : launch_heads<false>(tq, a, NH, st);
     if (e != cudaSuccess || a.splits == 1) return e;
-    mla_combine_kernel<<<dim3(kHG, a.H / NH, a.T), 128, 0, st>>>(a, NH);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(kHG, a.H / NH, a.T);
+    cfg.blockDim = dim3(128, 1, 1);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, mla_combine_kernel, a, NH);
 }
 
 }  // namespace dsa
