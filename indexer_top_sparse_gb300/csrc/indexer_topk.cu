@@ -109,8 +109,9 @@ __device__ void cluster_topk(const uint32_t *keys, int n_local, int pos0, int n_
     if (n_valid <= K) {
         // every valid position is selected; positions are contiguous from 0,
         // so slot == position
+        const uint32_t kb = smem_u32(keys);
         for (int l = tid; l < n_local; l += kT) {
-            if (keys[l] != 0u && pos0 + l < n_valid) out[pos0 + l] = pos0 + l;
+            if (lds32(kb + 4 * l) != 0u && pos0 + l < n_valid) out[pos0 + l] = pos0 + l;
         }
         if (my == 0) {
             for (int i = (n_valid > 0 ? n_valid : 0) + tid; i < K; i += kT) out[i] = -1;
@@ -119,6 +120,7 @@ __device__ void cluster_topk(const uint32_t *keys, int n_local, int pos0, int n_
         return;
     }
 
+    const uint32_t kb = smem_u32(keys);
     uint32_t prefix = 0, mask = 0;
     int krem = K;
     for (int pass = 0; pass < 4; ++pass) {
@@ -130,9 +132,19 @@ __device__ void cluster_topk(const uint32_t *keys, int n_local, int pos0, int n_
         } else {
             for (int d = tid; d < kHist; d += kT) h[d] = 0u;
             __syncthreads();
-            for (int l = tid; l < n_local; l += kT) {
-                uint32_t k = keys[l];
-                if (k != 0u && (k & mask) == prefix) atomicAdd(&h[(k >> shift) & 0xFFu], 1u);
+            const uint32_t hb = smem_u32(h);
+            int l = tid;
+            for (; l + 3 * kT < n_local; l += 4 * kT) {
+                uint32_t k4[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) k4[u] = lds32(kb + 4 * (l + u * kT));
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    if (k4[u] != 0u && (k4[u] & mask) == prefix) red_shared_add(hb + 4 * ((k4[u] >> shift) & 0xFFu), 1u);
+            }
+            for (; l < n_local; l += kT) {
+                const uint32_t k = lds32(kb + 4 * l);
+                if (k != 0u && (k & mask) == prefix) red_shared_add(hb + 4 * ((k >> shift) & 0xFFu), 1u);
             }
         }
         cluster.sync();
@@ -191,7 +203,7 @@ __device__ void cluster_topk(const uint32_t *keys, int n_local, int pos0, int n_
     const int l0 = min(n_local, tid * seg), l1 = min(n_local, l0 + seg);
     int n_gt = 0, n_eq = 0;
     for (int l = l0; l < l1; ++l) {
-        uint32_t k = keys[l];
+        uint32_t k = lds32(kb + 4 * l);
         if (k == 0u) continue;
         uint32_t m = k & mask;
         n_gt += m > prefix;
@@ -225,7 +237,7 @@ __device__ void cluster_topk(const uint32_t *keys, int n_local, int pos0, int n_
     (void)gt_before_seg;
     int slot = out_before_cta + sel_before_seg, eq_rank = eq_rank0;
     for (int l = l0; l < l1; ++l) {
-        uint32_t k = keys[l];
+        uint32_t k = lds32(kb + 4 * l);
         if (k == 0u) continue;
         uint32_t m = k & mask;
         bool sel = m > prefix;
@@ -465,7 +477,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool valid = gi < gn && pos <= pos_first + gi;
                 const uint32_t key = valid ? score_key(acc) : 0u;
                 sKeys[(size_t)gi * key_cap + l] = key;
-                if (valid) atomicAdd(&sHist0[gi * kHist + (key >> 24)], 1u);
+                if (valid) red_shared_add(smem_u32(&sHist0[gi * kHist + (key >> 24)]), 1u);
                 if (kWriteScores && valid && pos < a.ld_scores) a.scores[(size_t)(t0 + gi) * a.ld_scores + pos] = acc;
             }
             tc_fence_before();
@@ -695,7 +707,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
                 const bool valid = pos <= pos_last;
                 const uint32_t key = valid ? score_key(sc) : 0u;
                 sKeys[i * kTileM + row] = key;
-                if (valid) atomicAdd(&sHist0[key >> 24], 1u);
+                if (valid) red_shared_add(smem_u32(&sHist0[key >> 24]), 1u);
                 if (kWriteScores && valid && pos < a.ld_scores) a.scores[(size_t)t0 * a.ld_scores + pos] = sc;
             }
         }
