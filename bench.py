@@ -189,6 +189,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--l2", default="rotate", choices=["rotate", "flush"],
+                    help="between timed steps: alternate two copies of every step input (default) or write a "
+                         "512 MiB buffer")
     ap.add_argument("--batch", type=int, default=32,
                     help="sequences per rank (default 32, the benchmark workload; smaller only for profiling)")
     args = ap.parse_args()
@@ -207,7 +210,7 @@ def main():
                            [1] * args.batch, H=128, K=2048, page_size=64, permute=True, seed=args.seed + rank)
     cfg = {"workload": wl.name, "B": wl.B, "N": int(wl.seq_lens[0]), "K": wl.K, "H": wl.H, "H_I": 64, "d_I": 128,
            "D": 576, "D_v": 512, "page_size": wl.page_size, "global_batch": wl.B * max(world, 1),
-           "l2": "flushed between steps (512 MiB device write)", "parallelism": f"replicas{max(world, 1)}"}
+           "parallelism": f"replicas{max(world, 1)}"}
 
     if args.impl == "reference":
         if rank != 0:
@@ -244,21 +247,38 @@ def main():
     def bf16(bits):
         return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
 
-    k_idx, kv = bf16(wl.k_idx), bf16(wl.kv)
-    q_idx, q = bf16(wl.q_idx), bf16(wl.q)
-    head_w = torch.from_numpy(wl.head_w).to(dev)
-    pt, sl, cq = (torch.from_numpy(a).to(dev) for a in (wl.page_table, wl.seq_lens, wl.cu_q))
+    # Step inputs.  With --l2 rotate, two separate copies of every input (the
+    # caches included) alternate between steps: a step reads buffers last
+    # touched two steps earlier, with far more than the L2 capacity read in
+    # between, so no step finds its data in L2.
+    copies = 2 if args.l2 == "rotate" else 1
+    sets = []
+    for _ in range(copies):
+        sets.append({"k_idx": bf16(wl.k_idx), "kv": bf16(wl.kv), "q_idx": bf16(wl.q_idx), "q": bf16(wl.q),
+                     "head_w": torch.from_numpy(wl.head_w).to(dev), "pt": torch.from_numpy(wl.page_table).to(dev),
+                     "sl": torch.from_numpy(wl.seq_lens).to(dev), "cq": torch.from_numpy(wl.cu_q).to(dev)})
+    in_bytes = sum(v.numel() * v.element_size() for v in sets[0].values())
+    cfg["l2"] = (f"inputs larger than L2: {copies} alternating copies of every step input "
+                 f"({in_bytes / 2**30:.2f} GiB each), no flush" if copies > 1 else
+                 "flushed between steps (512 MiB device write)")
+    k_idx, kv = sets[0]["k_idx"], sets[0]["kv"]
+    q_idx, q, head_w = sets[0]["q_idx"], sets[0]["q"], sets[0]["head_w"]
+    pt, sl, cq = sets[0]["pt"], sets[0]["sl"], sets[0]["cq"]
     idx = torch.empty((wl.T, wl.K), dtype=torch.int32, device=dev)
     out = torch.empty((wl.T, wl.H, 512), dtype=torch.bfloat16, device=dev)
     ws = d.Workspace(max(d.index_topk_workspace_size(wl.B, wl.T, wl.K, wl.max_pages, wl.page_size),
                          d.sparse_mla_workspace_size(wl.T, wl.H, wl.K)), dev)
     launches_per_step = 2 + (1 if d.sparse_mla_workspace_size(wl.T, wl.H, wl.K) > 256 else 0)
-    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev) if copies == 1 else None
     stream = torch.cuda.current_stream(dev)
 
-    def run_step(qi, hw, qq, ptab, slen, cuq):
-        d.dsa_index_topk(qi, hw, k_idx, ptab, slen, cuq, wl.K, indices=idx, workspace=ws)
-        d.dsa_sparse_mla(qq, kv, ptab, slen, cuq, idx, wl.scale, out=out, workspace=ws)
+    def between_steps():
+        if flush is not None:
+            flush.zero_()
+
+    def run_step(qi, hw, qq, ptab, slen, cuq, c=0):
+        d.dsa_index_topk(qi, hw, sets[c]["k_idx"], ptab, slen, cuq, wl.K, indices=idx, workspace=ws)
+        d.dsa_sparse_mla(qq, sets[c]["kv"], ptab, slen, cuq, idx, wl.scale, out=out, workspace=ws)
 
     def barrier():
         torch.cuda.synchronize(dev)
@@ -272,20 +292,24 @@ def main():
     while time.perf_counter() - t_soak < 1.0:           # bring clocks to their loaded state
         run_step(q_idx, head_w, q, pt, sl, cq)
         torch.cuda.synchronize(dev)
-    for _ in range(args.warmup):
-        flush.zero_()
-        run_step(q_idx, head_w, q, pt, sl, cq)
+    for i in range(args.warmup):
+        between_steps()
+        c = i % copies
+        st_ = sets[c]
+        run_step(st_["q_idx"], st_["head_w"], st_["q"], st_["pt"], st_["sl"], st_["cq"], c)
     ws.check()
 
-    # ---- device-resident timing, per kernel, L2 flushed before every step
+    # ---- device-resident timing, per kernel (no L2 reuse between steps)
     barrier()
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     for i in range(args.steps):
-        flush.zero_()
+        between_steps()
+        st_ = sets[(args.warmup + i) % copies]
         ev[i][0].record(stream)
-        d.dsa_index_topk(q_idx, head_w, k_idx, pt, sl, cq, wl.K, indices=idx, workspace=ws)
+        d.dsa_index_topk(st_["q_idx"], st_["head_w"], st_["k_idx"], st_["pt"], st_["sl"], st_["cq"], wl.K,
+                         indices=idx, workspace=ws)
         ev[i][1].record(stream)
-        d.dsa_sparse_mla(q, kv, pt, sl, cq, idx, wl.scale, out=out, workspace=ws)
+        d.dsa_sparse_mla(st_["q"], st_["kv"], st_["pt"], st_["sl"], st_["cq"], idx, wl.scale, out=out, workspace=ws)
         ev[i][2].record(stream)
     barrier()
     t_idx = [e[0].elapsed_time(e[1]) * 1e-3 for e in ev]
@@ -309,11 +333,11 @@ def main():
     barrier()
     e2e_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     for i in range(args.steps):
-        flush.zero_()
+        between_steps()
         e2e_ev[i][0].record(stream)
         for k in h_in:
             d_in[k].copy_(h_in[k], non_blocking=True)
-        run_step(d_in["q_idx"], d_in["head_w"], d_in["q"], d_in["pt"], d_in["sl"], d_in["cq"])
+        run_step(d_in["q_idx"], d_in["head_w"], d_in["q"], d_in["pt"], d_in["sl"], d_in["cq"], (i + 1) % copies)
         h_out.copy_(out, non_blocking=True)
         e2e_ev[i][1].record(stream)
     barrier()
