@@ -608,35 +608,48 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
     if constexpr (kPair) cluster_barrier();
 }
 
-// Merge split partials: block = (head, head group, query row), 128 threads x 4 dims.
+// Merge split partials: block = (4 heads, head group, query row), warp = head,
+// lane = 16 value dims (4 float4).  Splits are folded in with a running max, so
+// every load of a split is independent of the previous split's arithmetic.
 __global__ void __launch_bounds__(128) mla_combine_kernel(MlaArgs a, int NH) {
-    const int hl = blockIdx.x, hg = blockIdx.y, t = blockIdx.z;
+    const int hg = blockIdx.y, t = blockIdx.z;
+    const int hl = 4 * blockIdx.x + (threadIdx.x >> 5), lane = threadIdx.x & 31;
     grid_dep_wait();  // the partials of the attention kernel launched just before
     if (hl >= NH) return;
-    const int h = hg * NH + hl;
     const size_t base = ((size_t)t * gridDim.y + hg) * a.splits;
-    float M = -CUDART_INF_F;
-    for (int s = 0; s < a.splits; ++s) M = fmaxf(M, a.part_ml[((base + s) * kHG + hl) * 2]);
-    const float ref = M == -CUDART_INF_F ? 0.0f : M;
-    float Lsum = 0.0f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float M = -CUDART_INF_F, L = 0.0f;
+    float4 acc[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 2
     for (int s = 0; s < a.splits; ++s) {
-        const float ms = a.part_ml[((base + s) * kHG + hl) * 2];
-        const float ls = a.part_ml[((base + s) * kHG + hl) * 2 + 1];
-        const float w = ls > 0.0f ? exp2f(ms - ref) : 0.0f;
-        Lsum += ls * w;
-        const float4 v = reinterpret_cast<const float4 *>(a.part_o + ((base + s) * kHG + hl) * kDv)[threadIdx.x];
-        acc.x += w * v.x;
-        acc.y += w * v.y;
-        acc.z += w * v.z;
-        acc.w += w * v.w;
+        const size_t slot = (base + s) * kHG + hl;
+        const float m = __ldcg(a.part_ml + slot * 2), l = __ldcg(a.part_ml + slot * 2 + 1);
+        const float4 *src = reinterpret_cast<const float4 *>(a.part_o + slot * kDv) + lane;
+        float4 v[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) v[k] = __ldcg(src + 32 * k);
+        if (l > 0.0f) {
+            const float Mn = fmaxf(M, m);
+            const float cs = M == -CUDART_INF_F ? 0.0f : exp2f(M - Mn), cn = exp2f(m - Mn);
+            L = L * cs + l * cn;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                acc[k].x = acc[k].x * cs + v[k].x * cn;
+                acc[k].y = acc[k].y * cs + v[k].y * cn;
+                acc[k].z = acc[k].z * cs + v[k].z * cn;
+                acc[k].w = acc[k].w * cs + v[k].w * cn;
+            }
+            M = Mn;
+        }
     }
-    const float inv = Lsum > 0.0f ? 1.0f / Lsum : 0.0f;
-    uint32_t *o = reinterpret_cast<uint32_t *>(a.out + ((size_t)t * a.H + h) * kDv);
-    o[threadIdx.x * 2] = pack_bf16(acc.x * inv, acc.y * inv);
-    o[threadIdx.x * 2 + 1] = pack_bf16(acc.z * inv, acc.w * inv);
-    if (a.lse && threadIdx.x == 0)
-        a.lse[(size_t)t * a.H + h] = Lsum > 0.0f ? ref * 0.69314718055994531f + logf(Lsum) : -CUDART_INF_F;
+    const float inv = L > 0.0f ? 1.0f / L : 0.0f;
+    uint2 *o = reinterpret_cast<uint2 *>(a.out + ((size_t)t * a.H + hg * NH + hl) * kDv) + lane;
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+        o[32 * k] = make_uint2(pack_bf16(acc[k].x * inv, acc[k].y * inv), pack_bf16(acc[k].z * inv, acc[k].w * inv));
+    if (a.lse && lane == 0)
+        a.lse[(size_t)t * a.H + hg * NH + hl] = L > 0.0f ? M * 0.69314718055994531f + logf(L) : -CUDART_INF_F;
 }
 
 }  // namespace
@@ -683,7 +696,7 @@ cudaError_t launch_sparse_mla(const CUtensorMap &tq, const MlaArgs &a, int NH, b
     const cudaError_t e = fp8 ? launch_heads<true>(tq, a, NH, st) : launch_heads<false>(tq, a, NH, st);
     if (e != cudaSuccess || a.splits == 1) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(kHG, a.H / NH, a.T);
+    cfg.gridDim = dim3((NH + 3) / 4, a.H / NH, a.T);
     cfg.blockDim = dim3(128, 1, 1);
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
