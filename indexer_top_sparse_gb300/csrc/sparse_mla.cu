@@ -246,22 +246,33 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
         // in parallel, so that the copy loop below never waits on the index
         // or page-table loads
         const int n_keys = n_tiles * kKeys;
-        for (int k = threadIdx.x; k < n_keys; k += kProd * 32) {
-            const int slot = k_begin + k;
+        constexpr int kPer = kMaxKeysPerSplit / (kProd * 32);  // keys per gather thread, at most
+        int idxv[kPer], pagev[kPer];
+        // all index loads first, then all page-table loads, then the table
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+            const int k = threadIdx.x + u * kProd * 32, slot = k_begin + k;
+            idxv[u] = k < n_keys && slot < k_end ? __ldg(idx_row + slot) : -1;
+        }
+#pragma unroll
+        for (int u = 0; u < kPer; ++u)
+            pagev[u] = idxv[u] >= 0 && idxv[u] <= pos ? __ldg(pt_row + idxv[u] / a.page_size) : -1;
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+            const int k = threadIdx.x + u * kProd * 32;
+            if (k >= n_keys) break;  // n_keys is a multiple of 64: warp-uniform
+            const int idx = idxv[u];
             int row = 0;  // invalid slots read row 0 and are masked by the softmax
             bool v = false;
-            if (slot < k_end) {
-                const int idx = __ldg(idx_row + slot);
-                if (idx > pos) {
-                    report_error(a.err, kErrBadIndex);
-                } else if (idx >= 0) {
-                    const int page = __ldg(pt_row + idx / a.page_size);
-                    if (page < 0 || (int64_t)page >= a.num_pages) {
-                        report_error(a.err, kErrBadPage);
-                    } else {
-                        row = page * a.page_size + idx % a.page_size;
-                        v = true;
-                    }
+            if (idx > pos) {
+                report_error(a.err, kErrBadIndex);
+            } else if (idx >= 0) {
+                const int page = pagev[u];
+                if (page < 0 || (int64_t)page >= a.num_pages) {
+                    report_error(a.err, kErrBadPage);
+                } else {
+                    row = page * a.page_size + idx % a.page_size;
+                    v = true;
                 }
             }
             st->rows[k] = row;
@@ -270,22 +281,6 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
         }
         bar_sync(kBarProd, kProd * 32);  // gather warps only
         if (threadIdx.x == 0) mbar_arrive(&bars->table);  // publishes the row / validity table
-        // Prefetch this warp's rows of every tile past the first kStages into
-        // L2, in tile order, so that the copies into a freed buffer wait for
-        // L2 rather than for the memory.
-        for (int k = lane; k < n_tiles * kKPW; k += 32) {
-            const int tile = k / kKPW;
-            if (tile < kStages) continue;
-            const int key = tile * kKeys + key0 + k % kKPW;
-            if (!((st->valid[key >> 5] >> (key & 31)) & 1u)) continue;
-            const size_t row = (size_t)st->rows[key];
-            if constexpr (kF8) {
-                prefetch_l2_bulk(a.kv + row * kDv, kDv);
-                prefetch_l2_bulk(a.kv_rope + row * 128, 128);
-            } else {
-                prefetch_l2_bulk(a.kv + row * (kD * 2), kD * 2);
-            }
-        }
         // FP8: lane l holds bytes 16l..16l+15 (dims 16l..16l+15) of each of
         // the warp's keys, loaded one tile ahead so that the loads overlap the
         // wait for a free stage
