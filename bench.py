@@ -13,6 +13,14 @@ sum of all ranks' tokens over the slowest rank's time.
 
 --impl reference times the CPU oracle (plain single-threaded C, fp64) on this
 machine's host cores, on a bounded sample of the same workload.
+
+--workload selects one of the other measured workloads (same JSON line, with
+config.workload naming it): decode_b64_mixed_fp8 (64 sequences, lengths
+uniform in [4096, 131072], MXFP8 index keys, FP8 latent rows), prefill_16k
+(one 16384-token sequence, causal, bf16) and prefill_131k_chunked_fp8 (one
+131072-token sequence in 32 chunks of 4096 queries against the paged cache,
+MXFP8 / FP8).  Their caches are drawn on the device (seeded torch generator)
+and quantised by the library's own quantisers.
 """
 from __future__ import annotations
 
@@ -179,6 +187,197 @@ def aggregate_rate(tokens_per_rank: int, world: int, seconds_max: float) -> floa
     return tokens_per_rank * max(world, 1) / seconds_max
 
 
+# ---------------------------------------------------------------- other workloads
+
+def attention_flops(rows_sel: np.ndarray, H: int) -> float:
+    """QK over 576 dims and PV over 512 dims for every (query, selected key, head)."""
+    return float(np.sum(rows_sel.astype(np.float64))) * H * 2.0 * (576 + 512)
+
+
+def run_other_workload(args, world, rank, local_rank):
+    """Timed steps of the mixed-length FP8 decode, the 16k prefill or the 131k
+    chunked FP8 prefill (one GPU per rank, independent replicas)."""
+    import torch
+    import indexer_top_sparse_gb300 as d
+    from indexer_top_sparse_gb300.inputs import make_page_table
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(args.seed + 1000 * rank)
+
+    def normal_bf16(*shape):
+        return torch.randn(*shape, generator=gen, device=dev, dtype=torch.float32).to(torch.bfloat16)
+
+    H, K, ps, scale = 128, 2048, 64, float(1.0 / np.sqrt(192.0))
+    fp8 = args.workload.endswith("fp8")
+    if args.workload == "decode_b64_mixed_fp8":
+        lens = np.random.default_rng(args.seed + rank + 7919).integers(4096, 131072, size=64, endpoint=True)
+        lens = lens.astype(np.int32)
+        chunks = [(lens, np.ones(64, np.int32))]
+        permute, copies = True, 2
+    elif args.workload == "prefill_16k":
+        chunks = [(np.array([16384], np.int32), np.array([16384], np.int32))]
+        permute, copies = False, 1
+    else:
+        chunks = [(np.array([4096 * (c + 1)], np.int32), np.array([4096], np.int32)) for c in range(32)]
+        permute, copies = True, 1
+    cache_lens = chunks[-1][0]
+    pt_np, P = make_page_table(np.random.default_rng(args.seed + rank), cache_lens, ps, permute)
+    T_all = int(sum(int(n.sum()) for _, n in chunks))
+    pt = torch.from_numpy(pt_np).to(dev)
+
+    sets = []
+    for _ in range(copies):
+        k_bf, kv_bf = normal_bf16(P, ps, 128), normal_bf16(P, ps, 576)
+        st = {"q_idx": normal_bf16(T_all, 64, 128), "q": normal_bf16(T_all, H, 576),
+              "head_w": torch.randn(T_all, 64, generator=gen, device=dev) / 8.0}
+        if fp8:
+            st["k_idx"], st["k_sc"] = d.dsa_quant_mxfp8(k_bf)
+            st["kv"], st["rope"], st["rsc"] = d.dsa_quant_fp8_rows(kv_bf)
+            st["qi8"] = torch.empty((T_all, 64, 128), dtype=torch.uint8, device=dev)
+            st["qi_sc"] = torch.empty((T_all, 64, 4), dtype=torch.uint8, device=dev)
+        else:
+            st["k_idx"], st["kv"] = k_bf, kv_bf
+        del k_bf, kv_bf
+        sets.append(st)
+    torch.cuda.synchronize(dev)
+    in_bytes = sum(v.numel() * v.element_size() for k, v in sets[0].items() if k not in ("qi8", "qi_sc"))
+
+    # per-chunk views and small tensors
+    plan = []
+    q0 = 0
+    for sl_np, nq_np in chunks:
+        B = len(sl_np)
+        cq_np = np.zeros(B + 1, np.int32)
+        cq_np[1:] = np.cumsum(nq_np)
+        T = int(cq_np[-1])
+        plan.append({"r0": q0, "T": T, "B": B, "sl": torch.from_numpy(sl_np).to(dev),
+                     "cq": torch.from_numpy(cq_np).to(dev), "pt": pt[:B], "sl_np": sl_np, "cq_np": cq_np})
+        q0 += T
+    idx = torch.empty((max(c["T"] for c in plan), K), dtype=torch.int32, device=dev)
+    out = torch.empty((T_all, H, 512), dtype=torch.bfloat16, device=dev)
+    ws = d.Workspace(max(max(d.index_topk_workspace_size(c["B"], c["T"], K, pt.shape[1], ps) for c in plan),
+                         max(d.sparse_mla_workspace_size(c["T"], H, K) for c in plan)), dev)
+    stream = torch.cuda.current_stream(dev)
+    launches = 0
+
+    def step(st, ev=None):
+        nonlocal launches
+        n = 0
+        for c in plan:
+            r0, T = c["r0"], c["T"]
+            if ev is not None:
+                ev[0].append(torch.cuda.Event(enable_timing=True))
+                ev[0][-1].record(stream)
+            if fp8:
+                d.dsa_quant_mxfp8(st["q_idx"][r0:r0 + T], q=st["qi8"][r0:r0 + T], scales=st["qi_sc"][r0:r0 + T])
+                d.dsa_index_topk(st["qi8"][r0:r0 + T], st["head_w"][r0:r0 + T], st["k_idx"], c["pt"], c["sl"],
+                                 c["cq"], K, indices=idx[:T], workspace=ws, q_idx_scale=st["qi_sc"][r0:r0 + T],
+                                 k_idx_scale=st["k_sc"], dtype="mxfp8")
+                n += 2
+            else:
+                d.dsa_index_topk(st["q_idx"][r0:r0 + T], st["head_w"][r0:r0 + T], st["k_idx"], c["pt"], c["sl"],
+                                 c["cq"], K, indices=idx[:T], workspace=ws)
+                n += 1
+            if ev is not None:
+                ev[1].append(torch.cuda.Event(enable_timing=True))
+                ev[1][-1].record(stream)
+            if fp8:
+                d.dsa_sparse_mla(st["q"][r0:r0 + T], st["kv"], c["pt"], c["sl"], c["cq"], idx[:T], scale,
+                                 out=out[r0:r0 + T], workspace=ws, kv_rope=st["rope"], kv_scale=st["rsc"],
+                                 dtype="fp8_rowscale")
+            else:
+                d.dsa_sparse_mla(st["q"][r0:r0 + T], st["kv"], c["pt"], c["sl"], c["cq"], idx[:T], scale,
+                                 out=out[r0:r0 + T], workspace=ws)
+            n += 1 + (1 if d.sparse_mla_workspace_size(T, H, K) > 256 else 0)
+            if ev is not None:
+                ev[2].append(torch.cuda.Event(enable_timing=True))
+                ev[2][-1].record(stream)
+        launches = n
+
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    for i in range(args.warmup):
+        step(sets[i % copies])
+    ws.check()
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    evs = []
+    for i in range(args.steps):
+        ev = ([], [], [])
+        step(sets[(args.warmup + i) % copies], ev)
+        evs.append(ev)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    ws.check()
+    t_idx = sum(a.elapsed_time(b) for ev in evs for a, b in zip(ev[0], ev[1])) * 1e-3 / args.steps
+    t_mla = sum(a.elapsed_time(b) for ev in evs for a, b in zip(ev[1], ev[2])) * 1e-3 / args.steps
+    t_step = max_over_ranks([t_idx + t_mla], dev)[0]
+
+    # algorithmic bytes and flops
+    pos_all, sel_all, idx_bytes, mla_b, n_hist = [], [], 0.0, 0.0, 0.0
+    for c in plan:
+        for b in range(c["B"]):
+            nq = int(c["cq_np"][b + 1] - c["cq_np"][b])
+            p = int(c["sl_np"][b]) - nq + np.arange(nq)
+            n = (p + 1).astype(np.float64)
+            sel = np.minimum(n, K)
+            sel_all.append(sel)
+            n_hist += float(n.sum())
+            key_b = 132 if fp8 else 256
+            idx_bytes += float(np.sum(n * key_b + 64 * 128 * (1 if fp8 else 2) + (256 if fp8 else 0) + 256 + 4 * K
+                                      + 4 * np.ceil(n / ps)))
+            mla_b += float(np.sum(sel * (644 if fp8 else 1152) + H * 1152 + H * 1024 + 4 * K + 4 * np.ceil(n / ps)))
+    sel_all = np.concatenate(sel_all)
+    f_mla = attention_flops(sel_all, H)
+    f_idx = n_hist * 64 * 128 * 2.0
+    hbm, peak_kind = peaks()
+    try:
+        pk = json.load(open(PEAKS_FILE))
+        bf16_peak = float(pk["bf16_tflops"])
+    except Exception:
+        bf16_peak = 1900.0
+    tokens = T_all * max(world, 1)
+    line = {"metric": METRIC, "value": tokens / t_step, "unit": "tokens/s", "n_gpus": max(world, 1),
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "e4m3/bf16" if fp8 else "bf16",
+            "data": "synthetic (seeded N(0,1) drawn on the device; FP8 caches made by the library's quantisers)",
+            "config": {"workload": args.workload, "H": H, "K": K, "H_I": 64, "d_I": 128, "page_size": ps,
+                       "query_rows": T_all, "cached_positions": int(np.sum(cache_lens)), "chunks": len(plan),
+                       "parallelism": f"replicas{max(world, 1)}",
+                       "l2": (f"inputs larger than L2: {copies} alternating cop{'ies' if copies > 1 else 'y'} of "
+                              f"every step input ({in_bytes / 2**30:.2f} GiB each), no flush")},
+            "kernels": {"indexer_topk": {"seconds_per_step": t_idx, "algorithmic_bytes": idx_bytes,
+                                         "achieved_gbs": idx_bytes / t_idx / 1e9, "flops": f_idx,
+                                         "achieved_tflops": f_idx / t_idx / 1e12},
+                        "sparse_mla": {"seconds_per_step": t_mla, "algorithmic_bytes": mla_b,
+                                       "achieved_gbs": mla_b / t_mla / 1e9, "flops": f_mla,
+                                       "achieved_tflops": f_mla / t_mla / 1e12}},
+            "gpu_launches": launches * args.steps, "clocks": clk}
+    if args.workload.startswith("prefill"):
+        line["roofline"] = {"bound": "tensor", "kernel": "sparse_mla", "achieved": f_mla / t_mla / 1e12,
+                            "peak": bf16_peak, "unit": "TFLOP/s", "frac": f_mla / t_mla / 1e12 / bf16_peak,
+                            "traffic": None}
+    else:
+        dom = "indexer_topk" if t_idx >= t_mla else "sparse_mla"
+        ach = (idx_bytes / t_idx if dom == "indexer_topk" else mla_b / t_mla) / 1e9
+        line["roofline"] = {"bound": "hbm", "kernel": dom, "achieved": ach, "peak": hbm, "peak_kind": peak_kind,
+                            "unit": "GB/s", "frac": ach / hbm, "traffic": None}
+        line["step_roofline"] = {"bytes": idx_bytes + mla_b, "achieved_gbs": (idx_bytes + mla_b) / t_step / 1e9,
+                                 "frac": (idx_bytes + mla_b) / t_step / 1e9 / hbm}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
 # ---------------------------------------------------------------- main
 
 def main():
@@ -192,6 +391,8 @@ def main():
     ap.add_argument("--l2", default="rotate", choices=["rotate", "flush"],
                     help="between timed steps: alternate two copies of every step input (default) or write a "
                          "512 MiB buffer")
+    ap.add_argument("--workload", default="decode_b32_n32768",
+                    choices=["decode_b32_n32768", "decode_b64_mixed_fp8", "prefill_16k", "prefill_131k_chunked_fp8"])
     ap.add_argument("--batch", type=int, default=32,
                     help="sequences per rank (default 32, the benchmark workload; smaller only for profiling)")
     args = ap.parse_args()
@@ -201,6 +402,14 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.workload != "decode_b32_n32768":
+        if args.impl == "reference":
+            if rank == 0:
+                print(json.dumps({"impl": "reference", "unavailable": "the oracle baseline is timed on the "
+                                  "decode_b32_n32768 workload only"}), flush=True)
+            return
+        run_other_workload(args, world, rank, local_rank)
+        return
 
     from indexer_top_sparse_gb300.inputs import decode_b32_n32k, make_workload
     if args.batch == 32:

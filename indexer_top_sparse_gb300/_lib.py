@@ -282,6 +282,8 @@ def dsa_quant_mxfp8(x, *, q=None, scales=None, stream=None):
         scales = torch.empty(x.shape[:-1] + (x.shape[-1] // 32,), dtype=torch.uint8, device=x.device)
     _need(q, "q", torch.uint8, None, x.device)
     _need(scales, "scales", torch.uint8, None, x.device)
+    if q.numel() != x.numel() or scales.numel() != x.numel() // 32:
+        raise ValueError("q must hold one byte per element of x and scales one byte per 32 elements")
     _check("dsa_quant_mxfp8", lib.dsa_quant_mxfp8(_ptr(x), x.numel(), _ptr(q), _ptr(scales), _stream(stream)))
     return q, scales
 
@@ -298,6 +300,11 @@ def dsa_quant_fp8_rows(kv, *, nope=None, rope=None, scale=None, stream=None):
     nope = torch.empty(lead + (512,), dtype=torch.uint8, device=kv.device) if nope is None else nope
     rope = torch.empty(lead + (64,), dtype=torch.bfloat16, device=kv.device) if rope is None else rope
     scale = torch.empty(lead, dtype=torch.float32, device=kv.device) if scale is None else scale
+    _need(nope, "nope", torch.uint8, None, kv.device)
+    _need(rope, "rope", torch.bfloat16, None, kv.device)
+    _need(scale, "scale", torch.float32, None, kv.device)
+    if nope.numel() != rows * 512 or rope.numel() != rows * 64 or scale.numel() != rows:
+        raise ValueError("nope, rope and scale must hold rows x 512, rows x 64 and rows elements")
     _check("dsa_quant_fp8_rows", lib.dsa_quant_fp8_rows(_ptr(kv), rows, _ptr(nope), _ptr(rope), _ptr(scale),
                                                         _stream(stream)))
     return nope, rope, scale
