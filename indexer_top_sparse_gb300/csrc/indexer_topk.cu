@@ -550,7 +550,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
     uint8_t *sKs = sK + (size_t)a.stages * kF8TileBytes;  // scale_slots x 128 positions x 4 scale bytes
     uint32_t *sKeys = reinterpret_cast<uint32_t *>(sKs + (size_t)scale_slots * kTileM * 4);
     float *sW = reinterpret_cast<float *>(sKeys + key_cap);
-    float *sQs = sW + kHI;                                // [64][4] 2^(q scale)
+    float *sQs = sW + kHI;                                // [4 groups][64 heads] 2^(q scale)
     float *sPart = sQs + kHI * 4;                         // [2][128] per-half partial scores
     uint32_t *sHist0 = reinterpret_cast<uint32_t *>(sPart + 2 * kTileM);
     int32_t *sRows = reinterpret_cast<int32_t *>(sHist0 + kHist);
@@ -593,8 +593,8 @@ __global__ void __launch_bounds__(kF8Threads, 1)
         fence_mbar_init();
     }
     for (int i = threadIdx.x; i < kHI; i += kF8Threads) sW[i] = __ldg(a.head_w + (size_t)t0 * kHI + i);
-    for (int i = threadIdx.x; i < kHI * 4; i += kF8Threads)
-        sQs[i] = e8m0_value(__ldg(a.q_scale + (size_t)t0 * kHI * 4 + i));
+    for (int i = threadIdx.x; i < kHI * 4; i += kF8Threads)  // input layout [head][group]
+        sQs[(i & 3) * kHI + (i >> 2)] = e8m0_value(__ldg(a.q_scale + (size_t)t0 * kHI * 4 + i));
     for (int i = threadIdx.x; i < kHist; i += kF8Threads) sHist0[i] = 0u;
     for (int j = threadIdx.x; j < 2 * n_tiles; j += kF8Threads) {
         const int p0 = tile0 * kTileM + j * kBox;
@@ -680,22 +680,41 @@ __global__ void __launch_bounds__(kF8Threads, 1)
             if (!ok) break;
             tc_fence_after();
             const uint32_t ks = *reinterpret_cast<const uint32_t *>(sKs + (size_t)slot * kTileM * 4 + row * 4);
-            float acc[32];
+            // acc[j] = sum_g 2^(sq_jg) 2^(sk_g) D_jg over this thread's 32 heads,
+            // in pairs of heads (paired fp32 multiply-add, each lane rounded as fmaf)
+            float2 acc[16];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) acc[j] = 0.0f;
+            for (int j = 0; j < 16; ++j) acc[j] = make_float2(0.0f, 0.0f);
 #pragma unroll
             for (int g = 0; g < 4; ++g) {
                 uint32_t r[32];
                 tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(buf * 256 + g * kHI + hh * 32), r);
                 tmem_wait_ld();
                 const float skg = e8m0_value((ks >> (8 * g)) & 0xFFu);
+                const float2 sk2 = make_float2(skg, skg);
+                const float4 *qs4 = reinterpret_cast<const float4 *>(sQs + g * kHI + hh * 32);
 #pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    acc[j] = fmaf(__uint_as_float(r[j]), sQs[(hh * 32 + j) * 4 + g] * skg, acc[j]);
+                for (int k = 0; k < 8; ++k) {
+                    const float4 q4 = qs4[k];
+                    const float2 s01 = __fmul2_rn(make_float2(q4.x, q4.y), sk2);
+                    const float2 s23 = __fmul2_rn(make_float2(q4.z, q4.w), sk2);
+                    acc[2 * k] = __ffma2_rn(make_float2(__uint_as_float(r[4 * k]), __uint_as_float(r[4 * k + 1])), s01,
+                                            acc[2 * k]);
+                    acc[2 * k + 1] = __ffma2_rn(
+                        make_float2(__uint_as_float(r[4 * k + 2]), __uint_as_float(r[4 * k + 3])), s23, acc[2 * k + 1]);
+                }
             }
-            float part = 0.0f;
+            float2 part2 = make_float2(0.0f, 0.0f);
+            const float4 *w4 = reinterpret_cast<const float4 *>(sW + hh * 32);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) part = fmaf(sW[hh * 32 + j], fmaxf(acc[j], 0.0f), part);
+            for (int k = 0; k < 8; ++k) {
+                const float4 w = w4[k];
+                part2 = __ffma2_rn(make_float2(w.x, w.y),
+                                   make_float2(fmaxf(acc[2 * k].x, 0.0f), fmaxf(acc[2 * k].y, 0.0f)), part2);
+                part2 = __ffma2_rn(make_float2(w.z, w.w),
+                                   make_float2(fmaxf(acc[2 * k + 1].x, 0.0f), fmaxf(acc[2 * k + 1].y, 0.0f)), part2);
+            }
+            const float part = part2.x + part2.y;
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars->tempty[buf]);
