@@ -27,6 +27,7 @@ constexpr size_t kErrBytes = 256;  // error word block at the start of every wor
 // ---------------------------------------------------------------- tuning knobs
 // 0 = automatic.  Set through dsa_set_tuning(); read on every call.
 std::atomic<int> g_idx_cluster{0}, g_idx_stages{0}, g_idx_group{0}, g_mla_splits{0}, g_topk_cluster{0};
+std::atomic<int> g_mla_pair{0};  // 0 automatic (pair the two 64-head CTAs of a 128-head query), 1 pair, -1 never
 
 int sm_count() {
     int dev = 0, n = 0;
@@ -337,6 +338,7 @@ int dsa_set_tuning(const char *name, int value) {
     else if (!strcmp(name, "indexer_stages")) g_idx_stages = value;
     else if (!strcmp(name, "indexer_group")) g_idx_group = value;
     else if (!strcmp(name, "mla_splits")) g_mla_splits = value;
+    else if (!strcmp(name, "mla_pair")) g_mla_pair = value;
     else if (!strcmp(name, "topk_cluster")) g_topk_cluster = value;
     else return -1;
     return 0;
@@ -475,7 +477,8 @@ dsa_status dsa_sparse_mla(const void *q, const void *kv_cache, const void *kv_ro
     a.scale_log2 = scale * 1.4426950408889634f;
     CUtensorMap tq;
     if (!encode_2d_bf16(&tq, q, 576, (uint64_t)T * H, (uint32_t)NH)) return DSA_ERR_CUDA;
-    return cuda_status(dsa::launch_sparse_mla(tq, a, NH, fp8, static_cast<cudaStream_t>(stream)));
+    return cuda_status(
+        dsa::launch_sparse_mla(tq, a, NH, fp8, g_mla_pair.load() >= 0, static_cast<cudaStream_t>(stream)));
 }
 
 dsa_status dsa_quant_mxfp8(const void *x, int64_t n, void *q, void *e8m0, void *stream) {

@@ -81,7 +81,10 @@ int mla_key_tile();
 // q [T*H, 576] bf16, box 64 x NH, 128-byte swizzle.
 // fp8: the cache holds E4M3 latent dims with one fp32 scale per row (kv,
 // kv_rope, kv_scale), dequantised to bf16 on the way into shared memory.
-cudaError_t launch_sparse_mla(const CUtensorMap &tm_q, const MlaArgs &a, int NH, bool fp8, cudaStream_t st);
+// pair: with 128 heads, run the two 64-head CTAs of a query as a cluster that
+// shares every gathered row.
+cudaError_t launch_sparse_mla(const CUtensorMap &tm_q, const MlaArgs &a, int NH, bool fp8, bool pair,
+                              cudaStream_t st);
 
 // Quantisers (quant.cu).
 cudaError_t launch_quant_mxfp8(const uint16_t *x, int64_t n, uint8_t *q, uint8_t *e8m0, cudaStream_t st);

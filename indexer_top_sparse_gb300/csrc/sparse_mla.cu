@@ -679,16 +679,16 @@ static cudaError_t launch_tc(const CUtensorMap &tq, const MlaArgs &a, cudaStream
 }
 
 template <bool kF8>
-static cudaError_t launch_heads(const CUtensorMap &tq, const MlaArgs &a, int NH, cudaStream_t st) {
-    if (NH == 64 && a.H == 128) return launch_tc<64, true, kF8>(tq, a, st);
+static cudaError_t launch_heads(const CUtensorMap &tq, const MlaArgs &a, int NH, bool pair, cudaStream_t st) {
+    if (NH == 64 && a.H == 128 && pair) return launch_tc<64, true, kF8>(tq, a, st);
     if (NH == 64) return launch_tc<64, false, kF8>(tq, a, st);
     if (NH == 32) return launch_tc<32, false, kF8>(tq, a, st);
     if (NH == 16) return launch_tc<16, false, kF8>(tq, a, st);
     return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_sparse_mla(const CUtensorMap &tq, const MlaArgs &a, int NH, bool fp8, cudaStream_t st) {
-    const cudaError_t e = fp8 ? launch_heads<true>(tq, a, NH, st) : launch_heads<false>(tq, a, NH, st);
+cudaError_t launch_sparse_mla(const CUtensorMap &tq, const MlaArgs &a, int NH, bool fp8, bool pair, cudaStream_t st) {
+    const cudaError_t e = fp8 ? launch_heads<true>(tq, a, NH, pair, st) : launch_heads<false>(tq, a, NH, pair, st);
     if (e != cudaSuccess || a.splits == 1) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((NH + 3) / 4, a.H / NH, a.T);

@@ -124,3 +124,15 @@ def test_reference_max_moves_across_tiles(orc, order, H):
         _compare(orc, wl, idx)
     finally:
         d.set_tuning("mla_splits", 0)
+
+
+def test_unpaired_128_heads_matches(orc):
+    # the two 64-head CTAs of a 128-head query without the shared gather
+    import indexer_top_sparse_gb300 as d
+    rng = np.random.default_rng(128)
+    wl = make_workload("mla", [3000, 700], [1, 1], H=128, K=1024, page_size=64, seed=128, with_idx=False)
+    d.set_tuning("mla_pair", -1)
+    try:
+        _compare(orc, wl, _random_indices(rng, wl, 1024, pad_frac=0.05))
+    finally:
+        d.set_tuning("mla_pair", 0)
