@@ -27,7 +27,10 @@ constexpr size_t kErrBytes = 256;  // error word block at the start of every wor
 // ---------------------------------------------------------------- tuning knobs
 // 0 = automatic.  Set through dsa_set_tuning(); read on every call.
 std::atomic<int> g_idx_cluster{0}, g_idx_stages{0}, g_idx_group{0}, g_mla_splits{0}, g_topk_cluster{0};
-std::atomic<int> g_mla_pair{0};  // 0 automatic (pair the two 64-head CTAs of a 128-head query), 1 pair, -1 never
+// 1: run the two 64-head CTAs of a 128-head query as a pair sharing each
+// gathered row; 0 (automatic) and -1: independent CTAs, measured slightly
+// faster on GB300 (both read a row at about the same time, the second from L2)
+std::atomic<int> g_mla_pair{0};
 
 int sm_count() {
     int dev = 0, n = 0;
@@ -478,7 +481,7 @@ dsa_status dsa_sparse_mla(const void *q, const void *kv_cache, const void *kv_ro
     CUtensorMap tq;
     if (!encode_2d_bf16(&tq, q, 576, (uint64_t)T * H, (uint32_t)NH)) return DSA_ERR_CUDA;
     return cuda_status(
-        dsa::launch_sparse_mla(tq, a, NH, fp8, g_mla_pair.load() >= 0, static_cast<cudaStream_t>(stream)));
+        dsa::launch_sparse_mla(tq, a, NH, fp8, g_mla_pair.load() > 0, static_cast<cudaStream_t>(stream)));
 }
 
 dsa_status dsa_quant_mxfp8(const void *x, int64_t n, void *q, void *e8m0, void *stream) {

@@ -126,12 +126,29 @@ def test_reference_max_moves_across_tiles(orc, order, H):
         d.set_tuning("mla_splits", 0)
 
 
-def test_unpaired_128_heads_matches(orc):
-    # the two 64-head CTAs of a 128-head query without the shared gather
+@pytest.mark.parametrize("fp8", [False, True])
+def test_paired_128_heads_matches(orc, fp8):
+    # the two 64-head CTAs of a 128-head query as a cluster sharing each row
     import indexer_top_sparse_gb300 as d
     rng = np.random.default_rng(128)
     wl = make_workload("mla", [3000, 700], [1, 1], H=128, K=1024, page_size=64, seed=128, with_idx=False)
-    d.set_tuning("mla_pair", -1)
+    if fp8:
+        nope, rope, sc = orc.quant_fp8_rows(wl.kv)
+        idx = _random_indices(rng, wl, 1024, pad_frac=0.05)
+        d.set_tuning("mla_pair", 1)
+        try:
+            ws = d.Workspace(d.sparse_mla_workspace_size(wl.T, wl.H, idx.shape[1]))
+            out = d.dsa_sparse_mla(dev_bf16(wl.q), dev(nope), dev(wl.page_table), dev(wl.seq_lens), dev(wl.cu_q),
+                                   dev(idx), wl.scale, workspace=ws, kv_rope=dev_bf16(rope), kv_scale=dev(sc),
+                                   dtype="fp8_rowscale")
+            ws.check()
+        finally:
+            d.set_tuning("mla_pair", 0)
+        ref, _ = orc.sparse_mla(wl.q, nope, wl.page_table, wl.cu_q, idx, wl.scale, wl.page_size,
+                                dtype=orc.KV_FP8_ROWSCALE, kv_rope=rope, kv_scale=sc)
+        np.testing.assert_allclose(out.float().cpu().numpy(), ref, atol=ATOL, rtol=RTOL)
+        return
+    d.set_tuning("mla_pair", 1)
     try:
         _compare(orc, wl, _random_indices(rng, wl, 1024, pad_frac=0.05))
     finally:
