@@ -91,7 +91,8 @@ const char *dsa_status_string(dsa_status s);
  * (shared-memory ring depth 2..4), "indexer_group" (query rows per cluster:
  * 1, 2 or 4), "mla_splits" (key splits per query row), "mla_pair" (with 128
  * heads, run the two 64-head CTAs of a query as a cluster sharing every
- * gathered row: 1 yes; 0 (automatic) or -1 no), "topk_cluster".
+ * gathered row: 1 yes, -1 no, 0 automatic = yes when the launch needs more
+ * than one wave of CTAs), "topk_cluster".
  * Returns 0, or -1 for an unknown name.  Results do not depend on them. */
 int dsa_set_tuning(const char *name, int value);
 

@@ -28,8 +28,7 @@ constexpr size_t kErrBytes = 256;  // error word block at the start of every wor
 // 0 = automatic.  Set through dsa_set_tuning(); read on every call.
 std::atomic<int> g_idx_cluster{0}, g_idx_stages{0}, g_idx_group{0}, g_mla_splits{0}, g_topk_cluster{0};
 // 1: run the two 64-head CTAs of a 128-head query as a pair sharing each
-// gathered row; 0 (automatic) and -1: independent CTAs, measured slightly
-// faster on GB300 (both read a row at about the same time, the second from L2)
+// gathered row; -1: independent CTAs; 0: automatic (see mla_pair).
 std::atomic<int> g_mla_pair{0};
 
 int sm_count() {
@@ -236,6 +235,17 @@ int mla_splits(int T, int H, int K) {
     const int nsm = sm_count();
     if (pairs >= nsm) return min_splits;
     return std::max(min_splits, std::min<int>(max_splits, (int)(nsm / pairs)));
+}
+
+// Pairs only when the launch takes more than one wave of CTAs.  Within one
+// wave the two independent CTAs of a query read each row at about the same
+// time, the second from L2, and skip the pair's forwarding (measured 2 us
+// faster on the 32-row decode); across waves they drift apart, the second
+// read misses L2, and the pair is faster (3-6 % on prefill).
+bool mla_pair(int T, int H, int splits) {
+    const int forced = g_mla_pair.load();
+    if (forced != 0) return forced > 0;
+    return mla_heads_per_cta(H) == 64 && H == 128 && (long long)T * mla_groups(H) * splits > sm_count();
 }
 
 dsa_status cuda_status(cudaError_t e) {
@@ -481,7 +491,7 @@ dsa_status dsa_sparse_mla(const void *q, const void *kv_cache, const void *kv_ro
     CUtensorMap tq;
     if (!encode_2d_bf16(&tq, q, 576, (uint64_t)T * H, (uint32_t)NH)) return DSA_ERR_CUDA;
     return cuda_status(
-        dsa::launch_sparse_mla(tq, a, NH, fp8, g_mla_pair.load() > 0, static_cast<cudaStream_t>(stream)));
+        dsa::launch_sparse_mla(tq, a, NH, fp8, mla_pair(T, H, splits), static_cast<cudaStream_t>(stream)));
 }
 
 dsa_status dsa_quant_mxfp8(const void *x, int64_t n, void *q, void *e8m0, void *stream) {

@@ -60,12 +60,29 @@ __device__ __forceinline__ uint32_t score_key(float x) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+constexpr int kCandCap = 128;   // threshold-bucket keys one CTA may hand to the bucket selection
+constexpr int kAllCap = 512;    // the same for the whole cluster
+constexpr int kMaxSelThreads = 320;
+
 struct __align__(16) SelectSmem {
     uint32_t hist[2][kHist];
     uint32_t tot[kHist];
     int32_t scan[2][16];
     int32_t cnt[4];       // this CTA's (n_gt, n_eq) for the cluster exchange; [2] = abort flag
     uint32_t bcast[4];    // digit, count-above
+    // bucket selection: published [keys above the bucket, bucket keys kept, overflow, pos0]
+    int32_t pub[4];
+    uint32_t ncand;
+    uint32_t pad_[3];
+    uint32_t cand_key[kCandCap];
+    int32_t cand_loc[kCandCap];
+    uint32_t all_key[kAllCap];
+    int32_t all_pos[kAllCap];
+    int32_t all_cta[kAllCap];
+    int32_t cta_off[kMaxCluster + 1];
+    int32_t cta_gt[kMaxCluster];
+    int32_t cta_sel[kMaxCluster];
+    int32_t seg_sel[kMaxSelThreads];
 };
 
 // Exclusive scan of one int per thread across the CTA (kT threads).
@@ -90,6 +107,146 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int32_t *warp_tot, in
     __syncthreads();
     if (total) *total = all;
     return before + x - v;
+}
+
+// Final step of the selection once two radix digits have fixed the top 16
+// bits of the threshold (prefix under mask) and krem keys are still needed
+// from that 16-bit bucket, which typically holds a few dozen keys: every CTA
+// counts its keys above the bucket per thread segment and lists its bucket
+// keys; all CTAs copy the cluster's list and rank it by (key descending,
+// position ascending), mark their own bucket keys selected (all ones) or not
+// (zero) in place, and write their selected positions in order after those
+// of the lower-ranked CTAs.  Returns false, with every CTA agreeing, when the
+// bucket is too large for this path (the caller continues digit by digit).
+template <int kT>
+__device__ bool select_from_bucket(uint32_t kb, int n_local, int pos0, int K, int32_t *out, SelectSmem &ss,
+                                   uint32_t prefix, uint32_t mask, int krem) {
+    static_assert(kT <= kMaxSelThreads, "segment counters");
+    cg::cluster_group cluster = cg::this_cluster();
+    const int C = (int)cluster.num_blocks(), my = (int)cluster.block_rank();
+    const int tid = threadIdx.x;
+    if (tid == 0) ss.ncand = 0u;
+    ss.seg_sel[tid] = 0;
+    if (tid < kMaxCluster) ss.cta_sel[tid] = 0;
+    __syncthreads();
+    const int seg = (n_local + kT - 1) / kT;
+    const int l0 = min(n_local, tid * seg), l1 = min(n_local, l0 + seg);
+    int n_gt = 0;
+    // loads four at a time, then the tests (keeps several loads in flight)
+    for (int l = l0; l < l1; l += 4) {
+        uint32_t k4[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) k4[u] = l + u < l1 ? lds32(kb + 4 * (l + u)) : 0u;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const uint32_t k = k4[u], m = k & mask;
+            n_gt += k != 0u && m > prefix;
+            if (k != 0u && m == prefix) {
+                const uint32_t c = atomicAdd(&ss.ncand, 1u);
+                if (c < (uint32_t)kCandCap) {
+                    ss.cand_key[c] = k;
+                    ss.cand_loc[c] = l + u;
+                }
+            }
+        }
+    }
+    int cta_gt = 0;
+    block_exclusive_scan<kT>(n_gt, ss.scan[1], &cta_gt);
+    if (tid == 0) {
+        ss.pub[0] = cta_gt;
+        ss.pub[1] = (int)min(ss.ncand, (uint32_t)kCandCap);
+        ss.pub[2] = ss.ncand > (uint32_t)kCandCap;
+        ss.pub[3] = pos0;
+    }
+    cluster.sync();
+    if (tid < C) {
+        const int4 p = *reinterpret_cast<const int4 *>(cluster.map_shared_rank(ss.pub, tid));
+        ss.cta_gt[tid] = p.x;
+        ss.cta_off[tid + 1] = p.z ? -1 : p.y;  // -1 marks an overflow
+        ss.all_pos[tid] = p.w;                 // pos0 of each CTA, until the list is copied
+    }
+    __syncthreads();
+    bool fits = true;
+    int total = 0;
+    int pos0s[kMaxCluster];
+    for (int c = 0; c < C; ++c) {
+        const int n = ss.cta_off[c + 1];
+        fits = fits && n >= 0;
+        pos0s[c] = ss.all_pos[c];
+        total += max(n, 0);
+    }
+    fits = fits && total <= kAllCap;
+    __syncthreads();
+    if (!fits) {
+        cluster.sync();  // nobody reuses the shared state another CTA may still read
+        return false;
+    }
+    if (tid == 0) {
+        int o = 0;
+        for (int c = 0; c < C; ++c) {
+            const int n = ss.cta_off[c + 1];
+            ss.cta_off[c] = o;
+            o += n;
+        }
+        ss.cta_off[C] = o;
+    }
+    __syncthreads();
+    for (int i = tid; i < total; i += kT) {
+        int c = 0;
+        while (c + 1 < C && ss.cta_off[c + 1] <= i) ++c;
+        const int li = i - ss.cta_off[c];
+        const uint32_t k = cluster.map_shared_rank(ss.cand_key, c)[li];
+        const int l = cluster.map_shared_rank(ss.cand_loc, c)[li];
+        ss.all_key[i] = k;
+        ss.all_pos[i] = pos0s[c] + l;
+        ss.all_cta[i] = c;
+    }
+    __syncthreads();
+    cluster_arrive();  // done reading the other CTAs; the matching wait is at the end
+    const uint32_t ak = smem_u32(ss.all_key), ap = smem_u32(ss.all_pos);
+    for (int i = tid; i < total; i += kT) {
+        const uint32_t ki = ss.all_key[i];
+        const int pi = ss.all_pos[i];
+        int r = 0;
+        int j = 0;
+        for (; j + 4 <= total; j += 4) {
+            uint32_t kj[4];
+            int pj[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                kj[u] = lds32(ak + 4 * (j + u));
+                pj[u] = (int)lds32(ap + 4 * (j + u));
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) r += (kj[u] > ki) || (kj[u] == ki && pj[u] < pi);
+        }
+        for (; j < total; ++j) {
+            const uint32_t kj = lds32(ak + 4 * j);
+            r += (kj > ki) || (kj == ki && (int)lds32(ap + 4 * j) < pi);
+        }
+        const bool sel = r < krem;
+        const int c = ss.all_cta[i];
+        if (sel) atomicAdd(&ss.cta_sel[c], 1);
+        if (c == my) {
+            const int l = pi - pos0;
+            sts32(kb + 4 * l, sel ? 0xFFFFFFFFu : 0u);
+            if (sel) atomicAdd(&ss.seg_sel[l / seg], 1);
+        }
+    }
+    __syncthreads();
+    int base = 0;
+    for (int c = 0; c < my; ++c) base += ss.cta_gt[c] + ss.cta_sel[c];
+    int slot = base + block_exclusive_scan<kT>(n_gt + ss.seg_sel[tid], ss.scan[0], nullptr);
+    for (int l = l0; l < l1; l += 4) {
+        uint32_t k4[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) k4[u] = l + u < l1 ? lds32(kb + 4 * (l + u)) : 0u;
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            if (k4[u] != 0u && (k4[u] & mask) > prefix && slot < K) out[slot++] = pos0 + l + u;
+    }
+    cluster_wait();  // nobody leaves while another CTA may still read its candidates
+    return true;
 }
 
 // Cluster-wide exact Top-K over keys held in shared memory.
@@ -195,6 +352,7 @@ __device__ void cluster_topk(const uint32_t *keys, int n_local, int pos0, int n_
         const bool done = ss.tot[digit] == (uint32_t)krem;
         __syncthreads();
         if (done) break;
+        if (pass == 1 && select_from_bucket<kT>(kb, n_local, pos0, K, out, ss, prefix, mask, krem)) return;
     }
 
     // count (key > threshold) and (key == threshold) in this CTA, by contiguous

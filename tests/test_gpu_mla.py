@@ -126,6 +126,20 @@ def test_reference_max_moves_across_tiles(orc, order, H):
         d.set_tuning("mla_splits", 0)
 
 
+@pytest.mark.parametrize("pair", [0, -1])
+def test_128_heads_over_several_waves(orc, pair):
+    # 200 query rows x 2 head groups: more CTAs than SMs, so the automatic
+    # choice pairs the two head groups; -1 keeps them independent
+    import indexer_top_sparse_gb300 as d
+    rng = np.random.default_rng(129)
+    wl = make_workload("mla", [600, 300], [120, 80], H=128, K=192, page_size=64, seed=129, with_idx=False)
+    d.set_tuning("mla_pair", pair)
+    try:
+        _compare(orc, wl, _random_indices(rng, wl, 192, pad_frac=0.05))
+    finally:
+        d.set_tuning("mla_pair", 0)
+
+
 @pytest.mark.parametrize("fp8", [False, True])
 def test_paired_128_heads_matches(orc, fp8):
     # the two 64-head CTAs of a 128-head query as a cluster sharing each row

@@ -1,5 +1,6 @@
 """GPU Top-K from given fp32 scores: bit-exact against the oracle's full-sort
-selection on the same scores, over ragged lengths, exact ties, signed zeros
+selection on the same scores, over ragged lengths, exact ties (in buckets
+too large and small enough for the final in-bucket ranking), signed zeros
 and every cluster size."""
 import numpy as np
 import pytest
@@ -45,6 +46,24 @@ def test_topk_every_cluster_size(orc, C):
     finally:
         d.set_tuning("topk_cluster", 0)
     assert np.array_equal(got, orc.topk_rows(s, lens, 2048))
+
+
+@pytest.mark.parametrize("C", [1, 4, 16])
+@pytest.mark.parametrize("K", [1, 333, 2048])
+def test_topk_ties_inside_small_bucket(orc, C, K):
+    # scores on a 1/1024 grid in [0, 3): a bucket of the top 16 key bits spans
+    # 8 grid values, about 50 keys at this length, each value ~7 times, so the
+    # threshold bucket is ranked directly and its ties split by position
+    import indexer_top_sparse_gb300 as d
+    rng = np.random.default_rng(70 + C + K)
+    s = (rng.integers(0, 3072, size=(3, 20000)) / 1024.0).astype(np.float32)
+    lens = np.array([20000, 19999, 4097], np.int32)
+    d.set_tuning("topk_cluster", C)
+    try:
+        got = d.dsa_topk_from_scores(dev(s), dev(lens), K).cpu().numpy()
+    finally:
+        d.set_tuning("topk_cluster", 0)
+    assert np.array_equal(got, orc.topk_rows(s, lens, K))
 
 
 def test_topk_all_equal_takes_lowest_positions(orc):
