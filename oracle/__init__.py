@@ -28,7 +28,7 @@ _lock = threading.Lock()
 _lib = None
 
 IDX_BF16, IDX_MXFP8 = 0, 1
-KV_BF16, KV_FP8_ROWSCALE = 0, 1
+KV_BF16, KV_FP8_ROWSCALE, KV_FP8_TILE128 = 0, 1, 2
 
 
 def build(force: bool = False) -> str:
@@ -61,6 +61,8 @@ def _load():
             lib.orc_quant_mxfp8.restype = None
             lib.orc_quant_fp8_rows.argtypes = [P, i64, P, P, P]
             lib.orc_quant_fp8_rows.restype = None
+            lib.orc_quant_fp8_tiles.argtypes = [P, i64, P, P, P]
+            lib.orc_quant_fp8_tiles.restype = None
             lib.orc_index_scores_row.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P, P, P, P, i64, P,
                                                  i32, i64, P]
             lib.orc_index_scores_row.restype = ctypes.c_int
@@ -131,6 +133,21 @@ def quant_fp8_rows(kv_bf16_bits: np.ndarray):
     rope = np.empty(kv.shape[:-1] + (64,), np.uint16)
     scale = np.empty(kv.shape[:-1], np.float32)
     _load().orc_quant_fp8_rows(_p(kv), rows, _p(nope), _p(rope), _p(scale))
+    return nope, rope, scale
+
+
+def quant_fp8_tiles(kv_bf16_bits: np.ndarray):
+    """FP8 tile quantisation of [..., 576] bf16 latent rows, one scale per
+    128 latent dims.  Returns (nope e4m3 [..., 512] uint8, rope bf16 bits
+    [..., 64] uint16, scale fp32 [..., 4])."""
+    kv = _c(kv_bf16_bits, np.uint16)
+    if kv.shape[-1] != 576:
+        raise ValueError("last dim must be 576")
+    rows = kv.size // 576
+    nope = np.empty(kv.shape[:-1] + (512,), np.uint8)
+    rope = np.empty(kv.shape[:-1] + (64,), np.uint16)
+    scale = np.empty(kv.shape[:-1] + (4,), np.float32)
+    _load().orc_quant_fp8_tiles(_p(kv), rows, _p(nope), _p(rope), _p(scale))
     return nope, rope, scale
 
 
@@ -206,7 +223,8 @@ def sparse_mla(q, kv_cache, page_table, cu_q, indices, scale, page_size, *, dtyp
     """Sparse MLA attention for query rows `rows` (None: all T).
     q [T, H, D] bf16 bits; kv_cache [pages, page_size, D] bf16 bits (or
     [pages, page_size, 512] e4m3 with kv_rope [..., 64] bf16 and kv_scale
-    [pages, page_size] fp32); indices [T, K] logical positions, -1 skipped.
+    [pages, page_size] fp32, or [pages, page_size, 4] fp32 for KV_FP8_TILE128);
+    indices [T, K] logical positions, -1 skipped.
     Returns (out [n_rows, H, Dv] fp32, lse [n_rows, H] fp32)."""
     q = _c(q, np.uint16)
     T, H, Dq = q.shape

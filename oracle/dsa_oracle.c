@@ -36,6 +36,15 @@
  *    index Q/K, and FP8 E4M3 for the main KV cache (per-row fp32 scale on the
  *    512 latent dims, rope dims kept bf16).  Element and scale encodings follow
  *    the OCP 8-bit floating point and OCP Microscaling v1.0 definitions.
+ *  - FP8 KV at the pages' per-token-head-tile granularity ("Day-0 Inference
+ *    Adaptation and Optimization for Hybrid Attention Architectures", §4
+ *    Optimization 2; "Optimizing Inference for Hybrid Attention LLMs: A
+ *    Practical Guide to Day-0 Adaptation", §4 Hierarchical Quantization;
+ *    "Day0 Inference Support and Performance Optimization for New-Architecture
+ *    LLMs", §5 Tiered Quantization, item 2): within each token's
+ *    latent row every tile of 128 consecutive elements has its own scale, so
+ *    the 512 latent dims carry four fp32 scales; each tile uses the row rule
+ *    above on its own amax.  The rope dims stay bf16.
  *
  * Every function here is pinned by a CPU test against something other than
  * itself (brute force, closed forms, library routines on special cases,
@@ -50,6 +59,7 @@
 #define ORC_IDX_MXFP8 1
 #define ORC_KV_BF16 0
 #define ORC_KV_FP8_ROWSCALE 1
+#define ORC_KV_FP8_TILE128 2
 
 /* ------------------------------------------------------------------------ */
 /* Scalar codecs, from the format definitions.                              */
@@ -402,6 +412,36 @@ int orc_index_topk(int dtype, int H_I, int d_I, const void *q_idx, const uint8_t
     return 0;
 }
 
+/* FP8 KV tile quantiser: as orc_quant_fp8_rows, but every tile of 128
+ * latent dims (dims 128j..128j+127, j = 0..3) has its own scale
+ * scale[r*4 + j] = fl32(amax_j / 448) (1 when amax_j is 0), and its elements
+ * are E4M3_rne_sat(fl32(x / scale[r*4 + j])). */
+void orc_quant_fp8_tiles(const uint16_t *kv, int64_t rows, uint8_t *nope, uint16_t *rope, float *scale)
+{
+    int64_t r;
+    int j, d;
+    for (r = 0; r < rows; ++r) {
+        const uint16_t *row = kv + r * 576;
+        for (j = 0; j < 4; ++j) {
+            float amax = 0.0f, s;
+            for (d = 128 * j; d < 128 * (j + 1); ++d) {
+                float v = (float)fabs(orc_bf16_to_f64(row[d]));
+                if (v > amax)
+                    amax = v;
+            }
+            s = (amax == 0.0f) ? 1.0f : amax / 448.0f;
+            scale[r * 4 + j] = s;
+            for (d = 128 * j; d < 128 * (j + 1); ++d) {
+                float xv = (float)orc_bf16_to_f64(row[d]);
+                float y = xv / s;
+                nope[r * 512 + d] = orc_f64_to_e4m3_sat((double)y);
+            }
+        }
+        for (d = 0; d < 64; ++d)
+            rope[r * 64 + d] = row[512 + d];
+    }
+}
+
 /* ------------------------------------------------------------------------ */
 /* Sparse MLA attention.                                                    */
 /* ------------------------------------------------------------------------ */
@@ -412,6 +452,8 @@ static double orc_kv_elem(int dtype, const void *kv, const uint16_t *kv_rope, co
 {
     if (dtype == ORC_KV_BF16)
         return orc_bf16_to_f64(((const uint16_t *)kv)[row * D + d]);
+    if (d < 512 && dtype == ORC_KV_FP8_TILE128)
+        return orc_e4m3_to_f64(((const uint8_t *)kv)[row * 512 + d]) * (double)kv_scale[row * 4 + d / 128];
     if (d < 512)
         return orc_e4m3_to_f64(((const uint8_t *)kv)[row * 512 + d]) * (double)kv_scale[row];
     return orc_bf16_to_f64(kv_rope[row * 64 + (d - 512)]);

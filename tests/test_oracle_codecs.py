@@ -162,3 +162,42 @@ def test_fp8_row_quant_matches_library_cast(orc):
         y = np.clip(y, -448.0, 448.0).astype(np.float32)
         ref = torch.from_numpy(y).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
         assert np.array_equal(nope[r], ref), r
+
+
+def test_fp8_tile_quant_matches_library_cast(orc):
+    # one scale per 128 latent dims: tiles of very different magnitude, an
+    # all-zero tile (scale 1) and an all-zero row
+    rng = np.random.default_rng(5)
+    kv = rng.standard_normal((7, 576)).astype(np.float32)
+    kv[1, 128:256] = 0.0
+    kv[2, :512] = 0.0
+    kv[3, 256:384] *= np.float32(1e-3)
+    kv[4, 384:512] *= np.float32(300.0)
+    bits = bf16_bits(kv)
+    nope, rope, scale = orc.quant_fp8_tiles(bits)
+    assert scale.shape == (7, 4)
+    assert np.array_equal(rope, bits[:, 512:])
+    xv = bf16_to_f32(bits)
+    for r in range(7):
+        for j in range(4):
+            tile = xv[r, 128 * j:128 * (j + 1)]
+            amax = np.float32(np.abs(tile).max())
+            s = np.float32(1.0) if amax == 0 else np.float32(amax / np.float32(448.0))
+            assert scale[r, j] == s, (r, j)
+            y = np.clip((tile / s).astype(np.float32), -448.0, 448.0).astype(np.float32)
+            ref = torch.from_numpy(y).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+            assert np.array_equal(nope[r, 128 * j:128 * (j + 1)], ref), (r, j)
+
+
+def test_fp8_tile_quant_equals_row_quant_when_tiles_share_amax(orc):
+    # with the same amax in all four tiles the tile scales all equal the row
+    # scale, so the two quantisers must produce the same codes
+    rng = np.random.default_rng(6)
+    kv = rng.standard_normal((5, 576)).astype(np.float32)
+    for j in range(4):
+        kv[:, 128 * j + 7] = np.float32(9.5)
+    bits = bf16_bits(kv)
+    n_t, r_t, s_t = orc.quant_fp8_tiles(bits)
+    n_r, r_r, s_r = orc.quant_fp8_rows(bits)
+    assert np.array_equal(n_t, n_r) and np.array_equal(r_t, r_r)
+    assert np.array_equal(s_t, np.repeat(s_r[:, None], 4, axis=1))

@@ -108,3 +108,45 @@ def test_fp8_quantised_cache_close_to_bf16_attention(orc):
                           dtype=orc.KV_FP8_ROWSCALE, kv_rope=rope, kv_scale=sc, D=576, Dv=512, num_pages=P)
     b, _ = orc.sparse_mla(q, kv, pt, np.array([0, 1], np.int32), sel, 1 / math.sqrt(192), ps)
     np.testing.assert_allclose(a, b, atol=6e-2, rtol=3e-2)
+
+
+def test_fp8_tile_path_equals_bf16_path_on_representable_values(orc):
+    # power-of-two scales that differ per 128-dim tile: the dequantised values
+    # are exact in bf16, so the tile path must equal the bf16 path; a wrong
+    # tile index (or the row scale) changes the result
+    n, ps, H = 40, 16, 3
+    rng = np.random.default_rng(26)
+    pt, P = make_page_table(rng, [n], ps)
+    codes = rng.integers(0, 256, size=(P, ps, 512)).astype(np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x31
+    codes[(codes & 0x78) >= 0x60] &= 0x9F
+    rope = bf16_bits(rng.standard_normal((P, ps, 64)).astype(np.float32))
+    scale = (2.0 ** rng.integers(-4, 3, size=(P, ps, 4))).astype(np.float32)
+    scale[..., 2] *= np.float32(8.0)
+    table = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).double().numpy()
+    deq = table[codes] * np.repeat(scale, 128, axis=-1).astype(np.float64)
+    full = np.concatenate([bf16_bits(deq.astype(np.float32)), rope], axis=-1)
+    assert np.array_equal(bf16_to_f32(full[..., :512]), deq.astype(np.float32))
+    q = bf16_bits(rng.standard_normal((1, H, 576)).astype(np.float32) * np.float32(0.05))
+    sel = rng.choice(n, 24, replace=False).astype(np.int32)[None, :]
+    a, la = orc.sparse_mla(q, codes, pt, np.array([0, 1], np.int32), sel, 0.1, ps, dtype=orc.KV_FP8_TILE128,
+                           kv_rope=rope, kv_scale=scale, D=576, Dv=512, num_pages=P)
+    b, lb = orc.sparse_mla(q, full, pt, np.array([0, 1], np.int32), sel, 0.1, ps)
+    np.testing.assert_allclose(a, b, rtol=1e-12, atol=1e-9)
+    np.testing.assert_allclose(la, lb, rtol=1e-12)
+
+
+def test_fp8_tile_quantised_cache_close_to_bf16_attention(orc):
+    n, ps, H = 128, 64, 8
+    rng = np.random.default_rng(27)
+    pt, P = make_page_table(rng, [n], ps)
+    kv = rng.standard_normal((P, ps, 576)).astype(np.float32)
+    kv[..., 256:384] *= np.float32(0.01)                    # a quiet tile: finer scale than the row's
+    kv = bf16_bits(kv)
+    nope, rope, sc = orc.quant_fp8_tiles(kv)
+    q = bf16_bits(rng.standard_normal((1, H, 576)).astype(np.float32))
+    sel = rng.choice(n, 64, replace=False).astype(np.int32)[None, :]
+    a, _ = orc.sparse_mla(q, nope, pt, np.array([0, 1], np.int32), sel, 1 / math.sqrt(192), ps,
+                          dtype=orc.KV_FP8_TILE128, kv_rope=rope, kv_scale=sc, D=576, Dv=512, num_pages=P)
+    b, _ = orc.sparse_mla(q, kv, pt, np.array([0, 1], np.int32), sel, 1 / math.sqrt(192), ps)
+    np.testing.assert_allclose(a, b, atol=6e-2, rtol=3e-2)
