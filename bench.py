@@ -214,6 +214,8 @@ def run_other_workload(args, world, rank, local_rank):
 
     H, K, ps, scale = 128, 2048, 64, float(1.0 / np.sqrt(192.0))
     fp8 = args.workload.endswith("fp8")
+    kv_fmt = "fp8_tile128" if args.kv_scales == "tile128" else "fp8_rowscale"
+    row_b = 512 + 128 + (16 if kv_fmt == "fp8_tile128" else 4)   # e4m3 latent + bf16 rope + fp32 scales
     if args.workload == "decode_b64_mixed_fp8":
         lens = np.random.default_rng(args.seed + rank + 7919).integers(4096, 131072, size=64, endpoint=True)
         lens = lens.astype(np.int32)
@@ -237,7 +239,8 @@ def run_other_workload(args, world, rank, local_rank):
               "head_w": torch.randn(T_all, 64, generator=gen, device=dev) / 8.0}
         if fp8:
             st["k_idx"], st["k_sc"] = d.dsa_quant_mxfp8(k_bf)
-            st["kv"], st["rope"], st["rsc"] = d.dsa_quant_fp8_rows(kv_bf)
+            quant = d.dsa_quant_fp8_tiles if kv_fmt == "fp8_tile128" else d.dsa_quant_fp8_rows
+            st["kv"], st["rope"], st["rsc"] = quant(kv_bf)
             st["qi8"] = torch.empty((T_all, 64, 128), dtype=torch.uint8, device=dev)
             st["qi_sc"] = torch.empty((T_all, 64, 4), dtype=torch.uint8, device=dev)
         else:
@@ -289,7 +292,7 @@ def run_other_workload(args, world, rank, local_rank):
             if fp8:
                 d.dsa_sparse_mla(st["q"][r0:r0 + T], st["kv"], c["pt"], c["sl"], c["cq"], idx[:T], scale,
                                  out=out[r0:r0 + T], workspace=ws, kv_rope=st["rope"], kv_scale=st["rsc"],
-                                 dtype="fp8_rowscale")
+                                 dtype=kv_fmt)
             else:
                 d.dsa_sparse_mla(st["q"][r0:r0 + T], st["kv"], c["pt"], c["sl"], c["cq"], idx[:T], scale,
                                  out=out[r0:r0 + T], workspace=ws)
@@ -334,7 +337,7 @@ def run_other_workload(args, world, rank, local_rank):
             key_b = 132 if fp8 else 256
             idx_bytes += float(np.sum(n * key_b + 64 * 128 * (1 if fp8 else 2) + (256 if fp8 else 0) + 256 + 4 * K
                                       + 4 * np.ceil(n / ps)))
-            mla_b += float(np.sum(sel * (644 if fp8 else 1152) + H * 1152 + H * 1024 + 4 * K + 4 * np.ceil(n / ps)))
+            mla_b += float(np.sum(sel * (row_b if fp8 else 1152) + H * 1152 + H * 1024 + 4 * K + 4 * np.ceil(n / ps)))
     sel_all = np.concatenate(sel_all)
     f_mla = attention_flops(sel_all, H)
     f_idx = n_hist * 64 * 128 * 2.0
@@ -351,6 +354,7 @@ def run_other_workload(args, world, rank, local_rank):
             "data": "synthetic (seeded N(0,1) drawn on the device; FP8 caches made by the library's quantisers)",
             "config": {"workload": args.workload, "H": H, "K": K, "H_I": 64, "d_I": 128, "page_size": ps,
                        "query_rows": T_all, "cached_positions": int(np.sum(cache_lens)), "chunks": len(plan),
+                       "kv_cache": kv_fmt if fp8 else "bf16",
                        "parallelism": f"replicas{max(world, 1)}",
                        "l2": (f"inputs larger than L2: {copies} alternating cop{'ies' if copies > 1 else 'y'} of "
                               f"every step input ({in_bytes / 2**30:.2f} GiB each), no flush")},
@@ -393,6 +397,8 @@ def main():
                          "512 MiB buffer")
     ap.add_argument("--workload", default="decode_b32_n32768",
                     choices=["decode_b32_n32768", "decode_b64_mixed_fp8", "prefill_16k", "prefill_131k_chunked_fp8"])
+    ap.add_argument("--kv-scales", default="row", choices=["row", "tile128"],
+                    help="FP8 workloads: one fp32 scale per latent row (default) or per 128 latent dims")
     ap.add_argument("--batch", type=int, default=32,
                     help="sequences per rank (default 32, the benchmark workload; smaller only for profiling)")
     args = ap.parse_args()

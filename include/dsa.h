@@ -74,8 +74,11 @@ typedef enum {
 typedef enum { DSA_IDX_BF16 = 0, DSA_IDX_MXFP8 = 1 } dsa_idx_dtype;
 
 /* Main KV cache element type.  FP8_ROWSCALE: the 512 latent dims are E4M3 with
- * one fp32 scale per row, the 64 rope dims stay bf16. */
-typedef enum { DSA_KV_BF16 = 0, DSA_KV_FP8_ROWSCALE = 1 } dsa_kv_dtype;
+ * one fp32 scale per row, the 64 rope dims stay bf16.  FP8_TILE128: the same
+ * with one fp32 scale per tile of 128 latent dims (four per row), the
+ * per-token-head-tile granularity of "Day-0 Inference Adaptation and
+ * Optimization for Hybrid Attention Architectures", §4 Optimization 2. */
+typedef enum { DSA_KV_BF16 = 0, DSA_KV_FP8_ROWSCALE = 1, DSA_KV_FP8_TILE128 = 2 } dsa_kv_dtype;
 
 /* Fixed dimensions of this build. */
 #define DSA_INDEX_HEADS 64
@@ -158,9 +161,12 @@ dsa_status dsa_topk_from_scores(const float *scores, int64_t ld, const int32_t *
 /* Sparse MLA attention over the selected rows.
  *   q          [T, H, 576] bf16 query (latent 512 + rope 64)
  *   kv_cache   BF16: [num_pages, page_size, 576] bf16 latent rows
- *              FP8_ROWSCALE: [num_pages, page_size, 512] e4m3 latent dims
- *   kv_rope    FP8_ROWSCALE only: [num_pages, page_size, 64] bf16 rope dims
- *   kv_scale   FP8_ROWSCALE only: [num_pages, page_size] fp32 row scales
+ *              FP8_ROWSCALE / FP8_TILE128: [num_pages, page_size, 512] e4m3
+ *              latent dims
+ *   kv_rope    FP8 only: [num_pages, page_size, 64] bf16 rope dims
+ *   kv_scale   FP8_ROWSCALE: [num_pages, page_size] fp32 row scales;
+ *              FP8_TILE128: [num_pages, page_size, 4] fp32, entry j scales
+ *              latent dims 128j..128j+127
  *   indices    [T, K] int32 logical positions; entries < 0 are skipped
  *   out        [T, H, 512] bf16 OUT: sum_i softmax_i(scale * q_h . kv_i) kv_i[0:512]
  *   lse        [T, H] fp32 OUT (natural-log log-sum-exp of the scaled logits)
@@ -192,6 +198,16 @@ dsa_status dsa_quant_mxfp8(const void *x, int64_t n, void *q, void *e8m0, void *
  *   kv [rows, 576] bf16 in; nope [rows, 512] e4m3, rope [rows, 64] bf16 and
  *   scale [rows] fp32 out. */
 dsa_status dsa_quant_fp8_rows(const void *kv, int64_t rows, void *nope, void *rope, float *scale, void *stream);
+
+/* As dsa_quant_fp8_rows with one scale per tile of 128 latent dims: tile j
+ * (dims 128j..128j+127) has s_j = amax_j / 448 (1 when amax_j is 0) and
+ * elements E4M3(x / s_j); the per-token-head-tile format of "Day-0 Inference
+ * Adaptation and Optimization for Hybrid Attention Architectures", §4
+ * Optimization 2 (and "Day0 Inference Support and Performance Optimization
+ * for New-Architecture LLMs", §5 item 2).
+ *   kv [rows, 576] bf16 in; nope [rows, 512] e4m3, rope [rows, 64] bf16 and
+ *   scale [rows, 4] fp32 out. */
+dsa_status dsa_quant_fp8_tiles(const void *kv, int64_t rows, void *nope, void *rope, float *scale, void *stream);
 
 /* ---------------------------------------------------------------- no-allocation variant */
 

@@ -22,12 +22,13 @@ DSA_OK = 0
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "CUDA error", 4: "page id out of range",
           5: "selected index out of range", 6: "device wait timed out"}
 IDX_DTYPES = {"bf16": 0, "mxfp8": 1}
-KV_DTYPES = {"bf16": 0, "fp8_rowscale": 1}
+KV_DTYPES = {"bf16": 0, "fp8_rowscale": 1, "fp8_tile128": 2}
 
 # Every symbol include/dsa.h declares.
 EXPORTS = ("dsa_status_string", "dsa_set_tuning", "dsa_index_topk_workspace_size", "dsa_sparse_mla_workspace_size",
            "dsa_workspace_init", "dsa_get_error", "dsa_index_topk", "dsa_index_scores", "dsa_topk_from_scores",
-           "dsa_sparse_mla", "dsa_sparse_mla_static", "dsa_quant_mxfp8", "dsa_quant_fp8_rows")
+           "dsa_sparse_mla", "dsa_sparse_mla_static", "dsa_quant_mxfp8", "dsa_quant_fp8_rows",
+           "dsa_quant_fp8_tiles")
 
 
 class DSAError(RuntimeError):
@@ -83,6 +84,8 @@ def load(build_if_missing: bool = True):
         lib.dsa_quant_mxfp8.restype = c_int
         lib.dsa_quant_fp8_rows.argtypes = [P, i64, P, P, P, P]
         lib.dsa_quant_fp8_rows.restype = c_int
+        lib.dsa_quant_fp8_tiles.argtypes = [P, i64, P, P, P, P]
+        lib.dsa_quant_fp8_tiles.restype = c_int
         _lib = lib
         return lib
 
@@ -236,16 +239,16 @@ def dsa_sparse_mla(q, kv_cache, page_table, seq_lens, cu_q, indices, scale, *, o
     if D != 576:
         raise ValueError("q must be [T, H, 576]")
     _need(kv_cache, "kv_cache", torch.bfloat16 if dt == 0 else torch.uint8, 3, dev)
-    if dt == 1:
+    if dt in (1, 2):
         _need(kv_rope, "kv_rope", torch.bfloat16, 3, dev)
-        _need(kv_scale, "kv_scale", torch.float32, 2, dev)
+        _need(kv_scale, "kv_scale", torch.float32, 2 if dt == 1 else 3, dev)
         pp, pps = kv_cache.shape[0], kv_cache.shape[1]
-        if (kv_cache.shape[2] != 512 or tuple(kv_rope.shape) != (pp, pps, 64)
-                or tuple(kv_scale.shape) != (pp, pps)):
-            raise ValueError("FP8 cache: kv_cache [pages, page_size, 512] e4m3, kv_rope [.., 64] bf16, "
-                             "kv_scale [pages, page_size] fp32")
+        sshape = (pp, pps) if dt == 1 else (pp, pps, 4)
+        if kv_cache.shape[2] != 512 or tuple(kv_rope.shape) != (pp, pps, 64) or tuple(kv_scale.shape) != sshape:
+            raise ValueError("FP8 cache: kv_cache [pages, page_size, 512] e4m3, kv_rope [.., 64] bf16, kv_scale "
+                             "[pages, page_size] (fp8_rowscale) or [pages, page_size, 4] (fp8_tile128) fp32")
     elif kv_rope is not None or kv_scale is not None:
-        raise ValueError("kv_rope / kv_scale are for dtype='fp8_rowscale' only")
+        raise ValueError("kv_rope / kv_scale are for the FP8 dtypes only")
     elif kv_cache.shape[2] != 576:
         raise ValueError("kv_cache must be [pages, page_size, 576] bf16")
     _need(page_table, "page_table", torch.int32, 2, dev)
@@ -291,6 +294,17 @@ def dsa_quant_mxfp8(x, *, q=None, scales=None, stream=None):
 def dsa_quant_fp8_rows(kv, *, nope=None, rope=None, scale=None, stream=None):
     """FP8 row quantisation of [..., 576] bf16 latent rows.  Returns
     (nope e4m3 [..., 512] uint8, rope [..., 64] bf16, scale [...] fp32)."""
+    return _quant_fp8(kv, 1, nope, rope, scale, stream)
+
+
+def dsa_quant_fp8_tiles(kv, *, nope=None, rope=None, scale=None, stream=None):
+    """FP8 quantisation of [..., 576] bf16 latent rows with one scale per 128
+    latent dims.  Returns (nope e4m3 [..., 512] uint8, rope [..., 64] bf16,
+    scale [..., 4] fp32)."""
+    return _quant_fp8(kv, 4, nope, rope, scale, stream)
+
+
+def _quant_fp8(kv, tiles, nope, rope, scale, stream):
     lib = load()
     _need(kv, "kv", torch.bfloat16)
     if kv.shape[-1] != 576:
@@ -299,12 +313,13 @@ def dsa_quant_fp8_rows(kv, *, nope=None, rope=None, scale=None, stream=None):
     rows = kv.numel() // 576
     nope = torch.empty(lead + (512,), dtype=torch.uint8, device=kv.device) if nope is None else nope
     rope = torch.empty(lead + (64,), dtype=torch.bfloat16, device=kv.device) if rope is None else rope
-    scale = torch.empty(lead, dtype=torch.float32, device=kv.device) if scale is None else scale
+    if scale is None:
+        scale = torch.empty(lead if tiles == 1 else lead + (tiles,), dtype=torch.float32, device=kv.device)
     _need(nope, "nope", torch.uint8, None, kv.device)
     _need(rope, "rope", torch.bfloat16, None, kv.device)
     _need(scale, "scale", torch.float32, None, kv.device)
-    if nope.numel() != rows * 512 or rope.numel() != rows * 64 or scale.numel() != rows:
-        raise ValueError("nope, rope and scale must hold rows x 512, rows x 64 and rows elements")
-    _check("dsa_quant_fp8_rows", lib.dsa_quant_fp8_rows(_ptr(kv), rows, _ptr(nope), _ptr(rope), _ptr(scale),
-                                                        _stream(stream)))
+    if nope.numel() != rows * 512 or rope.numel() != rows * 64 or scale.numel() != rows * tiles:
+        raise ValueError(f"nope, rope and scale must hold rows x 512, rows x 64 and rows x {tiles} elements")
+    fn = "dsa_quant_fp8_rows" if tiles == 1 else "dsa_quant_fp8_tiles"
+    _check(fn, getattr(lib, fn)(_ptr(kv), rows, _ptr(nope), _ptr(rope), _ptr(scale), _stream(stream)))
     return nope, rope, scale

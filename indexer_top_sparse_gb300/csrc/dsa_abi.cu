@@ -454,8 +454,9 @@ dsa_status dsa_sparse_mla(const void *q, const void *kv_cache, const void *kv_ro
     const int NH = mla_heads_per_cta(H);
     if (NH == 0 || H > 1024 || T > 65535) return DSA_ERR_UNSUPPORTED;
     if ((long long)num_pages * page_size > (1LL << 31)) return DSA_ERR_UNSUPPORTED;
-    if (dtype != DSA_KV_BF16 && dtype != DSA_KV_FP8_ROWSCALE) return DSA_ERR_UNSUPPORTED;
-    const bool fp8 = dtype == DSA_KV_FP8_ROWSCALE;
+    if (dtype != DSA_KV_BF16 && dtype != DSA_KV_FP8_ROWSCALE && dtype != DSA_KV_FP8_TILE128)
+        return DSA_ERR_UNSUPPORTED;
+    const bool fp8 = dtype != DSA_KV_BF16;
     if (fp8 && (!kv_rope || !kv_scale || !aligned16(kv_rope) || (reinterpret_cast<uintptr_t>(kv_scale) & 3u)))
         return DSA_ERR_INVALID_ARG;
     if (workspace_bytes < dsa_sparse_mla_workspace_size(T, H, K)) return DSA_ERR_INVALID_ARG;
@@ -467,6 +468,7 @@ dsa_status dsa_sparse_mla(const void *q, const void *kv_cache, const void *kv_ro
     a.kv = static_cast<const uint8_t *>(kv_cache);
     a.kv_rope = fp8 ? static_cast<const uint8_t *>(kv_rope) : nullptr;
     a.kv_scale = fp8 ? kv_scale : nullptr;
+    a.kv_scales = dtype == DSA_KV_FP8_TILE128 ? 4 : 1;
     a.page_table = page_table;
     a.seq_lens = seq_lens;
     a.cu_q = cu_q;
@@ -508,6 +510,16 @@ dsa_status dsa_quant_fp8_rows(const void *kv, int64_t rows, void *nope, void *ro
     return cuda_status(dsa::launch_quant_fp8_rows(static_cast<const uint16_t *>(kv), rows,
                                                   static_cast<uint8_t *>(nope), static_cast<uint16_t *>(rope), scale,
                                                   static_cast<cudaStream_t>(stream)));
+}
+
+dsa_status dsa_quant_fp8_tiles(const void *kv, int64_t rows, void *nope, void *rope, float *scale, void *stream) {
+    if (rows < 0 || (rows > 0 && (!kv || !nope || !rope || !scale))) return DSA_ERR_INVALID_ARG;
+    if (rows > 0 && (!aligned16(kv) || !aligned16(nope) || (reinterpret_cast<uintptr_t>(rope) & 3u) ||
+                     (reinterpret_cast<uintptr_t>(scale) & 3u)))
+        return DSA_ERR_INVALID_ARG;
+    return cuda_status(dsa::launch_quant_fp8_tiles(static_cast<const uint16_t *>(kv), rows,
+                                                   static_cast<uint8_t *>(nope), static_cast<uint16_t *>(rope), scale,
+                                                   static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

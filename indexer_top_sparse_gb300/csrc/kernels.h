@@ -56,7 +56,8 @@ struct MlaArgs {
     const uint16_t *q;          // [T, H, 576] bf16
     const uint8_t *kv;          // [num_pages*page_size, 576] bf16 rows, or [.., 512] E4M3 (FP8 rows)
     const uint8_t *kv_rope;     // FP8 rows: [num_pages*page_size, 64] bf16 rope dims
-    const float *kv_scale;      // FP8 rows: [num_pages*page_size] fp32 row scales
+    const float *kv_scale;      // FP8 rows: [num_pages*page_size, kv_scales] fp32 scales
+    int kv_scales;              // FP8: scales per row, 1 (one per row) or 4 (one per 128 latent dims)
     const int32_t *page_table;  // [B, max_pages]
     const int32_t *seq_lens;    // [B]
     const int32_t *cu_q;        // [B+1]
@@ -88,6 +89,8 @@ cudaError_t launch_sparse_mla(const CUtensorMap &tm_q, const MlaArgs &a, int NH,
 
 // Quantisers (quant.cu).
 cudaError_t launch_quant_mxfp8(const uint16_t *x, int64_t n, uint8_t *q, uint8_t *e8m0, cudaStream_t st);
+cudaError_t launch_quant_fp8_tiles(const uint16_t *kv, int64_t rows, uint8_t *nope, uint16_t *rope, float *scale,
+                                   cudaStream_t st);
 cudaError_t launch_quant_fp8_rows(const uint16_t *kv, int64_t rows, uint8_t *nope, uint16_t *rope, float *scale,
                                   cudaStream_t st);
 

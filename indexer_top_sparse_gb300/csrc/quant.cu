@@ -7,7 +7,8 @@
 //   saturating at +-448); an all-zero block gets scale byte 127.
 //   FP8 for the latent KV cache: the 512 latent dims of a row share one fp32
 //   scale s = amax / 448 (1 if amax is 0), elements E4M3(x / s); the 64 rope
-//   dims stay bf16.
+//   dims stay bf16.  The tile variant gives every 128 latent dims their own
+//   scale by the same rule (the per-token-head-tile granularity, same §4).
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
@@ -77,9 +78,13 @@ __global__ void quant_mxfp8_kernel(const uint16_t *__restrict__ x, int64_t n_blo
 }
 
 // One warp per 576-wide latent row: lane l handles latent dims 16l..16l+15
-// and rope dims 2l, 2l+1.
+// and rope dims 2l, 2l+1.  kTiles scales per row: the amax is reduced over
+// the 32 / kTiles lanes of a tile.
+template <int kTiles>
 __global__ void quant_fp8_rows_kernel(const uint16_t *__restrict__ kv, int64_t rows, uint8_t *__restrict__ nope,
                                       uint16_t *__restrict__ rope, float *__restrict__ scale) {
+    static_assert(kTiles == 1 || kTiles == 4, "one scale per row or per 128 dims");
+    constexpr int kLanes = 32 / kTiles;
     const int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (row >= rows) return;
@@ -94,7 +99,7 @@ __global__ void quant_fp8_rows_kernel(const uint16_t *__restrict__ kv, int64_t r
         amax = fmaxf(amax, fabsf(bf16_bits_to_float(w[i] >> 16)));
     }
 #pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    for (int o = kLanes / 2; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
     const float s = amax == 0.0f ? 1.0f : __fdiv_rn(amax, 448.0f);
     uint32_t out[4];
 #pragma unroll
@@ -107,7 +112,7 @@ __global__ void quant_fp8_rows_kernel(const uint16_t *__restrict__ kv, int64_t r
     }
     reinterpret_cast<uint4 *>(nope + row * 512)[lane] = make_uint4(out[0], out[1], out[2], out[3]);
     reinterpret_cast<uint32_t *>(rope + row * 64)[lane] = reinterpret_cast<const uint32_t *>(r + 512)[lane];
-    if (lane == 0) scale[row] = s;
+    if (lane % kLanes == 0) scale[row * kTiles + lane / kLanes] = s;
 }
 
 }  // namespace
@@ -122,7 +127,14 @@ cudaError_t launch_quant_mxfp8(const uint16_t *x, int64_t n, uint8_t *q, uint8_t
 cudaError_t launch_quant_fp8_rows(const uint16_t *kv, int64_t rows, uint8_t *nope, uint16_t *rope, float *scale,
                                   cudaStream_t st) {
     if (rows == 0) return cudaSuccess;
-    quant_fp8_rows_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(kv, rows, nope, rope, scale);
+    quant_fp8_rows_kernel<1><<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(kv, rows, nope, rope, scale);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quant_fp8_tiles(const uint16_t *kv, int64_t rows, uint8_t *nope, uint16_t *rope, float *scale,
+                                   cudaStream_t st) {
+    if (rows == 0) return cudaSuccess;
+    quant_fp8_rows_kernel<4><<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(kv, rows, nope, rope, scale);
     return cudaGetLastError();
 }
 

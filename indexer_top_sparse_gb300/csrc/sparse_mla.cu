@@ -19,7 +19,8 @@
 //               16-byte cp.async copies place each 576-wide bf16 row into nine
 //               64-column regions in the 128-byte-swizzle layout.  For the FP8
 //               cache the 512 E4M3 latent dims go through registers (loaded a
-//               tile ahead), are multiplied by the row scale and stored as
+//               tile ahead), are multiplied by their scale (the row's, or
+//               the one of their 128-dim tile) and stored as
 //               bf16; the rope dims are copied as they are.
 //   warp 8      tcgen05 issuer: S[64 heads x 64 keys] = Q . K_tile^T (M = 64,
 //               K-major operands, 36 steps of K = 16, double-buffered in
@@ -292,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
                 for (int j = 0; j < kKPW; ++j) {
                     const int row = st->rows[key0 + j];
                     f8v[j] = __ldg(reinterpret_cast<const uint4 *>(a.kv + (size_t)row * kDv) + lane);
-                    f8s[j] = __ldg(a.kv_scale + row);
+                    f8s[j] = __ldg(a.kv_scale + (size_t)row * a.kv_scales + ((lane * a.kv_scales) >> 5));
                 }
             }
         }
@@ -352,7 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
                     for (int j = 0; j < kKPW; ++j) {
                         const int row = nrows[key0 + j];
                         f8v[j] = __ldg(reinterpret_cast<const uint4 *>(a.kv + (size_t)row * kDv) + lane);
-                        f8s[j] = __ldg(a.kv_scale + row);
+                        f8s[j] = __ldg(a.kv_scale + (size_t)row * a.kv_scales + ((lane * a.kv_scales) >> 5));
                     }
                 }
             }

@@ -3,9 +3,9 @@ C-ABI exactly as the benchmark launches it (default tuning, whole batch in
 one call), and sampled query rows are checked against the oracle row by row.
 Index sets must agree except at near-threshold positions (1e-3 relative of
 the K-th oracle score); attention, fed the GPU's own indices, must match the
-oracle within 2e-2 / 1e-2 (bf16) or 6e-2 / 3e-2 (FP8).  FP8 caches are made
-by each side's own quantiser from the same bf16 draws (the two quantisers
-agree bit for bit, see test_gpu_quant.py)."""
+oracle within 2e-2 / 1e-2 (bf16) or 6e-2 / 3e-2 (FP8).  FP8 caches (one scale
+per row, or per 128-dim tile) are made by each side's own quantiser from the
+same bf16 draws (the two quantisers agree bit for bit, see test_gpu_quant.py)."""
 import numpy as np
 import pytest
 import torch
@@ -16,7 +16,7 @@ from indexer_top_sparse_gb300.inputs import decode_b32_n32k, decode_b64_mixed, m
 pytestmark = pytest.mark.gpu
 
 
-def _gpu_path(wl, fp8=False):
+def _gpu_path(wl, fp8=False, kv_fmt="fp8_rowscale"):
     """The production calls on the whole batch; returns indices and out."""
     import indexer_top_sparse_gb300 as d
     pt, sl, cq = dev(wl.page_table), dev(wl.seq_lens), dev(wl.cu_q)
@@ -28,9 +28,10 @@ def _gpu_path(wl, fp8=False):
         idx = d.dsa_index_topk(q_idx, dev(wl.head_w), k_idx, pt, sl, cq, wl.K, workspace=ws,
                                q_idx_scale=q_sc, k_idx_scale=k_sc, dtype="mxfp8")
         del k_idx, k_sc
-        nope, rope, rsc = d.dsa_quant_fp8_rows(dev_bf16(wl.kv))
+        quant = d.dsa_quant_fp8_tiles if kv_fmt == "fp8_tile128" else d.dsa_quant_fp8_rows
+        nope, rope, rsc = quant(dev_bf16(wl.kv))
         out = d.dsa_sparse_mla(dev_bf16(wl.q), nope, pt, sl, cq, idx, wl.scale, workspace=ws, kv_rope=rope,
-                               kv_scale=rsc, dtype="fp8_rowscale")
+                               kv_scale=rsc, dtype=kv_fmt)
     else:
         idx = d.dsa_index_topk(dev_bf16(wl.q_idx), dev(wl.head_w), dev_bf16(wl.k_idx), pt, sl, cq, wl.K,
                                workspace=ws)
@@ -52,7 +53,7 @@ def _sequence_view(wl, t):
     return view
 
 
-def _check_rows(orc, wl, rows, idx, out, fp8=False):
+def _check_rows(orc, wl, rows, idx, out, fp8=False, kv_fmt="fp8_rowscale"):
     pos = wl.query_pos()
     atol, rtol = (6e-2, 3e-2) if fp8 else (2e-2, 1e-2)
     near = 0
@@ -67,9 +68,11 @@ def _check_rows(orc, wl, rows, idx, out, fp8=False):
             ref_idx, ref_sc = orc.index_topk(q8, wl.head_w[v["rows"]], k8, v["pt"], v["sl"], v["cq"], wl.K,
                                              wl.page_size, dtype=orc.IDX_MXFP8, q_scale=qs, k_scale=ks, rows=r,
                                              want_scores=True)
-            nope, rope, rsc = orc.quant_fp8_rows(v["kv"])
+            tiles = kv_fmt == "fp8_tile128"
+            nope, rope, rsc = (orc.quant_fp8_tiles if tiles else orc.quant_fp8_rows)(v["kv"])
             ref_out, _ = orc.sparse_mla(q, nope, v["pt"], v["cq"], g_idx, wl.scale, wl.page_size,
-                                        dtype=orc.KV_FP8_ROWSCALE, kv_rope=rope, kv_scale=rsc, rows=r)
+                                        dtype=orc.KV_FP8_TILE128 if tiles else orc.KV_FP8_ROWSCALE,
+                                        kv_rope=rope, kv_scale=rsc, rows=r)
         else:
             ref_idx, ref_sc = orc.index_topk(q_idx, wl.head_w[v["rows"]], v["k_idx"], v["pt"], v["sl"], v["cq"],
                                              wl.K, wl.page_size, rows=r, want_scores=True)
@@ -85,12 +88,13 @@ def test_decode_b32_n32768_bf16(orc):
     _check_rows(orc, wl, [0, 13, 31], idx, out)
 
 
-def test_decode_b64_mixed_lengths_fp8(orc):
+@pytest.mark.parametrize("kv_fmt", ["fp8_rowscale", "fp8_tile128"])
+def test_decode_b64_mixed_lengths_fp8(orc, kv_fmt):
     wl = decode_b64_mixed(0)
-    idx, out = _gpu_path(wl, fp8=True)
+    idx, out = _gpu_path(wl, fp8=True, kv_fmt=kv_fmt)
     lens = wl.seq_lens
     rows = [int(np.argmin(lens)), int(np.argmax(lens)), 37]
-    _check_rows(orc, wl, rows, idx, out, fp8=True)
+    _check_rows(orc, wl, rows, idx, out, fp8=True, kv_fmt=kv_fmt)
 
 
 def test_prefill_16k_bf16(orc):

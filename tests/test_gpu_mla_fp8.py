@@ -1,5 +1,6 @@
 """GPU sparse MLA on the FP8 latent cache (E4M3 latent dims with one fp32
-scale per row, bf16 rope dims) against the oracle fed the same FP8 codes.
+scale per row or per 128-dim tile, bf16 rope dims) against the oracle fed the
+same FP8 codes.
 The bar is the bf16 path's 2e-2 absolute / 1e-2 relative, tighter than the
 6e-2 / 3e-2 allowed for FP8: the kernel's only extra rounding is the bf16 of
 each dequantised value.  (The E4M3 rounding itself, FP8 cache against the
@@ -27,45 +28,51 @@ def _random_indices(rng, wl, K, pad_frac=0.0):
     return idx
 
 
-def _run(wl, nope, rope, sc, idx):
+FMT = {"fp8_rowscale": ("quant_fp8_rows", "KV_FP8_ROWSCALE"), "fp8_tile128": ("quant_fp8_tiles", "KV_FP8_TILE128")}
+
+
+def _run(wl, nope, rope, sc, idx, fmt="fp8_rowscale"):
     import indexer_top_sparse_gb300 as d
     lse = torch.empty((wl.T, wl.H), dtype=torch.float32, device="cuda")
     ws = d.Workspace(d.sparse_mla_workspace_size(wl.T, wl.H, idx.shape[1]))
     out = d.dsa_sparse_mla(dev_bf16(wl.q), dev(nope), dev(wl.page_table), dev(wl.seq_lens), dev(wl.cu_q), dev(idx),
                            wl.scale, lse=lse, workspace=ws, kv_rope=dev_bf16(rope), kv_scale=dev(sc),
-                           dtype="fp8_rowscale")
+                           dtype=fmt)
     ws.check()
     return out.float().cpu().numpy(), lse.cpu().numpy()
 
 
-def _compare(orc, wl, idx):
-    nope, rope, sc = orc.quant_fp8_rows(wl.kv)
-    out, lse = _run(wl, nope, rope, sc, idx)
+def _compare(orc, wl, idx, fmt="fp8_rowscale"):
+    quant, kvdt = FMT[fmt]
+    nope, rope, sc = getattr(orc, quant)(wl.kv)
+    out, lse = _run(wl, nope, rope, sc, idx, fmt)
     ref, ref_lse = orc.sparse_mla(wl.q, nope, wl.page_table, wl.cu_q, idx, wl.scale, wl.page_size,
-                                  dtype=orc.KV_FP8_ROWSCALE, kv_rope=rope, kv_scale=sc)
+                                  dtype=getattr(orc, kvdt), kv_rope=rope, kv_scale=sc)
     np.testing.assert_allclose(out, ref, atol=2e-2, rtol=1e-2)
     fin = np.isfinite(ref_lse)
     np.testing.assert_allclose(lse[fin], ref_lse[fin], rtol=1e-3, atol=1e-3)
     assert np.all(np.isneginf(lse[~fin]))
 
 
+@pytest.mark.parametrize("fmt", list(FMT))
 @pytest.mark.parametrize("H", [16, 64, 128])
-def test_fp8_decode_heads(orc, H):
+def test_fp8_decode_heads(orc, H, fmt):
     rng = np.random.default_rng(200 + H)
     wl = make_workload("mla8", [3000, 513, 70], [1, 1, 1], H=H, K=512, page_size=64, seed=200 + H, with_idx=False)
-    _compare(orc, wl, _random_indices(rng, wl, 512))
+    _compare(orc, wl, _random_indices(rng, wl, 512), fmt)
 
 
+@pytest.mark.parametrize("fmt", list(FMT))
 @pytest.mark.parametrize("H", [64, 128])
 @pytest.mark.parametrize("splits", [1, 3])
-def test_fp8_splits_and_padding(orc, splits, H):
+def test_fp8_splits_and_padding(orc, splits, H, fmt):
     import indexer_top_sparse_gb300 as d
     rng = np.random.default_rng(300 + splits)
     wl = make_workload("mla8", [4000, 900], [1, 1], H=H, K=1000, page_size=64, seed=300 + splits, with_idx=False)
     idx = _random_indices(rng, wl, 1000, pad_frac=0.1)
     d.set_tuning("mla_splits", splits)
     try:
-        _compare(orc, wl, idx)
+        _compare(orc, wl, idx, fmt)
     finally:
         d.set_tuning("mla_splits", 0)
 
@@ -85,4 +92,25 @@ def test_fp8_zero_rows_and_wide_scales(orc):
     out, _ = _run(wl, nope, rope, sc, idx)
     ref, _ = orc.sparse_mla(wl.q, nope, wl.page_table, wl.cu_q, idx, wl.scale, wl.page_size,
                             dtype=orc.KV_FP8_ROWSCALE, kv_rope=rope, kv_scale=sc)
+    np.testing.assert_allclose(out, ref, atol=2e-2 * max(1.0, np.abs(ref).max()), rtol=1e-2)
+
+
+def test_fp8_tile_scales_differ_within_a_row(orc):
+    # tiles of one row whose magnitudes differ by 2^10: the kernel must take
+    # each 128-dim tile's own scale (another tile's would be off by 2^4 to
+    # 2^10).  Larger spreads make the logits so large that the accepted bf16
+    # rounding of each dequantised value decides between near-tied keys.
+    from indexer_top_sparse_gb300.inputs import bf16_bits, bf16_to_f32
+    rng = np.random.default_rng(19)
+    wl = make_workload("mla8", [1200, 300], [1, 1], H=64, K=400, page_size=64, seed=19, with_idx=False)
+    kv = bf16_to_f32(wl.kv).reshape(-1, 576)
+    kv[:, 128:256] *= np.float32(2.0 ** -6)
+    kv[:, 384:512] *= np.float32(2.0 ** 4)
+    wl.kv = bf16_bits(kv.reshape(wl.kv.shape).astype(np.float32))
+    wl.scale = 0.01
+    nope, rope, sc = orc.quant_fp8_tiles(wl.kv)
+    idx = _random_indices(rng, wl, 400)
+    out, _ = _run(wl, nope, rope, sc, idx, "fp8_tile128")
+    ref, _ = orc.sparse_mla(wl.q, nope, wl.page_table, wl.cu_q, idx, wl.scale, wl.page_size,
+                            dtype=orc.KV_FP8_TILE128, kv_rope=rope, kv_scale=sc)
     np.testing.assert_allclose(out, ref, atol=2e-2 * max(1.0, np.abs(ref).max()), rtol=1e-2)

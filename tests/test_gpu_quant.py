@@ -1,6 +1,6 @@
 """GPU quantisers against the oracle's codecs, bit for bit: MXFP8 blocks of 32
-(E8M0 scale + E4M3 elements) and FP8 latent rows (fp32 row scale + E4M3 latent
-dims, bf16 rope dims), over N(0,1) data and the edge cases (all-zero blocks,
+(E8M0 scale + E4M3 elements) and FP8 latent rows (fp32 scale per row or per
+128-dim tile + E4M3 latent dims, bf16 rope dims), over N(0,1) data and the edge cases (all-zero blocks,
 tiny and huge magnitudes, exact ties to even)."""
 import numpy as np
 import pytest
@@ -41,6 +41,25 @@ def test_fp8_rows_bit_exact(orc):
     import indexer_top_sparse_gb300 as d
     nope, rope, sc = d.dsa_quant_fp8_rows(dev_bf16(bits))
     rn, rr, rs = orc.quant_fp8_rows(bits)
+    assert np.array_equal(sc.cpu().numpy(), rs)
+    assert np.array_equal(nope.cpu().numpy(), rn)
+    assert np.array_equal(rope.view(torch.int16).cpu().numpy().view(np.uint16), rr)
+
+
+def test_fp8_tiles_bit_exact(orc):
+    # one scale per 128 latent dims: all-zero tiles next to live ones, tiles of
+    # very different magnitude in one row, a ragged row count
+    rng = np.random.default_rng(2)
+    x = _data(rng, (301, 576))
+    x[7, :512] = 0.0
+    x[9, 128:256] = 0.0
+    x[10, 384:512] *= np.float32(1e20)
+    x[11, 256:384] *= np.float32(1e-20)
+    bits = bf16_bits(x)
+    import indexer_top_sparse_gb300 as d
+    nope, rope, sc = d.dsa_quant_fp8_tiles(dev_bf16(bits))
+    rn, rr, rs = orc.quant_fp8_tiles(bits)
+    assert tuple(sc.shape) == (301, 4)
     assert np.array_equal(sc.cpu().numpy(), rs)
     assert np.array_equal(nope.cpu().numpy(), rn)
     assert np.array_equal(rope.view(torch.int16).cpu().numpy().view(np.uint16), rr)
