@@ -63,6 +63,9 @@ def _load():
             lib.orc_quant_fp8_rows.restype = None
             lib.orc_quant_fp8_tiles.argtypes = [P, i64, P, P, P]
             lib.orc_quant_fp8_tiles.restype = None
+            lib.orc_cache_append.argtypes = [P, P, P, i32, P, P, i32, i32, i32, i64, ctypes.c_int, P, P,
+                                             ctypes.c_int, P, P, P]
+            lib.orc_cache_append.restype = ctypes.c_int
             lib.orc_index_scores_row.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P, P, P, P, i64, P,
                                                  i32, i64, P]
             lib.orc_index_scores_row.restype = ctypes.c_int
@@ -149,6 +152,46 @@ def quant_fp8_tiles(kv_bf16_bits: np.ndarray):
     scale = np.empty(kv.shape[:-1] + (4,), np.float32)
     _load().orc_quant_fp8_tiles(_p(kv), rows, _p(nope), _p(rope), _p(scale))
     return nope, rope, scale
+
+
+def _writable(a, dtype, name):
+    if a is None:
+        return None
+    if a.dtype != dtype or not a.flags.c_contiguous or not a.flags.writeable:
+        raise ValueError(f"{name} must be a writable C-contiguous {np.dtype(dtype).name} array")
+    return a
+
+
+def cache_append(page_table, seq_lens, cu_q, page_size, *, k_new=None, kv_new=None, idx_dtype=IDX_BF16,
+                 k_cache=None, k_scale=None, kv_dtype=KV_BF16, kv_cache=None, kv_rope=None, kv_scale=None,
+                 num_pages=None):
+    """Write new tokens' index keys (k_new [T, 128] bf16 bits) and latent rows
+    (kv_new [T, 576] bf16 bits) into the paged caches, in place, quantising to
+    the caches' formats.  Token t of sequence b is at position
+    seq_lens[b] - (cu_q[b+1] - cu_q[b]) + (t - cu_q[b]).  Cache arrays:
+    k_cache [pages, page_size, 128] (uint16 bf16 bits, or uint8 e4m3 with
+    k_scale [..., 4] uint8); kv_cache [pages, page_size, 576] uint16, or
+    [..., 512] uint8 with kv_rope [..., 64] uint16 and kv_scale [...] or
+    [..., 4] float32.  Returns the C status (0, or -1 if a token's page id was
+    out of range)."""
+    pt = _c(page_table, np.int32)
+    B, maxp = pt.shape
+    cq = _c(cu_q, np.int32)
+    T = int(cq[-1])
+    kn = None if k_new is None else _c(k_new, np.uint16)
+    vn = None if kv_new is None else _c(kv_new, np.uint16)
+    kc = _writable(k_cache, np.uint16 if idx_dtype == IDX_BF16 else np.uint8, "k_cache")
+    ks = _writable(k_scale, np.uint8, "k_scale")
+    vc = _writable(kv_cache, np.uint16 if kv_dtype == KV_BF16 else np.uint8, "kv_cache")
+    vr = _writable(kv_rope, np.uint16, "kv_rope")
+    vs = _writable(kv_scale, np.float32, "kv_scale")
+    if num_pages is None:
+        num_pages = (kc if kc is not None else vc).shape[0]
+    rc = _load().orc_cache_append(_p(kn), _p(vn), _p(pt), maxp, _p(_c(seq_lens, np.int32)), _p(cq), B, T,
+                                  page_size, num_pages, idx_dtype, _p(kc), _p(ks), kv_dtype, _p(vc), _p(vr), _p(vs))
+    if rc == -3:
+        raise RuntimeError("orc_cache_append: token outside cu_q")
+    return rc
 
 
 # ---------------------------------------------------------------- indexer / top-K

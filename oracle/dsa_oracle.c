@@ -45,6 +45,10 @@
  *    latent row every tile of 128 consecutive elements has its own scale, so
  *    the 512 latent dims carry four fp32 scales; each tile uses the row rule
  *    above on its own amax.  The rope dims stay bf16.
+ *  - Cache append ("Optimizing Inference for Hybrid Attention LLMs: A
+ *    Practical Guide to Day-0 Adaptation", §4 key points 1-2): new tokens'
+ *    index keys and latent rows quantised by the codecs above straight into
+ *    their page slots.
  *
  * Every function here is pinned by a CPU test against something other than
  * itself (brute force, closed forms, library routines on special cases,
@@ -526,6 +530,66 @@ int orc_sparse_mla_row(int dtype, int H, int D, int Dv, const uint16_t *q, const
     free(logit);
     free(acc);
     return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Cache append.                                                            */
+/* ------------------------------------------------------------------------ */
+
+/* New tokens' index keys and latent rows written into their page slots, each
+ * quantised on the way in to the cache's format ("Optimizing Inference for
+ * Hybrid Attention LLMs: A Practical Guide to Day-0 Adaptation", §4
+ * Hierarchical Quantization, key points 1 and 2: per-token block formats that
+ * line up with the page layout, quantised on the indexer's data path with no
+ * extra round trip).  Token t of sequence b (t in cu_q[b]..cu_q[b+1]-1) is at
+ * position seq_lens[b] - (cu_q[b+1] - cu_q[b]) + (t - cu_q[b]), i.e. the new
+ * tokens are the last positions of their sequence, as queries are.
+ *   k_new [T, 128] bf16 -> k_cache: bf16 [rows, 128], or MXFP8 codes
+ *                          [rows, 128] with e8m0 k_scale [rows, 4]
+ *   kv_new [T, 576] bf16 -> kv_cache: bf16 [rows, 576], or FP8 e4m3 [rows, 512]
+ *                          with kv_rope [rows, 64] bf16 and kv_scale [rows]
+ *                          (row scales) or [rows, 4] (tile scales)
+ * Either pair may be NULL (that cache is not written).  Returns 0, or -1 on a
+ * page id outside [0, num_pages) or a negative position (nothing is written
+ * for that token), -3 on a token outside cu_q. */
+int orc_cache_append(const uint16_t *k_new, const uint16_t *kv_new, const int32_t *page_table,
+                     int32_t max_pages_per_seq, const int32_t *seq_lens, const int32_t *cu_q, int32_t B, int32_t T,
+                     int32_t page_size, int64_t num_pages, int idx_dtype, void *k_cache, uint8_t *k_scale,
+                     int kv_dtype, void *kv_cache, uint16_t *kv_rope, float *kv_scale)
+{
+    int32_t t;
+    int rc = 0, d;
+    for (t = 0; t < T; ++t) {
+        int b = orc_seq_of(cu_q, B, t);
+        int64_t pos, row;
+        if (b < 0)
+            return -3;
+        pos = orc_query_pos(seq_lens, cu_q, b, t);
+        row = pos < 0 ? -1 : orc_phys_row(page_table + (int64_t)b * max_pages_per_seq, page_size, num_pages, pos);
+        if (row < 0) {
+            rc = -1;
+            continue;
+        }
+        if (k_new && k_cache) {
+            const uint16_t *src = k_new + (int64_t)t * 128;
+            if (idx_dtype == ORC_IDX_BF16)
+                for (d = 0; d < 128; ++d)
+                    ((uint16_t *)k_cache)[row * 128 + d] = src[d];
+            else
+                orc_quant_mxfp8(src, 128, (uint8_t *)k_cache + row * 128, k_scale + row * 4);
+        }
+        if (kv_new && kv_cache) {
+            const uint16_t *src = kv_new + (int64_t)t * 576;
+            if (kv_dtype == ORC_KV_BF16)
+                for (d = 0; d < 576; ++d)
+                    ((uint16_t *)kv_cache)[row * 576 + d] = src[d];
+            else if (kv_dtype == ORC_KV_FP8_TILE128)
+                orc_quant_fp8_tiles(src, 1, (uint8_t *)kv_cache + row * 512, kv_rope + row * 64, kv_scale + row * 4);
+            else
+                orc_quant_fp8_rows(src, 1, (uint8_t *)kv_cache + row * 512, kv_rope + row * 64, kv_scale + row);
+        }
+    }
+    return rc;
 }
 
 /* Batch driver: query rows t (rows == NULL: all T) of q [T, H, D]; indices
