@@ -382,6 +382,84 @@ def run_other_workload(args, world, rank, local_rank):
         torch.distributed.destroy_process_group()
 
 
+def run_append_workload(args, world, rank, local_rank):
+    """Cache append of one 131072-token sequence (a long prefill's keys): the
+    new index keys go into an MXFP8 cache and the new latent rows into an FP8
+    cache with tile-128 scales, written straight into permuted pages.
+    HBM-bound: bf16 rows in, quantised rows out."""
+    import torch
+    import indexer_top_sparse_gb300 as d
+    from indexer_top_sparse_gb300.inputs import make_page_table
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(args.seed + 1000 * rank)
+    T, ps = 131072, 64
+    pt_np, P = make_page_table(np.random.default_rng(args.seed + rank), [T], ps, True)
+    pt = torch.from_numpy(pt_np).to(dev)
+    sl = torch.tensor([T], dtype=torch.int32, device=dev)
+    cq = torch.tensor([0, T], dtype=torch.int32, device=dev)
+    copies = 2   # alternating inputs, each far larger than L2
+    src = [(torch.randn(T, 128, generator=gen, device=dev).to(torch.bfloat16),
+            torch.randn(T, 576, generator=gen, device=dev).to(torch.bfloat16)) for _ in range(copies)]
+    kc = torch.empty((P, ps, 128), dtype=torch.uint8, device=dev)
+    ksc = torch.empty((P, ps, 4), dtype=torch.uint8, device=dev)
+    kv = torch.empty((P, ps, 512), dtype=torch.uint8, device=dev)
+    rope = torch.empty((P, ps, 64), dtype=torch.bfloat16, device=dev)
+    vsc = torch.empty((P, ps, 4), dtype=torch.float32, device=dev)
+    ws = d.Workspace(256, dev)
+
+    def step(i):
+        k_new, kv_new = src[i % copies]
+        d.dsa_cache_append(pt, sl, cq, k_new=k_new, kv_new=kv_new, k_cache=kc, k_scale=ksc, kv_cache=kv,
+                           kv_rope=rope, kv_scale=vsc, idx_dtype="mxfp8", kv_dtype="fp8_tile128", workspace=ws)
+
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    for i in range(args.warmup):
+        step(i)
+    ws.check()
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(args.steps):
+        step(args.warmup + i)
+    e1.record()
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    ws.check()
+    t_step = max_over_ranks([e0.elapsed_time(e1) * 1e-3 / args.steps], dev)[0]
+    # bytes: bf16 key and latent row in; e4m3 key + 4 e8m0, e4m3 latent + bf16 rope + 4 fp32 out; the
+    # page table row and the two small per-sequence arrays
+    row_bytes = (128 * 2 + 576 * 2) + (128 + 4) + (512 + 128 + 16)
+    nbytes = float(T) * row_bytes + 4 * pt.shape[1] + 12
+    hbm, peak_kind = peaks()
+    ach = nbytes / t_step / 1e9
+    line = {"metric": "cache append tokens/s (index key MXFP8 + latent FP8 tile-128 into pages)",
+            "value": T * max(world, 1) / t_step, "unit": "tokens/s", "n_gpus": max(world, 1), "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * t_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16->e4m3", "data": "synthetic (seeded N(0,1) drawn on the device)",
+            "config": {"workload": args.workload, "tokens": T, "page_size": ps, "pages": P,
+                       "parallelism": f"replicas{max(world, 1)}",
+                       "l2": f"inputs larger than L2: {copies} alternating copies of the new rows "
+                             f"({T * 1408 / 2**20:.0f} MiB each), no flush"},
+            "roofline": {"bound": "hbm", "kernel": "cache_append", "achieved": ach, "peak": hbm,
+                         "peak_kind": peak_kind, "unit": "GB/s", "frac": ach / hbm, "traffic": None},
+            "gpu_launches": args.steps, "clocks": clk}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
 # ---------------------------------------------------------------- main
 
 def main():
@@ -396,7 +474,8 @@ def main():
                     help="between timed steps: alternate two copies of every step input (default) or write a "
                          "512 MiB buffer")
     ap.add_argument("--workload", default="decode_b32_n32768",
-                    choices=["decode_b32_n32768", "decode_b64_mixed_fp8", "prefill_16k", "prefill_131k_chunked_fp8"])
+                    choices=["decode_b32_n32768", "decode_b64_mixed_fp8", "prefill_16k", "prefill_131k_chunked_fp8",
+                             "append_131k_fp8"])
     ap.add_argument("--kv-scales", default="row", choices=["row", "tile128"],
                     help="FP8 workloads: one fp32 scale per latent row (default) or per 128 latent dims")
     ap.add_argument("--batch", type=int, default=32,
@@ -414,7 +493,10 @@ def main():
                 print(json.dumps({"impl": "reference", "unavailable": "the oracle baseline is timed on the "
                                   "decode_b32_n32768 workload only"}), flush=True)
             return
-        run_other_workload(args, world, rank, local_rank)
+        if args.workload == "append_131k_fp8":
+            run_append_workload(args, world, rank, local_rank)
+        else:
+            run_other_workload(args, world, rank, local_rank)
         return
 
     from indexer_top_sparse_gb300.inputs import decode_b32_n32k, make_workload

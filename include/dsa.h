@@ -209,6 +209,35 @@ dsa_status dsa_quant_fp8_rows(const void *kv, int64_t rows, void *nope, void *ro
  *   scale [rows, 4] fp32 out. */
 dsa_status dsa_quant_fp8_tiles(const void *kv, int64_t rows, void *nope, void *rope, float *scale, void *stream);
 
+/* ---------------------------------------------------------------- cache append */
+
+/* Writes new tokens' index keys and latent rows into their page slots,
+ * quantised on the way to each cache's format: the per-token block formats
+ * line up with the page layout, so nothing is staged ("Optimizing Inference
+ * for Hybrid Attention LLMs: A Practical Guide to Day-0 Adaptation", §4
+ * Hierarchical Quantization, key points 1-2).
+ *   k_new      [T, 128] bf16 new index keys, or NULL (index cache untouched)
+ *   kv_new     [T, 576] bf16 new latent rows, or NULL (KV cache untouched)
+ *   page_table, max_pages_per_seq, seq_lens, cu_q, B: as for dsa_index_topk;
+ *              seq_lens already counts the new tokens, and the new tokens of
+ *              sequence b (cu_q[b]..cu_q[b+1]-1) are its last positions
+ *   idx_dtype  BF16: k_cache [num_pages, page_size, 128] bf16, k_scale NULL;
+ *              MXFP8: k_cache e4m3 codes, k_scale [num_pages, page_size, 4]
+ *              e8m0 (dsa_quant_mxfp8's format)
+ *   kv_dtype   BF16: kv_cache [num_pages, page_size, 576] bf16;
+ *              FP8_ROWSCALE / FP8_TILE128: kv_cache [.., 512] e4m3, kv_rope
+ *              [.., 64] bf16, kv_scale [num_pages, page_size] or [.., 4] fp32
+ *              (dsa_quant_fp8_rows / dsa_quant_fp8_tiles formats)
+ * Rows of other positions are not touched.  A token whose page id is out of
+ * range, or whose position would be negative, writes nothing and is reported
+ * through the workspace (DSA_ERR_BAD_PAGE / DSA_ERR_INVALID_ARG from
+ * dsa_get_error).  The workspace needs at least 256 bytes (its error word). */
+dsa_status dsa_cache_append(const void *k_new, const void *kv_new, const int32_t *page_table,
+                            int32_t max_pages_per_seq, const int32_t *seq_lens, const int32_t *cu_q, int32_t B,
+                            int32_t T, int32_t page_size, int64_t num_pages, dsa_idx_dtype idx_dtype, void *k_cache,
+                            void *k_scale, dsa_kv_dtype kv_dtype, void *kv_cache, void *kv_rope, float *kv_scale,
+                            void *workspace, size_t workspace_bytes, void *stream);
+
 /* ---------------------------------------------------------------- no-allocation variant */
 
 /* dsa_sparse_mla without a workspace, for callers that cannot allocate device

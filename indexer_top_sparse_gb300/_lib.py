@@ -28,7 +28,7 @@ KV_DTYPES = {"bf16": 0, "fp8_rowscale": 1, "fp8_tile128": 2}
 EXPORTS = ("dsa_status_string", "dsa_set_tuning", "dsa_index_topk_workspace_size", "dsa_sparse_mla_workspace_size",
            "dsa_workspace_init", "dsa_get_error", "dsa_index_topk", "dsa_index_scores", "dsa_topk_from_scores",
            "dsa_sparse_mla", "dsa_sparse_mla_static", "dsa_quant_mxfp8", "dsa_quant_fp8_rows",
-           "dsa_quant_fp8_tiles")
+           "dsa_quant_fp8_tiles", "dsa_cache_append")
 
 
 class DSAError(RuntimeError):
@@ -86,6 +86,8 @@ def load(build_if_missing: bool = True):
         lib.dsa_quant_fp8_rows.restype = c_int
         lib.dsa_quant_fp8_tiles.argtypes = [P, i64, P, P, P, P]
         lib.dsa_quant_fp8_tiles.restype = c_int
+        lib.dsa_cache_append.argtypes = [P, P, P, i32, P, P, i32, i32, i32, i64, c_int, P, P, c_int, P, P, P, P, sz, P]
+        lib.dsa_cache_append.restype = c_int
         _lib = lib
         return lib
 
@@ -270,6 +272,56 @@ def dsa_sparse_mla(q, kv_cache, page_table, seq_lens, cu_q, indices, scale, *, o
                                                 _ptr(indices), B, T, H, K, float(scale), ps, dt, _ptr(out),
                                                 _ptr(lse), _ptr(workspace.buf), workspace.nbytes, _stream(stream)))
     return out
+
+
+def dsa_cache_append(page_table, seq_lens, cu_q, *, k_new=None, kv_new=None, k_cache=None, k_scale=None,
+                     kv_cache=None, kv_rope=None, kv_scale=None, idx_dtype="bf16", kv_dtype="bf16", workspace=None,
+                     stream=None):
+    """Write new tokens' index keys (k_new [T, 128] bf16) and latent rows
+    (kv_new [T, 576] bf16) into their page slots, quantised to the caches'
+    formats (see include/dsa.h).  The caches are updated in place."""
+    lib = load()
+    it, kt = IDX_DTYPES[idx_dtype], KV_DTYPES[kv_dtype]
+    _need(page_table, "page_table", torch.int32, 2)
+    dev = page_table.device
+    _need(seq_lens, "seq_lens", torch.int32, 1, dev)
+    _need(cu_q, "cu_q", torch.int32, 1, dev)
+    B = seq_lens.shape[0]
+    if cu_q.shape[0] != B + 1:
+        raise ValueError("cu_q must have B + 1 entries")
+    T, ps, P = None, None, None
+    if k_new is not None:
+        _need(k_new, "k_new", torch.bfloat16, 2, dev)
+        _need(k_cache, "k_cache", torch.bfloat16 if it == 0 else torch.uint8, 3, dev)
+        if k_new.shape[1] != 128 or k_cache.shape[2] != 128:
+            raise ValueError("k_new [T, 128] and k_cache [pages, page_size, 128]")
+        if it == 1:
+            _need(k_scale, "k_scale", torch.uint8, 3, dev)
+            if tuple(k_scale.shape) != tuple(k_cache.shape[:2]) + (4,):
+                raise ValueError("k_scale must be [pages, page_size, 4] uint8")
+        T, P, ps = k_new.shape[0], k_cache.shape[0], k_cache.shape[1]
+    if kv_new is not None:
+        _need(kv_new, "kv_new", torch.bfloat16, 2, dev)
+        _need(kv_cache, "kv_cache", torch.bfloat16 if kt == 0 else torch.uint8, 3, dev)
+        if kv_new.shape[1] != 576 or kv_cache.shape[2] != (576 if kt == 0 else 512):
+            raise ValueError("kv_new [T, 576]; kv_cache [pages, page_size, 576] bf16 or [.., 512] e4m3")
+        if kt != 0:
+            _need(kv_rope, "kv_rope", torch.bfloat16, 3, dev)
+            _need(kv_scale, "kv_scale", torch.float32, 2 if kt == 1 else 3, dev)
+            sshape = tuple(kv_cache.shape[:2]) + (() if kt == 1 else (4,))
+            if tuple(kv_rope.shape) != tuple(kv_cache.shape[:2]) + (64,) or tuple(kv_scale.shape) != sshape:
+                raise ValueError("kv_rope [pages, page_size, 64] bf16 and kv_scale [pages, page_size(, 4)] fp32")
+        if T is not None and (kv_new.shape[0] != T or kv_cache.shape[0] != P or kv_cache.shape[1] != ps):
+            raise ValueError("k_new / kv_new and the two caches must agree on T, pages and page size")
+        T, P, ps = kv_new.shape[0], kv_cache.shape[0], kv_cache.shape[1]
+    if T is None:
+        return
+    if workspace is None:
+        workspace = Workspace(256, dev, stream)
+    _check("dsa_cache_append", lib.dsa_cache_append(_ptr(k_new), _ptr(kv_new), _ptr(page_table), page_table.shape[1],
+                                                    _ptr(seq_lens), _ptr(cu_q), B, T, ps, P, it, _ptr(k_cache),
+                                                    _ptr(k_scale), kt, _ptr(kv_cache), _ptr(kv_rope), _ptr(kv_scale),
+                                                    _ptr(workspace.buf), workspace.nbytes, _stream(stream)))
 
 
 def dsa_quant_mxfp8(x, *, q=None, scales=None, stream=None):

@@ -21,6 +21,7 @@ namespace {
 using dsa::IndexerArgs;
 using dsa::MlaArgs;
 using dsa::TopkArgs;
+using dsa::AppendArgs;
 
 constexpr size_t kErrBytes = 256;  // error word block at the start of every workspace
 
@@ -510,6 +511,49 @@ dsa_status dsa_quant_fp8_rows(const void *kv, int64_t rows, void *nope, void *ro
     return cuda_status(dsa::launch_quant_fp8_rows(static_cast<const uint16_t *>(kv), rows,
                                                   static_cast<uint8_t *>(nope), static_cast<uint16_t *>(rope), scale,
                                                   static_cast<cudaStream_t>(stream)));
+}
+
+dsa_status dsa_cache_append(const void *k_new, const void *kv_new, const int32_t *page_table,
+                            int32_t max_pages_per_seq, const int32_t *seq_lens, const int32_t *cu_q, int32_t B,
+                            int32_t T, int32_t page_size, int64_t num_pages, dsa_idx_dtype idx_dtype, void *k_cache,
+                            void *k_scale, dsa_kv_dtype kv_dtype, void *kv_cache, void *kv_rope, float *kv_scale,
+                            void *workspace, size_t workspace_bytes, void *stream) {
+    const bool do_k = k_new != nullptr && k_cache != nullptr, do_kv = kv_new != nullptr && kv_cache != nullptr;
+    if (T < 0 || B < 0 || (T > 0 && B == 0) || page_size <= 0 || num_pages < 0 || max_pages_per_seq < 0)
+        return DSA_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < kErrBytes || !aligned16(workspace)) return DSA_ERR_INVALID_ARG;
+    if (idx_dtype != DSA_IDX_BF16 && idx_dtype != DSA_IDX_MXFP8) return DSA_ERR_UNSUPPORTED;
+    if (kv_dtype != DSA_KV_BF16 && kv_dtype != DSA_KV_FP8_ROWSCALE && kv_dtype != DSA_KV_FP8_TILE128)
+        return DSA_ERR_UNSUPPORTED;
+    if (T == 0 || (!do_k && !do_kv)) return DSA_OK;
+    if (!page_table || !seq_lens || !cu_q) return DSA_ERR_INVALID_ARG;
+    if (do_k && (!aligned16(k_new) || !aligned16(k_cache) || (idx_dtype == DSA_IDX_MXFP8 && !k_scale)))
+        return DSA_ERR_INVALID_ARG;
+    const bool kv_fp8 = kv_dtype != DSA_KV_BF16;
+    if (do_kv && (!aligned16(kv_new) || !aligned16(kv_cache) ||
+                  (kv_fp8 && (!kv_rope || !kv_scale || (reinterpret_cast<uintptr_t>(kv_rope) & 3u) ||
+                              (reinterpret_cast<uintptr_t>(kv_scale) & 3u)))))
+        return DSA_ERR_INVALID_ARG;
+    AppendArgs a{};
+    a.k_new = do_k ? static_cast<const uint16_t *>(k_new) : nullptr;
+    a.kv_new = do_kv ? static_cast<const uint16_t *>(kv_new) : nullptr;
+    a.page_table = page_table;
+    a.seq_lens = seq_lens;
+    a.cu_q = cu_q;
+    a.max_pages = max_pages_per_seq;
+    a.B = B;
+    a.page_size = page_size;
+    a.T = T;
+    a.num_pages = num_pages;
+    a.k_cache = do_k ? k_cache : nullptr;
+    a.k_scale = static_cast<uint8_t *>(k_scale);
+    a.kv_cache = do_kv ? kv_cache : nullptr;
+    a.kv_rope = static_cast<uint16_t *>(kv_rope);
+    a.kv_scale = kv_scale;
+    a.err = reinterpret_cast<uint32_t *>(workspace);
+    const int kv_scales = kv_dtype == DSA_KV_BF16 ? 0 : (kv_dtype == DSA_KV_FP8_TILE128 ? 4 : 1);
+    return cuda_status(dsa::launch_cache_append(a, idx_dtype == DSA_IDX_MXFP8, kv_scales,
+                                                static_cast<cudaStream_t>(stream)));
 }
 
 dsa_status dsa_quant_fp8_tiles(const void *kv, int64_t rows, void *nope, void *rope, float *scale, void *stream) {

@@ -91,6 +91,25 @@ cudaError_t launch_sparse_mla(const CUtensorMap &tm_q, const MlaArgs &a, int NH,
 cudaError_t launch_quant_mxfp8(const uint16_t *x, int64_t n, uint8_t *q, uint8_t *e8m0, cudaStream_t st);
 cudaError_t launch_quant_fp8_tiles(const uint16_t *kv, int64_t rows, uint8_t *nope, uint16_t *rope, float *scale,
                                    cudaStream_t st);
+
+// Cache append: new tokens' index keys / latent rows into their page slots.
+struct AppendArgs {
+    const uint16_t *k_new;      // [T, 128] bf16 or null
+    const uint16_t *kv_new;     // [T, 576] bf16 or null
+    const int32_t *page_table;  // [B, max_pages]
+    const int32_t *seq_lens;    // [B], counting the new tokens
+    const int32_t *cu_q;        // [B + 1]: new tokens of sequence b are cu_q[b]..cu_q[b+1]-1
+    int max_pages, B, page_size;
+    int64_t T, num_pages;
+    void *k_cache;              // [rows, 128] bf16 or e4m3 (null: not written)
+    uint8_t *k_scale;           // MXFP8: [rows, 4] e8m0
+    void *kv_cache;             // [rows, 576] bf16 or [rows, 512] e4m3 (null: not written)
+    uint16_t *kv_rope;          // FP8: [rows, 64] bf16
+    float *kv_scale;            // FP8: [rows] or [rows, 4] fp32
+    uint32_t *err;              // workspace error word
+};
+// kv_scales: 0 bf16 latent rows, 1 FP8 with a row scale, 4 FP8 with tile scales.
+cudaError_t launch_cache_append(const AppendArgs &a, bool idx_mxfp8, int kv_scales, cudaStream_t st);
 cudaError_t launch_quant_fp8_rows(const uint16_t *kv, int64_t rows, uint8_t *nope, uint16_t *rope, float *scale,
                                   cudaStream_t st);
 
