@@ -478,6 +478,8 @@ def main():
                              "append_131k_fp8"])
     ap.add_argument("--kv-scales", default="row", choices=["row", "tile128"],
                     help="FP8 workloads: one fp32 scale per latent row (default) or per 128 latent dims")
+    ap.add_argument("--graph", action="store_true",
+                    help="also time the decode step captured once in a CUDA graph and replayed")
     ap.add_argument("--batch", type=int, default=32,
                     help="sequences per rank (default 32, the benchmark workload; smaller only for profiling)")
     args = ap.parse_args()
@@ -596,7 +598,24 @@ def main():
         run_step(st_["q_idx"], st_["head_w"], st_["q"], st_["pt"], st_["sl"], st_["cq"], c)
     ws.check()
 
-    # ---- device-resident timing, per kernel (no L2 reuse between steps)
+    # ---- device-resident timing of whole steps (no L2 reuse between steps):
+    # events only around each step, so the kernels of a step overlap as they
+    # do in use (programmatic dependent launch)
+    barrier()
+    s_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    for i in range(args.steps):
+        between_steps()
+        st_ = sets[(args.warmup + i) % copies]
+        s_ev[i][0].record(stream)
+        run_step(st_["q_idx"], st_["head_w"], st_["q"], st_["pt"], st_["sl"], st_["cq"], (args.warmup + i) % copies)
+        s_ev[i][1].record(stream)
+    barrier()
+    total = sum(e[0].elapsed_time(e[1]) * 1e-3 for e in s_ev)
+    ws.check()
+
+    # ---- the same steps with an event between the kernels: per-kernel times
+    # for the roofline (the event stops the overlap, so these sum to a little
+    # more than the step)
     barrier()
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     for i in range(args.steps):
@@ -611,8 +630,33 @@ def main():
     barrier()
     t_idx = [e[0].elapsed_time(e[1]) * 1e-3 for e in ev]
     t_mla = [e[1].elapsed_time(e[2]) * 1e-3 for e in ev]
-    total = sum(t_idx) + sum(t_mla)
     ws.check()
+
+    # ---- optional: the same step captured in a CUDA graph (one per input
+    # copy) and replayed, timed with events around each replay
+    t_graph = None
+    if args.graph:
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        graphs = []
+        for c in range(copies):
+            g = torch.cuda.CUDAGraph()
+            st_ = sets[c]
+            with torch.cuda.graph(g, stream=side):
+                run_step(st_["q_idx"], st_["head_w"], st_["q"], st_["pt"], st_["sl"], st_["cq"], c)
+            graphs.append(g)
+        stream.wait_stream(side)
+        for i in range(args.warmup):
+            graphs[i % copies].replay()
+        barrier()
+        g_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+        for i in range(args.steps):
+            g_ev[i][0].record(stream)
+            graphs[(args.warmup + i) % copies].replay()
+            g_ev[i][1].record(stream)
+        barrier()
+        t_graph = sum(e[0].elapsed_time(e[1]) * 1e-3 for e in g_ev)
+        ws.check()
 
     # ---- end to end through the public API: pinned host inputs -> device ->
     # kernels -> output back to pinned host memory, every step
@@ -644,6 +688,8 @@ def main():
 
     # ---- max over ranks
     t_max, e2e_max = max_over_ranks([total, e2e_total], dev)
+    if t_graph is not None:
+        t_graph = max_over_ranks([t_graph], dev)[0]
     tokens = wl.T * args.steps
 
     if rank == 0:
@@ -675,6 +721,10 @@ def main():
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk,
         }
+        if t_graph is not None:
+            line["graph"] = {"value": aggregate_rate(tokens, world, t_graph), "unit": "tokens/s",
+                             "ms_per_step": 1e3 * t_graph / args.steps,
+                             "note": "the step captured once per input copy in a CUDA graph, replayed"}
         if world <= 1 and not args.no_cpu_baseline:
             rate, units, spent = oracle_rate(wl, 10.0, 16)
             line["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": 1, "kind": "oracle",

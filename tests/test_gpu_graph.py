@@ -1,0 +1,69 @@
+"""The library's calls are safe to capture in a CUDA graph (no allocation,
+no host synchronisation, no pageable copy when the caller passes the outputs
+and the workspace): a decode step captured once and replayed on new inputs
+gives bit for bit what the same calls give eagerly, for the bf16 path and
+for the FP8 path with its Q quantisation (index-Q quantise -> indexer + Top-K
+-> sparse MLA -> split combine, chained by programmatic dependent launch)."""
+import numpy as np
+import pytest
+import torch
+
+from _util import dev, dev_bf16
+from indexer_top_sparse_gb300.inputs import make_workload
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_decode_step_replays_in_a_cuda_graph(fp8):
+    import indexer_top_sparse_gb300 as d
+    wl = make_workload("graph", [3000, 700, 64, 2049], [1, 1, 1, 1], H=128, K=512, page_size=64, seed=77)
+    pt, sl, cq = dev(wl.page_table), dev(wl.seq_lens), dev(wl.cu_q)
+    q_idx, head_w, q = dev_bf16(wl.q_idx), dev(wl.head_w), dev_bf16(wl.q)
+    idx = torch.empty((wl.T, wl.K), dtype=torch.int32, device="cuda")
+    out = torch.empty((wl.T, wl.H, 512), dtype=torch.bfloat16, device="cuda")
+    ws = d.Workspace(max(d.index_topk_workspace_size(wl.B, wl.T, wl.K, wl.max_pages, wl.page_size),
+                         d.sparse_mla_workspace_size(wl.T, wl.H, wl.K)))
+    if fp8:
+        k8, ks = d.dsa_quant_mxfp8(dev_bf16(wl.k_idx))
+        nope, rope, vsc = d.dsa_quant_fp8_tiles(dev_bf16(wl.kv))
+        q8 = torch.empty((wl.T, 64, 128), dtype=torch.uint8, device="cuda")
+        qs = torch.empty((wl.T, 64, 4), dtype=torch.uint8, device="cuda")
+    else:
+        k_idx, kv = dev_bf16(wl.k_idx), dev_bf16(wl.kv)
+
+    def step():
+        if fp8:
+            d.dsa_quant_mxfp8(q_idx, q=q8, scales=qs)
+            d.dsa_index_topk(q8, head_w, k8, pt, sl, cq, wl.K, indices=idx, workspace=ws, q_idx_scale=qs,
+                             k_idx_scale=ks, dtype="mxfp8")
+            d.dsa_sparse_mla(q, nope, pt, sl, cq, idx, wl.scale, out=out, workspace=ws, kv_rope=rope,
+                             kv_scale=vsc, dtype="fp8_tile128")
+        else:
+            d.dsa_index_topk(q_idx, head_w, k_idx, pt, sl, cq, wl.K, indices=idx, workspace=ws)
+            d.dsa_sparse_mla(q, kv, pt, sl, cq, idx, wl.scale, out=out, workspace=ws)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for _ in range(2):
+            step()                       # warm up outside the capture
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        step()
+    rng = np.random.default_rng(3)
+    for trial in range(2):
+        # new step inputs, written in place into the captured buffers
+        q_idx.copy_(torch.from_numpy(rng.standard_normal(tuple(q_idx.shape)).astype(np.float32)).to(q_idx))
+        q.copy_(torch.from_numpy(rng.standard_normal(tuple(q.shape)).astype(np.float32)).to(q))
+        step()
+        torch.cuda.synchronize()
+        want_idx, want_out = idx.clone(), out.clone()
+        idx.fill_(-7)
+        out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        ws.check()
+        assert torch.equal(idx, want_idx), trial
+        assert torch.equal(out.view(torch.int16), want_out.view(torch.int16)), trial
