@@ -122,10 +122,10 @@ dsa_status dsa_get_error(void *workspace, void *stream);
 
 /* Fused indexer + Top-K.
  *   q_idx        [T, 64, 128]  bf16, or e4m3 codes for MXFP8
- *   q_idx_scale  [T, 64, 4]    e8m0 bytes (MXFP8 only, else NULL)
+ *   q_idx_scale  [T, 64, 4]    e8m0 bytes, 4-byte aligned (MXFP8 only, else NULL)
  *   head_w       [T, 64]       fp32 per-head weights
  *   k_idx_cache  [num_pages, page_size, 128]  bf16, or e4m3 codes for MXFP8
- *   k_idx_scale  [num_pages, page_size, 4]    e8m0 bytes (MXFP8 only)
+ *   k_idx_scale  [num_pages, page_size, 4]    e8m0 bytes, 16-byte aligned (MXFP8 only)
  *   page_table   [B, max_pages_per_seq] int32; seq_lens [B]; cu_q [B+1] int32
  *   indices      [T, K] int32 OUT: for every query row, the min(K, pos(t)+1)
  *                positions with the highest scores (ties: lower position

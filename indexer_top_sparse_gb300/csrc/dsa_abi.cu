@@ -267,7 +267,8 @@ dsa_status index_common(const void *q_idx, const uint8_t *q_idx_scale, const flo
     if (workspace_bytes < dsa_index_topk_workspace_size(B, T, K, max_pages_per_seq, page_size))
         return DSA_ERR_INVALID_ARG;
     if (dtype != DSA_IDX_BF16 && dtype != DSA_IDX_MXFP8) return DSA_ERR_UNSUPPORTED;
-    if (dtype == DSA_IDX_MXFP8 && (!q_idx_scale || !k_idx_scale || !aligned16(k_idx_scale)))
+    if (dtype == DSA_IDX_MXFP8 && (!q_idx_scale || !k_idx_scale || !aligned16(k_idx_scale) ||
+                                   (reinterpret_cast<uintptr_t>(q_idx_scale) & 3u)))
         return DSA_ERR_INVALID_ARG;
     if (page_size % 64 != 0) return DSA_ERR_UNSUPPORTED;
     if (T == 0) return DSA_OK;

@@ -47,11 +47,6 @@ constexpr int kThreads = 192;
 constexpr int kHist = 256;
 constexpr int kMaxCluster = 16;
 
-// 2^(byte - 127) of an E8M0 scale byte (byte 0 is the subnormal 2^-127).
-__device__ __forceinline__ float e8m0_value(uint32_t byte) {
-    return byte ? __uint_as_float(byte << 23) : __uint_as_float(0x00400000u);
-}
-
 // Order-preserving map from a finite float to uint32 (larger float -> larger
 // key); -0 is folded onto +0.  Every finite value maps above 0x007FFFFF, so 0
 // marks "not a candidate".
@@ -671,10 +666,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 // MXFP8 variant: q_idx and the index-key cache are E4M3 with one E8M0 scale per
 // 32 consecutive values ("Day-0 Inference Adaptation and Optimization for
 // Hybrid Attention Architectures", §4 Optimization 2).  A 128-byte K-major row
-// holds all 128 dims of a position, and one kind::f8f6f4 MMA (K = 32) covers
-// exactly one scale group, so each tile runs four MMAs into four accumulators
-// and the epilogue applies 2^(scale_q + scale_k) per group before the ReLU:
-//     score = sum_j w_j ReLU( sum_g 2^(sq_jg + sk_g) * (q_jg . k_g) ).
+// holds all 128 dims of a position, and one block-scaled MMA
+// (kind::mxf8f6f4, K = 32) covers exactly one scale group: the tensor core
+// multiplies each group's products by 2^(scale_q + scale_k) itself, so the
+// four MMAs of a tile accumulate into one accumulator
+//     score = sum_j w_j ReLU( sum_g 2^(sq_jg + sk_g) * (q_jg . k_g) )
+// and the epilogue is the bf16 kernel's ReLU and head weighting.  The scales
+// go to TMEM: the query's once, each key tile's (128 positions x 4 groups)
+// into one of two scale buffers, written by four epilogue warps (one per lane
+// quadrant) one tile ahead of the MMA.
 // One query row per cluster (decode); warps: 0 TMA, 1 MMA, 2..9 epilogue
 // (two per TMEM lane quadrant, 32 heads each).
 constexpr int kF8Threads = 320;
@@ -686,11 +686,15 @@ struct __align__(16) F8Bars {
     uint64_t empty[8];
     uint64_t tfull[2];
     uint64_t tempty[2];
+    uint64_t sf_full[2];  // a key tile's scales are in TMEM scale buffer i & 1
     uint64_t qbar;
     uint64_t drain;
     uint32_t tmem_slot;
     int abort;
 };
+// TMEM columns of the MXFP8 kernel: accumulators (2 x 64 heads), the query's
+// scales, the key scale buffers (4-aligned).
+constexpr uint32_t kF8AccCols = kHI, kF8SfQ = 2 * kHI, kF8SfK = kF8SfQ + 4;
 
 template <bool kWriteScores>
 __global__ void __launch_bounds__(kF8Threads, 1)
@@ -708,8 +712,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
     uint8_t *sKs = sK + (size_t)a.stages * kF8TileBytes;  // scale_slots x 128 positions x 4 scale bytes
     uint32_t *sKeys = reinterpret_cast<uint32_t *>(sKs + (size_t)scale_slots * kTileM * 4);
     float *sW = reinterpret_cast<float *>(sKeys + key_cap);
-    float *sQs = sW + kHI;                                // [4 groups][64 heads] 2^(q scale)
-    float *sPart = sQs + kHI * 4;                         // [2][128] per-half partial scores
+    float *sPart = sW + kHI;                              // [2][128] per-half partial scores
     uint32_t *sHist0 = reinterpret_cast<uint32_t *>(sPart + 2 * kTileM);
     int32_t *sRows = reinterpret_cast<int32_t *>(sHist0 + kHist);
     SelectSmem *ss = reinterpret_cast<SelectSmem *>(sRows + ((2 * a.tiles_cap + 3) & ~3));
@@ -744,6 +747,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bars->tfull[i], 1);
             mbar_init(&bars->tempty[i], 8);
+            mbar_init(&bars->sf_full[i], 4);
         }
         mbar_init(&bars->qbar, 1);
         mbar_init(&bars->drain, 1);
@@ -751,8 +755,6 @@ __global__ void __launch_bounds__(kF8Threads, 1)
         fence_mbar_init();
     }
     for (int i = threadIdx.x; i < kHI; i += kF8Threads) sW[i] = __ldg(a.head_w + (size_t)t0 * kHI + i);
-    for (int i = threadIdx.x; i < kHI * 4; i += kF8Threads)  // input layout [head][group]
-        sQs[(i & 3) * kHI + (i >> 2)] = e8m0_value(__ldg(a.q_scale + (size_t)t0 * kHI * 4 + i));
     for (int i = threadIdx.x; i < kHist; i += kF8Threads) sHist0[i] = 0u;
     for (int j = threadIdx.x; j < 2 * n_tiles; j += kF8Threads) {
         const int p0 = tile0 * kTileM + j * kBox;
@@ -804,19 +806,20 @@ __global__ void __launch_bounds__(kF8Threads, 1)
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_e4m3_f32(kTileM, kHI);
             bool ok = mbar_wait(&bars->qbar, 0, a.err, 0x221, abort);
             const uint32_t q_base = smem_u32(sQ);
             for (int i = 0; ok && i < n_tiles; ++i) {
                 const int s = i % a.stages, buf = i & 1;
                 if (!mbar_wait(&bars->full[s], (i / a.stages) & 1, a.err, 0x222, abort)) break;
                 if (i >= 2 && !mbar_wait(&bars->tempty[buf], ((i >> 1) & 1) ^ 1, a.err, 0x223, abort)) break;
+                if (!mbar_wait(&bars->sf_full[buf], (i >> 1) & 1, a.err, 0x224, abort)) break;
                 tc_fence_after();
                 const uint32_t k_base = smem_u32(sK + (size_t)s * kF8TileBytes);
 #pragma unroll
-                for (int g = 0; g < 4; ++g)  // one scale group of 32 dims per MMA
-                    mma_f8_ss(tmem + (uint32_t)(buf * 256 + g * kHI), sdesc_kmajor_sw128(k_base + g * 32),
-                              sdesc_kmajor_sw128(q_base + g * 32), idesc, 0u);
+                for (int g = 0; g < 4; ++g)  // one scale group of 32 dims per MMA, scale byte g
+                    mma_mxf8_ss(tmem + (uint32_t)(buf * kF8AccCols), sdesc_kmajor_sw128(k_base + g * 32),
+                                sdesc_kmajor_sw128(q_base + g * 32), idesc_mxf8_e4m3(kTileM, kHI, g, g),
+                                tmem + kF8SfK + 4u * buf, tmem + kF8SfQ, g > 0 ? 1u : 0u);
                 mma_commit(&bars->empty[s]);
                 mma_commit(&bars->tfull[buf]);
             }
@@ -830,47 +833,61 @@ __global__ void __launch_bounds__(kF8Threads, 1)
         // epilogue: warp -> (TMEM lane quadrant, half of the heads)
         const int quad = warp & 3, hh = (warp - 2) >> 2;
         const int row = quad * 32 + lane;
+        const uint32_t lanes = (uint32_t)(quad * 32) << 16;
+        // The hh == 0 warps (one per lane quadrant) write the block scales to
+        // TMEM: row r's four group scales in lane r % 32 of every quadrant,
+        // column base + r / 32, group g in byte g.
+        const bool sf_writer = hh == 0;
+        auto write_key_scales = [&](int j) -> bool {
+            if (!mbar_wait(&bars->full[j % a.stages], (j / a.stages) & 1, a.err, 0x322, abort)) return false;
+            const uint8_t *ks = sKs + (size_t)(j % scale_slots) * kTileM * 4;
+            uint32_t w[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) w[c] = *reinterpret_cast<const uint32_t *>(ks + (lane + 32 * c) * 4);
+            tmem_st4(tmem + lanes + kF8SfK + 4u * (j & 1), w);
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->sf_full[j & 1]);
+            return true;
+        };
         bool ok = true;
+        if (sf_writer && n_tiles > 0) {
+            uint32_t w[4];  // the query's scales, input layout [head][group]; heads >= 64 unused
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int h = lane + 32 * c;
+                w[c] = h < kHI ? __ldg(reinterpret_cast<const uint32_t *>(a.q_scale + ((size_t)t0 * kHI + h) * 4))
+                               : 0x7F7F7F7Fu;
+            }
+            tmem_st4(tmem + lanes + kF8SfQ, w);
+            ok = write_key_scales(0);  // waits for the stores above too
+        }
         for (int i = 0; i < n_tiles; ++i) {
-            const int buf = i & 1, slot = i % scale_slots;
-            ok = mbar_wait(&bars->tfull[buf], (i >> 1) & 1, a.err, 0x321, abort);
+            const int buf = i & 1;
+            // the next tile's scales: its buffer was last read by the MMA of
+            // tile i - 1, whose accumulator this warp has already consumed
+            if (ok && sf_writer && i + 1 < n_tiles) ok = write_key_scales(i + 1);
+            if (ok) ok = mbar_wait(&bars->tfull[buf], (i >> 1) & 1, a.err, 0x321, abort);
             ok = bar_and(2, 256, ok);
             if (!ok) break;
             tc_fence_after();
-            const uint32_t ks = *reinterpret_cast<const uint32_t *>(sKs + (size_t)slot * kTileM * 4 + row * 4);
-            // acc[j] = sum_g 2^(sq_jg) 2^(sk_g) D_jg over this thread's 32 heads,
-            // in pairs of heads (paired fp32 multiply-add, each lane rounded as fmaf)
-            float2 acc[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) acc[j] = make_float2(0.0f, 0.0f);
-#pragma unroll
-            for (int g = 0; g < 4; ++g) {
-                uint32_t r[32];
-                tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(buf * 256 + g * kHI + hh * 32), r);
-                tmem_wait_ld();
-                const float skg = e8m0_value((ks >> (8 * g)) & 0xFFu);
-                const float2 sk2 = make_float2(skg, skg);
-                const float4 *qs4 = reinterpret_cast<const float4 *>(sQs + g * kHI + hh * 32);
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const float4 q4 = qs4[k];
-                    const float2 s01 = __fmul2_rn(make_float2(q4.x, q4.y), sk2);
-                    const float2 s23 = __fmul2_rn(make_float2(q4.z, q4.w), sk2);
-                    acc[2 * k] = __ffma2_rn(make_float2(__uint_as_float(r[4 * k]), __uint_as_float(r[4 * k + 1])), s01,
-                                            acc[2 * k]);
-                    acc[2 * k + 1] = __ffma2_rn(
-                        make_float2(__uint_as_float(r[4 * k + 2]), __uint_as_float(r[4 * k + 3])), s23, acc[2 * k + 1]);
-                }
-            }
+            uint32_t r[32];
+            tmem_ld32(tmem + lanes + (uint32_t)(buf * kF8AccCols + hh * 32), r);
+            tmem_wait_ld();
             float2 part2 = make_float2(0.0f, 0.0f);
             const float4 *w4 = reinterpret_cast<const float4 *>(sW + hh * 32);
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
                 const float4 w = w4[k];
                 part2 = __ffma2_rn(make_float2(w.x, w.y),
-                                   make_float2(fmaxf(acc[2 * k].x, 0.0f), fmaxf(acc[2 * k].y, 0.0f)), part2);
+                                   make_float2(fmaxf(__uint_as_float(r[4 * k]), 0.0f),
+                                               fmaxf(__uint_as_float(r[4 * k + 1]), 0.0f)),
+                                   part2);
                 part2 = __ffma2_rn(make_float2(w.z, w.w),
-                                   make_float2(fmaxf(acc[2 * k + 1].x, 0.0f), fmaxf(acc[2 * k + 1].y, 0.0f)), part2);
+                                   make_float2(fmaxf(__uint_as_float(r[4 * k + 2]), 0.0f),
+                                               fmaxf(__uint_as_float(r[4 * k + 3]), 0.0f)),
+                                   part2);
             }
             const float part = part2.x + part2.y;
             tc_fence_before();
@@ -936,7 +953,7 @@ size_t indexer_smem_bytes(int G, int stages, int tiles_cap) {
 size_t indexer_mxfp8_smem_bytes(int stages, int tiles_cap) {
     return 1024 + (size_t)kHI * kDI + (size_t)stages * kF8TileBytes + (size_t)(stages + 2) * kTileM * 4 +
            (size_t)tiles_cap * kTileM * 4 +
-           (size_t)(kHI + kHI * 4 + 2 * kTileM + kHist) * 4 + (size_t)((2 * tiles_cap + 3) & ~3) * 4 +
+           (size_t)(kHI + 2 * kTileM + kHist) * 4 + (size_t)((2 * tiles_cap + 3) & ~3) * 4 +
            sizeof(SelectSmem) + sizeof(F8Bars);
 }
 

@@ -226,6 +226,22 @@ __device__ __forceinline__ void mma_f8_ss(uint32_t d_tmem, uint64_t a_desc, uint
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+// D[tmem] (+)= A[smem] * B[smem]^T with block scaling, kind::mxf8f6f4 (E4M3
+// inputs, fp32 accumulate, K = 32): every row of A and every column of B is
+// multiplied by its E8M0 scale for this K block.  The scales live in TMEM:
+// the scale of row r sits in lane r % 32 (the same in every lane quadrant),
+// column sf + r / 32, byte `sf_id` of that 32-bit column (sf_id comes with the
+// instruction descriptor).  sf_a / sf_b are column addresses, 4-aligned.
+__device__ __forceinline__ void mma_mxf8_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t sf_a, uint32_t sf_b, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+            d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sf_a), "r"(sf_b), "r"(accumulate)
+        : "memory");
+}
 // Arrive once on `bar` when every tcgen05.mma issued so far by this thread
 // has completed.
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {
@@ -327,6 +343,11 @@ __device__ __forceinline__ void tmem_st(uint32_t taddr, const uint32_t (&r)[N]) 
     else if constexpr (N == 16) tmem_st16(taddr, r);
     else tmem_st8(taddr, r);
 }
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, const uint32_t (&r)[4]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};" ::"r"(taddr), "r"(r[0]), "r"(r[1]),
+                 "r"(r[2]), "r"(r[3])
+                 : "memory");
+}
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // Named barrier over `count` threads that also ANDs a predicate across them.
@@ -388,6 +409,15 @@ __host__ __device__ constexpr uint32_t idesc_e4m3_f32(uint32_t M, uint32_t N) {
     return (1u << 4)            // D format: f32
            | ((N >> 3) << 17)   // N / 8   (A, B format 0 = E4M3)
            | ((M >> 4) << 24);  // M / 16
+}
+// Instruction descriptor, kind::mxf8f6f4 with block scaling: E4M3 A and B
+// (both K-major), fp32 D, E8M0 scales; sf_a / sf_b select the scale byte.
+__host__ __device__ constexpr uint32_t idesc_mxf8_e4m3(uint32_t M, uint32_t N, uint32_t sf_a, uint32_t sf_b) {
+    return (sf_b << 4)          // B scale byte
+           | ((N >> 3) << 17)   // N / 8   (A, B format 0 = E4M3)
+           | (1u << 23)         // scale format: E8M0
+           | ((M >> 4) << 24)   // M / 16
+           | (sf_a << 29);      // A scale byte
 }
 // Same with A stored MN-major (transpose bit for A).
 __host__ __device__ constexpr uint32_t idesc_bf16_f32_amn(uint32_t M, uint32_t N) {
