@@ -433,6 +433,52 @@ __device__ __forceinline__ int find_seq(const int32_t *cu_q, int B, int t) {
     return lo;
 }
 
+// Longest-first order of the grid: the clusters of one launch start in grid
+// order as SMs free up, so a long query row that starts late sets the launch's
+// length.  Grid row `row` takes the query row with the row-th longest causal
+// history (ties: lower row first).  Up to kRankMax rows (and kRankSeqMax
+// sequences) every CTA ranks them itself in `scratch` (2 kRankMax + 2 ints,
+// shared memory that is free until the selection); longer batches are taken
+// last row first, which is longest first within a causal prefill.  Returns
+// the query row and its sequence (*b).  Every thread of the CTA calls this
+// (it has block barriers); row < a.T.
+constexpr int kRankMax = 256, kRankSeqMax = 1024;
+static_assert(sizeof(SelectSmem) >= (2 * kRankMax + 2) * sizeof(int), "ranking scratch fits the selection block");
+template <int kT>
+__device__ int ordered_query(const IndexerArgs &a, int row, int *scratch, int *b) {
+    if (a.T > kRankMax || a.B > kRankSeqMax) {
+        const int t = a.T - 1 - row;
+        *b = find_seq(a.cu_q, a.B, t);
+        return t;
+    }
+    int *pos = scratch, *seq = scratch + kRankMax + 1;
+    for (int s = threadIdx.x; s < a.B; s += kT) {
+        const int c0 = __ldg(a.cu_q + s), c1 = __ldg(a.cu_q + s + 1), len = __ldg(a.seq_lens + s);
+        for (int i = c0; i < c1; ++i) {
+            pos[i] = len - (c1 - c0) + (i - c0);  // position of query row i
+            seq[i] = s;
+        }
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < a.T; i += kT) {
+        const int pi = pos[i];
+        int rank = 0;
+        for (int j = 0; j < a.T; ++j) {
+            const int pj = pos[j];
+            rank += (pj > pi) || (pj == pi && j < i);
+        }
+        if (rank == row) {
+            pos[kRankMax] = i;
+            seq[kRankMax] = seq[i];
+        }
+    }
+    __syncthreads();
+    const int t = pos[kRankMax];
+    *b = seq[kRankMax];
+    __syncthreads();  // the scratch is free again
+    return t;
+}
+
 template <int G, bool kWriteScores>
 __global__ void __launch_bounds__(kThreads, 1)
     indexer_topk_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
@@ -460,13 +506,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---- which query rows this cluster serves
     int b, t0, gn;
     {
-        const int g = blockIdx.y;
         if (G == 1) {
-            if (g >= a.T) return;
-            t0 = g;
-            b = find_seq(a.cu_q, a.B, t0);
+            if ((int)blockIdx.y >= a.T) return;
+            t0 = ordered_query<kThreads>(a, blockIdx.y, reinterpret_cast<int *>(ss), &b);
             gn = 1;
         } else {
+            const int g = gridDim.y - 1 - blockIdx.y;  // last (longest, in a causal prefill) groups first
             int acc = 0;
             b = -1;
             for (int s = 0; s < a.B; ++s) {
@@ -673,10 +718,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 //     score = sum_j w_j ReLU( sum_g 2^(sq_jg + sk_g) * (q_jg . k_g) )
 // and the epilogue is the bf16 kernel's ReLU and head weighting.  The scales
 // go to TMEM: the query's once, each key tile's (128 positions x 4 groups)
-// into one of two scale buffers, written by four epilogue warps (one per lane
-// quadrant) one tile ahead of the MMA.
-// One query row per cluster (decode); warps: 0 TMA, 1 MMA, 2..9 epilogue
-// (two per TMEM lane quadrant, 32 heads each).
+// into one of two scale buffers, written by four warps (one per lane
+// quadrant) ahead of the MMA.
+// One query row per cluster (decode); warps: 0 TMA, 1 MMA, 2..5 epilogue
+// (one per TMEM lane quadrant, thread = position, all 64 heads), 6..9 block
+// scales into TMEM.
 constexpr int kF8Threads = 320;
 constexpr int kF8TileBytes = kTileM * kDI;      // 16 KB of E4M3 keys per tile
 constexpr int kF8BoxBytes = kBox * kDI;         // 8 KB per 64-row box
@@ -684,17 +730,19 @@ constexpr int kF8BoxBytes = kBox * kDI;         // 8 KB per 64-row box
 struct __align__(16) F8Bars {
     uint64_t full[8];
     uint64_t empty[8];
-    uint64_t tfull[2];
-    uint64_t tempty[2];
-    uint64_t sf_full[2];  // a key tile's scales are in TMEM scale buffer i & 1
+    uint64_t tfull[4];    // accumulator i % 4 holds tile i
+    uint64_t tempty[4];
+    uint64_t sf_full[4];  // tile i's key scales are in TMEM scale buffer i % 4
     uint64_t qbar;
     uint64_t drain;
     uint32_t tmem_slot;
     int abort;
 };
-// TMEM columns of the MXFP8 kernel: accumulators (2 x 64 heads), the query's
-// scales, the key scale buffers (4-aligned).
-constexpr uint32_t kF8AccCols = kHI, kF8SfQ = 2 * kHI, kF8SfK = kF8SfQ + 4;
+// TMEM columns of the MXFP8 kernel: kF8Bufs accumulators of 64 heads, the
+// query's scales, kF8Bufs key scale buffers (4-aligned).  Four of each keep the
+// scale writes (which share TMEM with the running MMA) a few tiles ahead.
+constexpr int kF8Bufs = 4;
+constexpr uint32_t kF8AccCols = kHI, kF8SfQ = kF8Bufs * kHI, kF8SfK = kF8SfQ + 4;
 
 template <bool kWriteScores>
 __global__ void __launch_bounds__(kF8Threads, 1)
@@ -705,15 +753,9 @@ __global__ void __launch_bounds__(kF8Threads, 1)
     const int key_cap = a.tiles_cap * kTileM;
     uint8_t *sQ = smem;                                   // 64 heads x 128 B
     uint8_t *sK = sQ + kHI * kDI;                         // stages x 16 KB
-    // Key scales get their own ring, two slots deeper than the key ring: the
-    // epilogue reads them after the MMA has released the key stage, but at
-    // most two tiles behind the MMA (the TMEM accumulators are double-buffered).
-    const int scale_slots = a.stages + 2;
-    uint8_t *sKs = sK + (size_t)a.stages * kF8TileBytes;  // scale_slots x 128 positions x 4 scale bytes
-    uint32_t *sKeys = reinterpret_cast<uint32_t *>(sKs + (size_t)scale_slots * kTileM * 4);
+    uint32_t *sKeys = reinterpret_cast<uint32_t *>(sK + (size_t)a.stages * kF8TileBytes);
     float *sW = reinterpret_cast<float *>(sKeys + key_cap);
-    float *sPart = sW + kHI;                              // [2][128] per-half partial scores
-    uint32_t *sHist0 = reinterpret_cast<uint32_t *>(sPart + 2 * kTileM);
+    uint32_t *sHist0 = reinterpret_cast<uint32_t *>(sW + kHI);
     int32_t *sRows = reinterpret_cast<int32_t *>(sHist0 + kHist);
     SelectSmem *ss = reinterpret_cast<SelectSmem *>(sRows + ((2 * a.tiles_cap + 3) & ~3));
     F8Bars *bars = reinterpret_cast<F8Bars *>(ss + 1);
@@ -722,10 +764,10 @@ __global__ void __launch_bounds__(kF8Threads, 1)
     const int C = (int)cluster.num_blocks();
     const int crank = (int)cluster.block_rank();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int t0 = blockIdx.y;
-    if (t0 >= a.T) return;
+    if ((int)blockIdx.y >= a.T) return;
     grid_dep_wait();  // inputs written by the kernel launched just before are visible
-    const int b = find_seq(a.cu_q, a.B, t0);
+    int b;
+    const int t0 = ordered_query<kF8Threads>(a, blockIdx.y, reinterpret_cast<int *>(ss), &b);
     const int nq_b = __ldg(a.cu_q + b + 1) - __ldg(a.cu_q + b);
     const int pos_last = __ldg(a.seq_lens + b) - nq_b + (t0 - __ldg(a.cu_q + b));
     const int n_total = pos_last + 1;
@@ -744,9 +786,9 @@ __global__ void __launch_bounds__(kF8Threads, 1)
             mbar_init(&bars->full[s], 1);
             mbar_init(&bars->empty[s], 1);
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kF8Bufs; ++i) {
             mbar_init(&bars->tfull[i], 1);
-            mbar_init(&bars->tempty[i], 8);
+            mbar_init(&bars->tempty[i], 4);
             mbar_init(&bars->sf_full[i], 4);
         }
         mbar_init(&bars->qbar, 1);
@@ -787,14 +829,12 @@ __global__ void __launch_bounds__(kF8Threads, 1)
                 issued = i + 1;
                 uint32_t bytes = 0;
                 for (int h = 0; h < 2; ++h)
-                    if (sRows[2 * i + h] >= 0) bytes += kF8BoxBytes + kBox * 4;
+                    if (sRows[2 * i + h] >= 0) bytes += kF8BoxBytes;
                 mbar_arrive_expect_tx(&bars->full[s], bytes);
                 for (int h = 0; h < 2; ++h) {
                     const int row = sRows[2 * i + h];
                     if (row < 0) continue;
                     tma_load_2d(sK + (size_t)s * kF8TileBytes + h * kF8BoxBytes, &tm_k, &bars->full[s], 0, row);
-                    uint8_t *dst = sKs + (size_t)(i % scale_slots) * kTileM * 4 + h * kBox * 4;
-                    bulk_load(dst, a.k_scale + (size_t)row * 4, kBox * 4, &bars->full[s]);
                 }
             }
             if (*abort) {
@@ -809,17 +849,18 @@ __global__ void __launch_bounds__(kF8Threads, 1)
             bool ok = mbar_wait(&bars->qbar, 0, a.err, 0x221, abort);
             const uint32_t q_base = smem_u32(sQ);
             for (int i = 0; ok && i < n_tiles; ++i) {
-                const int s = i % a.stages, buf = i & 1;
+                const int s = i % a.stages, buf = i % kF8Bufs;
+                const uint32_t round = (uint32_t)(i / kF8Bufs) & 1u;
                 if (!mbar_wait(&bars->full[s], (i / a.stages) & 1, a.err, 0x222, abort)) break;
-                if (i >= 2 && !mbar_wait(&bars->tempty[buf], ((i >> 1) & 1) ^ 1, a.err, 0x223, abort)) break;
-                if (!mbar_wait(&bars->sf_full[buf], (i >> 1) & 1, a.err, 0x224, abort)) break;
+                if (i >= kF8Bufs && !mbar_wait(&bars->tempty[buf], round ^ 1u, a.err, 0x223, abort)) break;
+                if (!mbar_wait(&bars->sf_full[buf], round, a.err, 0x224, abort)) break;
                 tc_fence_after();
                 const uint32_t k_base = smem_u32(sK + (size_t)s * kF8TileBytes);
 #pragma unroll
                 for (int g = 0; g < 4; ++g)  // one scale group of 32 dims per MMA, scale byte g
                     mma_mxf8_ss(tmem + (uint32_t)(buf * kF8AccCols), sdesc_kmajor_sw128(k_base + g * 32),
                                 sdesc_kmajor_sw128(q_base + g * 32), idesc_mxf8_e4m3(kTileM, kHI, g, g),
-                                tmem + kF8SfK + 4u * buf, tmem + kF8SfQ, g > 0 ? 1u : 0u);
+                                tmem + kF8SfK + 4u * (uint32_t)buf, tmem + kF8SfQ, g > 0 ? 1u : 0u);
                 mma_commit(&bars->empty[s]);
                 mma_commit(&bars->tfull[buf]);
             }
@@ -829,56 +870,26 @@ __global__ void __launch_bounds__(kF8Threads, 1)
                 mbar_wait(&bars->drain, 0, nullptr, 0, &no_abort);
             }
         }
-    } else {
-        // epilogue: warp -> (TMEM lane quadrant, half of the heads)
-        const int quad = warp & 3, hh = (warp - 2) >> 2;
+    } else if (warp < 6) {
+        // epilogue: warp -> TMEM lane quadrant; thread = one position, all 64 heads
+        const int quad = warp & 3;
         const int row = quad * 32 + lane;
         const uint32_t lanes = (uint32_t)(quad * 32) << 16;
-        // The hh == 0 warps (one per lane quadrant) write the block scales to
-        // TMEM: row r's four group scales in lane r % 32 of every quadrant,
-        // column base + r / 32, group g in byte g.
-        const bool sf_writer = hh == 0;
-        auto write_key_scales = [&](int j) -> bool {
-            if (!mbar_wait(&bars->full[j % a.stages], (j / a.stages) & 1, a.err, 0x322, abort)) return false;
-            const uint8_t *ks = sKs + (size_t)(j % scale_slots) * kTileM * 4;
-            uint32_t w[4];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) w[c] = *reinterpret_cast<const uint32_t *>(ks + (lane + 32 * c) * 4);
-            tmem_st4(tmem + lanes + kF8SfK + 4u * (j & 1), w);
-            tmem_wait_st();
+        for (int i = 0; i < n_tiles; ++i) {
+            const int buf = i % kF8Bufs;
+            if (!mbar_wait(&bars->tfull[buf], (uint32_t)(i / kF8Bufs) & 1u, a.err, 0x321, abort)) break;
+            tc_fence_after();
+            uint32_t r[64];
+            tmem_ld32(tmem + lanes + (uint32_t)(buf * kF8AccCols), *reinterpret_cast<uint32_t(*)[32]>(r));
+            tmem_ld32(tmem + lanes + (uint32_t)(buf * kF8AccCols + 32), *reinterpret_cast<uint32_t(*)[32]>(r + 32));
+            tmem_wait_ld();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->sf_full[j & 1]);
-            return true;
-        };
-        bool ok = true;
-        if (sf_writer && n_tiles > 0) {
-            uint32_t w[4];  // the query's scales, input layout [head][group]; heads >= 64 unused
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const int h = lane + 32 * c;
-                w[c] = h < kHI ? __ldg(reinterpret_cast<const uint32_t *>(a.q_scale + ((size_t)t0 * kHI + h) * 4))
-                               : 0x7F7F7F7Fu;
-            }
-            tmem_st4(tmem + lanes + kF8SfQ, w);
-            ok = write_key_scales(0);  // waits for the stores above too
-        }
-        for (int i = 0; i < n_tiles; ++i) {
-            const int buf = i & 1;
-            // the next tile's scales: its buffer was last read by the MMA of
-            // tile i - 1, whose accumulator this warp has already consumed
-            if (ok && sf_writer && i + 1 < n_tiles) ok = write_key_scales(i + 1);
-            if (ok) ok = mbar_wait(&bars->tfull[buf], (i >> 1) & 1, a.err, 0x321, abort);
-            ok = bar_and(2, 256, ok);
-            if (!ok) break;
-            tc_fence_after();
-            uint32_t r[32];
-            tmem_ld32(tmem + lanes + (uint32_t)(buf * kF8AccCols + hh * 32), r);
-            tmem_wait_ld();
+            if (lane == 0) mbar_arrive(&bars->tempty[buf]);  // the accumulator is in registers
             float2 part2 = make_float2(0.0f, 0.0f);
-            const float4 *w4 = reinterpret_cast<const float4 *>(sW + hh * 32);
+            const float4 *w4 = reinterpret_cast<const float4 *>(sW);
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
+            for (int k = 0; k < 16; ++k) {
                 const float4 w = w4[k];
                 part2 = __ffma2_rn(make_float2(w.x, w.y),
                                    make_float2(fmaxf(__uint_as_float(r[4 * k]), 0.0f),
@@ -889,20 +900,65 @@ __global__ void __launch_bounds__(kF8Threads, 1)
                                                fmaxf(__uint_as_float(r[4 * k + 3]), 0.0f)),
                                    part2);
             }
-            const float part = part2.x + part2.y;
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->tempty[buf]);
-            sPart[hh * kTileM + row] = part;
-            bar_sync(2, 256);
-            if (hh == 0) {
-                const float sc = sPart[row] + sPart[kTileM + row];
-                const int pos = (tile0 + i) * kTileM + row;
-                const bool valid = pos <= pos_last;
-                const uint32_t key = valid ? score_key(sc) : 0u;
-                sKeys[i * kTileM + row] = key;
-                if (valid) red_shared_add(smem_u32(&sHist0[key >> 24]), 1u);
-                if (kWriteScores && valid && pos < a.ld_scores) a.scores[(size_t)t0 * a.ld_scores + pos] = sc;
+            const float sc = part2.x + part2.y;
+            const int pos = (tile0 + i) * kTileM + row;
+            const bool valid = pos <= pos_last;
+            const uint32_t key = valid ? score_key(sc) : 0u;
+            sKeys[i * kTileM + row] = key;
+            if (valid) red_shared_add(smem_u32(&sHist0[key >> 24]), 1u);
+            if (kWriteScores && valid && pos < a.ld_scores) a.scores[(size_t)t0 * a.ld_scores + pos] = sc;
+        }
+    } else {
+        // block scales into TMEM, ahead of the MMA: warp -> lane quadrant.
+        // Row r's four group scales go to lane r % 32 of every quadrant,
+        // column base + r / 32, group g in byte g.
+        const int quad = warp & 3;
+        const uint32_t lanes = (uint32_t)(quad * 32) << 16;
+        if (n_tiles > 0) {
+            uint32_t w[4];  // the query's scales, input layout [head][group]; heads >= 64 unused
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int h = lane + 32 * c;
+                w[c] = h < kHI ? __ldg(reinterpret_cast<const uint32_t *>(a.q_scale + ((size_t)t0 * kHI + h) * 4))
+                               : 0x7F7F7F7Fu;
+            }
+            tmem_st4(tmem + lanes + kF8SfQ, w);
+        }
+        // The key scales come straight from the cache with plain loads (a
+        // warp's 32 rows are 128 contiguous bytes), issued kF8Bufs tiles
+        // ahead: they need only the page rows, not the key tile, and leave the
+        // bulk-copy engine to the key tiles.  Rows of a half that is past the
+        // sequence get scale 1 (their scores are never used).
+        const uint32_t *kscale = reinterpret_cast<const uint32_t *>(a.k_scale);
+        auto load_scales = [&](int j, uint32_t (&w)[4]) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int base = sRows[2 * j + (c >> 1)];  // rows 0-63: first box, 64-127: second
+                w[c] = base >= 0 ? __ldg(kscale + base + lane + 32 * (c & 1)) : 0x7F7F7F7Fu;
+            }
+        };
+        uint32_t wq[kF8Bufs][4];
+#pragma unroll
+        for (int u = 0; u < kF8Bufs; ++u)
+            if (u < n_tiles) load_scales(u, wq[u]);
+        bool sf_ok = true;
+        for (int j0 = 0; sf_ok && j0 < n_tiles; j0 += kF8Bufs) {
+#pragma unroll
+            for (int u = 0; u < kF8Bufs; ++u) {
+                const int j = j0 + u;
+                if (j >= n_tiles) break;
+                // buffer u was last read by the MMA of tile j - kF8Bufs
+                if (j >= kF8Bufs &&
+                    !mbar_wait(&bars->tfull[u], (uint32_t)((j - kF8Bufs) / kF8Bufs) & 1u, a.err, 0x323, abort)) {
+                    sf_ok = false;
+                    break;
+                }
+                tmem_st4(tmem + lanes + kF8SfK + 4u * (uint32_t)u, wq[u]);
+                tmem_wait_st();  // (the first time also the query's scales)
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->sf_full[u]);
+                if (j + kF8Bufs < n_tiles) load_scales(j + kF8Bufs, wq[u]);
             }
         }
     }
@@ -951,9 +1007,8 @@ size_t indexer_smem_bytes(int G, int stages, int tiles_cap) {
 }
 
 size_t indexer_mxfp8_smem_bytes(int stages, int tiles_cap) {
-    return 1024 + (size_t)kHI * kDI + (size_t)stages * kF8TileBytes + (size_t)(stages + 2) * kTileM * 4 +
-           (size_t)tiles_cap * kTileM * 4 +
-           (size_t)(kHI + 2 * kTileM + kHist) * 4 + (size_t)((2 * tiles_cap + 3) & ~3) * 4 +
+    return 1024 + (size_t)kHI * kDI + (size_t)stages * kF8TileBytes + (size_t)tiles_cap * kTileM * 4 +
+           (size_t)(kHI + kHist) * 4 + (size_t)((2 * tiles_cap + 3) & ~3) * 4 +
            sizeof(SelectSmem) + sizeof(F8Bars);
 }
 
