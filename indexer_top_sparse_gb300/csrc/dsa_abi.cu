@@ -31,6 +31,9 @@ std::atomic<int> g_idx_cluster{0}, g_idx_stages{0}, g_idx_group{0}, g_mla_splits
 // 1: run the two 64-head CTAs of a 128-head query as a pair sharing each
 // gathered row; -1: independent CTAs; 0: automatic (see mla_pair).
 std::atomic<int> g_mla_pair{0};
+// 1: stream-K sparse MLA whenever it applies; -1: never; 0: when the split
+// grid would leave SMs idle (see mla_sk_ctas)
+std::atomic<int> g_mla_sk{0};
 
 int sm_count() {
     int dev = 0, n = 0;
@@ -249,6 +252,32 @@ bool mla_pair(int T, int H, int splits) {
     return mla_heads_per_cta(H) == 64 && H == 128 && (long long)T * mla_groups(H) * splits > sm_count();
 }
 
+// Stream-K sparse MLA: CTAs (one per SM) for T rows of H heads with K keys,
+// or 0 for the split grid.  It applies with 64-head CTAs when every CTA gets
+// 2..tpr key tiles (so a CTA's run spans at most two (row, head group) pairs
+// and its row table fits).  Automatically only where it measured faster on
+// GB300: the split grid has fewer CTAs than SMs with one split per (row, head
+// group) (64 x 4k-128k FP8 decode: 137 -> 131 us).  With two or more splits
+// (32 x 32768 decode) the even share of 13.5 instead of 16 tiles per CTA was
+// slower (60 against 57 us, and a larger combine): the two head groups of a
+// row no longer gather the same rows at the same time.
+int mla_sk_ctas(int T, int H, int K) {
+    const int forced = g_mla_sk.load();
+    if (forced < 0 || mla_heads_per_cta(H) != 64 || g_mla_splits.load() > 0 || g_mla_pair.load() > 0 || T <= 0 ||
+        K <= 0)
+        return 0;
+    const int nsm = sm_count(), tile = dsa::mla_key_tile(), tpr = ceil_div(K, tile);
+    const long long groups = mla_groups(H), units = (long long)T * groups * tpr;
+    if (forced == 0) {
+        const int splits = mla_splits(T, H, K);
+        if (splits > 1 || (long long)T * groups * splits >= nsm) return 0;
+    }
+    const long long per = (units + nsm - 1) / nsm;
+    if (units < 2LL * nsm || per > tpr || per * tile > 2048) return 0;
+    return nsm;
+}
+size_t mla_sk_workspace(int ctas) { return kErrBytes + (size_t)2 * ctas * 64 * (512 + 2) * sizeof(float); }
+
 dsa_status cuda_status(cudaError_t e) {
     if (e == cudaSuccess) return DSA_OK;
     fprintf(stderr, "[dsa] CUDA error: %s\n", cudaGetErrorString(e));
@@ -330,7 +359,19 @@ dsa_status index_common(const void *q_idx, const uint8_t *q_idx_scale, const flo
                                                 scores != nullptr, static_cast<cudaStream_t>(stream)));
 }
 
+size_t split_workspace_size(int32_t T, int32_t H, int32_t K) {
+    if (T <= 0 || H <= 0 || K <= 0) return kErrBytes;
+    const int splits = mla_splits(T, H, K);
+    if (splits <= 1) return kErrBytes;
+    const size_t rows = (size_t)T * mla_groups(H) * splits * 64;
+    return kErrBytes + rows * 512 * sizeof(float) + rows * 2 * sizeof(float);
+}
+
 }  // namespace
+
+namespace dsa {
+size_t mla_split_workspace_size(int32_t T, int32_t H, int32_t K) { return split_workspace_size(T, H, K); }
+}  // namespace dsa
 
 extern "C" {
 
@@ -354,6 +395,7 @@ int dsa_set_tuning(const char *name, int value) {
     else if (!strcmp(name, "indexer_group")) g_idx_group = value;
     else if (!strcmp(name, "mla_splits")) g_mla_splits = value;
     else if (!strcmp(name, "mla_pair")) g_mla_pair = value;
+    else if (!strcmp(name, "mla_stream_k")) g_mla_sk = value;
     else if (!strcmp(name, "topk_cluster")) g_topk_cluster = value;
     else return -1;
     return 0;
@@ -370,11 +412,9 @@ size_t dsa_index_topk_workspace_size(int32_t B, int32_t T, int32_t K, int32_t ma
 }
 
 size_t dsa_sparse_mla_workspace_size(int32_t T, int32_t H, int32_t K) {
-    if (T <= 0 || H <= 0 || K <= 0) return kErrBytes;
-    const int splits = mla_splits(T, H, K);
-    if (splits <= 1) return kErrBytes;
-    const size_t rows = (size_t)T * mla_groups(H) * splits * 64;
-    return kErrBytes + rows * 512 * sizeof(float) + rows * 2 * sizeof(float);
+    const size_t split = split_workspace_size(T, H, K);
+    const int sk = mla_sk_ctas(T, H, K);
+    return sk > 0 ? std::max(split, mla_sk_workspace(sk)) : split;
 }
 
 dsa_status dsa_workspace_init(void *workspace, size_t workspace_bytes, void *stream) {
@@ -461,7 +501,8 @@ dsa_status dsa_sparse_mla(const void *q, const void *kv_cache, const void *kv_ro
     const bool fp8 = dtype != DSA_KV_BF16;
     if (fp8 && (!kv_rope || !kv_scale || !aligned16(kv_rope) || (reinterpret_cast<uintptr_t>(kv_scale) & 3u)))
         return DSA_ERR_INVALID_ARG;
-    if (workspace_bytes < dsa_sparse_mla_workspace_size(T, H, K)) return DSA_ERR_INVALID_ARG;
+    // (a workspace of the split grid's size is enough: stream-K then stays off)
+    if (workspace_bytes < split_workspace_size(T, H, K)) return DSA_ERR_INVALID_ARG;
     if (T == 0) return DSA_OK;
     const int splits = mla_splits(T, H, K);
     const int tile = dsa::mla_key_tile();
@@ -490,12 +531,21 @@ dsa_status dsa_sparse_mla(const void *q, const void *kv_cache, const void *kv_ro
     a.page_size = page_size;
     a.splits = splits;
     a.keys_per_split = ceil_div(ceil_div(K, splits), tile) * tile;
+    const bool pair = mla_pair(T, H, splits);
+    const int sk = pair ? 0 : mla_sk_ctas(T, H, K);
+    if (sk > 0 && workspace_bytes >= mla_sk_workspace(sk)) {
+        a.sk_ctas = sk;
+        a.sk_tpr = ceil_div(K, tile);
+        a.sk_units = (int64_t)T * mla_groups(H) * a.sk_tpr;
+        a.part_o = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + kErrBytes);
+        a.part_ml = a.part_o + (size_t)2 * sk * 64 * 512;
+    }
     a.scale = scale;
     a.scale_log2 = scale * 1.4426950408889634f;
     CUtensorMap tq;
     if (!encode_2d_bf16(&tq, q, 576, (uint64_t)T * H, (uint32_t)NH)) return DSA_ERR_CUDA;
     return cuda_status(
-        dsa::launch_sparse_mla(tq, a, NH, fp8, mla_pair(T, H, splits), static_cast<cudaStream_t>(stream)));
+        dsa::launch_sparse_mla(tq, a, NH, fp8, pair, static_cast<cudaStream_t>(stream)));
 }
 
 dsa_status dsa_quant_mxfp8(const void *x, int64_t n, void *q, void *e8m0, void *stream) {

@@ -64,14 +64,20 @@ struct MlaArgs {
     const int32_t *indices;     // [T, K]
     uint16_t *out;              // [T, H, 512] bf16
     float *lse;                 // [T, H] or null
-    float *part_o;              // [T, H/64, splits, 64, 512] fp32 partial outputs (splits > 1)
-    float *part_ml;             // [T, H/64, splits, 64, 2] running max (log2 domain) and sum
+    float *part_o;              // [T, H/64, splits, 64, 512] fp32 partial outputs (splits > 1),
+                                // or [2 * sk_ctas, 64, 512] in stream-K mode
+    float *part_ml;             // the same slots x 2: running max (log2 domain) and sum
     uint32_t *err;
     int64_t num_pages;
     int32_t max_pages;
     int32_t B, T, H, K, page_size;
     int32_t splits;             // key splits per (query, head group)
     int32_t keys_per_split;     // multiple of the key tile
+    // stream-K mode (sk_ctas > 0): sk_ctas CTAs share the sk_units = T * (H/64)
+    // * sk_tpr key tiles evenly; CTA c takes units [c U / C, (c+1) U / C),
+    // which cover at most two (row, head group) pairs
+    int32_t sk_ctas, sk_tpr;
+    int64_t sk_units;
     float scale_log2;           // softmax scale * log2(e)
     float scale;                // softmax scale
 };
@@ -84,6 +90,9 @@ int mla_key_tile();
 // kv_rope, kv_scale), dequantised to bf16 on the way into shared memory.
 // pair: with 128 heads, run the two 64-head CTAs of a query as a cluster that
 // shares every gathered row.
+// Workspace bytes of the split grid (host; the stream-K layout may need more).
+size_t mla_split_workspace_size(int32_t T, int32_t H, int32_t K);
+// Stream-K mode (a.sk_ctas > 0) needs NH = 64 and no pair.
 cudaError_t launch_sparse_mla(const CUtensorMap &tm_q, const MlaArgs &a, int NH, bool fp8, bool pair,
                               cudaStream_t st);
 

@@ -68,7 +68,7 @@ extern "C" dsa_status dsa_sparse_mla_static(const void *q, const void *kv_cache,
                                             float scale, int32_t page_size, dsa_kv_dtype dtype, void *out,
                                             float *lse, void *stream) {
     // the same split choice as dsa_sparse_mla, so both give the same result
-    const size_t need = dsa_sparse_mla_workspace_size(T, H, K);
+    const size_t need = dsa::mla_split_workspace_size(T, H, K);
     if (need > kStaticScratchBytes) {
         fprintf(stderr,
                 "[dsa] dsa_sparse_mla_static: %zu bytes of split partials needed, the static scratch holds %zu; "

@@ -83,6 +83,7 @@ struct __align__(16) MlaBars {
     uint64_t kv_full[kStages], kv_empty[kStages], s_full[2];
     uint64_t peer_free[kStages];   // pairs: the peer's copy of this stage may be overwritten
     uint64_t p_full, o_done, o_full, q_full, drain, table;
+    uint64_t o_free;  // stream-K: the epilogue of segment 0 has read O
     uint32_t tmem_slot;
     int abort;
 };
@@ -168,7 +169,7 @@ __device__ __forceinline__ bool issue_s_tile(int i, MlaBars *bars, uint32_t kv_b
 // memory, so that each selected row is read from L2/HBM once.
 // kF8: the cache holds E4M3 latent dims + an fp32 scale per row + bf16 rope
 // dims; the gather warps dequantise the latent dims to bf16 through registers.
-template <int NH, bool kPair, bool kF8>
+template <int NH, bool kPair, bool kF8, bool kSK>
 __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, MlaArgs a) {
     using L = MlaLayout<NH>;
     extern __shared__ uint8_t smem_raw[];
@@ -178,18 +179,53 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
     MlaBars *bars = reinterpret_cast<MlaBars *>(smem + L::kMiscOff);
     MlaStats *st = reinterpret_cast<MlaStats *>(bars + 1);
 
-    const int hg = blockIdx.x, split = blockIdx.y, t = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int k_begin = split * a.keys_per_split;
-    const int k_end = min(a.K, k_begin + a.keys_per_split);
-    const int n_tiles = k_end > k_begin ? (k_end - k_begin + kKeys - 1) / kKeys : 0;
+    // What this CTA computes: one or two segments, each a run of consecutive
+    // key tiles of one (query row t, head group hg); tile i of the CTA
+    // belongs to segment 1 from seg[1].first on.  Split mode: the grid is
+    // (head group, key split, row), one segment.  Stream-K mode: one row of
+    // CTAs shares all (row, head group, key tile) units evenly, and a CTA's
+    // run may cross into the next (row, head group) once.
+    struct Seg {
+        int t, hg, j0, first;  // row, head group, its first key tile, first CTA-local tile
+    };
+    Seg seg[2];
+    int n_seg = 1, n_tiles;
+    if constexpr (kSK) {
+        const int64_t U = a.sk_units, C = a.sk_ctas, c = blockIdx.x;
+        const int64_t u0 = c * U / C, u1 = (c + 1) * U / C;
+        const int tpr = a.sk_tpr, G = a.H / NH;
+        n_tiles = (int)(u1 - u0);
+        const int64_t p0 = u0 / tpr, e0 = (p0 + 1) * tpr;
+        seg[0] = {(int)(p0 / G), (int)(p0 % G), (int)(u0 - p0 * tpr), 0};
+        seg[1] = seg[0];
+        if (u1 > e0) {
+            n_seg = 2;
+            seg[1] = {(int)((p0 + 1) / G), (int)((p0 + 1) % G), 0, (int)(e0 - u0)};
+        }
+    } else {
+        const int k_begin = blockIdx.y * a.keys_per_split;
+        const int k_end = min(a.K, k_begin + a.keys_per_split);
+        n_tiles = k_end > k_begin ? (k_end - k_begin + kKeys - 1) / kKeys : 0;
+        seg[0] = {(int)blockIdx.z, (int)blockIdx.x, k_begin / kKeys, 0};
+        seg[1] = seg[0];
+    }
+    const int s1 = n_seg == 2 ? seg[1].first : n_tiles;  // first tile of segment 1 (n_tiles if none)
+    const int t = seg[0].t, hg = seg[0].hg;
     // Inputs may come from the kernel launched just before this one (the
     // indexer's indices, or a caller's kernel); with programmatic dependent
     // launch this kernel starts early and waits here until they are visible.
     grid_dep_wait();
-    const int b = find_seq(a.cu_q, a.B, t);
-    const int pos = __ldg(a.seq_lens + b) - (__ldg(a.cu_q + b + 1) - __ldg(a.cu_q + b)) + (t - __ldg(a.cu_q + b));
-    const int32_t *idx_row = a.indices + (size_t)t * a.K;
+    int sbq[2], spos[2];
+    for (int s = 0; s < n_seg; ++s) {
+        const int tt = seg[s].t, bb = find_seq(a.cu_q, a.B, tt);
+        sbq[s] = bb;
+        spos[s] = __ldg(a.seq_lens + bb) - (__ldg(a.cu_q + bb + 1) - __ldg(a.cu_q + bb)) + (tt - __ldg(a.cu_q + bb));
+    }
+    if (n_seg == 1) {
+        sbq[1] = sbq[0];
+        spos[1] = spos[0];
+    }
 
     if (threadIdx.x == 0) {
         // a tile is complete after one cp.async completion arrival per gather
@@ -205,6 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
         mbar_init(&bars->p_full, kSmThreads / 32);
         mbar_init(&bars->o_done, 1);
         mbar_init(&bars->o_full, 1);
+        mbar_init(&bars->o_free, kSmThreads / 32);
         mbar_init(&bars->q_full, 1);
         mbar_init(&bars->drain, 1);
         mbar_init(&bars->table, 1);
@@ -231,7 +268,6 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
 
     if (warp < kProd) {
         // ---------------------------------------------------------------- gather
-        const int32_t *pt_row = a.page_table + (size_t)b * a.max_pages;
         // keys of a tile this CTA gathers: all of them, or its half when paired
         constexpr int kMine = kPair ? kKeys / 2 : kKeys;
         constexpr int kKPW = kMine / kProd;  // keys per gather warp
@@ -252,17 +288,22 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
         // all index loads first, then all page-table loads, then the table
 #pragma unroll
         for (int u = 0; u < kPer; ++u) {
-            const int k = threadIdx.x + u * kProd * 32, slot = k_begin + k;
-            idxv[u] = k < n_keys && slot < k_end ? __ldg(idx_row + slot) : -1;
+            const int k = threadIdx.x + u * kProd * 32, i = k / kKeys, s = i >= s1 ? 1 : 0;
+            const int slot = (seg[s].j0 + i - seg[s].first) * kKeys + k % kKeys;
+            idxv[u] = k < n_keys && slot < a.K ? __ldg(a.indices + (size_t)seg[s].t * a.K + slot) : -1;
         }
 #pragma unroll
-        for (int u = 0; u < kPer; ++u)
-            pagev[u] = idxv[u] >= 0 && idxv[u] <= pos ? __ldg(pt_row + idxv[u] / a.page_size) : -1;
+        for (int u = 0; u < kPer; ++u) {
+            const int k = threadIdx.x + u * kProd * 32, s = k / kKeys >= s1 ? 1 : 0;
+            pagev[u] = idxv[u] >= 0 && idxv[u] <= spos[s]
+                           ? __ldg(a.page_table + (size_t)sbq[s] * a.max_pages + idxv[u] / a.page_size)
+                           : -1;
+        }
 #pragma unroll
         for (int u = 0; u < kPer; ++u) {
             const int k = threadIdx.x + u * kProd * 32;
             if (k >= n_keys) break;  // n_keys is a multiple of 64: warp-uniform
-            const int idx = idxv[u];
+            const int idx = idxv[u], pos = spos[k / kKeys >= s1 ? 1 : 0];
             int row = 0;  // invalid slots read row 0 and are masked by the softmax
             bool v = false;
             if (idx > pos) {
@@ -391,6 +432,16 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
             const uint32_t q_base = smem_u32(sQ), kv_base = smem_u32(sKV);
             bool ok = mbar_wait(&bars->q_full, 0, a.err, 0x502, abort);
             uint32_t *const err = a.err;
+            // Before the logits of segment 1's first tile: the last logits of
+            // segment 0 have read Q, so its rows are replaced by segment 1's.
+            auto switch_q = [&](int i) -> bool {
+                if (!kSK || i != s1 || n_seg != 2) return true;
+                if (!mbar_wait(&bars->s_full[(i - 1) & 1], ((i - 1) >> 1) & 1, a.err, 0x50a, abort)) return false;
+                mbar_arrive_expect_tx(&bars->q_full, (uint32_t)(kRegions * NH * 128));
+                for (int r = 0; r < kRegions; ++r)
+                    tma_load_2d(sQ + r * kQRegion, &tm_q, &bars->q_full, 64 * r, seg[1].t * a.H + seg[1].hg * NH);
+                return mbar_wait(&bars->q_full, 1, a.err, 0x50b, abort);
+            };
             if (ok && n_tiles > 0) ok = issue_s_tile(0, bars, kv_base, q_base, tmem_s, idesc_s, err, abort);
             for (int i = 0; ok && i < n_tiles; ++i) {
                 // With a ring of 3+ tiles the next tile's logits are issued
@@ -398,9 +449,12 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
                 // 2 buffers the next tile is still loading, so this tile's
                 // P*V goes first (it frees the buffer the tile after needs).
                 if (kStages > 2 && i + 1 < n_tiles &&
-                    !(ok = issue_s_tile(i + 1, bars, kv_base, q_base, tmem_s, idesc_s, err, abort)))
+                    !(ok = switch_q(i + 1) && issue_s_tile(i + 1, bars, kv_base, q_base, tmem_s, idesc_s, err, abort)))
                     break;
                 if (!(ok = mbar_wait(&bars->p_full, i & 1, a.err, 0x504, abort))) break;
+                // segment 1 starts a fresh accumulator once segment 0's epilogue has read O
+                const int first = i >= s1 ? s1 : 0;
+                if (kSK && i == s1 && !(ok = mbar_wait(&bars->o_free, 0, a.err, 0x50c, abort))) break;
                 tc_fence_after();
                 const int stg = i % kStages;
                 const uint32_t kb = kv_base + stg * kTileBytes;
@@ -412,12 +466,13 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
 #pragma unroll
                     for (int j = 0; j < kKeys / 16; ++j)
                         mma_bf16_ss(tmem_o + c * 64, ad0 + (uint64_t)((2 * c * kRegionBytes + j * 2048) >> 4),
-                                    bd0 + (uint64_t)((j * 32) >> 4), idesc_o, (i > 0 || j > 0) ? 1u : 0u);
+                                    bd0 + (uint64_t)((j * 32) >> 4), idesc_o, (i > first || j > 0) ? 1u : 0u);
                 }
                 mma_commit(&bars->kv_empty[stg]);
                 mma_commit(&bars->o_done);
+                if (i + 1 == s1 && s1 < n_tiles) mma_commit(&bars->o_full);  // segment 0 is complete
                 if (kStages <= 2 && i + 1 < n_tiles &&
-                    !(ok = issue_s_tile(i + 1, bars, kv_base, q_base, tmem_s, idesc_s, err, abort)))
+                    !(ok = switch_q(i + 1) && issue_s_tile(i + 1, bars, kv_base, q_base, tmem_s, idesc_s, err, abort)))
                     break;
             }
             if (ok && n_tiles > 0) mma_commit(&bars->o_full);
@@ -440,8 +495,85 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
         const bool lead = (lane & 3) == 0;  // writes the per-head values
         float m_ref[2] = {-CUDART_INF_F, -CUDART_INF_F}, l_run[2] = {0.0f, 0.0f};
         bool ok = n_tiles == 0 || mbar_wait(&bars->table, 0, a.err, 0x509, abort);
+        // Epilogue of segment s: O / l (or the partial O, max and sum) for its
+        // row and head group.  Segment 0 of a two-segment CTA runs inside the
+        // tile loop and then hands O over to segment 1 (o_free).
+        auto epilogue = [&](int s, bool last) {
+            if (lead) {
+                if (hA < NH) {
+                    st->m_fin[hA] = m_ref[0];
+                    st->l_fin[hA] = l_run[0];
+                }
+                if (hB < NH) {
+                    st->m_fin[hB] = m_ref[1];
+                    st->l_fin[hB] = l_run[1];
+                }
+            }
+            if (last && tid_s == 0) grid_dep_launch();  // the split combine may start launching
+            if (ok && n_tiles > 0) ok = mbar_wait(&bars->o_full, (uint32_t)s & 1u, a.err, 0x508, abort);
+            ok = bar_and(kBarSm, kSmThreads, ok);
+            if (!ok) return;
+            tc_fence_after();
+            const int groups = a.H / NH, tt = seg[s].t, hgs = seg[s].hg;
+            const int h_base = hgs * NH;
+            const bool direct = !kSK && a.splits == 1;
+            // partial slot: stream-K (CTA, segment), else (row, head group, split)
+            const size_t slot_base = kSK ? ((size_t)blockIdx.x * 2 + s) * kHG
+                                         : (((size_t)tt * groups + hgs) * a.splits + blockIdx.y) * kHG;
+            constexpr int W = NH < 32 ? NH : 32;
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                const int d = c * 128 + quad * 32 + lane;
+#pragma unroll
+                for (int h0 = 0; h0 < NH; h0 += W) {
+                    uint32_t o[W];
+                    if (n_tiles > 0) {
+                        tmem_ld<W>(tmem_o + lane_off + c * 64 + h0, o);
+                        tmem_wait_ld();
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < W; ++j) o[j] = 0u;
+                    }
+                    if (direct) {
+#pragma unroll
+                        for (int j = 0; j < W; ++j) {
+                            const float l = st->l_fin[h0 + j];
+                            const float v = l > 0.0f ? __uint_as_float(o[j]) / l : 0.0f;
+                            a.out[((size_t)tt * a.H + h_base + h0 + j) * kDv + d] =
+                                __bfloat16_as_ushort(__float2bfloat16_rn(v));
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < W; ++j) a.part_o[(slot_base + h0 + j) * kDv + d] = __uint_as_float(o[j]);
+                    }
+                }
+            }
+            if (tid_s < NH) {
+                const float l = st->l_fin[tid_s], m = st->m_fin[tid_s];
+                if (direct) {
+                    if (a.lse)
+                        a.lse[(size_t)tt * a.H + h_base + tid_s] =
+                            l > 0.0f ? m * 0.69314718055994531f + logf(l) : -CUDART_INF_F;
+                } else {
+                    a.part_ml[(slot_base + tid_s) * 2 + 0] = l > 0.0f ? m : -CUDART_INF_F;
+                    a.part_ml[(slot_base + tid_s) * 2 + 1] = l;
+                }
+            }
+            if (!last) {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->o_free);  // O may be overwritten
+            }
+        };
         for (int i = 0; i < n_tiles; ++i) {
             const int sb = i & 1, stg = i % kStages;
+            if (kSK && i == s1) {
+                // segment 0 is done: write it out, start segment 1 afresh
+                epilogue(0, false);
+                if (!ok) break;
+                m_ref[0] = m_ref[1] = -CUDART_INF_F;
+                l_run[0] = l_run[1] = 0.0f;
+            }
             ok = mbar_wait(&bars->s_full[sb], (i >> 1) & 1, a.err, 0x505, abort);
             ok = bar_and(kBarSm, kSmThreads, ok);
             if (!ok) break;
@@ -536,64 +668,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars->p_full);
         }
-        if (lead) {
-            if (hA < NH) {
-                st->m_fin[hA] = m_ref[0];
-                st->l_fin[hA] = l_run[0];
-            }
-            if (hB < NH) {
-                st->m_fin[hB] = m_ref[1];
-                st->l_fin[hB] = l_run[1];
-            }
-        }
         // ---------------------------------------------------------------- epilogue
-        if (tid_s == 0) grid_dep_launch();  // the split combine may start launching
-        if (ok && n_tiles > 0) ok = mbar_wait(&bars->o_full, 0, a.err, 0x508, abort);
-        ok = bar_and(kBarSm, kSmThreads, ok);
-        if (ok) {
-            tc_fence_after();
-            const int groups = gridDim.x;
-            const int h_base = hg * NH;
-            constexpr int W = NH < 32 ? NH : 32;
-#pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
-                const int d = c * 128 + quad * 32 + lane;
-#pragma unroll
-                for (int h0 = 0; h0 < NH; h0 += W) {
-                    uint32_t o[W];
-                    if (n_tiles > 0) {
-                        tmem_ld<W>(tmem_o + lane_off + c * 64 + h0, o);
-                        tmem_wait_ld();
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < W; ++j) o[j] = 0u;
-                    }
-                    if (a.splits == 1) {
-#pragma unroll
-                        for (int j = 0; j < W; ++j) {
-                            const float l = st->l_fin[h0 + j];
-                            const float v = l > 0.0f ? __uint_as_float(o[j]) / l : 0.0f;
-                            a.out[((size_t)t * a.H + h_base + h0 + j) * kDv + d] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
-                        }
-                    } else {
-                        const size_t slot0 = (((size_t)t * groups + hg) * a.splits + split) * kHG + h0;
-#pragma unroll
-                        for (int j = 0; j < W; ++j) a.part_o[(slot0 + j) * kDv + d] = __uint_as_float(o[j]);
-                    }
-                }
-            }
-            if (tid_s < NH) {
-                const float l = st->l_fin[tid_s], m = st->m_fin[tid_s];
-                if (a.splits == 1) {
-                    if (a.lse)
-                        a.lse[(size_t)t * a.H + hg * NH + tid_s] = l > 0.0f ? m * 0.69314718055994531f + logf(l) : -CUDART_INF_F;
-                } else {
-                    const size_t slot0 = (((size_t)t * groups + hg) * a.splits + split) * kHG + tid_s;
-                    a.part_ml[slot0 * 2 + 0] = l > 0.0f ? m : -CUDART_INF_F;
-                    a.part_ml[slot0 * 2 + 1] = l;
-                }
-            }
-        }
+        epilogue(n_seg - 1, true);
     }
 
     tc_fence_before();
@@ -612,14 +688,30 @@ __global__ void __launch_bounds__(128) mla_combine_kernel(MlaArgs a, int NH) {
     const int hl = 4 * blockIdx.x + (threadIdx.x >> 5), lane = threadIdx.x & 31;
     grid_dep_wait();  // the partials of the attention kernel launched just before
     if (hl >= NH) return;
+    // the partials of (row t, head group hg): its splits, or in stream-K mode
+    // the CTAs whose unit runs overlap the pair's tiles (slot = 2 CTA + segment)
     const size_t base = ((size_t)t * gridDim.y + hg) * a.splits;
+    int64_t c_lo = 0, n_part = a.splits, pair = 0;
+    const int64_t U = a.sk_units, C = a.sk_ctas, tpr = a.sk_tpr;
+    if (C > 0) {
+        pair = (int64_t)t * gridDim.y + hg;
+        const int64_t u_lo = pair * tpr, u_hi = u_lo + tpr - 1;  // CTA of unit u: ((u + 1) C - 1) / U
+        c_lo = ((u_lo + 1) * C - 1) / U;
+        n_part = ((u_hi + 1) * C - 1) / U - c_lo + 1;
+    }
     float M = -CUDART_INF_F, L = 0.0f;
     float4 acc[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 2
-    for (int s = 0; s < a.splits; ++s) {
-        const size_t slot = (base + s) * kHG + hl;
+    for (int s = 0; s < n_part; ++s) {
+        size_t slot;
+        if (C > 0) {
+            const int64_t c = c_lo + s;
+            slot = (size_t)(2 * c + ((c * U / C) / tpr == pair ? 0 : 1)) * kHG + hl;
+        } else {
+            slot = (base + s) * kHG + hl;
+        }
         const float m = __ldcg(a.part_ml + slot * 2), l = __ldcg(a.part_ml + slot * 2 + 1);
         const float4 *src = reinterpret_cast<const float4 *>(a.part_o + slot * kDv) + lane;
         float4 v[4];
@@ -656,14 +748,14 @@ size_t mla_smem_bytes(int NH) {
 }
 int mla_key_tile() { return kKeys; }
 
-template <int NH, bool kPair, bool kF8>
+template <int NH, bool kPair, bool kF8, bool kSK = false>
 static cudaError_t launch_tc(const CUtensorMap &tq, const MlaArgs &a, cudaStream_t st) {
     const size_t smem = mla_smem_bytes(NH);
-    auto kern = sparse_mla_tc_kernel<NH, kPair, kF8>;
+    auto kern = sparse_mla_tc_kernel<NH, kPair, kF8, kSK>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(a.H / NH), (unsigned)a.splits, (unsigned)a.T);
+    cfg.gridDim = kSK ? dim3((unsigned)a.sk_ctas, 1, 1) : dim3((unsigned)(a.H / NH), (unsigned)a.splits, (unsigned)a.T);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
@@ -681,6 +773,7 @@ static cudaError_t launch_tc(const CUtensorMap &tq, const MlaArgs &a, cudaStream
 
 template <bool kF8>
 static cudaError_t launch_heads(const CUtensorMap &tq, const MlaArgs &a, int NH, bool pair, cudaStream_t st) {
+    if (NH == 64 && a.sk_ctas > 0 && !pair) return launch_tc<64, false, kF8, true>(tq, a, st);
     if (NH == 64 && a.H == 128 && pair) return launch_tc<64, true, kF8>(tq, a, st);
     if (NH == 64) return launch_tc<64, false, kF8>(tq, a, st);
     if (NH == 32) return launch_tc<32, false, kF8>(tq, a, st);
@@ -690,7 +783,7 @@ static cudaError_t launch_heads(const CUtensorMap &tq, const MlaArgs &a, int NH,
 
 cudaError_t launch_sparse_mla(const CUtensorMap &tq, const MlaArgs &a, int NH, bool fp8, bool pair, cudaStream_t st) {
     const cudaError_t e = fp8 ? launch_heads<true>(tq, a, NH, pair, st) : launch_heads<false>(tq, a, NH, pair, st);
-    if (e != cudaSuccess || a.splits == 1) return e;
+    if (e != cudaSuccess || (a.splits == 1 && a.sk_ctas == 0)) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((NH + 3) / 4, a.H / NH, a.T);
     cfg.blockDim = dim3(128, 1, 1);

@@ -167,3 +167,56 @@ def test_paired_128_heads_matches(orc, fp8):
         _compare(orc, wl, _random_indices(rng, wl, 1024, pad_frac=0.05))
     finally:
         d.set_tuning("mla_pair", 0)
+
+
+@pytest.mark.parametrize("case", ["k1000_h128", "k1000_h64", "k2048_h128"])
+@pytest.mark.parametrize("fp8", [False, True])
+def test_stream_k_matches(orc, case, fp8):
+    # one CTA per SM sharing all (row, head group, key tile) units: runs cross
+    # into the next (row, head group) every few tiles, the last tile of a row
+    # is ragged (K = 1000) and some indices are -1
+    import indexer_top_sparse_gb300 as d
+    K, H, T = {"k1000_h128": (1000, 128, 12), "k1000_h64": (1000, 64, 21), "k2048_h128": (2048, 128, 6)}[case]
+    rng = np.random.default_rng(140 + K + H + fp8)
+    lens = rng.integers(K + 10, 3 * K, size=T)
+    wl = make_workload("sk", lens, [1] * T, H=H, K=K, page_size=64, seed=int(lens[0]), with_idx=False)
+    idx = _random_indices(rng, wl, K, pad_frac=0.05)
+    d.set_tuning("mla_stream_k", 1)
+    try:
+        if fp8:
+            nope, rope, sc = orc.quant_fp8_tiles(wl.kv)
+            ws = d.Workspace(d.sparse_mla_workspace_size(wl.T, wl.H, K))
+            out = d.dsa_sparse_mla(dev_bf16(wl.q), dev(nope), dev(wl.page_table), dev(wl.seq_lens), dev(wl.cu_q),
+                                   dev(idx), wl.scale, workspace=ws, kv_rope=dev_bf16(rope), kv_scale=dev(sc),
+                                   dtype="fp8_tile128")
+            ws.check()
+            ref, _ = orc.sparse_mla(wl.q, nope, wl.page_table, wl.cu_q, idx, wl.scale, wl.page_size,
+                                    dtype=orc.KV_FP8_TILE128, kv_rope=rope, kv_scale=sc)
+            np.testing.assert_allclose(out.float().cpu().numpy(), ref, atol=ATOL, rtol=RTOL)
+        else:
+            _compare(orc, wl, idx)
+    finally:
+        d.set_tuning("mla_stream_k", 0)
+
+
+def test_stream_k_off_and_on_agree():
+    # the decode shape where stream-K is the automatic choice, against the
+    # split grid (stream-K off): the same attention up to summation order
+    import indexer_top_sparse_gb300 as d
+    rng = np.random.default_rng(150)
+    wl = make_workload("sk2", [4000] * 16, [1] * 16, H=128, K=2048, page_size=64, seed=150, with_idx=False)
+    idx = dev(_random_indices(rng, wl, 2048))
+    outs = []
+    for mode in (0, -1):
+        d.set_tuning("mla_stream_k", mode)
+        try:
+            ws = d.Workspace(d.sparse_mla_workspace_size(wl.T, wl.H, 2048))
+            lse = torch.empty((wl.T, wl.H), dtype=torch.float32, device="cuda")
+            o = d.dsa_sparse_mla(dev_bf16(wl.q), dev_bf16(wl.kv), dev(wl.page_table), dev(wl.seq_lens),
+                                 dev(wl.cu_q), idx, wl.scale, workspace=ws, lse=lse)
+            ws.check()
+            outs.append((o.float().cpu().numpy(), lse.cpu().numpy()))
+        finally:
+            d.set_tuning("mla_stream_k", 0)
+    np.testing.assert_allclose(outs[0][0], outs[1][0], atol=1e-2, rtol=1e-2)
+    np.testing.assert_allclose(outs[0][1], outs[1][1], atol=1e-4, rtol=1e-4)
