@@ -75,6 +75,7 @@ struct __align__(16) SelectSmem {
     int32_t all_pos[kAllCap];
     int32_t all_cta[kAllCap];
     int32_t cta_off[kMaxCluster + 1];
+    int32_t cta_pos0[kMaxCluster];  // first position of each CTA's run
     int32_t cta_gt[kMaxCluster];
     int32_t cta_sel[kMaxCluster];
     int32_t seg_sel[kMaxSelThreads];
@@ -158,16 +159,14 @@ __device__ bool select_from_bucket(uint32_t kb, int n_local, int pos0, int K, in
         const int4 p = *reinterpret_cast<const int4 *>(cluster.map_shared_rank(ss.pub, tid));
         ss.cta_gt[tid] = p.x;
         ss.cta_off[tid + 1] = p.z ? -1 : p.y;  // -1 marks an overflow
-        ss.all_pos[tid] = p.w;                 // pos0 of each CTA, until the list is copied
+        ss.cta_pos0[tid] = p.w;
     }
     __syncthreads();
     bool fits = true;
     int total = 0;
-    int pos0s[kMaxCluster];
     for (int c = 0; c < C; ++c) {
         const int n = ss.cta_off[c + 1];
         fits = fits && n >= 0;
-        pos0s[c] = ss.all_pos[c];
         total += max(n, 0);
     }
     fits = fits && total <= kAllCap;
@@ -193,7 +192,7 @@ __device__ bool select_from_bucket(uint32_t kb, int n_local, int pos0, int K, in
         const uint32_t k = cluster.map_shared_rank(ss.cand_key, c)[li];
         const int l = cluster.map_shared_rank(ss.cand_loc, c)[li];
         ss.all_key[i] = k;
-        ss.all_pos[i] = pos0s[c] + l;
+        ss.all_pos[i] = ss.cta_pos0[c] + l;
         ss.all_cta[i] = c;
     }
     __syncthreads();

@@ -212,20 +212,22 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
     }
     const int s1 = n_seg == 2 ? seg[1].first : n_tiles;  // first tile of segment 1 (n_tiles if none)
     const int t = seg[0].t, hg = seg[0].hg;
+    // segment of CTA-local tile i (always 0 in split mode); the per-segment
+    // values are picked with selects, so that they stay in registers
+    auto seg_of = [&](int i) { return kSK && i >= s1 ? 1 : 0; };
     // Inputs may come from the kernel launched just before this one (the
     // indexer's indices, or a caller's kernel); with programmatic dependent
     // launch this kernel starts early and waits here until they are visible.
     grid_dep_wait();
-    int sbq[2], spos[2];
-    for (int s = 0; s < n_seg; ++s) {
-        const int tt = seg[s].t, bb = find_seq(a.cu_q, a.B, tt);
-        sbq[s] = bb;
-        spos[s] = __ldg(a.seq_lens + bb) - (__ldg(a.cu_q + bb + 1) - __ldg(a.cu_q + bb)) + (tt - __ldg(a.cu_q + bb));
-    }
-    if (n_seg == 1) {
-        sbq[1] = sbq[0];
-        spos[1] = spos[0];
-    }
+    auto seq_pos = [&](int tt, int &bb, int &pp) {
+        bb = find_seq(a.cu_q, a.B, tt);
+        pp = __ldg(a.seq_lens + bb) - (__ldg(a.cu_q + bb + 1) - __ldg(a.cu_q + bb)) + (tt - __ldg(a.cu_q + bb));
+    };
+    int sb0, spos0, sb1, spos1;
+    seq_pos(seg[0].t, sb0, spos0);
+    sb1 = sb0;
+    spos1 = spos0;
+    if (kSK && n_seg == 2) seq_pos(seg[1].t, sb1, spos1);
 
     if (threadIdx.x == 0) {
         // a tile is complete after one cp.async completion arrival per gather
@@ -288,22 +290,24 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
         // all index loads first, then all page-table loads, then the table
 #pragma unroll
         for (int u = 0; u < kPer; ++u) {
-            const int k = threadIdx.x + u * kProd * 32, i = k / kKeys, s = i >= s1 ? 1 : 0;
-            const int slot = (seg[s].j0 + i - seg[s].first) * kKeys + k % kKeys;
-            idxv[u] = k < n_keys && slot < a.K ? __ldg(a.indices + (size_t)seg[s].t * a.K + slot) : -1;
+            const int k = threadIdx.x + u * kProd * 32, i = k / kKeys, s = seg_of(i);
+            const int j0 = s ? seg[1].j0 : seg[0].j0, first = s ? seg[1].first : 0, tt = s ? seg[1].t : seg[0].t;
+            const int slot = (j0 + i - first) * kKeys + k % kKeys;
+            idxv[u] = k < n_keys && slot < a.K ? __ldg(a.indices + (size_t)tt * a.K + slot) : -1;
         }
 #pragma unroll
         for (int u = 0; u < kPer; ++u) {
-            const int k = threadIdx.x + u * kProd * 32, s = k / kKeys >= s1 ? 1 : 0;
-            pagev[u] = idxv[u] >= 0 && idxv[u] <= spos[s]
-                           ? __ldg(a.page_table + (size_t)sbq[s] * a.max_pages + idxv[u] / a.page_size)
+            const int k = threadIdx.x + u * kProd * 32, s = seg_of(k / kKeys);
+            const int pos = s ? spos1 : spos0, bb = s ? sb1 : sb0;
+            pagev[u] = idxv[u] >= 0 && idxv[u] <= pos
+                           ? __ldg(a.page_table + (size_t)bb * a.max_pages + idxv[u] / a.page_size)
                            : -1;
         }
 #pragma unroll
         for (int u = 0; u < kPer; ++u) {
             const int k = threadIdx.x + u * kProd * 32;
             if (k >= n_keys) break;  // n_keys is a multiple of 64: warp-uniform
-            const int idx = idxv[u], pos = spos[k / kKeys >= s1 ? 1 : 0];
+            const int idx = idxv[u], pos = seg_of(k / kKeys) ? spos1 : spos0;
             int row = 0;  // invalid slots read row 0 and are masked by the softmax
             bool v = false;
             if (idx > pos) {
@@ -453,7 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
                     break;
                 if (!(ok = mbar_wait(&bars->p_full, i & 1, a.err, 0x504, abort))) break;
                 // segment 1 starts a fresh accumulator once segment 0's epilogue has read O
-                const int first = i >= s1 ? s1 : 0;
+                const int first = seg_of(i) ? s1 : 0;
                 if (kSK && i == s1 && !(ok = mbar_wait(&bars->o_free, 0, a.err, 0x50c, abort))) break;
                 tc_fence_after();
                 const int stg = i % kStages;
@@ -514,7 +518,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
             ok = bar_and(kBarSm, kSmThreads, ok);
             if (!ok) return;
             tc_fence_after();
-            const int groups = a.H / NH, tt = seg[s].t, hgs = seg[s].hg;
+            const int groups = a.H / NH, tt = s ? seg[1].t : seg[0].t, hgs = s ? seg[1].hg : seg[0].hg;
             const int h_base = hgs * NH;
             const bool direct = !kSK && a.splits == 1;
             // partial slot: stream-K (CTA, segment), else (row, head group, split)
