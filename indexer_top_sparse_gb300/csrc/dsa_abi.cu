@@ -267,14 +267,15 @@ int mla_sk_ctas(int T, int H, int K) {
         K <= 0)
         return 0;
     const int nsm = sm_count(), tile = dsa::mla_key_tile(), tpr = ceil_div(K, tile);
-    const long long groups = mla_groups(H), units = (long long)T * groups * tpr;
+    const int groups = mla_groups(H), cg = nsm / groups;  // CTAs per head group
+    const long long units = (long long)T * tpr;           // per head group
     if (forced == 0) {
         const int splits = mla_splits(T, H, K);
         if (splits > 1 || (long long)T * groups * splits >= nsm) return 0;
     }
-    const long long per = (units + nsm - 1) / nsm;
-    if (units < 2LL * nsm || per > tpr || per * tile > 2048) return 0;
-    return nsm;
+    const long long per = (units + cg - 1) / cg;
+    if (cg < 1 || units < 2LL * cg || per > tpr || per * tile > 2048) return 0;
+    return cg * groups;
 }
 size_t mla_sk_workspace(int ctas) { return kErrBytes + (size_t)2 * ctas * 64 * (512 + 2) * sizeof(float); }
 
@@ -536,7 +537,7 @@ dsa_status dsa_sparse_mla(const void *q, const void *kv_cache, const void *kv_ro
     if (sk > 0 && workspace_bytes >= mla_sk_workspace(sk)) {
         a.sk_ctas = sk;
         a.sk_tpr = ceil_div(K, tile);
-        a.sk_units = (int64_t)T * mla_groups(H) * a.sk_tpr;
+        a.sk_units = (int64_t)T * a.sk_tpr;
         a.part_o = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + kErrBytes);
         a.part_ml = a.part_o + (size_t)2 * sk * 64 * 512;
     }

@@ -73,9 +73,9 @@ struct MlaArgs {
     int32_t B, T, H, K, page_size;
     int32_t splits;             // key splits per (query, head group)
     int32_t keys_per_split;     // multiple of the key tile
-    // stream-K mode (sk_ctas > 0): sk_ctas CTAs share the sk_units = T * (H/64)
-    // * sk_tpr key tiles evenly; CTA c takes units [c U / C, (c+1) U / C),
-    // which cover at most two (row, head group) pairs
+    // stream-K mode (sk_ctas > 0): each head group's sk_ctas / (H/64) CTAs
+    // share its sk_units = T * sk_tpr (row, key tile) units evenly; CTA c of a
+    // head group takes units [c U / Cg, (c+1) U / Cg), at most two rows
     int32_t sk_ctas, sk_tpr;
     int64_t sk_units;
     float scale_log2;           // softmax scale * log2(e)

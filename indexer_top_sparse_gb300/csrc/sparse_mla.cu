@@ -192,16 +192,22 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
     Seg seg[2];
     int n_seg = 1, n_tiles;
     if constexpr (kSK) {
-        const int64_t U = a.sk_units, C = a.sk_ctas, c = blockIdx.x;
-        const int64_t u0 = c * U / C, u1 = (c + 1) * U / C;
-        const int tpr = a.sk_tpr, G = a.H / NH;
+        // each head group has sk_ctas / G CTAs that share its U = T * tpr
+        // (row, key tile) units the same way, so the CTAs of the head groups
+        // of a row gather the same rows at the same time
+        const int G = a.H / NH;
+        const int64_t Cg = a.sk_ctas / G, U = a.sk_units, c = blockIdx.x % Cg;
+        const int tpr = a.sk_tpr;
+        const int64_t u0 = c * U / Cg, u1 = (c + 1) * U / Cg;
         n_tiles = (int)(u1 - u0);
-        const int64_t p0 = u0 / tpr, e0 = (p0 + 1) * tpr;
-        seg[0] = {(int)(p0 / G), (int)(p0 % G), (int)(u0 - p0 * tpr), 0};
+        const int64_t r0 = u0 / tpr, e0 = (r0 + 1) * tpr;
+        seg[0] = {(int)r0, (int)(blockIdx.x / Cg), (int)(u0 - r0 * tpr), 0};
         seg[1] = seg[0];
         if (u1 > e0) {
             n_seg = 2;
-            seg[1] = {(int)((p0 + 1) / G), (int)((p0 + 1) % G), 0, (int)(e0 - u0)};
+            seg[1].t = (int)(r0 + 1);
+            seg[1].j0 = 0;
+            seg[1].first = (int)(e0 - u0);
         }
     } else {
         const int k_begin = blockIdx.y * a.keys_per_split;
@@ -695,13 +701,14 @@ __global__ void __launch_bounds__(128) mla_combine_kernel(MlaArgs a, int NH) {
     // the partials of (row t, head group hg): its splits, or in stream-K mode
     // the CTAs whose unit runs overlap the pair's tiles (slot = 2 CTA + segment)
     const size_t base = ((size_t)t * gridDim.y + hg) * a.splits;
-    int64_t c_lo = 0, n_part = a.splits, pair = 0;
-    const int64_t U = a.sk_units, C = a.sk_ctas, tpr = a.sk_tpr;
-    if (C > 0) {
-        pair = (int64_t)t * gridDim.y + hg;
-        const int64_t u_lo = pair * tpr, u_hi = u_lo + tpr - 1;  // CTA of unit u: ((u + 1) C - 1) / U
-        c_lo = ((u_lo + 1) * C - 1) / U;
-        n_part = ((u_hi + 1) * C - 1) / U - c_lo + 1;
+    int64_t c_lo = 0, n_part = a.splits;
+    const int64_t U = a.sk_units, Cg = a.sk_ctas / (int64_t)gridDim.y, tpr = a.sk_tpr;
+    if (Cg > 0) {
+        // head group hg's CTAs share U = T * tpr units; the CTA (within the
+        // head group) of unit u is ((u + 1) Cg - 1) / U
+        const int64_t u_lo = (int64_t)t * tpr, u_hi = u_lo + tpr - 1;
+        c_lo = ((u_lo + 1) * Cg - 1) / U;
+        n_part = ((u_hi + 1) * Cg - 1) / U - c_lo + 1;
     }
     float M = -CUDART_INF_F, L = 0.0f;
     float4 acc[4];
@@ -710,9 +717,9 @@ __global__ void __launch_bounds__(128) mla_combine_kernel(MlaArgs a, int NH) {
 #pragma unroll 2
     for (int s = 0; s < n_part; ++s) {
         size_t slot;
-        if (C > 0) {
-            const int64_t c = c_lo + s;
-            slot = (size_t)(2 * c + ((c * U / C) / tpr == pair ? 0 : 1)) * kHG + hl;
+        if (Cg > 0) {
+            const int64_t c = c_lo + s, cta = hg * Cg + c;
+            slot = (size_t)(2 * cta + ((c * U / Cg) / tpr == t ? 0 : 1)) * kHG + hl;
         } else {
             slot = (base + s) * kHG + hl;
         }
