@@ -146,7 +146,7 @@ bool plan_indexer(int B, int T, int max_len, IdxPlan *p) {
             if (c_force && C != c_force) continue;
             const int tiles_cap = ceil_div(tiles_max, C);
             if (!c_force && C > 1 && tiles_cap < 4) continue;
-            for (int stages = 4; stages >= 2; --stages) {
+            for (int stages = 6; stages >= 2; --stages) {
                 if (s_force && stages != s_force) continue;
                 size_t smem = dsa::indexer_smem_bytes(G, stages, tiles_cap);
                 // TMEM: 2*64*G columns per CTA; cap the CTAs per SM through
