@@ -24,10 +24,11 @@
  *
  * Conventions shared by every entry point
  *  - All tensor arguments are caller-owned DEVICE pointers, row-major, densely
- *    packed, 16-byte aligned.  Sizes are element counts.  The library never
- *    allocates, frees or synchronises on these calls (dsa_get_error and the
- *    *_sync helpers excepted); work is enqueued on `stream` (a cudaStream_t
- *    passed as void*, NULL = legacy default stream).
+ *    packed, 16-byte aligned (stated otherwise where a weaker rule holds).
+ *    Sizes are element counts.  The library never allocates, frees or
+ *    synchronises on these calls (dsa_get_error excepted); work is enqueued on
+ *    `stream` (a cudaStream_t passed as void*, NULL = legacy default stream),
+ *    so the calls can be captured in a CUDA graph.
  *  - Paged caches: logical position s of sequence b lives in physical row
  *    page_table[b * max_pages_per_seq + s / page_size] * page_size + s % page_size
  *    of a cache shaped [num_pages, page_size, row_width].
@@ -91,7 +92,7 @@ const char *dsa_status_string(dsa_status s);
 
 /* Launch-shape tuning knobs, read on every call (0 = automatic).  Names:
  * "indexer_cluster" (CTAs per cluster, power of two <= 16), "indexer_stages"
- * (shared-memory ring depth 2..4), "indexer_group" (query rows per cluster:
+ * (shared-memory ring depth 2..6, where it fits), "indexer_group" (query rows per cluster:
  * 1, 2 or 4), "mla_splits" (key splits per query row), "mla_pair" (with 128
  * heads, run the two 64-head CTAs of a query as a cluster sharing every
  * gathered row: 1 yes, -1 no, 0 automatic = yes when the launch needs more
@@ -112,7 +113,9 @@ size_t dsa_index_topk_workspace_size(int32_t B, int32_t T, int32_t K, int32_t ma
                                      int32_t page_size);
 
 /* Bytes of workspace dsa_sparse_mla needs for T query rows of H heads with K
- * selected slots each: the error word plus split-K partial results. */
+ * selected slots each: the error word plus the partial results of its key
+ * splits (or of its stream-K CTAs, when that mode applies; a workspace of only
+ * the split grid's size is accepted and keeps stream-K off). */
 size_t dsa_sparse_mla_workspace_size(int32_t T, int32_t H, int32_t K);
 
 /* Zero the error word of a workspace (enqueued on stream).  Call once after
