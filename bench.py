@@ -222,7 +222,8 @@ def run_other_workload(args, world, rank, local_rank):
         chunks = [(lens, np.ones(64, np.int32))]
         permute, copies = True, 2
     elif args.workload == "prefill_16k":
-        chunks = [(np.array([16384], np.int32), np.array([16384], np.int32))]
+        n = args.prefill_tokens
+        chunks = [(np.array([n], np.int32), np.array([n], np.int32))]
         permute, copies = False, 1
     else:
         chunks = [(np.array([4096 * (c + 1)], np.int32), np.array([4096], np.int32)) for c in range(32)]
@@ -482,6 +483,9 @@ def main():
                     help="also time the decode step captured once in a CUDA graph and replayed")
     ap.add_argument("--batch", type=int, default=32,
                     help="sequences per rank (default 32, the benchmark workload; smaller only for profiling)")
+    ap.add_argument("--prefill-tokens", type=int, default=16384,
+                    help="prefill_16k: tokens of the sequence (default 16384, the benchmark workload; smaller only "
+                         "for profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

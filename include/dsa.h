@@ -95,13 +95,18 @@ const char *dsa_status_string(dsa_status s);
  * (shared-memory ring depth 2..6, where it fits), "indexer_group" (query rows per cluster:
  * 1, 2 or 4), "mla_splits" (key splits per query row), "mla_pair" (with 128
  * heads, run the two 64-head CTAs of a query as a cluster sharing every
- * gathered row: 1 yes, -1 no, 0 automatic = yes when the launch needs more
- * than one wave of CTAs), "mla_stream_k" (64-head CTAs, one per SM, share
+ * gathered row: 1 yes, -1 or 0 no), "mla_stream_k" (64-head CTAs, one per SM, share
  * all (row, head group, key tile) units evenly instead of a split grid: 1 yes
  * where it applies, -1 no, 0 automatic = when the split grid would leave SMs
  * idle with one split per row; it needs the workspace
  * dsa_sparse_mla_workspace_size reports, and a
- * smaller workspace of the split grid's size keeps it off), "topk_cluster".
+ * smaller workspace of the split grid's size keeps it off), "mla_dsplit"
+ * (128 heads, bf16 cache: one CTA pair per query row and key split that
+ * splits the 576 latent dims between its two CTAs, so that every selected
+ * row is gathered once, and exchanges partial logits over distributed shared
+ * memory: 1 yes, -1 no (two 64-head CTAs per query, "mla_pair" and
+ * "mla_stream_k" then apply), 0 automatic = yes when the launch needs more
+ * than one wave of CTAs), "topk_cluster".
  * Returns 0, or -1 for an unknown name.  Results do not depend on them. */
 int dsa_set_tuning(const char *name, int value);
 

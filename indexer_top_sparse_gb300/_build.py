@@ -12,7 +12,7 @@ ROOT = os.path.dirname(PKG)
 SRC = os.path.join(PKG, "csrc")
 OUT = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT, "libdsa.so")
-SOURCES = ["dsa_abi.cu", "indexer_topk.cu", "sparse_mla.cu", "mla_static.cu", "quant.cu"]
+SOURCES = ["dsa_abi.cu", "indexer_topk.cu", "sparse_mla.cu", "sparse_mla_ds.cu", "mla_static.cu", "quant.cu"]
 HEADERS = ["ptx.cuh", "kernels.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -34,6 +34,10 @@ std::atomic<int> g_mla_pair{0};
 // 1: stream-K sparse MLA whenever it applies; -1: never; 0: when the split
 // grid would leave SMs idle (see mla_sk_ctas)
 std::atomic<int> g_mla_sk{0};
+// 1: 128-head bf16 sparse MLA on CTA pairs that split the latent dims
+// (sparse_mla_ds.cu); -1: the 64-head kernels of sparse_mla.cu; 0: automatic
+// (see mla_dsplit).
+std::atomic<int> g_mla_ds{0};
 
 int sm_count() {
     int dev = 0, n = 0;
@@ -241,15 +245,16 @@ int mla_splits(int T, int H, int K) {
     return std::max(min_splits, std::min<int>(max_splits, (int)(nsm / pairs)));
 }
 
-// Pairs only when the launch takes more than one wave of CTAs.  Within one
-// wave the two independent CTAs of a query read each row at about the same
-// time, the second from L2, and skip the pair's forwarding (measured 2 us
-// faster on the 32-row decode); across waves they drift apart, the second
-// read misses L2, and the pair is faster (3-6 % on prefill).
+// Pairs of 64-head CTAs that share every gathered row over distributed shared
+// memory: only when asked for.  Each CTA of a pair may overwrite the rows it
+// forwarded only after they have landed in the peer, and with that wait the
+// pair measured slower than independent CTAs on GB300 (131k chunked FP8
+// prefill: 221.5 against 216.2 ms of MLA; 32 x 32768 decode: 2 us slower).
+// 128-head bf16 launches of more than one wave take the dims-split pair.
 bool mla_pair(int T, int H, int splits) {
-    const int forced = g_mla_pair.load();
-    if (forced != 0) return forced > 0;
-    return mla_heads_per_cta(H) == 64 && H == 128 && (long long)T * mla_groups(H) * splits > sm_count();
+    (void)T;
+    (void)splits;
+    return g_mla_pair.load() > 0 && mla_heads_per_cta(H) == 64 && H == 128;
 }
 
 // Stream-K sparse MLA: CTAs (one per SM) for T rows of H heads with K keys,
@@ -276,6 +281,17 @@ int mla_sk_ctas(int T, int H, int K) {
     const long long per = (units + cg - 1) / cg;
     if (cg < 1 || units < 2LL * cg || per > tpr || per * tile > 2048) return 0;
     return cg * groups;
+}
+// The dims-split pair kernel (128 heads, bf16 cache) gathers each selected
+// row once and runs M = 128 logits MMAs, but exchanges 32 KB of partial
+// logits per 64-key tile over distributed shared memory.  Automatically when
+// the launch takes more than one wave of CTAs, where it measured faster on
+// GB300 (16k prefill: 19.8 against 24.9 ms); within one wave two independent
+// 64-head CTAs per query are faster (32 x 32768 decode: 64.2 against 67.5 us).
+bool mla_dsplit(int T, int H, bool fp8, int splits) {
+    const int forced = g_mla_ds.load();
+    if (forced < 0 || H != 128 || fp8) return false;
+    return forced > 0 || 2LL * T * splits > sm_count();
 }
 size_t mla_sk_workspace(int ctas) { return kErrBytes + (size_t)2 * ctas * 64 * (512 + 2) * sizeof(float); }
 
@@ -397,6 +413,7 @@ int dsa_set_tuning(const char *name, int value) {
     else if (!strcmp(name, "mla_splits")) g_mla_splits = value;
     else if (!strcmp(name, "mla_pair")) g_mla_pair = value;
     else if (!strcmp(name, "mla_stream_k")) g_mla_sk = value;
+    else if (!strcmp(name, "mla_dsplit")) g_mla_ds = value;
     else if (!strcmp(name, "topk_cluster")) g_topk_cluster = value;
     else return -1;
     return 0;
@@ -532,6 +549,10 @@ dsa_status dsa_sparse_mla(const void *q, const void *kv_cache, const void *kv_ro
     a.page_size = page_size;
     a.splits = splits;
     a.keys_per_split = ceil_div(ceil_div(K, splits), tile) * tile;
+    a.scale = scale;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    if (mla_dsplit(T, H, fp8, splits))
+        return cuda_status(dsa::launch_sparse_mla_ds(a, static_cast<cudaStream_t>(stream)));
     const bool pair = mla_pair(T, H, splits);
     const int sk = pair ? 0 : mla_sk_ctas(T, H, K);
     if (sk > 0 && workspace_bytes >= mla_sk_workspace(sk)) {
@@ -541,8 +562,6 @@ dsa_status dsa_sparse_mla(const void *q, const void *kv_cache, const void *kv_ro
         a.part_o = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + kErrBytes);
         a.part_ml = a.part_o + (size_t)2 * sk * 64 * 512;
     }
-    a.scale = scale;
-    a.scale_log2 = scale * 1.4426950408889634f;
     CUtensorMap tq;
     if (!encode_2d_bf16(&tq, q, 576, (uint64_t)T * H, (uint32_t)NH)) return DSA_ERR_CUDA;
     return cuda_status(

@@ -95,6 +95,14 @@ size_t mla_split_workspace_size(int32_t T, int32_t H, int32_t K);
 // Stream-K mode (a.sk_ctas > 0) needs NH = 64 and no pair.
 cudaError_t launch_sparse_mla(const CUtensorMap &tm_q, const MlaArgs &a, int NH, bool fp8, bool pair,
                               cudaStream_t st);
+// Merge the split partials of NH-head groups into out (and lse).
+cudaError_t launch_mla_combine(const MlaArgs &a, int NH, cudaStream_t st);
+
+// Sparse MLA for H = 128 with the latent dims split over a CTA pair
+// (sparse_mla_ds.cu): bf16 cache, split grid (no stream-K), the split
+// partial layout of launch_sparse_mla.
+size_t mla_ds_smem_bytes();
+cudaError_t launch_sparse_mla_ds(const MlaArgs &a, cudaStream_t st);
 
 // Quantisers (quant.cu).
 cudaError_t launch_quant_mxfp8(const uint16_t *x, int64_t n, uint8_t *q, uint8_t *e8m0, cudaStream_t st);

@@ -63,15 +63,32 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
+// The same with acquire semantics at cluster scope: for phases completed by
+// another CTA of the cluster (remote arrivals, bytes of its st.async stores),
+// so that what that CTA wrote before is visible afterwards.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
 // Wait for the phase with the given parity to complete.  Gives up after
 // kWaitLimitNs, records a timeout (with `where`) and returns false; *abort
 // (shared) is then set so that every role of the CTA stops waiting.
+// kCluster: the phase is completed from another CTA of the cluster.
+template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32_t *err, uint32_t where,
                                           volatile int *abort) {
-    if (mbar_try_wait(bar, parity)) return true;
+    auto try_wait = [&]() { return kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
+    if (try_wait()) return true;
     uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 0;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (try_wait()) return true;
         if ((it & 63) == 63) {
             if (*abort) return false;
             if (globaltimer_ns() - t0 > kWaitLimitNs) {
@@ -133,6 +150,15 @@ __device__ __forceinline__ void bulk_copy_to_peer(uint32_t remote_dst, const voi
         "r"(smem_u32(src)), "r"(bytes), "r"(remote_bar)
         : "memory");
 }
+// 16-byte store into another CTA's shared memory; completion is counted in
+// bytes (16) on that CTA's mbarrier.  Both addresses come from map_peer.
+__device__ __forceinline__ void st_async_peer16(uint32_t remote_addr, uint4 v, uint32_t remote_bar) {
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+            remote_addr),
+        "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(remote_bar)
+        : "memory");
+}
 __device__ __forceinline__ void cluster_barrier() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
@@ -188,6 +214,18 @@ __device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, ui
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// D[tmem] (+)= A[tmem] * B[smem]^T, kind::f16.  A (M x 16, bf16) sits in
+// TMEM with row m in lane m and elements 2j, 2j+1 of the row in column j
+// (low, high half), i.e. eight consecutive columns per K step.
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 // Shared-memory load and reduction through 32-bit shared addresses (generic
@@ -382,6 +420,19 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t addr) {
     return d;
 }
 
+// The same for rows of 64 bytes (32 bf16) with the 64-byte swizzle: 16-byte
+// chunk c of row r sits at r * 64 + ((c ^ ((r >> 1) & 3)) << 4) within a
+// 512-byte-aligned block, groups of 8 rows 512 bytes apart.
+__device__ __forceinline__ uint64_t sdesc_kmajor_sw64(uint32_t addr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((addr >> 4) & 0x3FFFu);
+    d |= (uint64_t)1u << 16;
+    d |= (uint64_t)(512u >> 4) << 32;
+    d |= (uint64_t)1u << 46;
+    d |= (uint64_t)4u << 61;                        // swizzle: 64 B
+    return d;
+}
+
 // Descriptor for an MN-major operand with the 128-byte swizzle: each K row
 // holds 64 contiguous bf16 of the M (or N) dimension in 128 bytes, 8 K rows
 // form a 1024-byte atom; `lbo` is the byte distance between consecutive
@@ -422,6 +473,10 @@ __host__ __device__ constexpr uint32_t idesc_mxf8_e4m3(uint32_t M, uint32_t N, u
 // Same with A stored MN-major (transpose bit for A).
 __host__ __device__ constexpr uint32_t idesc_bf16_f32_amn(uint32_t M, uint32_t N) {
     return idesc_bf16_f32(M, N) | (1u << 15);
+}
+// Same with B stored MN-major (transpose bit for B).
+__host__ __device__ constexpr uint32_t idesc_bf16_f32_bmn(uint32_t M, uint32_t N) {
+    return idesc_bf16_f32(M, N) | (1u << 16);
 }
 
 }  // namespace dsa

@@ -82,6 +82,10 @@ struct MlaLayout {
 struct __align__(16) MlaBars {
     uint64_t kv_full[kStages], kv_empty[kStages], s_full[2];
     uint64_t peer_free[kStages];   // pairs: the peer's copy of this stage may be overwritten
+    // pairs: every byte of this CTA's half of the stage's tile has landed in
+    // the peer, so the forwarding copies have finished reading it here and
+    // the rope region may take P
+    uint64_t fwd_done[kStages];
     uint64_t p_full, o_done, o_full, q_full, drain, table;
     uint64_t o_free;  // stream-K: the epilogue of segment 0 has read O
     uint32_t tmem_slot;
@@ -244,6 +248,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
             mbar_init(&bars->kv_full[i], kFullArrivals);
             mbar_init(&bars->kv_empty[i], 1);
             mbar_init(&bars->peer_free[i], 1);
+            mbar_init(&bars->fwd_done[i], 1);
         }
         for (int i = 0; i < 2; ++i) mbar_init(&bars->s_full[i], 1);
         mbar_init(&bars->p_full, kSmThreads / 32);
@@ -491,6 +496,16 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
                 mma_commit(&bars->drain);
                 mbar_wait(&bars->drain, 0, nullptr, 0, &no_abort);
             }
+        } else if (kPair && lane == 1) {
+            // Pairs: tell the peer as soon as each tile -- including the half
+            // the peer forwarded -- has landed here; the peer then knows that
+            // its forwarding copies have read the rows it may overwrite.
+            const uint32_t fwd_peer = map_peer(smem_u32(&bars->fwd_done[0]), peer);
+            for (int i = 0; i < n_tiles; ++i) {
+                const int stg = i % kStages;
+                if (!mbar_wait(&bars->kv_full[stg], (i / kStages) & 1, a.err, 0x514, abort)) break;
+                mbar_arrive_remote(fwd_peer + 8 * stg);
+            }
         }
     } else {
         // ---------------------------------------------------------------- softmax + epilogue
@@ -636,6 +651,10 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
                 if (hA < NH) st->alpha[sb][hA] = al[0];
                 if (hB < NH) st->alpha[sb][hB] = al[1];
             }
+            // pairs: the rope rows this CTA forwarded from this stage must have
+            // been read by their copies (they have landed in the peer) before
+            // P overwrites them
+            if (kPair && ok) ok = mbar_wait<true>(&bars->fwd_done[stg], (i / kStages) & 1, a.err, 0x513, abort);
             {
                 // P (bf16) as K-major [head][key] rows of 128 bytes with the
                 // 128-byte swizzle, over the tile's consumed rope region (the
@@ -792,9 +811,7 @@ static cudaError_t launch_heads(const CUtensorMap &tq, const MlaArgs &a, int NH,
     return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_sparse_mla(const CUtensorMap &tq, const MlaArgs &a, int NH, bool fp8, bool pair, cudaStream_t st) {
-    const cudaError_t e = fp8 ? launch_heads<true>(tq, a, NH, pair, st) : launch_heads<false>(tq, a, NH, pair, st);
-    if (e != cudaSuccess || (a.splits == 1 && a.sk_ctas == 0)) return e;
+cudaError_t launch_mla_combine(const MlaArgs &a, int NH, cudaStream_t st) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((NH + 3) / 4, a.H / NH, a.T);
     cfg.blockDim = dim3(128, 1, 1);
@@ -805,6 +822,12 @@ cudaError_t launch_sparse_mla(const CUtensorMap &tq, const MlaArgs &a, int NH, b
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, mla_combine_kernel, a, NH);
+}
+
+cudaError_t launch_sparse_mla(const CUtensorMap &tq, const MlaArgs &a, int NH, bool fp8, bool pair, cudaStream_t st) {
+    const cudaError_t e = fp8 ? launch_heads<true>(tq, a, NH, pair, st) : launch_heads<false>(tq, a, NH, pair, st);
+    if (e != cudaSuccess || (a.splits == 1 && a.sk_ctas == 0)) return e;
+    return launch_mla_combine(a, NH, st);
 }
 
 }  // namespace dsa

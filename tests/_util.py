@@ -35,6 +35,26 @@ def to_device(wl):
     return d
 
 
+class tuning:
+    """Set library tuning knobs for the duration of a with-block (0 = automatic
+    afterwards)."""
+
+    def __init__(self, **knobs):
+        self.knobs = knobs
+
+    def __enter__(self):
+        import indexer_top_sparse_gb300 as d
+        for k, v in self.knobs.items():
+            d.set_tuning(k, v)
+        return self
+
+    def __exit__(self, *exc):
+        import indexer_top_sparse_gb300 as d
+        for k in self.knobs:
+            d.set_tuning(k, 0)
+        return False
+
+
 def score_magnitude(q_bits, w, k_rows_bits):
     """sum_j |w_j| * max(q_j . k, 0) per key row (fp64), the natural scale of a
     score when the signed head weights let terms cancel."""

@@ -110,3 +110,47 @@ def test_prefill_131k_last_chunk_fp8(orc):
                        permute=True, seed=3)
     idx, out = _gpu_path(wl, fp8=True)
     _check_rows(orc, wl, [0, 2048, 4095], idx, out, fp8=True)
+
+
+def _max_excess(a, b, atol, rtol, rows=1024):
+    """max over all elements of |a - b| - (atol + rtol |b|), on the GPU in
+    row blocks (positive: out of tolerance somewhere)."""
+    worst = -float("inf")
+    for r0 in range(0, a.shape[0], rows):
+        x, y = a[r0:r0 + rows].float(), b[r0:r0 + rows].float()
+        worst = max(worst, ((x - y).abs() - (atol + rtol * y.abs())).max().item())
+    return worst
+
+
+def test_prefill_16k_every_row_on_every_kernel_form():
+    # Every query row of the 16k prefill (rows with a handful of valid keys,
+    # ragged last tiles, full 2048-key rows) on each 128-head kernel form: the
+    # dims-split pair, the 64-head pair (which forwards gathered rows to its
+    # peer) and independent 64-head CTAs; FP8 rows on the 64-head pair and
+    # independent CTAs.  Each form is within the attention tolerance of the
+    # oracle (sampled rows above), so any two agree within twice that.
+    import indexer_top_sparse_gb300 as d
+    from _util import tuning
+    wl = prefill(16384, seed=0)
+    pt, sl, cq = dev(wl.page_table), dev(wl.seq_lens), dev(wl.cu_q)
+    ws = d.Workspace(max(d.index_topk_workspace_size(wl.B, wl.T, wl.K, wl.max_pages, wl.page_size),
+                         d.sparse_mla_workspace_size(wl.T, wl.H, wl.K)))
+    idx = d.dsa_index_topk(dev_bf16(wl.q_idx), dev(wl.head_w), dev_bf16(wl.k_idx), pt, sl, cq, wl.K, workspace=ws)
+    q, kv = dev_bf16(wl.q), dev_bf16(wl.kv)
+    outs = {}
+    for name, knobs in (("dsplit", dict(mla_dsplit=1)), ("pair64", dict(mla_dsplit=-1, mla_pair=1)),
+                        ("indep64", dict(mla_dsplit=-1, mla_pair=-1))):
+        with tuning(**knobs):
+            outs[name] = d.dsa_sparse_mla(q, kv, pt, sl, cq, idx, wl.scale, workspace=ws)
+        ws.check()
+    for other in ("pair64", "indep64"):
+        assert _max_excess(outs[other], outs["dsplit"], 4e-2, 2e-2) <= 0, other
+    del outs
+    nope, rope, rsc = d.dsa_quant_fp8_rows(kv)
+    f8 = {}
+    for name, pair in (("pair64", 1), ("indep64", -1)):
+        with tuning(mla_pair=pair):
+            f8[name] = d.dsa_sparse_mla(q, nope, pt, sl, cq, idx, wl.scale, workspace=ws, kv_rope=rope, kv_scale=rsc,
+                                        dtype="fp8_rowscale")
+        ws.check()
+    assert _max_excess(f8["pair64"], f8["indep64"], 4e-2, 2e-2) <= 0

@@ -1,19 +1,23 @@
 """GPU sparse MLA against the oracle on the same indices: outputs within
 2e-2 absolute / 1e-2 relative (bf16 path), lse within 1e-3; covers 16, 64 and
 128 heads, -1 padding, a single selected key, rows with no valid key, every
-split count, and the paged gather."""
+split count, and the paged gather.  128-head bf16 cases run on both kernels:
+the CTA pair that splits the latent dims (KERNELS "dsplit", the automatic
+choice) and two 64-head CTAs per query ("heads64")."""
 import math
 
 import numpy as np
 import pytest
 import torch
 
-from _util import dev, dev_bf16, to_device
+from _util import dev, dev_bf16, to_device, tuning
 from indexer_top_sparse_gb300.inputs import make_workload
 
 pytestmark = pytest.mark.gpu
 
 ATOL, RTOL = 2e-2, 1e-2
+# value of the "mla_dsplit" knob for each 128-head bf16 kernel
+KERNELS = {"dsplit": 1, "heads64": -1}
 
 
 def _random_indices(rng, wl, K, pad_frac=0.0):
@@ -50,25 +54,22 @@ def _compare(orc, wl, idx, rows=None):
     assert np.all(np.isneginf(lse[rows][~fin]))
 
 
-@pytest.mark.parametrize("H", [16, 64, 128])
-def test_decode_heads(orc, H):
+@pytest.mark.parametrize("H,kernel", [(16, "heads64"), (64, "heads64"), (128, "dsplit"), (128, "heads64")])
+def test_decode_heads(orc, H, kernel):
     rng = np.random.default_rng(H)
     wl = make_workload("mla", [3000, 513, 70], [1, 1, 1], H=H, K=512, page_size=64, seed=H, with_idx=False)
-    _compare(orc, wl, _random_indices(rng, wl, 512))
+    with tuning(mla_dsplit=KERNELS[kernel]):
+        _compare(orc, wl, _random_indices(rng, wl, 512))
 
 
-@pytest.mark.parametrize("H", [64, 128])
+@pytest.mark.parametrize("H,kernel", [(64, "heads64"), (128, "dsplit"), (128, "heads64")])
 @pytest.mark.parametrize("splits", [1, 2, 3, 8])
-def test_every_split_count(orc, splits, H):
-    import indexer_top_sparse_gb300 as d
+def test_every_split_count(orc, splits, H, kernel):
     rng = np.random.default_rng(100 + splits)
     wl = make_workload("mla", [4000, 900], [1, 1], H=H, K=1000, page_size=64, seed=splits, with_idx=False)
     idx = _random_indices(rng, wl, 1000, pad_frac=0.1)
-    d.set_tuning("mla_splits", splits)
-    try:
+    with tuning(mla_splits=splits, mla_dsplit=KERNELS[kernel]):
         _compare(orc, wl, idx)
-    finally:
-        d.set_tuning("mla_splits", 0)
 
 
 def test_padding_single_key_and_empty_rows(orc):
@@ -87,6 +88,34 @@ def test_padding_single_key_and_empty_rows(orc):
     assert np.all(out[2] == 0) and np.all(np.isneginf(lse[2]))
 
 
+def test_dsplit_padding_single_key_empty_rows_and_ragged_tiles(orc):
+    # 128 heads on the dims-split pair: a row with -1 padding and a ragged last
+    # tile (K = 100), a single selected key, a row with no valid key, and a
+    # short sequence selected in full; one and two key splits
+    wl = make_workload("mla", [300, 300, 300, 50], [1, 1, 1, 1], H=128, K=100, page_size=32, seed=6, with_idx=False)
+    idx = np.full((4, 100), -1, np.int32)
+    idx[0, :90] = np.arange(0, 900, 10)[:90] % 300
+    idx[0] = np.where(np.arange(100) % 3 == 0, -1, idx[0])
+    idx[1, 77] = 123
+    idx[3, :50] = np.arange(50)
+    for splits in (1, 2):
+        with tuning(mla_splits=splits, mla_dsplit=1):
+            _compare(orc, wl, idx)
+            out, lse = _run(wl, idx)
+        v = wl.kv.reshape(-1, 576)[wl.page_table[1][123 // 32] * 32 + 123 % 32, :512]
+        from indexer_top_sparse_gb300.inputs import bf16_to_f32
+        np.testing.assert_allclose(out[1], np.broadcast_to(bf16_to_f32(v), (128, 512)), atol=1e-2, rtol=1e-2)
+        assert np.all(out[2] == 0) and np.all(np.isneginf(lse[2]))
+
+
+def test_dsplit_prefill_rows(orc):
+    # many query rows of one sequence (more clusters than fit at once)
+    rng = np.random.default_rng(8)
+    wl = make_workload("mla_prefill", [700], [700], H=128, K=256, page_size=64, permute=True, seed=8, with_idx=False)
+    with tuning(mla_dsplit=1):
+        _compare(orc, wl, _random_indices(rng, wl, 256, pad_frac=0.02), rows=[0, 1, 63, 64, 255, 256, 500, 699])
+
+
 def test_prefill_rows(orc):
     rng = np.random.default_rng(7)
     wl = make_workload("mla_prefill", [400], [400], H=16, K=128, page_size=64, permute=False, seed=7, with_idx=False)
@@ -99,9 +128,9 @@ def test_heads_32(orc):
     _compare(orc, wl, _random_indices(rng, wl, 700, pad_frac=0.05))
 
 
-@pytest.mark.parametrize("H", [64, 128])
+@pytest.mark.parametrize("H,kernel", [(64, "heads64"), (128, "dsplit"), (128, "heads64")])
 @pytest.mark.parametrize("order", ["rising", "falling"])
-def test_reference_max_moves_across_tiles(orc, order, H):
+def test_reference_max_moves_across_tiles(orc, order, H, kernel):
     # logits that grow (or shrink) strongly from one 128-key tile to the next,
     # so that the running maximum moves by far more than 2^8 between tiles
     from indexer_top_sparse_gb300.inputs import bf16_bits, bf16_to_f32
@@ -118,26 +147,19 @@ def test_reference_max_moves_across_tiles(orc, order, H):
     wl.kv = bf16_bits(kv.reshape(wl.kv.shape).astype(np.float32))
     wl.scale = 1.0
     idx = np.arange(K, dtype=np.int32)[None, :]
-    import indexer_top_sparse_gb300 as d
-    d.set_tuning("mla_splits", 1)
-    try:
+    with tuning(mla_splits=1, mla_dsplit=KERNELS[kernel]):
         _compare(orc, wl, idx)
-    finally:
-        d.set_tuning("mla_splits", 0)
 
 
-@pytest.mark.parametrize("pair", [0, -1])
-def test_128_heads_over_several_waves(orc, pair):
-    # 200 query rows x 2 head groups: more CTAs than SMs, so the automatic
-    # choice pairs the two head groups; -1 keeps them independent
-    import indexer_top_sparse_gb300 as d
+@pytest.mark.parametrize("pair,kernel", [(1, "heads64"), (-1, "heads64"), (0, "auto")])
+def test_128_heads_over_several_waves(orc, pair, kernel):
+    # 200 query rows x 2 head groups: more CTAs than SMs (several waves); the
+    # 64-head kernel with its head groups paired (1) or independent (-1), and
+    # the automatic choice (the dims-split pair at this size)
     rng = np.random.default_rng(129)
     wl = make_workload("mla", [600, 300], [120, 80], H=128, K=192, page_size=64, seed=129, with_idx=False)
-    d.set_tuning("mla_pair", pair)
-    try:
+    with tuning(mla_pair=pair, mla_dsplit=KERNELS.get(kernel, 0)):
         _compare(orc, wl, _random_indices(rng, wl, 192, pad_frac=0.05))
-    finally:
-        d.set_tuning("mla_pair", 0)
 
 
 @pytest.mark.parametrize("fp8", [False, True])
@@ -162,11 +184,8 @@ def test_paired_128_heads_matches(orc, fp8):
                                 dtype=orc.KV_FP8_ROWSCALE, kv_rope=rope, kv_scale=sc)
         np.testing.assert_allclose(out.float().cpu().numpy(), ref, atol=ATOL, rtol=RTOL)
         return
-    d.set_tuning("mla_pair", 1)
-    try:
+    with tuning(mla_pair=1, mla_dsplit=-1):
         _compare(orc, wl, _random_indices(rng, wl, 1024, pad_frac=0.05))
-    finally:
-        d.set_tuning("mla_pair", 0)
 
 
 @pytest.mark.parametrize("case", ["k1000_h128", "k1000_h64", "k2048_h128"])
@@ -182,6 +201,7 @@ def test_stream_k_matches(orc, case, fp8):
     wl = make_workload("sk", lens, [1] * T, H=H, K=K, page_size=64, seed=int(lens[0]), with_idx=False)
     idx = _random_indices(rng, wl, K, pad_frac=0.05)
     d.set_tuning("mla_stream_k", 1)
+    d.set_tuning("mla_dsplit", -1)
     try:
         if fp8:
             nope, rope, sc = orc.quant_fp8_tiles(wl.kv)
@@ -197,6 +217,7 @@ def test_stream_k_matches(orc, case, fp8):
             _compare(orc, wl, idx)
     finally:
         d.set_tuning("mla_stream_k", 0)
+        d.set_tuning("mla_dsplit", 0)
 
 
 def test_stream_k_off_and_on_agree():
@@ -209,6 +230,7 @@ def test_stream_k_off_and_on_agree():
     outs = []
     for mode in (0, -1):
         d.set_tuning("mla_stream_k", mode)
+        d.set_tuning("mla_dsplit", -1)
         try:
             ws = d.Workspace(d.sparse_mla_workspace_size(wl.T, wl.H, 2048))
             lse = torch.empty((wl.T, wl.H), dtype=torch.float32, device="cuda")
@@ -218,5 +240,26 @@ def test_stream_k_off_and_on_agree():
             outs.append((o.float().cpu().numpy(), lse.cpu().numpy()))
         finally:
             d.set_tuning("mla_stream_k", 0)
+            d.set_tuning("mla_dsplit", 0)
+    np.testing.assert_allclose(outs[0][0], outs[1][0], atol=1e-2, rtol=1e-2)
+    np.testing.assert_allclose(outs[0][1], outs[1][1], atol=1e-4, rtol=1e-4)
+
+
+def test_dsplit_and_heads64_agree_on_decode():
+    # the 32-row decode launch shape (two key splits) on both 128-head kernels:
+    # the same attention up to summation order
+    rng = np.random.default_rng(151)
+    wl = make_workload("ds", [5000] * 32, [1] * 32, H=128, K=2048, page_size=64, seed=151, with_idx=False)
+    idx = dev(_random_indices(rng, wl, 2048, pad_frac=0.01))
+    import indexer_top_sparse_gb300 as d
+    outs = []
+    for kernel in ("dsplit", "heads64"):
+        with tuning(mla_dsplit=KERNELS[kernel]):
+            ws = d.Workspace(d.sparse_mla_workspace_size(wl.T, wl.H, 2048))
+            lse = torch.empty((wl.T, wl.H), dtype=torch.float32, device="cuda")
+            o = d.dsa_sparse_mla(dev_bf16(wl.q), dev_bf16(wl.kv), dev(wl.page_table), dev(wl.seq_lens),
+                                 dev(wl.cu_q), idx, wl.scale, workspace=ws, lse=lse)
+            ws.check()
+            outs.append((o.float().cpu().numpy(), lse.cpu().numpy()))
     np.testing.assert_allclose(outs[0][0], outs[1][0], atol=1e-2, rtol=1e-2)
     np.testing.assert_allclose(outs[0][1], outs[1][1], atol=1e-4, rtol=1e-4)
