@@ -33,7 +33,9 @@
 // the latent part of Q 384..511.
 // Warps: 0-3 gather (cp.async into 128-byte-swizzled regions), 4 tcgen05
 // issuer, 5-8 exchange, 9-12 softmax (warp w reads TMEM lanes 32 (w % 4) ..);
-// warps 5-12 run the epilogue.  Key splits write the partial layout of
+// warps 5-12 run the epilogue.  Tiles whose 64 index slots hold no valid
+// position (the -1 padding of rows with fewer than K candidates) are skipped:
+// both CTAs build the same list of the others from the same row table.  Key splits write the partial layout of
 // sparse_mla.cu and are merged by its combine kernel.
 #include <cuda_bf16.h>
 #include <math_constants.h>
@@ -86,6 +88,8 @@ struct __align__(16) DsTable {
     uint32_t valid[kMaxKeys / 32];     // bit k % 32 of word k / 32: key k is valid
     float alpha[kHeads];               // this tile's rescale factor per head
     float m_fin[kHeads], l_fin[kHeads], inv_l[kHeads];
+    int32_t tile_list[kMaxKeys / kKeys];  // the split's tiles that hold a valid key, in order
+    int32_t n_work;                       // their number
 };
 
 __device__ __forceinline__ int find_seq(const int32_t *cu_q, int B, int t) {
@@ -209,7 +213,16 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_ds_kernel(MlaArgs a) {
             if (lane == 0) tab->valid[k >> 5] = bits;
         }
         bar_sync(kBarGather, kGather * 32);
+        // the tiles with at least one valid key (at most 32 per split)
+        if (warp == 0) {
+            const bool any = lane < n_tiles && (tab->valid[2 * lane] | tab->valid[2 * lane + 1]) != 0u;
+            const uint32_t mask = __ballot_sync(0xffffffffu, any);
+            if (any) tab->tile_list[__popc(mask & ((1u << lane) - 1u))] = lane;
+            if (lane == 0) tab->n_work = __popc(mask);
+        }
+        bar_sync(kBarGather, kGather * 32);
         if (threadIdx.x == 0) mbar_arrive(&bars->table);
+        const int n_work = tab->n_work;
         // warp w: keys 16 w .. 16 w + 15.  Latent regions: lane l copies chunk
         // l % 8 of keys 16 w + l / 8 + 4 m; rope: chunk l % 4 of this rank's
         // 64-byte half of keys 16 w + l / 4 + 8 m
@@ -217,13 +230,13 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_ds_kernel(MlaArgs a) {
         const int kr = warp * 16 + (lane >> 2), cr = lane & 3;
         const uint8_t *src_l = a.kv + 512 * rank + cl * 16;  // + row * 1152 + region * 128
         const uint8_t *src_r = a.kv + 1024 + 64 * rank + cr * 16;
-        for (int i = 0; i < n_tiles; ++i) {
+        for (int i = 0; i < n_work; ++i) {
             const int stg = i % kStages;
             bool ok = true;
             if (i >= kStages) ok = mbar_wait(&bars->kv_empty[stg], ((i / kStages) & 1) ^ 1, a.err, 0x601, abort);
             if (!__all_sync(0xffffffffu, ok)) break;
             uint8_t *dst = sKV + stg * kStageBytes;
-            const int32_t *rows = tab->rows + i * kKeys;
+            const int32_t *rows = tab->rows + tab->tile_list[i] * kKeys;
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
                 const int key = kl + 4 * m;
@@ -247,7 +260,9 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_ds_kernel(MlaArgs a) {
             constexpr uint32_t idesc_s = idesc_bf16_f32(kHeads, kKeys);
             constexpr uint32_t idesc_o = idesc_bf16_f32_amn(128, kHeads);  // V^T MN-major, P^T K-major
             const uint32_t kv_base = smem_u32(sKV), p_base = smem_u32(sP), qr_base = smem_u32(sQr);
-            bool ok = n_tiles > 0 && mbar_wait(&bars->q_full, 0, a.err, 0x602, abort);
+            bool ok = mbar_wait(&bars->table, 0, a.err, 0x60d, abort);
+            const int n_work = tab->n_work;
+            ok = ok && n_work > 0 && mbar_wait(&bars->q_full, 0, a.err, 0x602, abort);
             // logits of tile i into S buffer i & 1: its four latent regions
             // (A = Q in TMEM) and this CTA's two rope steps (A = Q in smem)
             auto ready_s = [&](int i) {
@@ -276,10 +291,10 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_ds_kernel(MlaArgs a) {
                 return true;
             };
             if (ok) ok = issue_s(0);
-            if (ok && n_tiles > 1) ok = issue_s(1);
-            for (int i = 0; ok && i < n_tiles; ++i) {
+            if (ok && n_work > 1) ok = issue_s(1);
+            for (int i = 0; ok && i < n_work; ++i) {
                 // the logits two tiles ahead go first when they can start now
-                bool pend = i + 2 < n_tiles;
+                bool pend = i + 2 < n_work;
                 if (pend && ready_s(i + 2)) {
                     if (!(ok = issue_s(i + 2))) break;
                     pend = false;
@@ -300,7 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_ds_kernel(MlaArgs a) {
                 mma_commit(&bars->o_done);
                 if (pend && !(ok = issue_s(i + 2))) break;
             }
-            if (ok && n_tiles > 0) mma_commit(&bars->o_full);
+            if (ok && n_work > 0) mma_commit(&bars->o_full);
             if (*abort) {
                 volatile int no_abort = 0;
                 mma_commit(&bars->drain);
@@ -315,11 +330,14 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_ds_kernel(MlaArgs a) {
         const uint32_t tl = tmem + lane_off;  // this warp's TMEM lanes
         const int h = quad * 32 + lane;       // head (S rows) or value dim (O^T rows) of this thread
         bool ok = true;
+        int n_work = 0;  // tiles with a valid key (known once the row table is built)
         if (!is_sm) {
             // ---------------------------------------------------------------- exchange
             const uint32_t x_peer = map_peer(smem_u32(sX), peer);
             const uint32_t x_full_peer = map_peer(smem_u32(&bars->x_full[0]), peer);
-            for (int i = 0; i < n_tiles; ++i) {
+            ok = __all_sync(0xffffffffu, mbar_wait(&bars->table, 0, a.err, 0x60e, abort));
+            n_work = ok ? tab->n_work : 0;
+            for (int i = 0; i < n_work; ++i) {
                 const int sb = i & 1;
                 ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[sb], (i >> 1) & 1, a.err, 0x607, abort));
                 if (!ok) break;
@@ -379,8 +397,9 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_ds_kernel(MlaArgs a) {
             int next0 = 0, next1 = 1;  // the tile each receive buffer expects next
             // (decisions to go on are taken by all four softmax warps together,
             // since they meet at named barriers inside the loop)
-            ok = bar_and(kBarSm, 128, n_tiles == 0 || mbar_wait(&bars->table, 0, a.err, 0x606, abort));
-            for (int i = 0; ok && i < n_tiles; ++i) {
+            ok = bar_and(kBarSm, 128, mbar_wait(&bars->table, 0, a.err, 0x606, abort));
+            n_work = ok ? tab->n_work : 0;
+            for (int i = 0; ok && i < n_work; ++i) {
                 const int sb = i & 1;
                 const uint8_t *xb = sX + sb * kXBytes;
                 ok = mbar_wait<true>(&bars->x_full[sb], (i >> 1) & 1, a.err, 0x609, abort);
@@ -414,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_ds_kernel(MlaArgs a) {
                 // every softmax thread has read buffer sb: it expects tile i + 2's
                 // partial logits next, and the other CTA may send them
                 bar_sync(kBarSm, 128);
-                if (tid_s == 0 && i + 2 < n_tiles) {
+                if (tid_s == 0 && i + 2 < n_work) {
                     mbar_arrive_expect_tx(&bars->x_full[sb], kXBytes);
                     mbar_arrive_remote(x_free_peer + sb * 8);
                 }
@@ -422,7 +441,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_ds_kernel(MlaArgs a) {
                 else next0 = i + 2;
                 // online softmax of head h over the tile's keys (log2 domain);
                 // the reference max moves only when the max grows by more than 2^8
-                const uint32_t v0 = tab->valid[2 * i], v1 = tab->valid[2 * i + 1];
+                const int tile = tab->tile_list[i];
+                const uint32_t v0 = tab->valid[2 * tile], v1 = tab->valid[2 * tile + 1];
                 float m4[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
 #pragma unroll
                 for (int j = 0; j < kKeys; ++j) {
@@ -488,13 +508,13 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_ds_kernel(MlaArgs a) {
                 // freed it: let bytes that may be on their way land (or the
                 // bounded wait run out) before this CTA can leave.
                 volatile int no_abort = 0;
-                if (next0 < n_tiles) mbar_wait<true>(&bars->x_full[0], (next0 >> 1) & 1, nullptr, 0, &no_abort);
-                if (next1 < n_tiles) mbar_wait<true>(&bars->x_full[1], (next1 >> 1) & 1, nullptr, 0, &no_abort);
+                if (next0 < n_work) mbar_wait<true>(&bars->x_full[0], (next0 >> 1) & 1, nullptr, 0, &no_abort);
+                if (next1 < n_work) mbar_wait<true>(&bars->x_full[1], (next1 >> 1) & 1, nullptr, 0, &no_abort);
             }
         }
         // ---------------------------------------------------------------- epilogue
         if (tid_s == 0) grid_dep_launch();  // the split combine may start launching
-        if (ok && n_tiles > 0) ok = mbar_wait(&bars->o_full, 0, a.err, 0x60c, abort);
+        if (ok && n_work > 0) ok = mbar_wait(&bars->o_full, 0, a.err, 0x60c, abort);
         ok = bar_and(kBarEpi, 256, ok && !*abort);  // also: m_fin / l_fin are written
         tc_fence_after();
         if (ok) {
@@ -504,7 +524,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_ds_kernel(MlaArgs a) {
 #pragma unroll 1
             for (int h0 = 0; h0 < kHeads; h0 += 32) {
                 uint32_t o[32];
-                if (n_tiles > 0) {
+                if (n_work > 0) {
                     tmem_ld32(tl + kColO + 128 * c + h0, o);
                     tmem_wait_ld();
                 } else {
