@@ -197,7 +197,9 @@ __global__ void __launch_bounds__(256) cache_append_kernel(AppendArgs a) {
         if (lane == 0) report_error(a.err, kErrBadLen);
         return;
     }
-    const int page = __ldg(a.page_table + (int64_t)b * a.max_pages + pos / a.page_size);
+    // a position past the sequence's page-table row is a bad page, unread
+    const int page = pos / a.page_size < a.max_pages ? __ldg(a.page_table + (int64_t)b * a.max_pages + pos / a.page_size)
+                                                     : -1;
     if (page < 0 || (int64_t)page >= a.num_pages) {
         if (lane == 0) report_error(a.err, kErrBadPage);
         return;

@@ -310,7 +310,9 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
         for (int u = 0; u < kPer; ++u) {
             const int k = threadIdx.x + u * kProd * 32, s = seg_of(k / kKeys);
             const int pos = s ? spos1 : spos0, bb = s ? sb1 : sb0;
-            pagev[u] = idxv[u] >= 0 && idxv[u] <= pos
+            // a position past the sequence's page-table row (seq_lens larger
+            // than max_pages * page_size) is reported as a bad page, unread
+            pagev[u] = idxv[u] >= 0 && idxv[u] <= pos && idxv[u] / a.page_size < a.max_pages
                            ? __ldg(a.page_table + (size_t)bb * a.max_pages + idxv[u] / a.page_size)
                            : -1;
         }

@@ -187,7 +187,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_ds_kernel(MlaArgs a) {
         }
 #pragma unroll
         for (int u = 0; u < kPer; ++u)
-            pagev[u] = idxv[u] >= 0 && idxv[u] <= pos
+            pagev[u] = idxv[u] >= 0 && idxv[u] <= pos && idxv[u] / a.page_size < a.max_pages
                            ? __ldg(a.page_table + (size_t)b * a.max_pages + idxv[u] / a.page_size)
                            : -1;
 #pragma unroll

@@ -3,19 +3,22 @@ no host synchronisation, no pageable copy when the caller passes the outputs
 and the workspace): a decode step captured once and replayed on new inputs
 gives bit for bit what the same calls give eagerly, for the bf16 path and
 for the FP8 path with its Q quantisation (index-Q quantise -> indexer + Top-K
--> sparse MLA -> split combine, chained by programmatic dependent launch)."""
+-> sparse MLA -> split combine, chained by programmatic dependent launch).
+The replayed step is also checked against the oracle on the new inputs:
+index sets within the near-threshold band, attention (fed the replay's
+indices) within 2e-2 / 1e-2."""
 import numpy as np
 import pytest
 import torch
 
-from _util import dev, dev_bf16
+from _util import check_index_sets, dev, dev_bf16
 from indexer_top_sparse_gb300.inputs import make_workload
 
 pytestmark = pytest.mark.gpu
 
 
 @pytest.mark.parametrize("fp8", [False, True])
-def test_decode_step_replays_in_a_cuda_graph(fp8):
+def test_decode_step_replays_in_a_cuda_graph(orc, fp8):
     import indexer_top_sparse_gb300 as d
     wl = make_workload("graph", [3000, 700, 64, 2049], [1, 1, 1, 1], H=128, K=512, page_size=64, seed=77)
     pt, sl, cq = dev(wl.page_table), dev(wl.seq_lens), dev(wl.cu_q)
@@ -67,3 +70,29 @@ def test_decode_step_replays_in_a_cuda_graph(fp8):
         ws.check()
         assert torch.equal(idx, want_idx), trial
         assert torch.equal(out.view(torch.int16), want_out.view(torch.int16)), trial
+        _check_against_oracle(orc, wl, fp8, q_idx, q, idx, out)
+
+
+def _bits(t):
+    return t.cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+def _check_against_oracle(orc, wl, fp8, q_idx, q, idx, out):
+    qi, qb = _bits(q_idx), _bits(q)
+    g_idx = idx.cpu().numpy()
+    if fp8:
+        q8, qs = orc.quant_mxfp8(qi)
+        k8, ks = orc.quant_mxfp8(wl.k_idx)
+        ref_idx, ref_sc = orc.index_topk(q8, wl.head_w, k8, wl.page_table, wl.seq_lens, wl.cu_q, wl.K, wl.page_size,
+                                         dtype=orc.IDX_MXFP8, q_scale=qs, k_scale=ks, want_scores=True)
+        nope, rope, vsc = orc.quant_fp8_tiles(wl.kv)
+        ref_out, _ = orc.sparse_mla(qb, nope, wl.page_table, wl.cu_q, g_idx, wl.scale, wl.page_size,
+                                    dtype=orc.KV_FP8_TILE128, kv_rope=rope, kv_scale=vsc)
+    else:
+        ref_idx, ref_sc = orc.index_topk(qi, wl.head_w, wl.k_idx, wl.page_table, wl.seq_lens, wl.cu_q, wl.K,
+                                         wl.page_size, want_scores=True)
+        ref_out, _ = orc.sparse_mla(qb, wl.kv, wl.page_table, wl.cu_q, g_idx, wl.scale, wl.page_size)
+    pos = wl.query_pos()
+    for t in range(wl.T):
+        check_index_sets(g_idx[t], ref_idx[t], ref_sc[t], int(pos[t]) + 1, wl.K)
+    np.testing.assert_allclose(out.float().cpu().numpy(), ref_out, atol=2e-2, rtol=1e-2)

@@ -220,7 +220,7 @@ def test_stream_k_matches(orc, case, fp8):
         d.set_tuning("mla_dsplit", 0)
 
 
-def test_stream_k_off_and_on_agree():
+def test_stream_k_off_and_on_agree(orc):
     # the decode shape where stream-K is the automatic choice, against the
     # split grid (stream-K off): the same attention up to summation order
     import indexer_top_sparse_gb300 as d
@@ -243,9 +243,26 @@ def test_stream_k_off_and_on_agree():
             d.set_tuning("mla_dsplit", 0)
     np.testing.assert_allclose(outs[0][0], outs[1][0], atol=1e-2, rtol=1e-2)
     np.testing.assert_allclose(outs[0][1], outs[1][1], atol=1e-4, rtol=1e-4)
+    _every_row_against_oracle(orc, wl, idx.cpu().numpy(), outs)
 
 
-def test_dsplit_and_heads64_agree_on_decode():
+def _every_row_against_oracle(orc, wl, idx, outs):
+    """Both runs against the oracle on every row (rows on a thread pool: the
+    oracle's calls release the interpreter lock)."""
+    import concurrent.futures as cf
+    import os
+    rows = [np.array([t], np.int32) for t in range(wl.T)]
+    with cf.ThreadPoolExecutor(max_workers=max(1, min(16, os.cpu_count() or 1))) as ex:
+        refs = list(ex.map(lambda r: orc.sparse_mla(wl.q, wl.kv, wl.page_table, wl.cu_q, idx, wl.scale,
+                                                    wl.page_size, rows=r), rows))
+    ref = np.concatenate([o for o, _ in refs])
+    ref_lse = np.concatenate([l for _, l in refs])
+    for o, lse in outs:
+        np.testing.assert_allclose(o, ref, atol=ATOL, rtol=RTOL)
+        np.testing.assert_allclose(lse, ref_lse, atol=1e-3, rtol=1e-3)
+
+
+def test_dsplit_and_heads64_agree_on_decode(orc):
     # the 32-row decode launch shape (two key splits) on both 128-head kernels:
     # the same attention up to summation order
     rng = np.random.default_rng(151)
@@ -263,3 +280,4 @@ def test_dsplit_and_heads64_agree_on_decode():
             outs.append((o.float().cpu().numpy(), lse.cpu().numpy()))
     np.testing.assert_allclose(outs[0][0], outs[1][0], atol=1e-2, rtol=1e-2)
     np.testing.assert_allclose(outs[0][1], outs[1][1], atol=1e-4, rtol=1e-4)
+    _every_row_against_oracle(orc, wl, idx.cpu().numpy(), outs)

@@ -92,7 +92,7 @@ def test_fp8_zero_rows_and_wide_scales(orc):
     out, _ = _run(wl, nope, rope, sc, idx)
     ref, _ = orc.sparse_mla(wl.q, nope, wl.page_table, wl.cu_q, idx, wl.scale, wl.page_size,
                             dtype=orc.KV_FP8_ROWSCALE, kv_rope=rope, kv_scale=sc)
-    np.testing.assert_allclose(out, ref, atol=2e-2 * max(1.0, np.abs(ref).max()), rtol=1e-2)
+    np.testing.assert_allclose(out, ref, atol=6e-2, rtol=3e-2)
 
 
 def test_fp8_tile_scales_differ_within_a_row(orc):
@@ -113,4 +113,4 @@ def test_fp8_tile_scales_differ_within_a_row(orc):
     out, _ = _run(wl, nope, rope, sc, idx, "fp8_tile128")
     ref, _ = orc.sparse_mla(wl.q, nope, wl.page_table, wl.cu_q, idx, wl.scale, wl.page_size,
                             dtype=orc.KV_FP8_TILE128, kv_rope=rope, kv_scale=sc)
-    np.testing.assert_allclose(out, ref, atol=2e-2 * max(1.0, np.abs(ref).max()), rtol=1e-2)
+    np.testing.assert_allclose(out, ref, atol=6e-2, rtol=3e-2)

@@ -1,7 +1,8 @@
 """GPU quantisers against the oracle's codecs, bit for bit: MXFP8 blocks of 32
 (E8M0 scale + E4M3 elements) and FP8 latent rows (fp32 scale per row or per
 128-dim tile + E4M3 latent dims, bf16 rope dims), over N(0,1) data and the edge cases (all-zero blocks,
-tiny and huge magnitudes, exact ties to even)."""
+tiny and huge magnitudes, blocks whose E8M0 scale clamps at 2^-127, exact
+ties to even)."""
 import numpy as np
 import pytest
 import torch
@@ -19,6 +20,12 @@ def _data(rng, shape):
     flat[1, :32] *= np.float32(1e-30)
     flat[2, 32:64] *= np.float32(1e30)
     flat[3, :32] = np.float32(1.0625) * np.float32(2.0) ** rng.integers(-20, 20, 32).astype(np.float32)
+    # blocks whose scale clamps to the smallest E8M0 byte (amax below 2^-119:
+    # bf16 subnormals and the smallest normals), and one near the bf16 maximum
+    flat[4, :32] *= np.float32(2.0 ** -130)
+    flat[4, 32:64] *= np.float32(2.0 ** -124)
+    flat[5, :32] *= np.float32(2.0 ** -121)
+    flat[5, 32:64] = np.float32(3.38e38) * np.sign(flat[5, 32:64])
     return x
 
 

@@ -145,6 +145,42 @@ def test_mxfp8_quant_properties(orc):
             assert np.all(np.abs(deq - blk)[normal] <= 2.0 ** -4 * np.abs(blk)[normal])
 
 
+def test_mxfp8_scale_clamps_to_the_e8m0_range(orc):
+    # OCP MX v1.0: the block scale is 2^X with X = floor(log2 amax) - 8 (the
+    # E4M3 emax), stored as the E8M0 byte X + 127, whose range is 2^-127 ..
+    # 2^127.  A block with amax below 2^-119 (the smallest bf16 normals and the
+    # bf16 subnormals) would need X < -127: the byte clamps to 0 and the
+    # elements are x / 2^-127 rounded to the nearest E4M3 (no saturation is
+    # possible there, |x| / 2^-127 < 2^8).  The largest finite bf16 magnitude
+    # (2 - 2^-7) 2^127 gives X = 119, byte 246, so bf16 input never reaches the
+    # upper end of the range.
+    rng = np.random.default_rng(31)
+    exps = [-133, -132, -131, -130, -129, -128, -127, -126, -125, -121, -120, -119, -118, -100]
+    x = np.zeros((len(exps) + 1, 32), np.float32)
+    for i, e in enumerate(exps):
+        x[i] = (rng.random(32).astype(np.float32) + np.float32(0.5)) * np.float32(2.0 ** e)
+        x[i, ::3] *= np.float32(-1.0)
+    bits = bf16_bits(x)
+    bits[-1] = np.where(np.arange(32) % 2 == 0, 0x7F7F, 0xFF00).astype(np.uint16)  # +max bf16, -2^127
+    xv = bf16_to_f32(bits).astype(np.float64)
+    q, e = orc.quant_mxfp8(bits)
+    table = _torch_e4m3_decode_all()
+    clamped = 0
+    for r in range(x.shape[0]):
+        amax = np.abs(xv[r]).max()
+        assert amax > 0.0
+        X = math.frexp(amax)[1] - 1 - 8            # floor(log2 amax) - 8, exact
+        want_byte = min(max(X + 127, 0), 254)
+        clamped += want_byte != X + 127
+        assert int(e[r, 0]) == want_byte, (r, amax, X)
+        sc = 2.0 ** (want_byte - 127)
+        for i in range(32):
+            want = _nearest_e4m3_bruteforce(min(max(xv[r, i] / sc, -448.0), 448.0), table)
+            assert table[int(q[r, i])] == table[want], (r, i)
+    assert int(e[-1, 0]) == 246
+    assert clamped >= 8    # the clamped blocks are really exercised
+
+
 def test_fp8_row_quant_matches_library_cast(orc):
     rng = np.random.default_rng(4)
     kv = rng.standard_normal((9, 576)).astype(np.float32)

@@ -31,13 +31,16 @@ def _indices(rng, wl):
     return idx
 
 
-def _call_static(lib, t, idx_d, wl, out, lse):
+def _call_static(lib, t, idx_d, wl, out, lse, kv=None, rope=None, scale=None, dtype=0):
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     P = ctypes.c_void_p
-    rc = lib.dsa_sparse_mla_static(P(t["q"].data_ptr()), P(t["kv"].data_ptr()), None, None, t["kv"].shape[0],
+    kv = t["kv"] if kv is None else kv
+    rc = lib.dsa_sparse_mla_static(P(t["q"].data_ptr()), P(kv.data_ptr()),
+                                   None if rope is None else P(rope.data_ptr()),
+                                   None if scale is None else P(scale.data_ptr()), kv.shape[0],
                                    P(t["page_table"].data_ptr()), t["page_table"].shape[1],
                                    P(t["seq_lens"].data_ptr()), P(t["cu_q"].data_ptr()), P(idx_d.data_ptr()), wl.B,
-                                   wl.T, wl.H, wl.K, ctypes.c_float(wl.scale), wl.page_size, 0,
+                                   wl.T, wl.H, wl.K, ctypes.c_float(wl.scale), wl.page_size, dtype,
                                    P(out.data_ptr()), P(lse.data_ptr()), stream)
     assert rc == 0, f"dsa_sparse_mla_static returned {rc}"
 
@@ -66,6 +69,53 @@ def test_static_scratch_matches_workspace_version_twice():
         np.testing.assert_allclose(out.float().cpu().numpy(), ref_out.float().cpu().numpy(), atol=2e-2, rtol=1e-2,
                                    err_msg=f"call {call}")
         np.testing.assert_allclose(lse.cpu().numpy(), ref_lse.cpu().numpy(), atol=1e-3, rtol=1e-3)
+
+
+@pytest.mark.parametrize("case", ["fp8_rowscale_h64", "bf16_h128_dims_split"])
+def test_static_other_kernels_match_workspace_version(orc, case):
+    # The FP8 latent cache (E4M3 rows with a row scale) and the 128-head
+    # dims-split CTA pair also run through the static scratch: each call is
+    # compared with dsa_sparse_mla on the same inputs and with the oracle.
+    import indexer_top_sparse_gb300 as d
+    from _util import tuning
+    lib = d.load()
+    H = 64 if case.startswith("fp8") else 128
+    rng = np.random.default_rng(5 + H)
+    wl = make_workload(f"static_{case}", [2500, 1300], [1, 1], H=H, K=1200, page_size=64, seed=5 + H,
+                       with_idx=False)
+    t = to_device(wl)
+    idx = _indices(rng, wl)
+    idx_d = dev(idx)
+    knobs = dict(mla_dsplit=1) if case.startswith("bf16") else dict(mla_dsplit=-1)
+    fp8 = case.startswith("fp8")
+    if fp8:
+        nope, rope, rsc = d.dsa_quant_fp8_rows(t["kv"])
+        kw = dict(kv_rope=rope, kv_scale=rsc, dtype="fp8_rowscale")
+    else:
+        nope, rope, rsc, kw = None, None, None, {}
+    with tuning(**knobs):
+        assert d.sparse_mla_workspace_size(wl.T, wl.H, wl.K) > 256, "the case must use split partials"
+        ref_out = torch.empty((wl.T, wl.H, 512), dtype=torch.bfloat16, device="cuda")
+        ref_lse = torch.empty((wl.T, wl.H), dtype=torch.float32, device="cuda")
+        ws = d.Workspace(d.sparse_mla_workspace_size(wl.T, wl.H, wl.K))
+        d.dsa_sparse_mla(t["q"], t["kv"] if not fp8 else nope, t["page_table"], t["seq_lens"], t["cu_q"], idx_d,
+                         wl.scale, out=ref_out, lse=ref_lse, workspace=ws, **kw)
+        ws.check()
+        for call in range(2):
+            out = torch.full_like(ref_out, float("nan"))
+            lse = torch.full_like(ref_lse, float("nan"))
+            _call_static(lib, t, idx_d, wl, out, lse, kv=nope, rope=rope, scale=rsc, dtype=1 if fp8 else 0)
+            torch.cuda.synchronize()
+            np.testing.assert_allclose(out.float().cpu().numpy(), ref_out.float().cpu().numpy(), atol=2e-2,
+                                       rtol=1e-2, err_msg=f"{case} call {call}")
+            np.testing.assert_allclose(lse.cpu().numpy(), ref_lse.cpu().numpy(), atol=1e-3, rtol=1e-3)
+    if fp8:
+        rn, rr, rs = orc.quant_fp8_rows(wl.kv)
+        want, _ = orc.sparse_mla(wl.q, rn, wl.page_table, wl.cu_q, idx, wl.scale, wl.page_size,
+                                 dtype=orc.KV_FP8_ROWSCALE, kv_rope=rr, kv_scale=rs)
+    else:
+        want, _ = orc.sparse_mla(wl.q, wl.kv, wl.page_table, wl.cu_q, idx, wl.scale, wl.page_size)
+    np.testing.assert_allclose(out.float().cpu().numpy(), want, atol=2e-2, rtol=1e-2, err_msg=f"{case} vs oracle")
 
 
 def test_static_rejects_requests_beyond_its_scratch():
