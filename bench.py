@@ -230,6 +230,7 @@ def measure_workload(name, args, dev, world, rank, steps, warmup, seed):
     fp8 = name.endswith("fp8")
     kv_fmt = "fp8_tile128" if args.kv_scales == "tile128" else "fp8_rowscale"
     row_b = 512 + 128 + (16 if kv_fmt == "fp8_tile128" else 4)   # e4m3 latent + bf16 rope + fp32 scales
+    use_graph = name == "decode_b1_n2048"
     if name == "decode_b1_n2048":
         H, K, ps = 16, 256, 2048
         chunks = [(np.array([2048], np.int32), np.array([1], np.int32))]
@@ -293,7 +294,7 @@ def measure_workload(name, args, dev, world, rank, steps, warmup, seed):
     stream = torch.cuda.current_stream(dev)
     launches = 0
 
-    def step(st, ev=None):
+    def step(st, ev=None, part="both"):
         nonlocal launches
         n = 0
         for c in plan:
@@ -301,7 +302,9 @@ def measure_workload(name, args, dev, world, rank, steps, warmup, seed):
             if ev is not None:
                 ev[0].append(torch.cuda.Event(enable_timing=True))
                 ev[0][-1].record(stream)
-            if fp8:
+            if part == "mla":
+                pass
+            elif fp8:
                 d.dsa_quant_mxfp8(st["q_idx"][r0:r0 + T], q=st["qi8"][r0:r0 + T], scales=st["qi_sc"][r0:r0 + T])
                 d.dsa_index_topk(st["qi8"][r0:r0 + T], st["head_w"][r0:r0 + T], st["k_idx"], c["pt"], c["sl"],
                                  c["cq"], K, indices=idx[:T], workspace=ws, q_idx_scale=st["qi_sc"][r0:r0 + T],
@@ -314,14 +317,17 @@ def measure_workload(name, args, dev, world, rank, steps, warmup, seed):
             if ev is not None:
                 ev[1].append(torch.cuda.Event(enable_timing=True))
                 ev[1][-1].record(stream)
-            if fp8:
+            if part == "index":
+                pass
+            elif fp8:
                 d.dsa_sparse_mla(st["q"][r0:r0 + T], st["kv"], c["pt"], c["sl"], c["cq"], idx[:T], scale,
                                  out=out[r0:r0 + T], workspace=ws, kv_rope=st["rope"], kv_scale=st["rsc"],
                                  dtype=kv_fmt)
+                n += 1 + (1 if d.sparse_mla_workspace_size(T, H, K) > 256 else 0)
             else:
                 d.dsa_sparse_mla(st["q"][r0:r0 + T], st["kv"], c["pt"], c["sl"], c["cq"], idx[:T], scale,
                                  out=out[r0:r0 + T], workspace=ws)
-            n += 1 + (1 if d.sparse_mla_workspace_size(T, H, K) > 256 else 0)
+                n += 1 + (1 if d.sparse_mla_workspace_size(T, H, K) > 256 else 0)
             if ev is not None:
                 ev[2].append(torch.cuda.Event(enable_timing=True))
                 ev[2][-1].record(stream)
@@ -335,31 +341,70 @@ def measure_workload(name, args, dev, world, rank, steps, warmup, seed):
     torch.cuda.synchronize(dev)
     if world > 1:
         torch.distributed.barrier()
-    # whole steps, events only around each step (the kernels of a step
-    # overlap through programmatic dependent launch as in use) ...
-    s_ev = []
-    for i in range(steps):
-        e = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-        e[0].record(stream)
-        step(sets[(warmup + i) % copies])
-        e[1].record(stream)
-        s_ev.append(e)
-    torch.cuda.synchronize(dev)
-    # ... then the same steps with an event between the calls, for the
-    # per-kernel times (that event stops the overlap)
-    evs = []
-    for i in range(steps):
-        ev = ([], [], [])
-        step(sets[(warmup + i) % copies], ev)
-        evs.append(ev)
-    torch.cuda.synchronize(dev)
-    if world > 1:
-        torch.distributed.barrier()
+    timing = "CUDA events on the launching stream around each step; per-kernel times from a second pass with an " \
+             "event between the calls"
+    if use_graph:
+        # A step of about 1 MB takes microseconds on the GPU, less than the
+        # host needs to issue its calls: eagerly issued steps would time the
+        # host.  The steps (each on its own input copy) are captured once in
+        # a CUDA graph -- whole steps, the indexer calls alone, the attention
+        # calls alone -- and each graph is replayed and timed as a whole.
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        graphs = {}
+        for part in ("both", "index", "mla"):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=side):
+                for i in range(steps):
+                    step(sets[(warmup + i) % copies], part=part)
+            graphs[part] = g
+        stream.wait_stream(side)
+        for g in graphs.values():
+            g.replay()
+        torch.cuda.synchronize(dev)
+
+        def replay_time(g):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            return e0.elapsed_time(e1) * 1e-3 / steps
+
+        t_step = max_over_ranks([replay_time(graphs["both"])], dev)[0]
+        t_idx, t_mla = replay_time(graphs["index"]), replay_time(graphs["mla"])
+        step(sets[0])  # the launch count of one whole step
+        torch.cuda.synchronize(dev)
+        timing = (f"one CUDA graph of {steps} steps (each on its own input copy) replayed and timed with CUDA events; "
+                  f"per-kernel times from graphs of the indexer calls alone and of the attention calls alone")
+        if world > 1:
+            torch.distributed.barrier()
+    else:
+        # whole steps, events only around each step (the kernels of a step
+        # overlap through programmatic dependent launch as in use) ...
+        s_ev = []
+        for i in range(steps):
+            e = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            e[0].record(stream)
+            step(sets[(warmup + i) % copies])
+            e[1].record(stream)
+            s_ev.append(e)
+        torch.cuda.synchronize(dev)
+        # ... then the same steps with an event between the calls, for the
+        # per-kernel times (that event stops the overlap)
+        evs = []
+        for i in range(steps):
+            ev = ([], [], [])
+            step(sets[(warmup + i) % copies], ev)
+            evs.append(ev)
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            torch.distributed.barrier()
+        t_step = max_over_ranks([sum(a.elapsed_time(b) for a, b in s_ev) * 1e-3 / steps], dev)[0]
+        t_idx = sum(a.elapsed_time(b) for ev in evs for a, b in zip(ev[0], ev[1])) * 1e-3 / steps
+        t_mla = sum(a.elapsed_time(b) for ev in evs for a, b in zip(ev[1], ev[2])) * 1e-3 / steps
     clk = clocks.stop()
     ws.check()
-    t_step = max_over_ranks([sum(a.elapsed_time(b) for a, b in s_ev) * 1e-3 / steps], dev)[0]
-    t_idx = sum(a.elapsed_time(b) for ev in evs for a, b in zip(ev[0], ev[1])) * 1e-3 / steps
-    t_mla = sum(a.elapsed_time(b) for ev in evs for a, b in zip(ev[1], ev[2])) * 1e-3 / steps
 
     # algorithmic bytes and flops
     sel_all, idx_bytes, mla_b, n_hist = [], 0.0, 0.0, 0.0
@@ -390,7 +435,8 @@ def measure_workload(name, args, dev, world, rank, steps, warmup, seed):
                        "kv_cache": kv_fmt if fp8 else "bf16",
                        "parallelism": f"replicas{max(world, 1)}",
                        "l2": (f"inputs larger than L2: {copies} alternating cop{'ies' if copies > 1 else 'y'} of "
-                              f"every step input ({in_bytes / 2**30:.3f} GiB each), no flush")},
+                              f"every step input ({in_bytes / 2**30:.3f} GiB each), no flush"),
+                       "timing": timing},
             "kernels": {"indexer_topk": {"seconds_per_step": t_idx, "algorithmic_bytes": idx_bytes,
                                          "achieved_gbs": idx_bytes / t_idx / 1e9, "flops": f_idx,
                                          "achieved_tflops": f_idx / t_idx / 1e12},

@@ -40,7 +40,8 @@
  *    chunk: the chunk's tokens are the last positions of the cached sequence.
  *  - Workspace: caller-owned device memory of at least the bytes reported by
  *    the matching *_workspace_size() call.  Its first 16 bytes hold a sticky
- *    device error word: call dsa_workspace_init() once after allocating it.
+ *    device error word (and the wait limit of dsa_workspace_set_wait_limit):
+ *    call dsa_workspace_init() once after allocating it.
  *    Kernels OR error bits into it; dsa_get_error() reads and clears it.
  *  - Return value: DSA_OK if the work was enqueued.  Argument problems found
  *    on the host return DSA_ERR_INVALID_ARG / DSA_ERR_UNSUPPORTED before any
@@ -130,6 +131,17 @@ dsa_status dsa_workspace_init(void *workspace, size_t workspace_bytes, void *str
 /* Synchronise `stream`, read the workspace's device error word, clear it and
  * return the first error it records (DSA_OK if none).  Not for the hot path. */
 dsa_status dsa_get_error(void *workspace, void *stream);
+
+/* Test hook for the failure path (the source pages have no counterpart).
+ * Every pipeline wait inside the kernels gives up after 200 ms, records
+ * DSA_ERR_TIMEOUT in the workspace's error word, and the kernel then drains
+ * its own copies and tensor-core work, frees its tensor memory and returns.
+ * This call (enqueued on `stream`) makes the kernels that use this workspace
+ * give up after `microseconds` instead, so that a test can make the waits run
+ * out on purpose; 0 restores the 200 ms default.  The setting lives in the
+ * workspace (word 2 of its error block): dsa_workspace_init resets it,
+ * dsa_get_error does not. */
+dsa_status dsa_workspace_set_wait_limit(void *workspace, uint32_t microseconds, void *stream);
 
 /* ---------------------------------------------------------------- indexer */
 

@@ -26,7 +26,7 @@ KV_DTYPES = {"bf16": 0, "fp8_rowscale": 1, "fp8_tile128": 2}
 
 # Every symbol include/dsa.h declares.
 EXPORTS = ("dsa_status_string", "dsa_set_tuning", "dsa_index_topk_workspace_size", "dsa_sparse_mla_workspace_size",
-           "dsa_workspace_init", "dsa_get_error", "dsa_index_topk", "dsa_index_scores", "dsa_topk_from_scores",
+           "dsa_workspace_init", "dsa_get_error", "dsa_workspace_set_wait_limit", "dsa_index_topk", "dsa_index_scores", "dsa_topk_from_scores",
            "dsa_sparse_mla", "dsa_sparse_mla_static", "dsa_quant_mxfp8", "dsa_quant_fp8_rows",
            "dsa_quant_fp8_tiles", "dsa_cache_append")
 
@@ -67,6 +67,8 @@ def load(build_if_missing: bool = True):
         lib.dsa_workspace_init.restype = c_int
         lib.dsa_get_error.argtypes = [P, P]
         lib.dsa_get_error.restype = c_int
+        lib.dsa_workspace_set_wait_limit.argtypes = [P, ctypes.c_uint32, P]
+        lib.dsa_workspace_set_wait_limit.restype = c_int
         idx_args = [P, P, P, P, P, i64, P, i32, P, P, i32, i32, i32, i32, c_int, P]
         lib.dsa_index_topk.argtypes = idx_args + [P, sz, P]
         lib.dsa_index_topk.restype = c_int
@@ -139,6 +141,12 @@ class Workspace:
         if nbytes > self.nbytes:
             self.__init__(nbytes, self.buf.device, stream)
         return self
+
+    def set_wait_limit(self, microseconds: int, stream=None) -> None:
+        """Test hook: kernels using this workspace give up a pipeline wait
+        after `microseconds` (0: the 200 ms default) and report a timeout."""
+        _check("dsa_workspace_set_wait_limit",
+               load().dsa_workspace_set_wait_limit(_ptr(self.buf), int(microseconds), _stream(stream)))
 
     def check(self, stream=None) -> None:
         """Synchronise and raise if a kernel recorded a device-side error."""

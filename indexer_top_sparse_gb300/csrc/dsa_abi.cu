@@ -295,6 +295,8 @@ bool mla_dsplit(int T, int H, bool fp8, int splits) {
 }
 size_t mla_sk_workspace(int ctas) { return kErrBytes + (size_t)2 * ctas * 64 * (512 + 2) * sizeof(float); }
 
+__global__ void set_word_kernel(uint32_t *word, uint32_t value) { *word = value; }
+
 dsa_status cuda_status(cudaError_t e) {
     if (e == cudaSuccess) return DSA_OK;
     fprintf(stderr, "[dsa] CUDA error: %s\n", cudaGetErrorString(e));
@@ -438,6 +440,14 @@ size_t dsa_sparse_mla_workspace_size(int32_t T, int32_t H, int32_t K) {
 dsa_status dsa_workspace_init(void *workspace, size_t workspace_bytes, void *stream) {
     if (!workspace || workspace_bytes < kErrBytes) return DSA_ERR_INVALID_ARG;
     return cuda_status(cudaMemsetAsync(workspace, 0, kErrBytes, static_cast<cudaStream_t>(stream)));
+}
+
+dsa_status dsa_workspace_set_wait_limit(void *workspace, uint32_t microseconds, void *stream) {
+    if (!workspace || !aligned16(workspace)) return DSA_ERR_INVALID_ARG;
+    // one 4-byte write of word 2 of the error block, ordered on the stream
+    set_word_kernel<<<1, 1, 0, static_cast<cudaStream_t>(stream)>>>(static_cast<uint32_t *>(workspace) + 2,
+                                                                       microseconds);
+    return cuda_status(cudaGetLastError());
 }
 
 dsa_status dsa_get_error(void *workspace, void *stream) {

@@ -309,6 +309,14 @@ __device__ void cluster_topk(const uint32_t *keys, int n_local, int pos0, int n_
             for (int c = 0; c < kMaxCluster; ++c) s += v[c];
             ss.tot[d] = s;
         }
+        // digit 0, nothing above it, unless a lane below finds the digit that
+        // holds the krem-th key: after an aborted wait the counts may add up
+        // to fewer than krem keys, and every CTA must still take the same
+        // (deterministic) branch, since the cluster barriers follow from it
+        if (tid == 0) {
+            ss.bcast[0] = 0u;
+            ss.bcast[1] = 0u;
+        }
         __syncthreads();
         if (tid < 32) {
             // digits from high to low: lane L owns digits 255-8L .. 248-8L

@@ -11,7 +11,8 @@ namespace dsa {
 
 // ---------------------------------------------------------------- error word
 // Layout of the first 16 bytes of every workspace: word 0 = OR of (1 << status)
-// bits, word 1 = where the first timeout happened (kernel-specific code).
+// bits, word 1 = where the first timeout happened (kernel-specific code),
+// word 2 = pipeline wait limit in microseconds (0: the default).
 enum : uint32_t {
     kErrBadLen = 1u << 1,
     kErrBadPage = 1u << 4,
@@ -33,6 +34,17 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 
 // A pipeline wait gives up after this long (the kernels take microseconds).
 constexpr uint64_t kWaitLimitNs = 200ull * 1000ull * 1000ull;  // 200 ms
+
+// Word 2 of the error block, when nonzero, replaces kWaitLimitNs with that
+// many microseconds (set by dsa_workspace_set_wait_limit, to test the
+// give-up path); waits without an error word use the default.
+__device__ __forceinline__ uint64_t wait_limit_ns(const uint32_t *err) {
+    if (err != nullptr) {
+        const uint32_t us = *reinterpret_cast<const volatile uint32_t *>(err + 2);
+        if (us != 0u) return (uint64_t)us * 1000ull;
+    }
+    return kWaitLimitNs;
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -86,12 +98,12 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32
                                           volatile int *abort) {
     auto try_wait = [&]() { return kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
     if (try_wait()) return true;
-    uint64_t t0 = globaltimer_ns();
+    const uint64_t t0 = globaltimer_ns(), limit = wait_limit_ns(err);
     for (uint32_t it = 0;; ++it) {
         if (try_wait()) return true;
         if ((it & 63) == 63) {
             if (*abort) return false;
-            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            if (globaltimer_ns() - t0 > limit) {
                 report_error(err, kErrTimeout, where);
                 *abort = 1;
                 return false;
