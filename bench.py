@@ -267,14 +267,12 @@ def measure_workload(name, args, dev, world, rank, steps, warmup, seed):
             st["k_idx"], st["k_sc"] = d.dsa_quant_mxfp8(k_bf)
             quant = d.dsa_quant_fp8_tiles if kv_fmt == "fp8_tile128" else d.dsa_quant_fp8_rows
             st["kv"], st["rope"], st["rsc"] = quant(kv_bf)
-            st["qi8"] = torch.empty((T_all, 64, 128), dtype=torch.uint8, device=dev)
-            st["qi_sc"] = torch.empty((T_all, 64, 4), dtype=torch.uint8, device=dev)
         else:
             st["k_idx"], st["kv"] = k_bf, kv_bf
         del k_bf, kv_bf
         sets.append(st)
     torch.cuda.synchronize(dev)
-    in_bytes = sum(v.numel() * v.element_size() for k, v in sets[0].items() if k not in ("qi8", "qi_sc"))
+    in_bytes = sum(v.numel() * v.element_size() for v in sets[0].values())
 
     # per-chunk views and small tensors
     plan = []
@@ -305,11 +303,11 @@ def measure_workload(name, args, dev, world, rank, steps, warmup, seed):
             if part == "mla":
                 pass
             elif fp8:
-                d.dsa_quant_mxfp8(st["q_idx"][r0:r0 + T], q=st["qi8"][r0:r0 + T], scales=st["qi_sc"][r0:r0 + T])
-                d.dsa_index_topk(st["qi8"][r0:r0 + T], st["head_w"][r0:r0 + T], st["k_idx"], c["pt"], c["sl"],
-                                 c["cq"], K, indices=idx[:T], workspace=ws, q_idx_scale=st["qi_sc"][r0:r0 + T],
-                                 k_idx_scale=st["k_sc"], dtype="mxfp8")
-                n += 2
+                # MXFP8 keys; the bf16 index query is quantised inside the indexer
+                d.dsa_index_topk(st["q_idx"][r0:r0 + T], st["head_w"][r0:r0 + T], st["k_idx"], c["pt"], c["sl"],
+                                 c["cq"], K, indices=idx[:T], workspace=ws, k_idx_scale=st["k_sc"],
+                                 dtype="mxfp8_qbf16")
+                n += 1
             else:
                 d.dsa_index_topk(st["q_idx"][r0:r0 + T], st["head_w"][r0:r0 + T], st["k_idx"], c["pt"], c["sl"],
                                  c["cq"], K, indices=idx[:T], workspace=ws)
@@ -417,8 +415,7 @@ def measure_workload(name, args, dev, world, rank, steps, warmup, seed):
             sel_all.append(sel)
             n_hist += float(n.sum())
             key_b = 132 if fp8 else 256
-            idx_bytes += float(np.sum(n * key_b + 64 * 128 * (1 if fp8 else 2) + (256 if fp8 else 0) + 256 + 4 * K
-                                      + 4 * np.ceil(n / ps)))
+            idx_bytes += float(np.sum(n * key_b + 64 * 128 * 2 + 256 + 4 * K + 4 * np.ceil(n / ps)))
             mla_b += float(np.sum(sel * (row_b if fp8 else 1152) + H * 1152 + H * 1024 + 4 * K + 4 * np.ceil(n / ps)))
     sel_all = np.concatenate(sel_all)
     f_mla = attention_flops(sel_all, H)

@@ -72,8 +72,13 @@ typedef enum {
 
 /* Index-path element type, shared by q_idx and k_idx.  MXFP8 is E4M3 with one
  * E8M0 scale byte per 32 consecutive elements ("Day-0 Inference Adaptation and
- * Optimization for Hybrid Attention Architectures", §4 Optimization 2). */
-typedef enum { DSA_IDX_BF16 = 0, DSA_IDX_MXFP8 = 1 } dsa_idx_dtype;
+ * Optimization for Hybrid Attention Architectures", §4 Optimization 2).
+ * MXFP8_QBF16: MXFP8 index keys with q_idx passed in bf16; the fused indexer
+ * quantises q_idx itself with dsa_quant_mxfp8's rule (the same codes and
+ * scales, so the same indices), which saves the separate quantisation launch
+ * of the query ("Day-0 Inference Adaptation and Optimization for Hybrid
+ * Attention Architectures", §3 Optimization 1, input preparation). */
+typedef enum { DSA_IDX_BF16 = 0, DSA_IDX_MXFP8 = 1, DSA_IDX_MXFP8_QBF16 = 2 } dsa_idx_dtype;
 
 /* Main KV cache element type.  FP8_ROWSCALE: the 512 latent dims are E4M3 with
  * one fp32 scale per row, the 64 rope dims stay bf16.  FP8_TILE128: the same
@@ -146,11 +151,11 @@ dsa_status dsa_workspace_set_wait_limit(void *workspace, uint32_t microseconds, 
 /* ---------------------------------------------------------------- indexer */
 
 /* Fused indexer + Top-K.
- *   q_idx        [T, 64, 128]  bf16, or e4m3 codes for MXFP8
+ *   q_idx        [T, 64, 128]  bf16 (BF16, MXFP8_QBF16), or e4m3 codes (MXFP8)
  *   q_idx_scale  [T, 64, 4]    e8m0 bytes, 4-byte aligned (MXFP8 only, else NULL)
  *   head_w       [T, 64]       fp32 per-head weights
- *   k_idx_cache  [num_pages, page_size, 128]  bf16, or e4m3 codes for MXFP8
- *   k_idx_scale  [num_pages, page_size, 4]    e8m0 bytes, 16-byte aligned (MXFP8 only)
+ *   k_idx_cache  [num_pages, page_size, 128]  bf16, or e4m3 codes (MXFP8, MXFP8_QBF16)
+ *   k_idx_scale  [num_pages, page_size, 4]    e8m0 bytes, 16-byte aligned (MXFP8, MXFP8_QBF16)
  *   page_table   [B, max_pages_per_seq] int32; seq_lens [B]; cu_q [B+1] int32
  *   indices      [T, K] int32 OUT: for every query row, the min(K, pos(t)+1)
  *                positions with the highest scores (ties: lower position

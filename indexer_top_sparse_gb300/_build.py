@@ -13,7 +13,7 @@ SRC = os.path.join(PKG, "csrc")
 OUT = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT, "libdsa.so")
 SOURCES = ["dsa_abi.cu", "indexer_topk.cu", "sparse_mla.cu", "sparse_mla_ds.cu", "mla_static.cu", "quant.cu"]
-HEADERS = ["ptx.cuh", "kernels.h"]
+HEADERS = ["ptx.cuh", "kernels.h", "mxfp8.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

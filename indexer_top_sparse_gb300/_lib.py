@@ -21,7 +21,7 @@ _lib = None
 DSA_OK = 0
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "CUDA error", 4: "page id out of range",
           5: "selected index out of range", 6: "device wait timed out"}
-IDX_DTYPES = {"bf16": 0, "mxfp8": 1}
+IDX_DTYPES = {"bf16": 0, "mxfp8": 1, "mxfp8_qbf16": 2}
 KV_DTYPES = {"bf16": 0, "fp8_rowscale": 1, "fp8_tile128": 2}
 
 # Every symbol include/dsa.h declares.
@@ -165,14 +165,14 @@ def _index_call(scores_ld, q_idx, head_w, k_idx_cache, page_table, seq_lens, cu_
                 workspace, q_idx_scale, k_idx_scale, dtype, stream):
     lib = load()
     dt = IDX_DTYPES[dtype]
-    elt = torch.bfloat16 if dt == 0 else torch.uint8
+    elt = torch.uint8 if dt == 1 else torch.bfloat16
     _need(q_idx, "q_idx", elt, 3)
     dev = q_idx.device
     T = q_idx.shape[0]
     if tuple(q_idx.shape[1:]) != (64, 128):
         raise ValueError("q_idx must be [T, 64, 128]")
     _need(head_w, "head_w", torch.float32, 2, dev)
-    _need(k_idx_cache, "k_idx_cache", elt, 3, dev)
+    _need(k_idx_cache, "k_idx_cache", torch.bfloat16 if dt == 0 else torch.uint8, 3, dev)
     if k_idx_cache.shape[2] != 128:
         raise ValueError("k_idx_cache must be [pages, page_size, 128]")
     _need(page_table, "page_table", torch.int32, 2, dev)
@@ -188,8 +188,14 @@ def _index_call(scores_ld, q_idx, head_w, k_idx_cache, page_table, seq_lens, cu_
         _need(k_idx_scale, "k_idx_scale", torch.uint8, 3, dev)
         if tuple(q_idx_scale.shape) != (T, 64, 4) or tuple(k_idx_scale.shape) != (P, ps, 4):
             raise ValueError("MXFP8 scales must be q_idx_scale [T, 64, 4] and k_idx_scale [pages, page_size, 4]")
+    elif dt == 2:
+        if q_idx_scale is not None:
+            raise ValueError("dtype='mxfp8_qbf16' takes q_idx in bf16 and no q_idx_scale")
+        _need(k_idx_scale, "k_idx_scale", torch.uint8, 3, dev)
+        if tuple(k_idx_scale.shape) != (P, ps, 4):
+            raise ValueError("k_idx_scale must be [pages, page_size, 4]")
     elif q_idx_scale is not None or k_idx_scale is not None:
-        raise ValueError("q_idx_scale / k_idx_scale are for dtype='mxfp8' only")
+        raise ValueError("q_idx_scale / k_idx_scale are for the MXFP8 dtypes only")
     if indices is None:
         indices = torch.empty((T, K), dtype=torch.int32, device=dev)
     _need(indices, "indices", torch.int32, 2, dev)

@@ -314,25 +314,30 @@ dsa_status index_common(const void *q_idx, const uint8_t *q_idx_scale, const flo
     if (!aligned16(q_idx) || !aligned16(k_idx_cache) || !aligned16(workspace)) return DSA_ERR_INVALID_ARG;
     if (workspace_bytes < dsa_index_topk_workspace_size(B, T, K, max_pages_per_seq, page_size))
         return DSA_ERR_INVALID_ARG;
-    if (dtype != DSA_IDX_BF16 && dtype != DSA_IDX_MXFP8) return DSA_ERR_UNSUPPORTED;
+    if (dtype != DSA_IDX_BF16 && dtype != DSA_IDX_MXFP8 && dtype != DSA_IDX_MXFP8_QBF16) return DSA_ERR_UNSUPPORTED;
     if (dtype == DSA_IDX_MXFP8 && (!q_idx_scale || !k_idx_scale || !aligned16(k_idx_scale) ||
                                    (reinterpret_cast<uintptr_t>(q_idx_scale) & 3u)))
+        return DSA_ERR_INVALID_ARG;
+    if (dtype == DSA_IDX_MXFP8_QBF16 && (q_idx_scale || !k_idx_scale || !aligned16(k_idx_scale)))
         return DSA_ERR_INVALID_ARG;
     if (page_size % 64 != 0) return DSA_ERR_UNSUPPORTED;
     if (T == 0) return DSA_OK;
     const long long max_len = (long long)max_pages_per_seq * page_size;
     if (max_len > (1LL << 30) || (long long)num_pages * page_size > (1LL << 31)) return DSA_ERR_UNSUPPORTED;
-    if (dtype == DSA_IDX_MXFP8) {
+    if (dtype == DSA_IDX_MXFP8 || dtype == DSA_IDX_MXFP8_QBF16) {
+        const bool quant_q = dtype == DSA_IDX_MXFP8_QBF16;
         int C = 1, stages = 2, tiles_cap = 1;
         size_t smem = 0;
         if (T > 65535 || !plan_indexer_mxfp8(T, (int)max_len, &C, &stages, &tiles_cap, &smem))
             return DSA_ERR_UNSUPPORTED;
         CUtensorMap tk, tq;
         if (!encode_rows128_u8(&tk, k_idx_cache, (uint64_t)num_pages * page_size)) return DSA_ERR_CUDA;
-        if (!encode_rows128_u8(&tq, q_idx, (uint64_t)T * 64)) return DSA_ERR_CUDA;
+        if (quant_q) tq = tk;  // unused: the kernel reads the bf16 query itself
+        else if (!encode_rows128_u8(&tq, q_idx, (uint64_t)T * 64)) return DSA_ERR_CUDA;
         IndexerArgs a{};
         a.head_w = head_w;
-        a.q_scale = q_idx_scale;
+        a.q_scale = quant_q ? nullptr : q_idx_scale;
+        a.q_bf16 = quant_q ? static_cast<const uint16_t *>(q_idx) : nullptr;
         a.k_scale = k_idx_scale;
         a.page_table = page_table;
         a.seq_lens = seq_lens;
@@ -349,7 +354,7 @@ dsa_status index_common(const void *q_idx, const uint8_t *q_idx_scale, const flo
         a.page_size = page_size;
         a.stages = stages;
         a.tiles_cap = tiles_cap;
-        return cuda_status(dsa::launch_indexer_mxfp8(tk, tq, a, C, smem, scores != nullptr,
+        return cuda_status(dsa::launch_indexer_mxfp8(tk, tq, a, C, smem, scores != nullptr, quant_q,
                                                      static_cast<cudaStream_t>(stream)));
     }
     IdxPlan plan;

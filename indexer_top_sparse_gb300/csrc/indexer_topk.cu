@@ -29,6 +29,7 @@
 
 #include "ptx.cuh"
 #include "kernels.h"
+#include "mxfp8.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -751,7 +752,11 @@ struct __align__(16) F8Bars {
 constexpr int kF8Bufs = 4;
 constexpr uint32_t kF8AccCols = kHI, kF8SfQ = kF8Bufs * kHI, kF8SfK = kF8SfQ + 4;
 
-template <bool kWriteScores>
+// kQuantQ: the query arrives in bf16 and is quantised here, by the scale
+// warps, with the standalone quantiser's rule (mxfp8.cuh): codes into the
+// query tile in the layout TMA would have written, scales into TMEM.  One
+// launch fewer per step than quantising it beforehand.
+template <bool kWriteScores, bool kQuantQ>
 __global__ void __launch_bounds__(kF8Threads, 1)
     indexer_topk_mxfp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
                               IndexerArgs a) {
@@ -825,9 +830,11 @@ __global__ void __launch_bounds__(kF8Threads, 1)
     if (warp == 0) {
         if (lane == 0) {
             tma_prefetch_desc(&tm_k);
-            tma_prefetch_desc(&tm_q);
-            mbar_arrive_expect_tx(&bars->qbar, (uint32_t)(kHI * kDI));
-            tma_load_2d(sQ, &tm_q, &bars->qbar, 0, t0 * kHI);
+            if constexpr (!kQuantQ) {
+                tma_prefetch_desc(&tm_q);
+                mbar_arrive_expect_tx(&bars->qbar, (uint32_t)(kHI * kDI));
+                tma_load_2d(sQ, &tm_q, &bars->qbar, 0, t0 * kHI);
+            }
             int issued = 0;
             for (int i = 0; i < n_tiles; ++i) {
                 const int s = i % a.stages;
@@ -921,13 +928,50 @@ __global__ void __launch_bounds__(kF8Threads, 1)
         // column base + r / 32, group g in byte g.
         const int quad = warp & 3;
         const uint32_t lanes = (uint32_t)(quad * 32) << 16;
+        // the query's scales, [head][group] (one word per head); the selection
+        // block is free scratch until the selection
+        uint32_t *sQS = reinterpret_cast<uint32_t *>(ss);
+        if constexpr (kQuantQ) {
+            // thread i of the four warps: head i / 2, dims 64 (i % 2) .. +63
+            // (two scale groups).  Codes go to the query tile as a TMA box of
+            // 64 rows x 128 bytes with the 128-byte swizzle would place them
+            // (16-byte chunk c of row h at h * 128 + ((c ^ (h % 8)) << 4)).
+            const int i = (warp - 6) * 32 + lane, h = i >> 1, half = i & 1;
+            const uint4 *src = reinterpret_cast<const uint4 *>(a.q_bf16 + ((size_t)t0 * kHI + h) * kDI + 64 * half);
+            uint4 v[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) v[k] = __ldg(src + k);
+            uint32_t sc = 0u;
+#pragma unroll
+            for (int g = 0; g < 2; ++g) {
+                const uint32_t w[16] = {v[4 * g].x,     v[4 * g].y,     v[4 * g].z,     v[4 * g].w,
+                                        v[4 * g + 1].x, v[4 * g + 1].y, v[4 * g + 1].z, v[4 * g + 1].w,
+                                        v[4 * g + 2].x, v[4 * g + 2].y, v[4 * g + 2].z, v[4 * g + 2].w,
+                                        v[4 * g + 3].x, v[4 * g + 3].y, v[4 * g + 3].z, v[4 * g + 3].w};
+                uint32_t out[8];
+                sc |= (uint32_t)mxfp8_block(w, out) << (8 * g);
+                const int c0 = 2 * (2 * half + g);  // first 16-byte chunk of this group in the row
+                uint8_t *row = sQ + h * 128;
+                *reinterpret_cast<uint4 *>(row + ((c0 ^ (h & 7)) << 4)) = make_uint4(out[0], out[1], out[2], out[3]);
+                *reinterpret_cast<uint4 *>(row + (((c0 + 1) ^ (h & 7)) << 4)) = make_uint4(out[4], out[5], out[6], out[7]);
+            }
+            // groups 2 half, 2 half + 1 of head h: bytes 2 half .. 2 half + 1 of its word
+            const uint32_t other = __shfl_xor_sync(0xffffffffu, sc, 1);
+            if (half == 0) sQS[h] = sc | (other << 16);
+            fence_proxy_async_smem();  // the codes are read by the tensor cores
+            bar_sync(3, 128);          // the four scale warps
+            if (threadIdx.x == 6 * 32) mbar_arrive(&bars->qbar);
+        }
         if (n_tiles > 0) {
             uint32_t w[4];  // the query's scales, input layout [head][group]; heads >= 64 unused
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 const int h = lane + 32 * c;
-                w[c] = h < kHI ? __ldg(reinterpret_cast<const uint32_t *>(a.q_scale + ((size_t)t0 * kHI + h) * 4))
-                               : 0x7F7F7F7Fu;
+                if constexpr (kQuantQ)
+                    w[c] = h < kHI ? sQS[h] : 0x7F7F7F7Fu;
+                else
+                    w[c] = h < kHI ? __ldg(reinterpret_cast<const uint32_t *>(a.q_scale + ((size_t)t0 * kHI + h) * 4))
+                                   : 0x7F7F7F7Fu;
             }
             tmem_st4(tmem + lanes + kF8SfQ, w);
         }
@@ -1019,10 +1063,10 @@ size_t indexer_mxfp8_smem_bytes(int stages, int tiles_cap) {
            sizeof(SelectSmem) + sizeof(F8Bars);
 }
 
-template <bool W>
+template <bool W, bool Q>
 static cudaError_t launch_f8(const CUtensorMap &tk, const CUtensorMap &tq, const IndexerArgs &a, int C, size_t smem,
                              cudaStream_t st) {
-    auto kern = indexer_topk_mxfp8_kernel<W>;
+    auto kern = indexer_topk_mxfp8_kernel<W, Q>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     if (C > 8) {
@@ -1047,12 +1091,16 @@ static cudaError_t launch_f8(const CUtensorMap &tk, const CUtensorMap &tq, const
 }
 
 cudaError_t launch_indexer_mxfp8(const CUtensorMap &tm_k, const CUtensorMap &tm_q, const IndexerArgs &a, int C,
-                                 size_t smem, bool write_scores, cudaStream_t st) {
-    return write_scores ? launch_f8<true>(tm_k, tm_q, a, C, smem, st) : launch_f8<false>(tm_k, tm_q, a, C, smem, st);
+                                 size_t smem, bool write_scores, bool quant_q, cudaStream_t st) {
+    if (quant_q)
+        return write_scores ? launch_f8<true, true>(tm_k, tm_q, a, C, smem, st)
+                            : launch_f8<false, true>(tm_k, tm_q, a, C, smem, st);
+    return write_scores ? launch_f8<true, false>(tm_k, tm_q, a, C, smem, st)
+                        : launch_f8<false, false>(tm_k, tm_q, a, C, smem, st);
 }
 
 int indexer_mxfp8_max_active_clusters(int C, size_t smem) {
-    auto kern = indexer_topk_mxfp8_kernel<false>;
+    auto kern = indexer_topk_mxfp8_kernel<false, false>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return 0;
     if (C > 8 && cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
         return 0;

@@ -13,6 +13,7 @@ namespace dsa {
 struct IndexerArgs {
     const float *head_w;        // [T, 64]
     const uint8_t *q_scale;     // MXFP8: [T, 64, 4] e8m0
+    const uint16_t *q_bf16;     // MXFP8 with the query quantised in the kernel: [T, 64, 128] bf16
     const uint8_t *k_scale;     // MXFP8: [rows, 4] e8m0
     const int32_t *page_table;  // [B, max_pages]
     const int32_t *seq_lens;    // [B]
@@ -47,8 +48,11 @@ cudaError_t launch_topk_from_scores(const TopkArgs &a, int C, size_t smem, cudaS
 int indexer_max_active_clusters(int G, int C, size_t smem);
 // MXFP8 variant (one query row per cluster).
 size_t indexer_mxfp8_smem_bytes(int stages, int tiles_cap);
+// quant_q: q_idx arrives in bf16 (a.q_bf16) and the kernel quantises it to
+// MXFP8 itself (tm_q unused); otherwise tm_q maps the E4M3 codes and
+// a.q_scale holds their scales.
 cudaError_t launch_indexer_mxfp8(const CUtensorMap &tm_k, const CUtensorMap &tm_q, const IndexerArgs &a, int C,
-                                 size_t smem, bool write_scores, cudaStream_t st);
+                                 size_t smem, bool write_scores, bool quant_q, cudaStream_t st);
 int indexer_mxfp8_max_active_clusters(int C, size_t smem);
 
 // Sparse MLA (sparse_mla.cu).

@@ -99,9 +99,12 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32
     auto try_wait = [&]() { return kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
     if (try_wait()) return true;
     const uint64_t t0 = globaltimer_ns(), limit = wait_limit_ns(err);
+    // the clock is read every 64 polls, or on every poll under a shortened
+    // limit (a poll may itself suspend the thread for a while)
+    const uint32_t every = limit < kWaitLimitNs ? 0u : 63u;
     for (uint32_t it = 0;; ++it) {
         if (try_wait()) return true;
-        if ((it & 63) == 63) {
+        if ((it & every) == every) {
             if (*abort) return false;
             if (globaltimer_ns() - t0 > limit) {
                 report_error(err, kErrTimeout, where);

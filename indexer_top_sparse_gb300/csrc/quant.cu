@@ -13,25 +13,12 @@
 #include <cuda_fp8.h>
 
 #include "kernels.h"
+#include "mxfp8.cuh"
 #include "ptx.cuh"
 
 namespace dsa {
 
 namespace {
-
-__device__ __forceinline__ float bf16_bits_to_float(uint32_t b) { return __uint_as_float(b << 16); }
-
-__device__ __forceinline__ uint8_t to_e4m3(float v) {
-    return (uint8_t)__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3);
-}
-
-// floor(log2(a)) of a positive finite float, subnormals included.
-__device__ __forceinline__ int floor_log2(float a) {
-    const uint32_t u = __float_as_uint(a);
-    const int e = (int)((u >> 23) & 0xFF);
-    if (e != 0) return e - 127;
-    return (31 - __clz((int)(u & 0x7FFFFF))) - 149;
-}
 
 // One thread per block of 32 values (64 bytes of bf16 in, 32 + 1 bytes out).
 __global__ void quant_mxfp8_kernel(const uint16_t *__restrict__ x, int64_t n_blocks, uint8_t *__restrict__ q,
@@ -48,31 +35,8 @@ __global__ void quant_mxfp8_kernel(const uint16_t *__restrict__ x, int64_t n_blo
         w[4 * i + 2] = v.z;
         w[4 * i + 3] = v.w;
     }
-    float amax = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        amax = fmaxf(amax, fabsf(bf16_bits_to_float(w[i] & 0xFFFFu)));
-        amax = fmaxf(amax, fabsf(bf16_bits_to_float(w[i] >> 16)));
-    }
     uint32_t out[8];
-    if (amax == 0.0f) {
-        e8m0[blk] = 127;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) out[i] = 0u;
-    } else {
-        int X = floor_log2(amax) - 8;
-        X = max(-127, min(127, X));
-        e8m0[blk] = (uint8_t)(X + 127);
-        const float inv = __uint_as_float((uint32_t)(127 - X) << 23);  // 2^-X, exact (X <= 119 for bf16 inputs)
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const uint32_t a = w[2 * i], b = w[2 * i + 1];
-            out[i] = (uint32_t)to_e4m3(bf16_bits_to_float(a & 0xFFFFu) * inv) |
-                     ((uint32_t)to_e4m3(bf16_bits_to_float(a >> 16) * inv) << 8) |
-                     ((uint32_t)to_e4m3(bf16_bits_to_float(b & 0xFFFFu) * inv) << 16) |
-                     ((uint32_t)to_e4m3(bf16_bits_to_float(b >> 16) * inv) << 24);
-        }
-    }
+    e8m0[blk] = mxfp8_block(w, out);
     uint4 *dst = reinterpret_cast<uint4 *>(q + blk * 32);
     dst[0] = make_uint4(out[0], out[1], out[2], out[3]);
     dst[1] = make_uint4(out[4], out[5], out[6], out[7]);

@@ -45,10 +45,10 @@ def _gpu_path(wl, fp8=False, kv_fmt="fp8_rowscale"):
     ws = d.Workspace(max(d.index_topk_workspace_size(wl.B, wl.T, wl.K, wl.max_pages, wl.page_size),
                          d.sparse_mla_workspace_size(wl.T, wl.H, wl.K)))
     if fp8:
-        q_idx, q_sc = d.dsa_quant_mxfp8(dev_bf16(wl.q_idx))
+        # MXFP8 index keys; the bf16 index query is quantised inside the indexer
         k_idx, k_sc = d.dsa_quant_mxfp8(dev_bf16(wl.k_idx))
-        idx = d.dsa_index_topk(q_idx, dev(wl.head_w), k_idx, pt, sl, cq, wl.K, workspace=ws,
-                               q_idx_scale=q_sc, k_idx_scale=k_sc, dtype="mxfp8")
+        idx = d.dsa_index_topk(dev_bf16(wl.q_idx), dev(wl.head_w), k_idx, pt, sl, cq, wl.K, workspace=ws,
+                               k_idx_scale=k_sc, dtype="mxfp8_qbf16")
         del k_idx, k_sc
         quant = d.dsa_quant_fp8_tiles if kv_fmt == "fp8_tile128" else d.dsa_quant_fp8_rows
         nope, rope, rsc = quant(dev_bf16(wl.kv))

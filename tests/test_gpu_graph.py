@@ -3,7 +3,9 @@ no host synchronisation, no pageable copy when the caller passes the outputs
 and the workspace): a decode step captured once and replayed on new inputs
 gives bit for bit what the same calls give eagerly, for the bf16 path and
 for the FP8 path with its Q quantisation (index-Q quantise -> indexer + Top-K
--> sparse MLA -> split combine, chained by programmatic dependent launch).
+-> sparse MLA -> split combine, chained by programmatic dependent launch), and
+for the FP8 path with the index query quantised inside the indexer (one
+launch fewer).
 The replayed step is also checked against the oracle on the new inputs:
 index sets within the near-threshold band, attention (fed the replay's
 indices) within 2e-2 / 1e-2."""
@@ -17,7 +19,7 @@ from indexer_top_sparse_gb300.inputs import make_workload
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("fp8", [False, True])
+@pytest.mark.parametrize("fp8", [False, True, "fused_q"])
 def test_decode_step_replays_in_a_cuda_graph(orc, fp8):
     import indexer_top_sparse_gb300 as d
     wl = make_workload("graph", [3000, 700, 64, 2049], [1, 1, 1, 1], H=128, K=512, page_size=64, seed=77)
@@ -36,7 +38,12 @@ def test_decode_step_replays_in_a_cuda_graph(orc, fp8):
         k_idx, kv = dev_bf16(wl.k_idx), dev_bf16(wl.kv)
 
     def step():
-        if fp8:
+        if fp8 == "fused_q":
+            d.dsa_index_topk(q_idx, head_w, k8, pt, sl, cq, wl.K, indices=idx, workspace=ws, k_idx_scale=ks,
+                             dtype="mxfp8_qbf16")
+            d.dsa_sparse_mla(q, nope, pt, sl, cq, idx, wl.scale, out=out, workspace=ws, kv_rope=rope,
+                             kv_scale=vsc, dtype="fp8_tile128")
+        elif fp8:
             d.dsa_quant_mxfp8(q_idx, q=q8, scales=qs)
             d.dsa_index_topk(q8, head_w, k8, pt, sl, cq, wl.K, indices=idx, workspace=ws, q_idx_scale=qs,
                              k_idx_scale=ks, dtype="mxfp8")

@@ -108,3 +108,29 @@ def test_mxfp8_scales_required():
     with pytest.raises(TypeError):
         d.dsa_index_topk(q, dev(wl.head_w), k, dev(wl.page_table), dev(wl.seq_lens), dev(wl.cu_q), 64,
                          dtype="mxfp8")
+
+
+@pytest.mark.parametrize("lens,nq", [([1, 63, 1000, 2049, 40000], [1, 1, 1, 1, 1]), ([700, 300], [40, 17])])
+def test_mxfp8_query_quantised_in_the_kernel(orc, lens, nq):
+    # dtype "mxfp8_qbf16": q_idx goes in as bf16 and the fused indexer
+    # quantises it itself.  Its codes and scales are the standalone
+    # quantiser's, so scores and indices equal those of the pre-quantised
+    # call bit for bit; they are also checked against the oracle.
+    import indexer_top_sparse_gb300 as d
+    from _util import dev_bf16
+    wl = make_workload("qq", lens, nq, H=16, K=512, page_size=64, seed=51, with_kv=False)
+    q, qs, k, ks = _quantised(orc, wl)
+    idx_ref, sc_ref = _run(wl, q, qs, k, ks, 512)
+    ld = int(wl.seq_lens.max())
+    scores = torch.full((wl.T, ld), float("nan"), dtype=torch.float32, device="cuda")
+    ws = d.Workspace(256)
+    args = (dev_bf16(wl.q_idx), dev(wl.head_w), dev(k), dev(wl.page_table), dev(wl.seq_lens), dev(wl.cu_q), 512)
+    idx, sc = d.dsa_index_scores(*args, scores, k_idx_scale=dev(ks), dtype="mxfp8_qbf16", workspace=ws)
+    ws.check()
+    idx2 = d.dsa_index_topk(*args, k_idx_scale=dev(ks), dtype="mxfp8_qbf16", workspace=ws)
+    ws.check()
+    idx, idx2, sc = idx.cpu().numpy(), idx2.cpu().numpy(), sc.cpu().numpy()
+    assert np.array_equal(idx, idx_ref) and np.array_equal(idx2, idx_ref)
+    fin = ~np.isnan(sc_ref)
+    assert np.array_equal(sc[fin].view(np.uint32), sc_ref[fin].view(np.uint32))
+    _check(orc, wl, 512)
