@@ -428,7 +428,7 @@ struct __align__(16) IdxBars {
     uint64_t tempty[2];
     uint64_t qbar;
     uint32_t tmem_slot;
-    int abort;
+    int abort[2];  // [0] a wait gave up; [1] wait limit in microseconds (0: default)
 };
 
 __device__ __forceinline__ int find_seq(const int32_t *cu_q, int B, int t) {
@@ -561,7 +561,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(&bars->qbar, 1);
         mbar_init(&bars->drain, 1);
-        bars->abort = 0;
+        bars->abort[0] = 0;
+        bars->abort[1] = wait_limit_us(a.err);
         fence_mbar_init();
     }
     for (int i = threadIdx.x; i < G * kHI; i += kThreads) {
@@ -586,7 +587,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars->tmem_slot;
-    volatile int *abort = &bars->abort;
+    volatile int *abort = bars->abort;
 
     if (warp == 0) {
         if (lane == 0) {
@@ -620,10 +621,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (*abort) {
                 // let copies still in flight land before shared memory is released
-                volatile int no_abort = 0;
-                mbar_wait(&bars->qbar, 0, nullptr, 0, &no_abort);
+                volatile int no_abort[2] = {0, 0};
+                mbar_wait(&bars->qbar, 0, nullptr, 0, no_abort);
                 for (int i = max(0, issued - a.stages); i < issued; ++i)
-                    mbar_wait(&bars->full[i % a.stages], (i / a.stages) & 1, nullptr, 0, &no_abort);
+                    mbar_wait(&bars->full[i % a.stages], (i / a.stages) & 1, nullptr, 0, no_abort);
             }
         }
     } else if (warp == 1) {
@@ -651,9 +652,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (*abort) {
                 // wait for every issued MMA before TMEM is released
-                volatile int no_abort = 0;
+                volatile int no_abort[2] = {0, 0};
                 mma_commit(&bars->drain);
-                mbar_wait(&bars->drain, 0, nullptr, 0, &no_abort);
+                mbar_wait(&bars->drain, 0, nullptr, 0, no_abort);
             }
         }
     } else {
@@ -744,7 +745,7 @@ struct __align__(16) F8Bars {
     uint64_t qbar;
     uint64_t drain;
     uint32_t tmem_slot;
-    int abort;
+    int abort[2];  // [0] a wait gave up; [1] wait limit in microseconds (0: default)
 };
 // TMEM columns of the MXFP8 kernel: kF8Bufs accumulators of 64 heads, the
 // query's scales, kF8Bufs key scale buffers (4-aligned).  Four of each keep the
@@ -805,7 +806,8 @@ __global__ void __launch_bounds__(kF8Threads, 1)
         }
         mbar_init(&bars->qbar, 1);
         mbar_init(&bars->drain, 1);
-        bars->abort = 0;
+        bars->abort[0] = 0;
+        bars->abort[1] = wait_limit_us(a.err);
         fence_mbar_init();
     }
     for (int i = threadIdx.x; i < kHI; i += kF8Threads) sW[i] = __ldg(a.head_w + (size_t)t0 * kHI + i);
@@ -825,7 +827,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars->tmem_slot;
-    volatile int *abort = &bars->abort;
+    volatile int *abort = bars->abort;
 
     if (warp == 0) {
         if (lane == 0) {
@@ -852,10 +854,10 @@ __global__ void __launch_bounds__(kF8Threads, 1)
                 }
             }
             if (*abort) {
-                volatile int no_abort = 0;
-                mbar_wait(&bars->qbar, 0, nullptr, 0, &no_abort);
+                volatile int no_abort[2] = {0, 0};
+                mbar_wait(&bars->qbar, 0, nullptr, 0, no_abort);
                 for (int i = max(0, issued - a.stages); i < issued; ++i)
-                    mbar_wait(&bars->full[i % a.stages], (i / a.stages) & 1, nullptr, 0, &no_abort);
+                    mbar_wait(&bars->full[i % a.stages], (i / a.stages) & 1, nullptr, 0, no_abort);
             }
         }
     } else if (warp == 1) {
@@ -879,9 +881,9 @@ __global__ void __launch_bounds__(kF8Threads, 1)
                 mma_commit(&bars->tfull[buf]);
             }
             if (*abort) {
-                volatile int no_abort = 0;
+                volatile int no_abort[2] = {0, 0};
                 mma_commit(&bars->drain);
-                mbar_wait(&bars->drain, 0, nullptr, 0, &no_abort);
+                mbar_wait(&bars->drain, 0, nullptr, 0, no_abort);
             }
         }
     } else if (warp < 6) {

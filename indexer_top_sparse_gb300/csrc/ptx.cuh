@@ -37,13 +37,9 @@ constexpr uint64_t kWaitLimitNs = 200ull * 1000ull * 1000ull;  // 200 ms
 
 // Word 2 of the error block, when nonzero, replaces kWaitLimitNs with that
 // many microseconds (set by dsa_workspace_set_wait_limit, to test the
-// give-up path); waits without an error word use the default.
-__device__ __forceinline__ uint64_t wait_limit_ns(const uint32_t *err) {
-    if (err != nullptr) {
-        const uint32_t us = *reinterpret_cast<const volatile uint32_t *>(err + 2);
-        if (us != 0u) return (uint64_t)us * 1000ull;
-    }
-    return kWaitLimitNs;
+// give-up path).  A kernel reads it once, at its start.
+__device__ __forceinline__ int wait_limit_us(const uint32_t *err) {
+    return err != nullptr ? (int)*reinterpret_cast<const volatile uint32_t *>(err + 2) : 0;
 }
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -89,26 +85,66 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t pa
         : "memory");
     return ok != 0;
 }
+// Non-blocking probes of the same phases (test_wait never suspends the thread).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ bool mbar_test_wait_cluster(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
 // Wait for the phase with the given parity to complete.  Gives up after
-// kWaitLimitNs, records a timeout (with `where`) and returns false; *abort
+// kWaitLimitNs, records a timeout (with `where`) and returns false; abort[0]
 // (shared) is then set so that every role of the CTA stops waiting.
+// abort[1] (shared, set at the kernel's start from wait_limit_us) nonzero
+// replaces the limit with that many microseconds: the wait then polls without
+// suspending and reads the clock on every poll, so that any wait longer than
+// the limit gives up (the test of the give-up path).
 // kCluster: the phase is completed from another CTA of the cluster.
 template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32_t *err, uint32_t where,
                                           volatile int *abort) {
     auto try_wait = [&]() { return kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
-    if (try_wait()) return true;
-    const uint64_t t0 = globaltimer_ns(), limit = wait_limit_ns(err);
-    // the clock is read every 64 polls, or on every poll under a shortened
-    // limit (a poll may itself suspend the thread for a while)
-    const uint32_t every = limit < kWaitLimitNs ? 0u : 63u;
-    for (uint32_t it = 0;; ++it) {
-        if (try_wait()) return true;
-        if ((it & every) == every) {
-            if (*abort) return false;
+    const int test_us = abort[1];
+    if (test_us != 0) {
+        auto test_wait = [&]() {
+            return kCluster ? mbar_test_wait_cluster(bar, parity) : mbar_test_wait(bar, parity);
+        };
+        const uint64_t t0 = globaltimer_ns(), limit = (uint64_t)test_us * 1000ull;
+        for (;;) {
+            if (test_wait()) return true;
+            if (abort[0]) return false;
             if (globaltimer_ns() - t0 > limit) {
                 report_error(err, kErrTimeout, where);
-                *abort = 1;
+                abort[0] = 1;
+                return false;
+            }
+        }
+    }
+    if (try_wait()) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 0;; ++it) {
+        if (try_wait()) return true;
+        if ((it & 63) == 63) {
+            if (abort[0]) return false;
+            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                report_error(err, kErrTimeout, where);
+                abort[0] = 1;
                 return false;
             }
         }

@@ -89,7 +89,7 @@ struct __align__(16) MlaBars {
     uint64_t p_full, o_done, o_full, q_full, drain, table;
     uint64_t o_free;  // stream-K: the epilogue of segment 0 has read O
     uint32_t tmem_slot;
-    int abort;
+    int abort[2];  // [0] a wait gave up; [1] wait limit in microseconds (0: default)
 };
 
 constexpr int kMaxKeysPerSplit = 2048;       // host keeps keys_per_split <= this
@@ -258,7 +258,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
         mbar_init(&bars->q_full, 1);
         mbar_init(&bars->drain, 1);
         mbar_init(&bars->table, 1);
-        bars->abort = 0;
+        bars->abort[0] = 0;
+        bars->abort[1] = wait_limit_us(a.err);
         fence_mbar_init();
     }
     if constexpr (NH < 64) {
@@ -277,7 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
     const uint32_t peer = kPair ? (cluster_rank() ^ 1u) : 0u;
     const uint32_t tmem_o = bars->tmem_slot;      // O^T chunk c: columns [64 c, 64 c + NH)
     const uint32_t tmem_s = tmem_o + 256;         // S buffer j at columns 256 + kKeys j (<= 384)
-    volatile int *abort = &bars->abort;
+    volatile int *abort = bars->abort;
 
     if (warp < kProd) {
         // ---------------------------------------------------------------- gather
@@ -436,8 +437,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
         }
         cp_async_wait_all();  // the CTA stays alive until every copy has landed
         if (warp == 0 && lane == 0 && *abort) {
-            volatile int no_abort = 0;
-            mbar_wait(&bars->q_full, 0, nullptr, 0, &no_abort);
+            volatile int no_abort[2] = {0, 0};
+            mbar_wait(&bars->q_full, 0, nullptr, 0, no_abort);
         }
     } else if (warp == kMmaWarp) {
         // ---------------------------------------------------------------- tcgen05 issuer
@@ -494,9 +495,9 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
             }
             if (ok && n_tiles > 0) mma_commit(&bars->o_full);
             if (*abort) {
-                volatile int no_abort = 0;
+                volatile int no_abort[2] = {0, 0};
                 mma_commit(&bars->drain);
-                mbar_wait(&bars->drain, 0, nullptr, 0, &no_abort);
+                mbar_wait(&bars->drain, 0, nullptr, 0, no_abort);
             }
         } else if (kPair && lane == 1) {
             // Pairs: tell the peer as soon as each tile -- including the half

@@ -80,7 +80,7 @@ struct __align__(16) DsBars {
     uint64_t x_free[2];   // the other CTA's receive buffer may take the next tile
     uint64_t q_full, p_full, o_done, o_full, drain, table;
     uint32_t tmem_slot;
-    int abort;
+    int abort[2];  // [0] a wait gave up; [1] wait limit in microseconds (0: default)
 };
 
 struct __align__(16) DsTable {
@@ -160,7 +160,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_ds_kernel(MlaArgs a) {
         mbar_init(&bars->o_full, 1);
         mbar_init(&bars->drain, 1);
         mbar_init(&bars->table, 1);
-        bars->abort = 0;
+        bars->abort[0] = 0;
+        bars->abort[1] = wait_limit_us(a.err);
         fence_mbar_init();
         // the receive buffers expect tiles 0 and 1 (bytes may land from the
         // cluster barrier below on)
@@ -172,7 +173,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_ds_kernel(MlaArgs a) {
     tc_fence_after();
     cluster_barrier();  // both CTAs' barriers are initialised before any remote arrival or store
     const uint32_t tmem = bars->tmem_slot;
-    volatile int *abort = &bars->abort;
+    volatile int *abort = bars->abort;
 
     if (warp < kGather) {
         // ---------------------------------------------------------------- gather
@@ -317,9 +318,9 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_ds_kernel(MlaArgs a) {
             }
             if (ok && n_work > 0) mma_commit(&bars->o_full);
             if (*abort) {
-                volatile int no_abort = 0;
+                volatile int no_abort[2] = {0, 0};
                 mma_commit(&bars->drain);
-                mbar_wait(&bars->drain, 0, nullptr, 0, &no_abort);
+                mbar_wait(&bars->drain, 0, nullptr, 0, no_abort);
             }
         }
     } else {
@@ -507,9 +508,9 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_ds_kernel(MlaArgs a) {
                 // The other CTA sends a tile into buffer j once this CTA has
                 // freed it: let bytes that may be on their way land (or the
                 // bounded wait run out) before this CTA can leave.
-                volatile int no_abort = 0;
-                if (next0 < n_work) mbar_wait<true>(&bars->x_full[0], (next0 >> 1) & 1, nullptr, 0, &no_abort);
-                if (next1 < n_work) mbar_wait<true>(&bars->x_full[1], (next1 >> 1) & 1, nullptr, 0, &no_abort);
+                volatile int no_abort[2] = {0, 0};
+                if (next0 < n_work) mbar_wait<true>(&bars->x_full[0], (next0 >> 1) & 1, nullptr, 0, no_abort);
+                if (next1 < n_work) mbar_wait<true>(&bars->x_full[1], (next1 >> 1) & 1, nullptr, 0, no_abort);
             }
         }
         // ---------------------------------------------------------------- epilogue
