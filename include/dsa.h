@@ -278,7 +278,9 @@ dsa_status dsa_cache_append(const void *k_new, const void *kv_new, const int32_t
  *   Arguments and results are those of dsa_sparse_mla (without workspace).
  *   Scratch: the split-K partials go to a fixed 32 MiB array in the library's
  *   device image, held by every GPU that loads the library until exit.  A
- *   request whose partials do not fit returns DSA_ERR_UNSUPPORTED.  The first
+ *   request whose partials do not fit returns DSA_ERR_UNSUPPORTED.  The array
+ *   holds the split grid's partials; stream-K (about 40 MB of partials on a
+ *   GPU of ~150 SMs) therefore stays off here, with the same results.  The first
  *   call on a device looks the array's address up (cudaGetSymbolAddress);
  *   make it before any stream capture.  Every call on a device shares the
  *   array: calls whose kernels overlap on the GPU race and must not be issued.

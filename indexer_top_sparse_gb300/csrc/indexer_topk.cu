@@ -588,6 +588,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = bars->tmem_slot;
     volatile int *abort = bars->abort;
+    const int wl = abort[1];  // test wait limit in microseconds (0: the default limit)
 
     if (warp == 0) {
         if (lane == 0) {
@@ -602,7 +603,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int issued = 0;
             for (int i = 0; i < n_tiles; ++i) {
                 const int s = i % a.stages;
-                if (i >= a.stages && !mbar_wait(&bars->empty[s], ((i / a.stages) & 1) ^ 1, a.err, 0x101, abort))
+                if (i >= a.stages && !mbar_wait(&bars->empty[s], ((i / a.stages) & 1) ^ 1, a.err, 0x101, abort, wl))
                     break;
                 issued = i + 1;
                 uint8_t *dst = sK + (size_t)s * kTileBytes;
@@ -631,12 +632,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             // ---------------- tcgen05 issuer
             constexpr uint32_t idesc = idesc_bf16_f32(kTileM, L::kN);
-            bool ok = mbar_wait(&bars->qbar, 0, a.err, 0x201, abort);
+            bool ok = mbar_wait(&bars->qbar, 0, a.err, 0x201, abort, wl);
             const uint32_t q_base = smem_u32(sQ);
             for (int i = 0; ok && i < n_tiles; ++i) {
                 const int s = i % a.stages, buf = i & 1;
-                if (!mbar_wait(&bars->full[s], (i / a.stages) & 1, a.err, 0x202, abort)) break;
-                if (i >= 2 && !mbar_wait(&bars->tempty[buf], ((i >> 1) & 1) ^ 1, a.err, 0x203, abort)) break;
+                if (!mbar_wait(&bars->full[s], (i / a.stages) & 1, a.err, 0x202, abort, wl)) break;
+                if (i >= 2 && !mbar_wait(&bars->tempty[buf], ((i >> 1) & 1) ^ 1, a.err, 0x203, abort, wl)) break;
                 tc_fence_after();
                 const uint32_t k_base = smem_u32(sK + (size_t)s * kTileBytes);
                 const uint32_t d = tmem + (uint32_t)(buf * L::kN);
@@ -663,7 +664,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row = quad * 32 + lane;
         for (int i = 0; i < n_tiles; ++i) {
             const int buf = i & 1;
-            const bool ok = mbar_wait(&bars->tfull[buf], (i >> 1) & 1, a.err, 0x301, abort);
+            const bool ok = mbar_wait(&bars->tfull[buf], (i >> 1) & 1, a.err, 0x301, abort, wl);
             if (!__all_sync(0xffffffffu, ok)) break;
             tc_fence_after();
             const int l = i * kTileM + row;          // local key slot
@@ -828,6 +829,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
     tc_fence_after();
     const uint32_t tmem = bars->tmem_slot;
     volatile int *abort = bars->abort;
+    const int wl = abort[1];  // test wait limit in microseconds (0: the default limit)
 
     if (warp == 0) {
         if (lane == 0) {
@@ -840,7 +842,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
             int issued = 0;
             for (int i = 0; i < n_tiles; ++i) {
                 const int s = i % a.stages;
-                if (i >= a.stages && !mbar_wait(&bars->empty[s], ((i / a.stages) & 1) ^ 1, a.err, 0x121, abort))
+                if (i >= a.stages && !mbar_wait(&bars->empty[s], ((i / a.stages) & 1) ^ 1, a.err, 0x121, abort, wl))
                     break;
                 issued = i + 1;
                 uint32_t bytes = 0;
@@ -862,14 +864,14 @@ __global__ void __launch_bounds__(kF8Threads, 1)
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            bool ok = mbar_wait(&bars->qbar, 0, a.err, 0x221, abort);
+            bool ok = mbar_wait(&bars->qbar, 0, a.err, 0x221, abort, wl);
             const uint32_t q_base = smem_u32(sQ);
             for (int i = 0; ok && i < n_tiles; ++i) {
                 const int s = i % a.stages, buf = i % kF8Bufs;
                 const uint32_t round = (uint32_t)(i / kF8Bufs) & 1u;
-                if (!mbar_wait(&bars->full[s], (i / a.stages) & 1, a.err, 0x222, abort)) break;
-                if (i >= kF8Bufs && !mbar_wait(&bars->tempty[buf], round ^ 1u, a.err, 0x223, abort)) break;
-                if (!mbar_wait(&bars->sf_full[buf], round, a.err, 0x224, abort)) break;
+                if (!mbar_wait(&bars->full[s], (i / a.stages) & 1, a.err, 0x222, abort, wl)) break;
+                if (i >= kF8Bufs && !mbar_wait(&bars->tempty[buf], round ^ 1u, a.err, 0x223, abort, wl)) break;
+                if (!mbar_wait(&bars->sf_full[buf], round, a.err, 0x224, abort, wl)) break;
                 tc_fence_after();
                 const uint32_t k_base = smem_u32(sK + (size_t)s * kF8TileBytes);
 #pragma unroll
@@ -893,7 +895,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
         const uint32_t lanes = (uint32_t)(quad * 32) << 16;
         for (int i = 0; i < n_tiles; ++i) {
             const int buf = i % kF8Bufs;
-            if (!mbar_wait(&bars->tfull[buf], (uint32_t)(i / kF8Bufs) & 1u, a.err, 0x321, abort)) break;
+            if (!mbar_wait(&bars->tfull[buf], (uint32_t)(i / kF8Bufs) & 1u, a.err, 0x321, abort, wl)) break;
             tc_fence_after();
             uint32_t r[64];
             tmem_ld32(tmem + lanes + (uint32_t)(buf * kF8AccCols), *reinterpret_cast<uint32_t(*)[32]>(r));
@@ -1002,7 +1004,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
                 if (j >= n_tiles) break;
                 // buffer u was last read by the MMA of tile j - kF8Bufs
                 if (j >= kF8Bufs &&
-                    !mbar_wait(&bars->tfull[u], (uint32_t)((j - kF8Bufs) / kF8Bufs) & 1u, a.err, 0x323, abort)) {
+                    !mbar_wait(&bars->tfull[u], (uint32_t)((j - kF8Bufs) / kF8Bufs) & 1u, a.err, 0x323, abort, wl)) {
                     sf_ok = false;
                     break;
                 }

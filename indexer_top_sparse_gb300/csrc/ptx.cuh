@@ -109,44 +109,50 @@ __device__ __forceinline__ bool mbar_test_wait_cluster(uint64_t *bar, uint32_t p
     return ok != 0;
 }
 // Wait for the phase with the given parity to complete.  Gives up after
-// kWaitLimitNs, records a timeout (with `where`) and returns false; abort[0]
+// kWaitLimitNs, records a timeout (with `where`) and returns false; *abort
 // (shared) is then set so that every role of the CTA stops waiting.
-// abort[1] (shared, set at the kernel's start from wait_limit_us) nonzero
-// replaces the limit with that many microseconds: the wait then polls without
-// suspending and reads the clock on every poll, so that any wait longer than
-// the limit gives up (the test of the give-up path).
 // kCluster: the phase is completed from another CTA of the cluster.
+// test_us nonzero (the kernel's copy of the workspace's wait limit, see
+// wait_limit_us) replaces the limit with that many microseconds, for the test
+// of the give-up path; see mbar_wait_test.
+template <bool kCluster>
+__device__ __noinline__ bool mbar_wait_test(uint64_t *bar, uint32_t parity, uint32_t *err, uint32_t where,
+                                            volatile int *abort, int test_us);
+
 template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32_t *err, uint32_t where,
-                                          volatile int *abort) {
+                                          volatile int *abort, int test_us = 0) {
+    if (test_us != 0) return mbar_wait_test<kCluster>(bar, parity, err, where, abort, test_us);
     auto try_wait = [&]() { return kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
-    const int test_us = abort[1];
-    if (test_us != 0) {
-        auto test_wait = [&]() {
-            return kCluster ? mbar_test_wait_cluster(bar, parity) : mbar_test_wait(bar, parity);
-        };
-        const uint64_t t0 = globaltimer_ns(), limit = (uint64_t)test_us * 1000ull;
-        for (;;) {
-            if (test_wait()) return true;
-            if (abort[0]) return false;
-            if (globaltimer_ns() - t0 > limit) {
-                report_error(err, kErrTimeout, where);
-                abort[0] = 1;
-                return false;
-            }
-        }
-    }
     if (try_wait()) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 0;; ++it) {
         if (try_wait()) return true;
         if ((it & 63) == 63) {
-            if (abort[0]) return false;
+            if (*abort) return false;
             if (globaltimer_ns() - t0 > kWaitLimitNs) {
                 report_error(err, kErrTimeout, where);
-                abort[0] = 1;
+                *abort = 1;
                 return false;
             }
+        }
+    }
+}
+
+// The wait under a test limit: it polls with the non-suspending test_wait and
+// reads the clock on every poll (a suspending try_wait can outlast a limit of
+// microseconds on its own), so any wait longer than the limit gives up.
+template <bool kCluster>
+__device__ __noinline__ bool mbar_wait_test(uint64_t *bar, uint32_t parity, uint32_t *err, uint32_t where,
+                                            volatile int *abort, int test_us) {
+    const uint64_t t0 = globaltimer_ns(), limit = (uint64_t)test_us * 1000ull;
+    for (;;) {
+        if (kCluster ? mbar_test_wait_cluster(bar, parity) : mbar_test_wait(bar, parity)) return true;
+        if (*abort) return false;
+        if (globaltimer_ns() - t0 > limit) {
+            report_error(err, kErrTimeout, where);
+            *abort = 1;
+            return false;
         }
     }
 }

@@ -148,9 +148,9 @@ __device__ __forceinline__ void dequant16(const uint4 v, const float s, uint32_t
 
 // Issue S = Q . K_tile^T for tile i into S buffer i&1 once the tile landed.
 __device__ __forceinline__ bool issue_s_tile(int i, MlaBars *bars, uint32_t kv_base, uint32_t q_base, uint32_t tmem_s,
-                                             uint32_t idesc_s, uint32_t *err, volatile int *abort) {
+                                             uint32_t idesc_s, uint32_t *err, volatile int *abort, int wl) {
     const int st = i % kStages;
-    if (!mbar_wait(&bars->kv_full[st], (i / kStages) & 1, err, 0x503, abort)) return false;
+    if (!mbar_wait(&bars->kv_full[st], (i / kStages) & 1, err, 0x503, abort, wl)) return false;
     fence_proxy_async_smem();  // the tile was written through the generic proxy
     tc_fence_after();
     // descriptors advance by (byte offset >> 4) in their start-address field
@@ -279,6 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
     const uint32_t tmem_o = bars->tmem_slot;      // O^T chunk c: columns [64 c, 64 c + NH)
     const uint32_t tmem_s = tmem_o + 256;         // S buffer j at columns 256 + kKeys j (<= 384)
     volatile int *abort = bars->abort;
+    const int wl = abort[1];  // test wait limit in microseconds (0: the default limit)
 
     if (warp < kProd) {
         // ---------------------------------------------------------------- gather
@@ -359,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
         for (int i = 0; i < n_tiles; ++i) {
             const int stg = i % kStages;
             bool ok = true;
-            if (i >= kStages) ok = mbar_wait(&bars->kv_empty[stg], ((i / kStages) & 1) ^ 1, a.err, 0x501, abort);
+            if (i >= kStages) ok = mbar_wait(&bars->kv_empty[stg], ((i / kStages) & 1) ^ 1, a.err, 0x501, abort, wl);
             if (!__all_sync(0xffffffffu, ok)) break;
             if (kPair && threadIdx.x == 0) {
                 // this stage is free here: the peer may send its half of tile i
@@ -423,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
                 fence_proxy_async_smem();  // written through the generic proxy, read by the bulk copy
                 __syncwarp();
                 if (lane == 0) {
-                    ok = mbar_wait(&bars->peer_free[stg], (i / kStages) & 1, a.err, 0x512, abort);
+                    ok = mbar_wait(&bars->peer_free[stg], (i / kStages) & 1, a.err, 0x512, abort, wl);
                     if (ok) {
                         const uint32_t rbar = map_peer(smem_u32(&bars->kv_full[stg]), peer);
                         for (int r = 0; r < kRegions; ++r) {
@@ -448,31 +449,31 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
             // are unused when NH < 64
             constexpr uint32_t idesc_o = idesc_bf16_f32_amn(128, 64);  // A (V^T) MN-major, B (P) K-major
             const uint32_t q_base = smem_u32(sQ), kv_base = smem_u32(sKV);
-            bool ok = mbar_wait(&bars->q_full, 0, a.err, 0x502, abort);
+            bool ok = mbar_wait(&bars->q_full, 0, a.err, 0x502, abort, wl);
             uint32_t *const err = a.err;
             // Before the logits of segment 1's first tile: the last logits of
             // segment 0 have read Q, so its rows are replaced by segment 1's.
             auto switch_q = [&](int i) -> bool {
                 if (!kSK || i != s1 || n_seg != 2) return true;
-                if (!mbar_wait(&bars->s_full[(i - 1) & 1], ((i - 1) >> 1) & 1, a.err, 0x50a, abort)) return false;
+                if (!mbar_wait(&bars->s_full[(i - 1) & 1], ((i - 1) >> 1) & 1, a.err, 0x50a, abort, wl)) return false;
                 mbar_arrive_expect_tx(&bars->q_full, (uint32_t)(kRegions * NH * 128));
                 for (int r = 0; r < kRegions; ++r)
                     tma_load_2d(sQ + r * kQRegion, &tm_q, &bars->q_full, 64 * r, seg[1].t * a.H + seg[1].hg * NH);
-                return mbar_wait(&bars->q_full, 1, a.err, 0x50b, abort);
+                return mbar_wait(&bars->q_full, 1, a.err, 0x50b, abort, wl);
             };
-            if (ok && n_tiles > 0) ok = issue_s_tile(0, bars, kv_base, q_base, tmem_s, idesc_s, err, abort);
+            if (ok && n_tiles > 0) ok = issue_s_tile(0, bars, kv_base, q_base, tmem_s, idesc_s, err, abort, wl);
             for (int i = 0; ok && i < n_tiles; ++i) {
                 // With a ring of 3+ tiles the next tile's logits are issued
                 // first, so that they overlap this tile's softmax; with only
                 // 2 buffers the next tile is still loading, so this tile's
                 // P*V goes first (it frees the buffer the tile after needs).
                 if (kStages > 2 && i + 1 < n_tiles &&
-                    !(ok = switch_q(i + 1) && issue_s_tile(i + 1, bars, kv_base, q_base, tmem_s, idesc_s, err, abort)))
+                    !(ok = switch_q(i + 1) && issue_s_tile(i + 1, bars, kv_base, q_base, tmem_s, idesc_s, err, abort, wl)))
                     break;
-                if (!(ok = mbar_wait(&bars->p_full, i & 1, a.err, 0x504, abort))) break;
+                if (!(ok = mbar_wait(&bars->p_full, i & 1, a.err, 0x504, abort, wl))) break;
                 // segment 1 starts a fresh accumulator once segment 0's epilogue has read O
                 const int first = seg_of(i) ? s1 : 0;
-                if (kSK && i == s1 && !(ok = mbar_wait(&bars->o_free, 0, a.err, 0x50c, abort))) break;
+                if (kSK && i == s1 && !(ok = mbar_wait(&bars->o_free, 0, a.err, 0x50c, abort, wl))) break;
                 tc_fence_after();
                 const int stg = i % kStages;
                 const uint32_t kb = kv_base + stg * kTileBytes;
@@ -490,7 +491,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
                 mma_commit(&bars->o_done);
                 if (i + 1 == s1 && s1 < n_tiles) mma_commit(&bars->o_full);  // segment 0 is complete
                 if (kStages <= 2 && i + 1 < n_tiles &&
-                    !(ok = switch_q(i + 1) && issue_s_tile(i + 1, bars, kv_base, q_base, tmem_s, idesc_s, err, abort)))
+                    !(ok = switch_q(i + 1) && issue_s_tile(i + 1, bars, kv_base, q_base, tmem_s, idesc_s, err, abort, wl)))
                     break;
             }
             if (ok && n_tiles > 0) mma_commit(&bars->o_full);
@@ -506,7 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
             const uint32_t fwd_peer = map_peer(smem_u32(&bars->fwd_done[0]), peer);
             for (int i = 0; i < n_tiles; ++i) {
                 const int stg = i % kStages;
-                if (!mbar_wait(&bars->kv_full[stg], (i / kStages) & 1, a.err, 0x514, abort)) break;
+                if (!mbar_wait(&bars->kv_full[stg], (i / kStages) & 1, a.err, 0x514, abort, wl)) break;
                 mbar_arrive_remote(fwd_peer + 8 * stg);
             }
         }
@@ -522,7 +523,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
         const int kc = 2 * (lane & 3);
         const bool lead = (lane & 3) == 0;  // writes the per-head values
         float m_ref[2] = {-CUDART_INF_F, -CUDART_INF_F}, l_run[2] = {0.0f, 0.0f};
-        bool ok = n_tiles == 0 || mbar_wait(&bars->table, 0, a.err, 0x509, abort);
+        bool ok = n_tiles == 0 || mbar_wait(&bars->table, 0, a.err, 0x509, abort, wl);
         // Epilogue of segment s: O / l (or the partial O, max and sum) for its
         // row and head group.  Segment 0 of a two-segment CTA runs inside the
         // tile loop and then hands O over to segment 1 (o_free).
@@ -538,7 +539,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
                 }
             }
             if (last && tid_s == 0) grid_dep_launch();  // the split combine may start launching
-            if (ok && n_tiles > 0) ok = mbar_wait(&bars->o_full, (uint32_t)s & 1u, a.err, 0x508, abort);
+            if (ok && n_tiles > 0) ok = mbar_wait(&bars->o_full, (uint32_t)s & 1u, a.err, 0x508, abort, wl);
             ok = bar_and(kBarSm, kSmThreads, ok);
             if (!ok) return;
             tc_fence_after();
@@ -602,7 +603,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
                 m_ref[0] = m_ref[1] = -CUDART_INF_F;
                 l_run[0] = l_run[1] = 0.0f;
             }
-            ok = mbar_wait(&bars->s_full[sb], (i >> 1) & 1, a.err, 0x505, abort);
+            ok = mbar_wait(&bars->s_full[sb], (i >> 1) & 1, a.err, 0x505, abort, wl);
             ok = bar_and(kBarSm, kSmThreads, ok);
             if (!ok) break;
             tc_fence_after();
@@ -657,7 +658,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
             // pairs: the rope rows this CTA forwarded from this stage must have
             // been read by their copies (they have landed in the peer) before
             // P overwrites them
-            if (kPair && ok) ok = mbar_wait<true>(&bars->fwd_done[stg], (i / kStages) & 1, a.err, 0x513, abort);
+            if (kPair && ok) ok = mbar_wait<true>(&bars->fwd_done[stg], (i / kStages) & 1, a.err, 0x513, abort, wl);
             {
                 // P (bf16) as K-major [head][key] rows of 128 bytes with the
                 // 128-byte swizzle, over the tile's consumed rope region (the
@@ -673,7 +674,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
                 }
             }
             // O^T of the previous tile must be complete before it is rescaled
-            if (i > 0) ok = mbar_wait(&bars->o_done, (i - 1) & 1, a.err, 0x507, abort);
+            if (i > 0) ok = mbar_wait(&bars->o_done, (i - 1) & 1, a.err, 0x507, abort, wl);
             const bool any = bar_or(kBarSm, kSmThreads,
                                     lead && ((hA < NH && al[0] != 1.0f) || (hB < NH && al[1] != 1.0f)));
             if (any && i > 0) {

@@ -174,6 +174,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_ds_kernel(MlaArgs a) {
     cluster_barrier();  // both CTAs' barriers are initialised before any remote arrival or store
     const uint32_t tmem = bars->tmem_slot;
     volatile int *abort = bars->abort;
+    const int wl = abort[1];  // test wait limit in microseconds (0: the default limit)
 
     if (warp < kGather) {
         // ---------------------------------------------------------------- gather
@@ -234,7 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_ds_kernel(MlaArgs a) {
         for (int i = 0; i < n_work; ++i) {
             const int stg = i % kStages;
             bool ok = true;
-            if (i >= kStages) ok = mbar_wait(&bars->kv_empty[stg], ((i / kStages) & 1) ^ 1, a.err, 0x601, abort);
+            if (i >= kStages) ok = mbar_wait(&bars->kv_empty[stg], ((i / kStages) & 1) ^ 1, a.err, 0x601, abort, wl);
             if (!__all_sync(0xffffffffu, ok)) break;
             uint8_t *dst = sKV + stg * kStageBytes;
             const int32_t *rows = tab->rows + tab->tile_list[i] * kKeys;
@@ -261,9 +262,9 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_ds_kernel(MlaArgs a) {
             constexpr uint32_t idesc_s = idesc_bf16_f32(kHeads, kKeys);
             constexpr uint32_t idesc_o = idesc_bf16_f32_amn(128, kHeads);  // V^T MN-major, P^T K-major
             const uint32_t kv_base = smem_u32(sKV), p_base = smem_u32(sP), qr_base = smem_u32(sQr);
-            bool ok = mbar_wait(&bars->table, 0, a.err, 0x60d, abort);
+            bool ok = mbar_wait(&bars->table, 0, a.err, 0x60d, abort, wl);
             const int n_work = tab->n_work;
-            ok = ok && n_work > 0 && mbar_wait(&bars->q_full, 0, a.err, 0x602, abort);
+            ok = ok && n_work > 0 && mbar_wait(&bars->q_full, 0, a.err, 0x602, abort, wl);
             // logits of tile i into S buffer i & 1: its four latent regions
             // (A = Q in TMEM) and this CTA's two rope steps (A = Q in smem)
             auto ready_s = [&](int i) {
@@ -272,8 +273,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_ds_kernel(MlaArgs a) {
             };
             auto issue_s = [&](int i) -> bool {
                 const int st = i % kStages, sb = i & 1;
-                if (!mbar_wait(&bars->kv_full[st], (i / kStages) & 1, a.err, 0x603, abort)) return false;
-                if (i >= 2 && !mbar_wait(&bars->s_free[sb], ((i - 2) >> 1) & 1, a.err, 0x604, abort)) return false;
+                if (!mbar_wait(&bars->kv_full[st], (i / kStages) & 1, a.err, 0x603, abort, wl)) return false;
+                if (i >= 2 && !mbar_wait(&bars->s_free[sb], ((i - 2) >> 1) & 1, a.err, 0x604, abort, wl)) return false;
                 fence_proxy_async_smem();  // the tile was written through the generic proxy
                 tc_fence_after();
                 const uint32_t kb = kv_base + st * kStageBytes, d = tmem + kColS + kKeys * sb;
@@ -300,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_ds_kernel(MlaArgs a) {
                     if (!(ok = issue_s(i + 2))) break;
                     pend = false;
                 }
-                if (!(ok = mbar_wait(&bars->p_full, i & 1, a.err, 0x605, abort))) break;
+                if (!(ok = mbar_wait(&bars->p_full, i & 1, a.err, 0x605, abort, wl))) break;
                 tc_fence_after();
                 // O^T chunk c (value dims 128 c ..) += V^T . P^T
                 const uint32_t kb = kv_base + (i % kStages) * kStageBytes, pb = p_base + (i & 1) * kPBytes;
@@ -336,11 +337,11 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_ds_kernel(MlaArgs a) {
             // ---------------------------------------------------------------- exchange
             const uint32_t x_peer = map_peer(smem_u32(sX), peer);
             const uint32_t x_full_peer = map_peer(smem_u32(&bars->x_full[0]), peer);
-            ok = __all_sync(0xffffffffu, mbar_wait(&bars->table, 0, a.err, 0x60e, abort));
+            ok = __all_sync(0xffffffffu, mbar_wait(&bars->table, 0, a.err, 0x60e, abort, wl));
             n_work = ok ? tab->n_work : 0;
             for (int i = 0; i < n_work; ++i) {
                 const int sb = i & 1;
-                ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[sb], (i >> 1) & 1, a.err, 0x607, abort));
+                ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[sb], (i >> 1) & 1, a.err, 0x607, abort, wl));
                 if (!ok) break;
                 tc_fence_after();
                 uint32_t s0[32], s1[32];
@@ -353,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_ds_kernel(MlaArgs a) {
                 // the other CTA's buffer sb is free once it has read tile i - 2
                 if (i >= 2)
                     ok = __all_sync(0xffffffffu,
-                                    mbar_wait<true>(&bars->x_free[sb], ((i - 2) >> 1) & 1, a.err, 0x608, abort));
+                                    mbar_wait<true>(&bars->x_free[sb], ((i - 2) >> 1) & 1, a.err, 0x608, abort, wl));
                 if (!ok) break;
                 const uint32_t dst = x_peer + sb * kXBytes + h * 16, bar = x_full_peer + sb * 8;
 #pragma unroll
@@ -398,13 +399,13 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_ds_kernel(MlaArgs a) {
             int next0 = 0, next1 = 1;  // the tile each receive buffer expects next
             // (decisions to go on are taken by all four softmax warps together,
             // since they meet at named barriers inside the loop)
-            ok = bar_and(kBarSm, 128, mbar_wait(&bars->table, 0, a.err, 0x606, abort));
+            ok = bar_and(kBarSm, 128, mbar_wait(&bars->table, 0, a.err, 0x606, abort, wl));
             n_work = ok ? tab->n_work : 0;
             for (int i = 0; ok && i < n_work; ++i) {
                 const int sb = i & 1;
                 const uint8_t *xb = sX + sb * kXBytes;
-                ok = mbar_wait<true>(&bars->x_full[sb], (i >> 1) & 1, a.err, 0x609, abort);
-                ok = bar_and(kBarSm, 128, ok && mbar_wait(&bars->s_full[sb], (i >> 1) & 1, a.err, 0x60a, abort));
+                ok = mbar_wait<true>(&bars->x_full[sb], (i >> 1) & 1, a.err, 0x609, abort, wl);
+                ok = bar_and(kBarSm, 128, ok && mbar_wait(&bars->s_full[sb], (i >> 1) & 1, a.err, 0x60a, abort, wl));
                 if (!ok) break;
                 tc_fence_after();
                 float s[kKeys];
@@ -477,7 +478,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_ds_kernel(MlaArgs a) {
                     *reinterpret_cast<uint4 *>(pb + h * 128 + ((c ^ (h & 7)) << 4)) =
                         make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]);
                 // the previous tile's P.V must be complete before O^T is rescaled
-                ok = bar_and(kBarSm, 128, i == 0 || mbar_wait(&bars->o_done, (i - 1) & 1, a.err, 0x60b, abort));
+                ok = bar_and(kBarSm, 128, i == 0 || mbar_wait(&bars->o_done, (i - 1) & 1, a.err, 0x60b, abort, wl));
                 if (!ok) break;
                 tc_fence_after();
                 if (bar_or(kBarSm, 128, al != 1.0f) && i > 0) {
@@ -515,7 +516,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_ds_kernel(MlaArgs a) {
         }
         // ---------------------------------------------------------------- epilogue
         if (tid_s == 0) grid_dep_launch();  // the split combine may start launching
-        if (ok && n_work > 0) ok = mbar_wait(&bars->o_full, 0, a.err, 0x60c, abort);
+        if (ok && n_work > 0) ok = mbar_wait(&bars->o_full, 0, a.err, 0x60c, abort, wl);
         ok = bar_and(kBarEpi, 256, ok && !*abort);  // also: m_fin / l_fin are written
         tc_fence_after();
         if (ok) {
