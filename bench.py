@@ -287,6 +287,9 @@ def measure_workload(name, args, dev, world, rank, steps, warmup, seed):
         q0 += T
     idx = torch.empty((max(c["T"] for c in plan), K), dtype=torch.int32, device=dev)
     out = torch.empty((T_all, H, 512), dtype=torch.bfloat16, device=dev)
+    if fp8 and args.q_quant == "separate":
+        qi8 = torch.empty((T_all, 64, 128), dtype=torch.uint8, device=dev)
+        qi_sc = torch.empty((T_all, 64, 4), dtype=torch.uint8, device=dev)
     ws = d.Workspace(max(max(d.index_topk_workspace_size(c["B"], c["T"], K, pt.shape[1], ps) for c in plan),
                          max(d.sparse_mla_workspace_size(c["T"], H, K) for c in plan)), dev)
     stream = torch.cuda.current_stream(dev)
@@ -302,6 +305,12 @@ def measure_workload(name, args, dev, world, rank, steps, warmup, seed):
                 ev[0][-1].record(stream)
             if part == "mla":
                 pass
+            elif fp8 and args.q_quant == "separate":
+                d.dsa_quant_mxfp8(st["q_idx"][r0:r0 + T], q=qi8[r0:r0 + T], scales=qi_sc[r0:r0 + T])
+                d.dsa_index_topk(qi8[r0:r0 + T], st["head_w"][r0:r0 + T], st["k_idx"], c["pt"], c["sl"], c["cq"], K,
+                                 indices=idx[:T], workspace=ws, q_idx_scale=qi_sc[r0:r0 + T], k_idx_scale=st["k_sc"],
+                                 dtype="mxfp8")
+                n += 2
             elif fp8:
                 # MXFP8 keys; the bf16 index query is quantised inside the indexer
                 d.dsa_index_topk(st["q_idx"][r0:r0 + T], st["head_w"][r0:r0 + T], st["k_idx"], c["pt"], c["sl"],
@@ -430,6 +439,9 @@ def measure_workload(name, args, dev, world, rank, steps, warmup, seed):
             "config": {"workload": name, "H": H, "K": K, "H_I": 64, "d_I": 128, "page_size": ps,
                        "query_rows": T_all, "cached_positions": int(np.sum(cache_lens)), "chunks": len(plan),
                        "kv_cache": kv_fmt if fp8 else "bf16",
+                       "tuning": getattr(args, "tuned", None) or "automatic",
+                       "index_query": ("bf16, quantised inside the indexer" if args.q_quant == "fused" else
+                                       "quantised to MXFP8 in its own launch") if fp8 else "bf16",
                        "parallelism": f"replicas{max(world, 1)}",
                        "l2": (f"inputs larger than L2: {copies} alternating cop{'ies' if copies > 1 else 'y'} of "
                               f"every step input ({in_bytes / 2**30:.3f} GiB each), no flush"),
@@ -605,6 +617,10 @@ def main():
                              "prefill_131k_chunked_fp8", "append_131k_fp8"])
     ap.add_argument("--no-workloads", action="store_true",
                     help="skip the other workloads the default run measures after the headline decode")
+    ap.add_argument("--tune", action="append", default=[], metavar="NAME=VALUE",
+                    help="set a library tuning knob (dsa_set_tuning) for the run, e.g. mla_dsplit=1")
+    ap.add_argument("--q-quant", default="fused", choices=["fused", "separate"],
+                    help="FP8 workloads: quantise the index query inside the indexer (default) or in its own launch")
     ap.add_argument("--kv-scales", default="row", choices=["row", "tile128"],
                     help="FP8 workloads: one fp32 scale per latent row (default) or per 128 latent dims")
     ap.add_argument("--graph", action="store_true",
@@ -618,6 +634,15 @@ def main():
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
 
+    tuned = {}
+    for kv in args.tune:
+        name, _, val = kv.partition("=")
+        tuned[name] = int(val)
+    args.tuned = tuned
+    if tuned and args.impl == "ours":
+        import indexer_top_sparse_gb300 as d
+        for name, val in tuned.items():
+            d.set_tuning(name, val)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
@@ -641,7 +666,7 @@ def main():
                            [1] * args.batch, H=128, K=2048, page_size=64, permute=True, seed=args.seed + rank)
     cfg = {"workload": wl.name, "B": wl.B, "N": int(wl.seq_lens[0]), "K": wl.K, "H": wl.H, "H_I": 64, "d_I": 128,
            "D": 576, "D_v": 512, "page_size": wl.page_size, "global_batch": wl.B * max(world, 1),
-           "parallelism": f"replicas{max(world, 1)}"}
+           "parallelism": f"replicas{max(world, 1)}", "tuning": tuned or "automatic"}
 
     if args.impl == "reference":
         if rank != 0:

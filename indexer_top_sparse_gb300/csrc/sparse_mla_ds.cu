@@ -404,8 +404,11 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_ds_kernel(MlaArgs a) {
             for (int i = 0; ok && i < n_work; ++i) {
                 const int sb = i & 1;
                 const uint8_t *xb = sX + sb * kXBytes;
-                ok = mbar_wait<true>(&bars->x_full[sb], (i >> 1) & 1, a.err, 0x609, abort, wl);
-                ok = bar_and(kBarSm, 128, ok && mbar_wait(&bars->s_full[sb], (i >> 1) & 1, a.err, 0x60a, abort, wl));
+                // This CTA's partial logits are read (and their TMEM buffer
+                // handed back to the MMA) as soon as they are ready, before
+                // the other CTA's partial has landed: the logits of tile
+                // i + 2 can then start during the exchange of tile i.
+                ok = bar_and(kBarSm, 128, mbar_wait(&bars->s_full[sb], (i >> 1) & 1, a.err, 0x60a, abort, wl));
                 if (!ok) break;
                 tc_fence_after();
                 float s[kKeys];
@@ -423,6 +426,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_ds_kernel(MlaArgs a) {
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars->s_free[sb]);
+                ok = bar_and(kBarSm, 128, mbar_wait<true>(&bars->x_full[sb], (i >> 1) & 1, a.err, 0x609, abort, wl));
+                if (!ok) break;
                 // full logits: this CTA's partial plus the other's
 #pragma unroll
                 for (int q = 0; q < kKeys / 4; ++q) {
