@@ -112,7 +112,9 @@ const char *dsa_status_string(dsa_status s);
  * row is gathered once, and exchanges partial logits over distributed shared
  * memory: 1 yes, -1 no (two 64-head CTAs per query, "mla_pair" and
  * "mla_stream_k" then apply), 0 automatic = yes when the launch needs more
- * than one wave of CTAs), "topk_cluster".
+ * than one wave of CTAs), "topk_cluster", "indexer_order" (0: the indexers
+ * take query rows longest first, so that the launch does not end on a long row
+ * started late; -1: plain grid order, for measuring what the order buys).
  * Returns 0, or -1 for an unknown name.  Results do not depend on them. */
 int dsa_set_tuning(const char *name, int value);
 

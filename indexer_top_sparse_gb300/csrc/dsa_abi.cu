@@ -38,6 +38,8 @@ std::atomic<int> g_mla_sk{0};
 // (sparse_mla_ds.cu); -1: the 64-head kernels of sparse_mla.cu; 0: automatic
 // (see mla_dsplit).
 std::atomic<int> g_mla_ds{0};
+// -1: the indexers take query rows in grid order; 0 (default): longest first
+std::atomic<int> g_idx_order{0};
 
 int sm_count() {
     int dev = 0, n = 0;
@@ -354,6 +356,7 @@ dsa_status index_common(const void *q_idx, const uint8_t *q_idx_scale, const flo
         a.page_size = page_size;
         a.stages = stages;
         a.tiles_cap = tiles_cap;
+        a.grid_order = g_idx_order.load() < 0;
         return cuda_status(dsa::launch_indexer_mxfp8(tk, tq, a, C, smem, scores != nullptr, quant_q,
                                                      static_cast<cudaStream_t>(stream)));
     }
@@ -379,6 +382,7 @@ dsa_status index_common(const void *q_idx, const uint8_t *q_idx_scale, const flo
     a.page_size = page_size;
     a.stages = plan.stages;
     a.tiles_cap = plan.tiles_cap;
+    a.grid_order = g_idx_order.load() < 0;
     return cuda_status(dsa::launch_indexer_bf16(tk, tq, a, plan.G, plan.C, plan.groups, plan.smem,
                                                 scores != nullptr, static_cast<cudaStream_t>(stream)));
 }
@@ -422,6 +426,7 @@ int dsa_set_tuning(const char *name, int value) {
     else if (!strcmp(name, "mla_stream_k")) g_mla_sk = value;
     else if (!strcmp(name, "mla_dsplit")) g_mla_ds = value;
     else if (!strcmp(name, "topk_cluster")) g_topk_cluster = value;
+    else if (!strcmp(name, "indexer_order")) g_idx_order = value;
     else return -1;
     return 0;
 }

@@ -454,6 +454,10 @@ constexpr int kRankMax = 256, kRankSeqMax = 1024;
 static_assert(sizeof(SelectSmem) >= (2 * kRankMax + 2) * sizeof(int), "ranking scratch fits the selection block");
 template <int kT>
 __device__ int ordered_query(const IndexerArgs &a, int row, int *scratch, int *b) {
+    if (a.grid_order) {
+        *b = find_seq(a.cu_q, a.B, row);
+        return row;
+    }
     if (a.T > kRankMax || a.B > kRankSeqMax) {
         const int t = a.T - 1 - row;
         *b = find_seq(a.cu_q, a.B, t);
@@ -519,7 +523,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             t0 = ordered_query<kThreads>(a, blockIdx.y, reinterpret_cast<int *>(ss), &b);
             gn = 1;
         } else {
-            const int g = gridDim.y - 1 - blockIdx.y;  // last (longest, in a causal prefill) groups first
+            // last (longest, in a causal prefill) groups first
+            const int g = a.grid_order ? (int)blockIdx.y : (int)(gridDim.y - 1 - blockIdx.y);
             int acc = 0;
             b = -1;
             for (int s = 0; s < a.B; ++s) {

@@ -27,6 +27,7 @@ struct IndexerArgs {
     int32_t B, T, K, page_size;
     int32_t stages;             // smem ring depth (<= 8)
     int32_t tiles_cap;          // 128-position tiles one CTA can hold keys for
+    int32_t grid_order;         // 1: query rows in grid order instead of longest first (measurement knob)
 };
 
 struct TopkArgs {

@@ -125,3 +125,19 @@ def test_bad_page_is_reported():
         ws.check()
     assert e.value.code == 4
     ws.check()  # the error word was cleared
+
+
+@pytest.mark.parametrize("G", [1, 4])
+def test_grid_order_gives_the_same_indices(orc, G):
+    # the longest-first row order is a scheduling choice only: with the rows
+    # taken in plain grid order the indices are the same, bit for bit (and
+    # match the oracle)
+    import indexer_top_sparse_gb300 as d
+    from _util import tuning
+    wl = make_workload("order", [900, 300, 2500], [40, 17, 3], H=16, K=256, page_size=64, seed=71, with_kv=False)
+    with tuning(indexer_group=G):
+        base, _ = _run(wl, 256)
+        with tuning(indexer_order=-1):
+            plain, _ = _run(wl, 256)
+        _check(orc, wl, 256)
+    assert np.array_equal(base, plain)
