@@ -66,10 +66,11 @@ def bf16_peaks():
 
 
 def kernel_source_hash(name: str) -> str:
-    path = os.path.join(ROOT, "indexer_top_sparse_gb300", "csrc", name)
+    """Hash of a kernel's source file and the headers every kernel includes."""
+    csrc = os.path.join(ROOT, "indexer_top_sparse_gb300", "csrc")
     h = hashlib.sha256()
-    for f in (path, os.path.join(ROOT, "indexer_top_sparse_gb300", "csrc", "ptx.cuh")):
-        h.update(open(f, "rb").read())
+    for f in (name, "ptx.cuh", "kernels.h", "mxfp8.cuh"):
+        h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
 
