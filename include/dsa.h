@@ -99,7 +99,7 @@ const char *dsa_status_string(dsa_status s);
 /* Launch-shape tuning knobs, read on every call (0 = automatic).  Names:
  * "indexer_cluster" (CTAs per cluster, power of two <= 16), "indexer_stages"
  * (shared-memory ring depth 2..6, where it fits), "indexer_group" (query rows per cluster:
- * 1, 2 or 4), "mla_splits" (key splits per query row), "mla_pair" (with 128
+ * 1, 2 or 4; the MXFP8 indexer takes at most 2), "mla_splits" (key splits per query row), "mla_pair" (with 128
  * heads, run the two 64-head CTAs of a query as a cluster sharing every
  * gathered row: 1 yes, -1 or 0 no), "mla_stream_k" (64-head CTAs, one per SM, share
  * all (row, head group, key tile) units evenly instead of a split grid: 1 yes

@@ -182,50 +182,57 @@ bool plan_indexer(int B, int T, int max_len, IdxPlan *p) {
     return found;
 }
 
-// Launch shape of the MXFP8 indexer (one query row per cluster): fewest
-// waves, then most CTAs in flight, then the deepest ring.
-bool plan_indexer_mxfp8(int T, int max_len, int *C_out, int *stages_out, int *tiles_cap_out, size_t *smem_out) {
+// Launch shape of the MXFP8 indexer: G query rows of one sequence per
+// cluster (2 when a sequence has more query rows than there are sequences,
+// i.e. prefill, if it fits; else 1), C CTAs per cluster, ring depth.
+// Preference as for the bf16 indexer: the fewest waves, then the most CTAs in
+// flight, then the deepest ring.
+bool plan_indexer_mxfp8(int B, int T, int max_len, IdxPlan *p) {
     static std::mutex mu;
-    static std::map<std::tuple<int, int, size_t>, int> cache;
+    static std::map<std::tuple<int, int, int, size_t>, int> cache;
     const size_t smax = max_smem_optin();
     const int tiles_max = std::max(1, ceil_div(max_len, 128));
-    const int c_force = g_idx_cluster.load(), s_force = g_idx_stages.load();
+    // (a forced group of 4 takes this kernel's largest, 2)
+    const int g_force = std::min(g_idx_group.load(), 2), c_force = g_idx_cluster.load(), s_force = g_idx_stages.load();
     bool found = false;
     long long best_waves = 0, best_used = 0;
     int best_stages = 0;
     int dev = 0;
     cudaGetDevice(&dev);
-    for (int C = 1; C <= 16; C <<= 1) {
-        if (c_force && C != c_force) continue;
-        const int tiles_cap = ceil_div(tiles_max, C);
-        if (!c_force && C > 1 && tiles_cap < 4) continue;
-        for (int stages = 6; stages >= 2; --stages) {
-            if (s_force && stages != s_force) continue;
-            const size_t smem = std::max(dsa::indexer_mxfp8_smem_bytes(stages, tiles_cap), (size_t)116 * 1024);
-            if (smem > smax) continue;
-            int resident;
-            {
-                std::lock_guard<std::mutex> g(mu);
-                auto key = std::make_tuple(dev * 64 + C, stages, smem);
-                auto it = cache.find(key);
-                if (it == cache.end()) it = cache.emplace(key, dsa::indexer_mxfp8_max_active_clusters(C, smem)).first;
-                resident = it->second;
-            }
-            if (resident <= 0) continue;
-            const long long waves = (T + resident - 1) / resident;
-            const long long used = (long long)std::min(T, resident) * C;
-            if (!found || waves < best_waves || (waves == best_waves && (used > best_used ||
-                                                                         (used == best_used && stages > best_stages)))) {
-                *C_out = C;
-                *stages_out = stages;
-                *tiles_cap_out = tiles_cap;
-                *smem_out = smem;
-                found = true;
-                best_waves = waves;
-                best_used = used;
-                best_stages = stages;
+    for (int G : {2, 1}) {
+        if (g_force ? G != g_force : (T <= B && G != 1)) continue;
+        const int groups = G == 1 ? T : ceil_div(T, G) + B;
+        for (int C = 1; C <= 16; C <<= 1) {
+            if (c_force && C != c_force) continue;
+            const int tiles_cap = ceil_div(tiles_max, C);
+            if (!c_force && C > 1 && tiles_cap < 4) continue;
+            for (int stages = 6; stages >= 2; --stages) {
+                if (s_force && stages != s_force) continue;
+                const size_t smem = std::max(dsa::indexer_mxfp8_smem_bytes(G, stages, tiles_cap), (size_t)116 * 1024);
+                if (smem > smax) continue;
+                int resident;
+                {
+                    std::lock_guard<std::mutex> g(mu);
+                    auto key = std::make_tuple(dev, G * 64 + C, stages, smem);
+                    auto it = cache.find(key);
+                    if (it == cache.end())
+                        it = cache.emplace(key, dsa::indexer_mxfp8_max_active_clusters(G, C, smem)).first;
+                    resident = it->second;
+                }
+                if (resident <= 0) continue;
+                const long long waves = (groups + resident - 1) / resident;
+                const long long used = (long long)std::min(groups, resident) * C;
+                if (!found || waves < best_waves ||
+                    (waves == best_waves && (used > best_used || (used == best_used && stages > best_stages)))) {
+                    *p = IdxPlan{G, C, stages, tiles_cap, groups, smem};
+                    found = true;
+                    best_waves = waves;
+                    best_used = used;
+                    best_stages = stages;
+                }
             }
         }
+        if (found) break;  // prefer the larger query group when it fits
     }
     return found;
 }
@@ -328,10 +335,8 @@ dsa_status index_common(const void *q_idx, const uint8_t *q_idx_scale, const flo
     if (max_len > (1LL << 30) || (long long)num_pages * page_size > (1LL << 31)) return DSA_ERR_UNSUPPORTED;
     if (dtype == DSA_IDX_MXFP8 || dtype == DSA_IDX_MXFP8_QBF16) {
         const bool quant_q = dtype == DSA_IDX_MXFP8_QBF16;
-        int C = 1, stages = 2, tiles_cap = 1;
-        size_t smem = 0;
-        if (T > 65535 || !plan_indexer_mxfp8(T, (int)max_len, &C, &stages, &tiles_cap, &smem))
-            return DSA_ERR_UNSUPPORTED;
+        IdxPlan plan;
+        if (!plan_indexer_mxfp8(B, T, (int)max_len, &plan) || plan.groups > 65535) return DSA_ERR_UNSUPPORTED;
         CUtensorMap tk, tq;
         if (!encode_rows128_u8(&tk, k_idx_cache, (uint64_t)num_pages * page_size)) return DSA_ERR_CUDA;
         if (quant_q) tq = tk;  // unused: the kernel reads the bf16 query itself
@@ -354,11 +359,11 @@ dsa_status index_common(const void *q_idx, const uint8_t *q_idx_scale, const flo
         a.T = T;
         a.K = K;
         a.page_size = page_size;
-        a.stages = stages;
-        a.tiles_cap = tiles_cap;
+        a.stages = plan.stages;
+        a.tiles_cap = plan.tiles_cap;
         a.grid_order = g_idx_order.load() < 0;
-        return cuda_status(dsa::launch_indexer_mxfp8(tk, tq, a, C, smem, scores != nullptr, quant_q,
-                                                     static_cast<cudaStream_t>(stream)));
+        return cuda_status(dsa::launch_indexer_mxfp8(tk, tq, a, plan.G, plan.C, plan.groups, plan.smem,
+                                                     scores != nullptr, quant_q, static_cast<cudaStream_t>(stream)));
     }
     IdxPlan plan;
     if (!plan_indexer(B, T, (int)max_len, &plan) || plan.groups > 65535) return DSA_ERR_UNSUPPORTED;

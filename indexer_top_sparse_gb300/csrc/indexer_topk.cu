@@ -735,9 +735,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 // go to TMEM: the query's once, each key tile's (128 positions x 4 groups)
 // into one of two scale buffers, written by four warps (one per lane
 // quadrant) ahead of the MMA.
-// One query row per cluster (decode); warps: 0 TMA, 1 MMA, 2..5 epilogue
-// (one per TMEM lane quadrant, thread = position, all 64 heads), 6..9 block
-// scales into TMEM.
+// One cluster serves G query rows of one sequence (G = 1 for decode, 2 in a
+// prefill, where consecutive rows read the same history): the G rows' queries
+// are stacked in the MMA's N dimension (64 G), so each key tile is read once
+// for all of them.  Warps: 0 TMA, 1 MMA, 2..5 epilogue (one per TMEM lane
+// quadrant, thread = position, all 64 heads of every row), 6..9 block scales
+// into TMEM.
 constexpr int kF8Threads = 320;
 constexpr int kF8TileBytes = kTileM * kDI;      // 16 KB of E4M3 keys per tile
 constexpr int kF8BoxBytes = kBox * kDI;         // 8 KB per 64-row box
@@ -745,37 +748,46 @@ constexpr int kF8BoxBytes = kBox * kDI;         // 8 KB per 64-row box
 struct __align__(16) F8Bars {
     uint64_t full[8];
     uint64_t empty[8];
-    uint64_t tfull[4];    // accumulator i % 4 holds tile i
+    uint64_t tfull[4];    // accumulator i % bufs holds tile i
     uint64_t tempty[4];
-    uint64_t sf_full[4];  // tile i's key scales are in TMEM scale buffer i % 4
+    uint64_t sf_full[4];  // tile i's key scales are in TMEM scale buffer i % bufs
     uint64_t qbar;
     uint64_t drain;
     uint32_t tmem_slot;
     int abort[2];  // [0] a wait gave up; [1] wait limit in microseconds (0: default)
 };
-// TMEM columns of the MXFP8 kernel: kF8Bufs accumulators of 64 heads, the
-// query's scales, kF8Bufs key scale buffers (4-aligned).  Four of each keep the
-// scale writes (which share TMEM with the running MMA) a few tiles ahead.
-constexpr int kF8Bufs = 4;
-constexpr uint32_t kF8AccCols = kHI, kF8SfQ = kF8Bufs * kHI, kF8SfK = kF8SfQ + 4;
+// TMEM columns of the MXFP8 kernel: kBufs accumulators of 64 G columns, the
+// queries' scales (4 columns: row r of the stacked queries in lane r % 32,
+// column r / 32), kBufs key scale buffers (4-aligned).  Several of each keep
+// the scale writes (which share TMEM with the running MMA) a few tiles ahead.
+template <int G>
+struct F8Layout {
+    static constexpr int kN = G * kHI;                   // MMA N: the stacked query rows' heads
+    static constexpr int kBufs = G == 1 ? 4 : 3;
+    static constexpr uint32_t kAccCols = kN, kSfQ = kBufs * kN, kSfK = kSfQ + 4;
+    static_assert(kSfK + 4 * kBufs <= 512, "TMEM");
+    static_assert(kN <= 128, "the query scales fill four TMEM columns at most");
+};
 
 // kQuantQ: the query arrives in bf16 and is quantised here, by the scale
 // warps, with the standalone quantiser's rule (mxfp8.cuh): codes into the
 // query tile in the layout TMA would have written, scales into TMEM.  One
 // launch fewer per step than quantising it beforehand.
-template <bool kWriteScores, bool kQuantQ>
+template <int G, bool kWriteScores, bool kQuantQ>
 __global__ void __launch_bounds__(kF8Threads, 1)
     indexer_topk_mxfp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
                               IndexerArgs a) {
+    using L = F8Layout<G>;
+    constexpr int kBufs = L::kBufs;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int key_cap = a.tiles_cap * kTileM;
-    uint8_t *sQ = smem;                                   // 64 heads x 128 B
-    uint8_t *sK = sQ + kHI * kDI;                         // stages x 16 KB
+    uint8_t *sQ = smem;                                   // G x 64 heads x 128 B
+    uint8_t *sK = sQ + G * kHI * kDI;                     // stages x 16 KB
     uint32_t *sKeys = reinterpret_cast<uint32_t *>(sK + (size_t)a.stages * kF8TileBytes);
-    float *sW = reinterpret_cast<float *>(sKeys + key_cap);
-    uint32_t *sHist0 = reinterpret_cast<uint32_t *>(sW + kHI);
-    int32_t *sRows = reinterpret_cast<int32_t *>(sHist0 + kHist);
+    float *sW = reinterpret_cast<float *>(sKeys + (size_t)G * key_cap);
+    uint32_t *sHist0 = reinterpret_cast<uint32_t *>(sW + G * kHI);
+    int32_t *sRows = reinterpret_cast<int32_t *>(sHist0 + G * kHist);
     SelectSmem *ss = reinterpret_cast<SelectSmem *>(sRows + ((2 * a.tiles_cap + 3) & ~3));
     F8Bars *bars = reinterpret_cast<F8Bars *>(ss + 1);
 
@@ -783,13 +795,34 @@ __global__ void __launch_bounds__(kF8Threads, 1)
     const int C = (int)cluster.num_blocks();
     const int crank = (int)cluster.block_rank();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if ((int)blockIdx.y >= a.T) return;
     grid_dep_wait();  // inputs written by the kernel launched just before are visible
-    int b;
-    const int t0 = ordered_query<kF8Threads>(a, blockIdx.y, reinterpret_cast<int *>(ss), &b);
+    // ---- which query rows this cluster serves
+    int b, t0, gn;
+    if (G == 1) {
+        if ((int)blockIdx.y >= a.T) return;
+        t0 = ordered_query<kF8Threads>(a, blockIdx.y, reinterpret_cast<int *>(ss), &b);
+        gn = 1;
+    } else {
+        // last (longest, in a causal prefill) groups first
+        const int g = a.grid_order ? (int)blockIdx.y : (int)(gridDim.y - 1 - blockIdx.y);
+        int acc = 0;
+        b = -1;
+        for (int s = 0; s < a.B; ++s) {
+            const int ng = (__ldg(a.cu_q + s + 1) - __ldg(a.cu_q + s) + G - 1) / G;
+            if (g < acc + ng) {
+                b = s;
+                break;
+            }
+            acc += ng;
+        }
+        if (b < 0) return;  // past the last group: the whole cluster leaves together
+        t0 = __ldg(a.cu_q + b) + (g - acc) * G;
+        gn = min(G, __ldg(a.cu_q + b + 1) - t0);
+    }
     const int nq_b = __ldg(a.cu_q + b + 1) - __ldg(a.cu_q + b);
-    const int pos_last = __ldg(a.seq_lens + b) - nq_b + (t0 - __ldg(a.cu_q + b));
-    const int n_total = pos_last + 1;
+    const int pos_first = __ldg(a.seq_lens + b) - nq_b + (t0 - __ldg(a.cu_q + b));
+    const int pos_last = pos_first + gn - 1;   // positions of rows t0 .. t0+gn-1
+    const int n_total = pos_last + 1;          // history the group needs
     const int tiles_total = (n_total + kTileM - 1) / kTileM;
     const int tpc = (tiles_total + C - 1) / C;
     const int tile0 = min(tiles_total, crank * tpc);
@@ -805,7 +838,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
             mbar_init(&bars->full[s], 1);
             mbar_init(&bars->empty[s], 1);
         }
-        for (int i = 0; i < kF8Bufs; ++i) {
+        for (int i = 0; i < kBufs; ++i) {
             mbar_init(&bars->tfull[i], 1);
             mbar_init(&bars->tempty[i], 4);
             mbar_init(&bars->sf_full[i], 4);
@@ -816,8 +849,15 @@ __global__ void __launch_bounds__(kF8Threads, 1)
         bars->abort[1] = wait_limit_us(a.err);
         fence_mbar_init();
     }
-    for (int i = threadIdx.x; i < kHI; i += kF8Threads) sW[i] = __ldg(a.head_w + (size_t)t0 * kHI + i);
-    for (int i = threadIdx.x; i < kHist; i += kF8Threads) sHist0[i] = 0u;
+    for (int i = threadIdx.x; i < G * kHI; i += kF8Threads)
+        sW[i] = i / kHI < gn ? __ldg(a.head_w + (size_t)t0 * kHI + i) : 0.0f;
+    for (int i = threadIdx.x; i < G * kHist; i += kF8Threads) sHist0[i] = 0u;
+    if constexpr (!kQuantQ && G > 1) {
+        // query rows past the group's last row feed MMA columns nobody reads; keep them finite
+        for (int i = gn * kHI * kDI / 16 + threadIdx.x; i < G * kHI * kDI / 16; i += kF8Threads)
+            reinterpret_cast<uint4 *>(sQ)[i] = make_uint4(0u, 0u, 0u, 0u);
+        fence_proxy_async_smem();
+    }
     for (int j = threadIdx.x; j < 2 * n_tiles; j += kF8Threads) {
         const int p0 = tile0 * kTileM + j * kBox;
         int row = -1;
@@ -841,8 +881,8 @@ __global__ void __launch_bounds__(kF8Threads, 1)
             tma_prefetch_desc(&tm_k);
             if constexpr (!kQuantQ) {
                 tma_prefetch_desc(&tm_q);
-                mbar_arrive_expect_tx(&bars->qbar, (uint32_t)(kHI * kDI));
-                tma_load_2d(sQ, &tm_q, &bars->qbar, 0, t0 * kHI);
+                mbar_arrive_expect_tx(&bars->qbar, (uint32_t)(gn * kHI * kDI));
+                for (int gi = 0; gi < gn; ++gi) tma_load_2d(sQ + gi * kHI * kDI, &tm_q, &bars->qbar, 0, (t0 + gi) * kHI);
             }
             int issued = 0;
             for (int i = 0; i < n_tiles; ++i) {
@@ -872,18 +912,18 @@ __global__ void __launch_bounds__(kF8Threads, 1)
             bool ok = mbar_wait(&bars->qbar, 0, a.err, 0x221, abort, wl);
             const uint32_t q_base = smem_u32(sQ);
             for (int i = 0; ok && i < n_tiles; ++i) {
-                const int s = i % a.stages, buf = i % kF8Bufs;
-                const uint32_t round = (uint32_t)(i / kF8Bufs) & 1u;
+                const int s = i % a.stages, buf = i % kBufs;
+                const uint32_t round = (uint32_t)(i / kBufs) & 1u;
                 if (!mbar_wait(&bars->full[s], (i / a.stages) & 1, a.err, 0x222, abort, wl)) break;
-                if (i >= kF8Bufs && !mbar_wait(&bars->tempty[buf], round ^ 1u, a.err, 0x223, abort, wl)) break;
+                if (i >= kBufs && !mbar_wait(&bars->tempty[buf], round ^ 1u, a.err, 0x223, abort, wl)) break;
                 if (!mbar_wait(&bars->sf_full[buf], round, a.err, 0x224, abort, wl)) break;
                 tc_fence_after();
                 const uint32_t k_base = smem_u32(sK + (size_t)s * kF8TileBytes);
 #pragma unroll
                 for (int g = 0; g < 4; ++g)  // one scale group of 32 dims per MMA, scale byte g
-                    mma_mxf8_ss(tmem + (uint32_t)(buf * kF8AccCols), sdesc_kmajor_sw128(k_base + g * 32),
-                                sdesc_kmajor_sw128(q_base + g * 32), idesc_mxf8_e4m3(kTileM, kHI, g, g),
-                                tmem + kF8SfK + 4u * (uint32_t)buf, tmem + kF8SfQ, g > 0 ? 1u : 0u);
+                    mma_mxf8_ss(tmem + (uint32_t)(buf * L::kAccCols), sdesc_kmajor_sw128(k_base + g * 32),
+                                sdesc_kmajor_sw128(q_base + g * 32), idesc_mxf8_e4m3(kTileM, L::kN, g, g),
+                                tmem + L::kSfK + 4u * (uint32_t)buf, tmem + L::kSfQ, g > 0 ? 1u : 0u);
                 mma_commit(&bars->empty[s]);
                 mma_commit(&bars->tfull[buf]);
             }
@@ -894,42 +934,50 @@ __global__ void __launch_bounds__(kF8Threads, 1)
             }
         }
     } else if (warp < 6) {
-        // epilogue: warp -> TMEM lane quadrant; thread = one position, all 64 heads
+        // epilogue: warp -> TMEM lane quadrant; thread = one position, all 64 heads of every row
         const int quad = warp & 3;
         const int row = quad * 32 + lane;
         const uint32_t lanes = (uint32_t)(quad * 32) << 16;
         for (int i = 0; i < n_tiles; ++i) {
-            const int buf = i % kF8Bufs;
-            if (!mbar_wait(&bars->tfull[buf], (uint32_t)(i / kF8Bufs) & 1u, a.err, 0x321, abort, wl)) break;
+            const int buf = i % kBufs;
+            if (!mbar_wait(&bars->tfull[buf], (uint32_t)(i / kBufs) & 1u, a.err, 0x321, abort, wl)) break;
             tc_fence_after();
-            uint32_t r[64];
-            tmem_ld32(tmem + lanes + (uint32_t)(buf * kF8AccCols), *reinterpret_cast<uint32_t(*)[32]>(r));
-            tmem_ld32(tmem + lanes + (uint32_t)(buf * kF8AccCols + 32), *reinterpret_cast<uint32_t(*)[32]>(r + 32));
+            uint32_t r[G][64];
+#pragma unroll
+            for (int gi = 0; gi < G; ++gi) {
+                tmem_ld32(tmem + lanes + (uint32_t)(buf * L::kAccCols + gi * kHI),
+                          *reinterpret_cast<uint32_t(*)[32]>(r[gi]));
+                tmem_ld32(tmem + lanes + (uint32_t)(buf * L::kAccCols + gi * kHI + 32),
+                          *reinterpret_cast<uint32_t(*)[32]>(r[gi] + 32));
+            }
             tmem_wait_ld();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars->tempty[buf]);  // the accumulator is in registers
-            float2 part2 = make_float2(0.0f, 0.0f);
-            const float4 *w4 = reinterpret_cast<const float4 *>(sW);
-#pragma unroll
-            for (int k = 0; k < 16; ++k) {
-                const float4 w = w4[k];
-                part2 = __ffma2_rn(make_float2(w.x, w.y),
-                                   make_float2(fmaxf(__uint_as_float(r[4 * k]), 0.0f),
-                                               fmaxf(__uint_as_float(r[4 * k + 1]), 0.0f)),
-                                   part2);
-                part2 = __ffma2_rn(make_float2(w.z, w.w),
-                                   make_float2(fmaxf(__uint_as_float(r[4 * k + 2]), 0.0f),
-                                               fmaxf(__uint_as_float(r[4 * k + 3]), 0.0f)),
-                                   part2);
-            }
-            const float sc = part2.x + part2.y;
             const int pos = (tile0 + i) * kTileM + row;
-            const bool valid = pos <= pos_last;
-            const uint32_t key = valid ? score_key(sc) : 0u;
-            sKeys[i * kTileM + row] = key;
-            if (valid) red_shared_add(smem_u32(&sHist0[key >> 24]), 1u);
-            if (kWriteScores && valid && pos < a.ld_scores) a.scores[(size_t)t0 * a.ld_scores + pos] = sc;
+#pragma unroll
+            for (int gi = 0; gi < G; ++gi) {
+                float2 part2 = make_float2(0.0f, 0.0f);
+                const float4 *w4 = reinterpret_cast<const float4 *>(sW + gi * kHI);
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    const float4 w = w4[k];
+                    part2 = __ffma2_rn(make_float2(w.x, w.y),
+                                       make_float2(fmaxf(__uint_as_float(r[gi][4 * k]), 0.0f),
+                                                   fmaxf(__uint_as_float(r[gi][4 * k + 1]), 0.0f)),
+                                       part2);
+                    part2 = __ffma2_rn(make_float2(w.z, w.w),
+                                       make_float2(fmaxf(__uint_as_float(r[gi][4 * k + 2]), 0.0f),
+                                                   fmaxf(__uint_as_float(r[gi][4 * k + 3]), 0.0f)),
+                                       part2);
+                }
+                const float sc = part2.x + part2.y;
+                const bool valid = gi < gn && pos <= pos_first + gi;
+                const uint32_t key = valid ? score_key(sc) : 0u;
+                sKeys[(size_t)gi * key_cap + i * kTileM + row] = key;
+                if (valid) red_shared_add(smem_u32(&sHist0[gi * kHist + (key >> 24)]), 1u);
+                if (kWriteScores && valid && pos < a.ld_scores) a.scores[(size_t)(t0 + gi) * a.ld_scores + pos] = sc;
+            }
         }
     } else {
         // block scales into TMEM, ahead of the MMA: warp -> lane quadrant.
@@ -937,55 +985,69 @@ __global__ void __launch_bounds__(kF8Threads, 1)
         // column base + r / 32, group g in byte g.
         const int quad = warp & 3;
         const uint32_t lanes = (uint32_t)(quad * 32) << 16;
-        // the query's scales, [head][group] (one word per head); the selection
-        // block is free scratch until the selection
+        // the queries' scales, [row][head][group] (one word per head); the
+        // selection block is free scratch until the selection
         uint32_t *sQS = reinterpret_cast<uint32_t *>(ss);
         if constexpr (kQuantQ) {
-            // thread i of the four warps: head i / 2, dims 64 (i % 2) .. +63
-            // (two scale groups).  Codes go to the query tile as a TMA box of
-            // 64 rows x 128 bytes with the 128-byte swizzle would place them
-            // (16-byte chunk c of row h at h * 128 + ((c ^ (h % 8)) << 4)).
+            // thread i of the four warps: head i / 2 of each row, dims
+            // 64 (i % 2) .. +63 (two scale groups).  Codes go to the query
+            // tile as a TMA box of 64 rows x 128 bytes with the 128-byte
+            // swizzle would place them (16-byte chunk c of row h at h * 128 +
+            // ((c ^ (h % 8)) << 4)); rows past the group's last row are zero.
             const int i = (warp - 6) * 32 + lane, h = i >> 1, half = i & 1;
-            const uint4 *src = reinterpret_cast<const uint4 *>(a.q_bf16 + ((size_t)t0 * kHI + h) * kDI + 64 * half);
-            uint4 v[8];
+#pragma unroll 1
+            for (int gi = 0; gi < G; ++gi) {
+                uint8_t *row = sQ + (gi * kHI + h) * 128;
+                uint32_t sc = 0u;
+                if (gi < gn) {
+                    const uint4 *src =
+                        reinterpret_cast<const uint4 *>(a.q_bf16 + ((size_t)(t0 + gi) * kHI + h) * kDI + 64 * half);
+                    uint4 v[8];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) v[k] = __ldg(src + k);
-            uint32_t sc = 0u;
+                    for (int k = 0; k < 8; ++k) v[k] = __ldg(src + k);
 #pragma unroll
-            for (int g = 0; g < 2; ++g) {
-                const uint32_t w[16] = {v[4 * g].x,     v[4 * g].y,     v[4 * g].z,     v[4 * g].w,
-                                        v[4 * g + 1].x, v[4 * g + 1].y, v[4 * g + 1].z, v[4 * g + 1].w,
-                                        v[4 * g + 2].x, v[4 * g + 2].y, v[4 * g + 2].z, v[4 * g + 2].w,
-                                        v[4 * g + 3].x, v[4 * g + 3].y, v[4 * g + 3].z, v[4 * g + 3].w};
-                uint32_t out[8];
-                sc |= (uint32_t)mxfp8_block(w, out) << (8 * g);
-                const int c0 = 2 * (2 * half + g);  // first 16-byte chunk of this group in the row
-                uint8_t *row = sQ + h * 128;
-                *reinterpret_cast<uint4 *>(row + ((c0 ^ (h & 7)) << 4)) = make_uint4(out[0], out[1], out[2], out[3]);
-                *reinterpret_cast<uint4 *>(row + (((c0 + 1) ^ (h & 7)) << 4)) = make_uint4(out[4], out[5], out[6], out[7]);
+                    for (int g = 0; g < 2; ++g) {
+                        const uint32_t w[16] = {v[4 * g].x,     v[4 * g].y,     v[4 * g].z,     v[4 * g].w,
+                                                v[4 * g + 1].x, v[4 * g + 1].y, v[4 * g + 1].z, v[4 * g + 1].w,
+                                                v[4 * g + 2].x, v[4 * g + 2].y, v[4 * g + 2].z, v[4 * g + 2].w,
+                                                v[4 * g + 3].x, v[4 * g + 3].y, v[4 * g + 3].z, v[4 * g + 3].w};
+                        uint32_t out[8];
+                        sc |= (uint32_t)mxfp8_block(w, out) << (8 * g);
+                        const int c0 = 2 * (2 * half + g);  // first 16-byte chunk of this group in the row
+                        *reinterpret_cast<uint4 *>(row + ((c0 ^ (h & 7)) << 4)) = make_uint4(out[0], out[1], out[2], out[3]);
+                        *reinterpret_cast<uint4 *>(row + (((c0 + 1) ^ (h & 7)) << 4)) =
+                            make_uint4(out[4], out[5], out[6], out[7]);
+                    }
+                } else {
+                    sc = 0x7F7Fu;
+#pragma unroll
+                    for (int c = 4 * half; c < 4 * half + 4; ++c)
+                        *reinterpret_cast<uint4 *>(row + (c << 4)) = make_uint4(0u, 0u, 0u, 0u);
+                }
+                // groups 2 half, 2 half + 1 of head h: bytes 2 half .. 2 half + 1 of its word
+                const uint32_t other = __shfl_xor_sync(0xffffffffu, sc, 1);
+                if (half == 0) sQS[gi * kHI + h] = sc | (other << 16);
             }
-            // groups 2 half, 2 half + 1 of head h: bytes 2 half .. 2 half + 1 of its word
-            const uint32_t other = __shfl_xor_sync(0xffffffffu, sc, 1);
-            if (half == 0) sQS[h] = sc | (other << 16);
             fence_proxy_async_smem();  // the codes are read by the tensor cores
             bar_sync(3, 128);          // the four scale warps
             if (threadIdx.x == 6 * 32) mbar_arrive(&bars->qbar);
         }
         if (n_tiles > 0) {
-            uint32_t w[4];  // the query's scales, input layout [head][group]; heads >= 64 unused
+            uint32_t w[4];  // stacked query row r = gi * 64 + head in lane r % 32, column r / 32
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
-                const int h = lane + 32 * c;
-                if constexpr (kQuantQ)
-                    w[c] = h < kHI ? sQS[h] : 0x7F7F7F7Fu;
+                const int r = lane + 32 * c, gi = r / kHI, h = r % kHI;
+                if (gi >= gn || gi >= G)
+                    w[c] = 0x7F7F7F7Fu;
+                else if constexpr (kQuantQ)
+                    w[c] = sQS[r];
                 else
-                    w[c] = h < kHI ? __ldg(reinterpret_cast<const uint32_t *>(a.q_scale + ((size_t)t0 * kHI + h) * 4))
-                                   : 0x7F7F7F7Fu;
+                    w[c] = __ldg(reinterpret_cast<const uint32_t *>(a.q_scale + ((size_t)(t0 + gi) * kHI + h) * 4));
             }
-            tmem_st4(tmem + lanes + kF8SfQ, w);
+            tmem_st4(tmem + lanes + L::kSfQ, w);
         }
         // The key scales come straight from the cache with plain loads (a
-        // warp's 32 rows are 128 contiguous bytes), issued kF8Bufs tiles
+        // warp's 32 rows are 128 contiguous bytes), issued kBufs tiles
         // ahead: they need only the page rows, not the key tile, and leave the
         // bulk-copy engine to the key tiles.  Rows of a half that is past the
         // sequence get scale 1 (their scores are never used).
@@ -997,28 +1059,28 @@ __global__ void __launch_bounds__(kF8Threads, 1)
                 w[c] = base >= 0 ? __ldg(kscale + base + lane + 32 * (c & 1)) : 0x7F7F7F7Fu;
             }
         };
-        uint32_t wq[kF8Bufs][4];
+        uint32_t wq[kBufs][4];
 #pragma unroll
-        for (int u = 0; u < kF8Bufs; ++u)
+        for (int u = 0; u < kBufs; ++u)
             if (u < n_tiles) load_scales(u, wq[u]);
         bool sf_ok = true;
-        for (int j0 = 0; sf_ok && j0 < n_tiles; j0 += kF8Bufs) {
+        for (int j0 = 0; sf_ok && j0 < n_tiles; j0 += kBufs) {
 #pragma unroll
-            for (int u = 0; u < kF8Bufs; ++u) {
+            for (int u = 0; u < kBufs; ++u) {
                 const int j = j0 + u;
                 if (j >= n_tiles) break;
-                // buffer u was last read by the MMA of tile j - kF8Bufs
-                if (j >= kF8Bufs &&
-                    !mbar_wait(&bars->tfull[u], (uint32_t)((j - kF8Bufs) / kF8Bufs) & 1u, a.err, 0x323, abort, wl)) {
+                // buffer u was last read by the MMA of tile j - kBufs
+                if (j >= kBufs &&
+                    !mbar_wait(&bars->tfull[u], (uint32_t)((j - kBufs) / kBufs) & 1u, a.err, 0x323, abort, wl)) {
                     sf_ok = false;
                     break;
                 }
-                tmem_st4(tmem + lanes + kF8SfK + 4u * (uint32_t)u, wq[u]);
-                tmem_wait_st();  // (the first time also the query's scales)
+                tmem_st4(tmem + lanes + L::kSfK + 4u * (uint32_t)u, wq[u]);
+                tmem_wait_st();  // (the first time also the queries' scales)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars->sf_full[u]);
-                if (j + kF8Bufs < n_tiles) load_scales(j + kF8Bufs, wq[u]);
+                if (j + kBufs < n_tiles) load_scales(j + kBufs, wq[u]);
             }
         }
     }
@@ -1028,8 +1090,16 @@ __global__ void __launch_bounds__(kF8Threads, 1)
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tmem, 512);
     if (threadIdx.x == 0) grid_dep_launch();  // scoring is done: the next kernel may begin launching
-    int32_t *out = a.indices + (size_t)t0 * a.K;
-    cluster_topk<kF8Threads>(sKeys, n_tiles * kTileM, tile0 * kTileM, n_total, a.K, out, *ss, sHist0);
+    // ---------------- selection, one query row at a time
+    for (int gi = 0; gi < G; ++gi) {
+        if (gi >= gn) {
+            cluster.sync();
+            continue;
+        }
+        int32_t *out = a.indices + (size_t)(t0 + gi) * a.K;
+        cluster_topk<kF8Threads>(sKeys + (size_t)gi * key_cap, n_tiles * kTileM, tile0 * kTileM, pos_first + gi + 1,
+                                 a.K, out, *ss, sHist0 + gi * kHist);
+    }
 }
 
 // Top-K of given score rows (test hook and standalone selection).
@@ -1066,16 +1136,16 @@ size_t indexer_smem_bytes(int G, int stages, int tiles_cap) {
     return 1024 + q + k + keys + w + sizeof(SelectSmem) + sizeof(IdxBars);
 }
 
-size_t indexer_mxfp8_smem_bytes(int stages, int tiles_cap) {
-    return 1024 + (size_t)kHI * kDI + (size_t)stages * kF8TileBytes + (size_t)tiles_cap * kTileM * 4 +
-           (size_t)(kHI + kHist) * 4 + (size_t)((2 * tiles_cap + 3) & ~3) * 4 +
-           sizeof(SelectSmem) + sizeof(F8Bars);
+size_t indexer_mxfp8_smem_bytes(int G, int stages, int tiles_cap) {
+    return 1024 + (size_t)G * kHI * kDI + (size_t)stages * kF8TileBytes + (size_t)G * tiles_cap * kTileM * 4 +
+           (size_t)G * (kHI + kHist) * 4 + (size_t)((2 * tiles_cap + 3) & ~3) * 4 + sizeof(SelectSmem) +
+           sizeof(F8Bars);
 }
 
-template <bool W, bool Q>
-static cudaError_t launch_f8(const CUtensorMap &tk, const CUtensorMap &tq, const IndexerArgs &a, int C, size_t smem,
-                             cudaStream_t st) {
-    auto kern = indexer_topk_mxfp8_kernel<W, Q>;
+template <int G, bool W, bool Q>
+static cudaError_t launch_f8(const CUtensorMap &tk, const CUtensorMap &tq, const IndexerArgs &a, int C, int groups,
+                             size_t smem, cudaStream_t st) {
+    auto kern = indexer_topk_mxfp8_kernel<G, W, Q>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     if (C > 8) {
@@ -1083,7 +1153,7 @@ static cudaError_t launch_f8(const CUtensorMap &tk, const CUtensorMap &tq, const
         if (e != cudaSuccess) return e;
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)C, (unsigned)a.T, 1);
+    cfg.gridDim = dim3((unsigned)C, (unsigned)groups, 1);
     cfg.blockDim = dim3(kF8Threads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
@@ -1099,17 +1169,25 @@ static cudaError_t launch_f8(const CUtensorMap &tk, const CUtensorMap &tq, const
     return cudaLaunchKernelEx(&cfg, kern, tk, tq, a);
 }
 
-cudaError_t launch_indexer_mxfp8(const CUtensorMap &tm_k, const CUtensorMap &tm_q, const IndexerArgs &a, int C,
-                                 size_t smem, bool write_scores, bool quant_q, cudaStream_t st) {
+template <int G>
+static cudaError_t launch_f8g(const CUtensorMap &tk, const CUtensorMap &tq, const IndexerArgs &a, int C, int groups,
+                              size_t smem, bool write_scores, bool quant_q, cudaStream_t st) {
     if (quant_q)
-        return write_scores ? launch_f8<true, true>(tm_k, tm_q, a, C, smem, st)
-                            : launch_f8<false, true>(tm_k, tm_q, a, C, smem, st);
-    return write_scores ? launch_f8<true, false>(tm_k, tm_q, a, C, smem, st)
-                        : launch_f8<false, false>(tm_k, tm_q, a, C, smem, st);
+        return write_scores ? launch_f8<G, true, true>(tk, tq, a, C, groups, smem, st)
+                            : launch_f8<G, false, true>(tk, tq, a, C, groups, smem, st);
+    return write_scores ? launch_f8<G, true, false>(tk, tq, a, C, groups, smem, st)
+                        : launch_f8<G, false, false>(tk, tq, a, C, groups, smem, st);
 }
 
-int indexer_mxfp8_max_active_clusters(int C, size_t smem) {
-    auto kern = indexer_topk_mxfp8_kernel<false, false>;
+cudaError_t launch_indexer_mxfp8(const CUtensorMap &tm_k, const CUtensorMap &tm_q, const IndexerArgs &a, int G, int C,
+                                 int groups, size_t smem, bool write_scores, bool quant_q, cudaStream_t st) {
+    if (G == 2) return launch_f8g<2>(tm_k, tm_q, a, C, groups, smem, write_scores, quant_q, st);
+    if (G == 1) return launch_f8g<1>(tm_k, tm_q, a, C, groups, smem, write_scores, quant_q, st);
+    return cudaErrorInvalidValue;
+}
+
+int indexer_mxfp8_max_active_clusters(int G, int C, size_t smem) {
+    auto kern = G == 2 ? indexer_topk_mxfp8_kernel<2, false, false> : indexer_topk_mxfp8_kernel<1, false, false>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return 0;
     if (C > 8 && cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
         return 0;

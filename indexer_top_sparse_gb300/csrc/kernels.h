@@ -47,14 +47,14 @@ cudaError_t launch_topk_from_scores(const TopkArgs &a, int C, size_t smem, cudaS
 // Clusters of C CTAs of the G-query indexer kernel with `smem` bytes that can
 // be resident at once (0 if the shape cannot launch).
 int indexer_max_active_clusters(int G, int C, size_t smem);
-// MXFP8 variant (one query row per cluster).
-size_t indexer_mxfp8_smem_bytes(int stages, int tiles_cap);
+// MXFP8 variant (G = 1 or 2 query rows of one sequence per cluster).
+size_t indexer_mxfp8_smem_bytes(int G, int stages, int tiles_cap);
 // quant_q: q_idx arrives in bf16 (a.q_bf16) and the kernel quantises it to
 // MXFP8 itself (tm_q unused); otherwise tm_q maps the E4M3 codes and
 // a.q_scale holds their scales.
-cudaError_t launch_indexer_mxfp8(const CUtensorMap &tm_k, const CUtensorMap &tm_q, const IndexerArgs &a, int C,
-                                 size_t smem, bool write_scores, bool quant_q, cudaStream_t st);
-int indexer_mxfp8_max_active_clusters(int C, size_t smem);
+cudaError_t launch_indexer_mxfp8(const CUtensorMap &tm_k, const CUtensorMap &tm_q, const IndexerArgs &a, int G, int C,
+                                 int groups, size_t smem, bool write_scores, bool quant_q, cudaStream_t st);
+int indexer_mxfp8_max_active_clusters(int G, int C, size_t smem);
 
 // Sparse MLA (sparse_mla.cu).
 struct MlaArgs {

@@ -95,9 +95,15 @@ def test_mxfp8_ring_depths(orc, stages):
         d.set_tuning("indexer_stages", 0)
 
 
-def test_mxfp8_prefill_causal(orc):
-    wl = make_workload("p", [700, 300], [40, 17], H=16, K=256, page_size=64, seed=41, with_kv=False)
-    _check(orc, wl, 256)
+@pytest.mark.parametrize("G", [1, 2])
+def test_mxfp8_prefill_causal(orc, G):
+    # G query rows of a sequence per cluster share each key tile (their
+    # queries stacked in the MMA's N); 17 rows leave a last group of one
+    import indexer_top_sparse_gb300 as d
+    from _util import tuning
+    wl = make_workload("p", [700, 300, 2100], [40, 17, 9], H=16, K=256, page_size=64, seed=41, with_kv=False)
+    with tuning(indexer_group=G):
+        _check(orc, wl, 256)
 
 
 def test_mxfp8_scales_required():
