@@ -56,17 +56,6 @@ __device__ __forceinline__ uint32_t score_key(float x) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Count this lane's key in its top-digit bin of hist.  The scores of a tile
-// fall into a handful of bins (the top byte is the sign and the high exponent
-// bits), and same-address shared-memory atomics serialise, so the lanes of a
-// warp that share a bin add together: one atomic per distinct bin and warp.
-// Every lane of the warp calls this.
-__device__ __forceinline__ void hist_add_warp(uint32_t *hist, uint32_t bin, bool valid) {
-    const uint32_t peers = __match_any_sync(0xffffffffu, valid ? bin : 0xFFFFFFFFu);
-    if (valid && (threadIdx.x & 31) == (uint32_t)(__ffs(peers) - 1))
-        red_shared_add(smem_u32(&hist[bin]), (uint32_t)__popc(peers));
-}
-
 constexpr int kCandCap = 128;   // threshold-bucket keys one CTA may hand to the bucket selection
 constexpr int kAllCap = 512;    // the same for the whole cluster
 constexpr int kMaxSelThreads = 320;
@@ -701,7 +690,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool valid = gi < gn && pos <= pos_first + gi;
                 const uint32_t key = valid ? score_key(acc) : 0u;
                 sKeys[(size_t)gi * key_cap + l] = key;
-                hist_add_warp(sHist0 + gi * kHist, key >> 24, valid);
+                if (valid) red_shared_add(smem_u32(&sHist0[gi * kHist + (key >> 24)]), 1u);
                 if (kWriteScores && valid && pos < a.ld_scores) a.scores[(size_t)(t0 + gi) * a.ld_scores + pos] = acc;
             }
             tc_fence_before();
@@ -986,7 +975,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
                 const bool valid = gi < gn && pos <= pos_first + gi;
                 const uint32_t key = valid ? score_key(sc) : 0u;
                 sKeys[(size_t)gi * key_cap + i * kTileM + row] = key;
-                hist_add_warp(sHist0 + gi * kHist, key >> 24, valid);
+                if (valid) red_shared_add(smem_u32(&sHist0[gi * kHist + (key >> 24)]), 1u);
                 if (kWriteScores && valid && pos < a.ld_scores) a.scores[(size_t)(t0 + gi) * a.ld_scores + pos] = sc;
             }
         }
