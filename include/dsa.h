@@ -114,14 +114,26 @@ const char *dsa_status_string(dsa_status s);
  * "mla_stream_k" then apply), 0 automatic = yes when the launch needs more
  * than one wave of CTAs), "topk_cluster", "indexer_order" (0: the indexers
  * take query rows longest first, so that the launch does not end on a long row
- * started late; -1: plain grid order, for measuring what the order buys).
+ * started late; -1: plain grid order, for measuring what the order buys),
+ * "indexer_flat" (bf16 indexer: one CTA per SM scores an even share of the
+ * 128-position tiles of all query rows, writes the rows' score keys and
+ * top-digit counts to the workspace, and the CTA that completes a row selects
+ * its Top-K: 1 yes where it applies (at most 512 query rows, rows of at most
+ * 49152 positions, the workspace dsa_index_topk_workspace_size reports), -1
+ * no, 0 automatic = yes when every query row is its own sequence and the
+ * rows hold at least 3 * 2^20 positions in all).
  * Returns 0, or -1 for an unknown name.  Results do not depend on them. */
 int dsa_set_tuning(const char *name, int value);
 
 /* ---------------------------------------------------------------- workspace */
 
 /* Bytes of workspace dsa_index_topk / dsa_index_scores / dsa_topk_from_scores
- * need (at least 16: the error word). */
+ * need: the 256-byte error block, plus, where the flat bf16 indexer applies
+ * (see "indexer_flat"), T x 2048 histogram words, T tile counters and
+ * T x max_pages_per_seq x page_size score keys of 4 bytes.  A workspace of
+ * only the error block is accepted and keeps the flat indexer off.  The flat
+ * indexer zeroes its counters and histograms itself (enqueued on the call's
+ * stream), so the workspace may be shared with dsa_sparse_mla. */
 size_t dsa_index_topk_workspace_size(int32_t B, int32_t T, int32_t K, int32_t max_pages_per_seq,
                                      int32_t page_size);
 
@@ -163,7 +175,9 @@ dsa_status dsa_workspace_set_wait_limit(void *workspace, uint32_t microseconds, 
  *                positions with the highest scores (ties: lower position
  *                first), ascending, followed by -1 padding.
  * page_size must be a multiple of 64; max_pages_per_seq * page_size bounds
- * every seq_lens[b].  Scores never leave the chip. */
+ * every seq_lens[b].  The cluster kernel keeps the scores on chip; the flat
+ * bf16 kernel (see "indexer_flat") passes 4-byte score keys through the
+ * workspace, 4 bytes per position (L2-resident at decode sizes). */
 dsa_status dsa_index_topk(const void *q_idx, const uint8_t *q_idx_scale, const float *head_w,
                           const void *k_idx_cache, const uint8_t *k_idx_scale, int64_t num_pages,
                           const int32_t *page_table, int32_t max_pages_per_seq, const int32_t *seq_lens,

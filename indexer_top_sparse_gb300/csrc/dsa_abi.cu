@@ -40,6 +40,9 @@ std::atomic<int> g_mla_sk{0};
 std::atomic<int> g_mla_ds{0};
 // -1: the indexers take query rows in grid order; 0 (default): longest first
 std::atomic<int> g_idx_order{0};
+// 1: the flat bf16 indexer whenever it applies; -1: never; 0: for one query
+// row per sequence (see plan_indexer_flat)
+std::atomic<int> g_idx_flat{0};
 
 int sm_count() {
     int dev = 0, n = 0;
@@ -182,6 +185,47 @@ bool plan_indexer(int B, int T, int max_len, IdxPlan *p) {
     return found;
 }
 
+// The flat bf16 indexer (one CTA per SM sharing all rows' tiles evenly; the
+// CTA that completes a row selects it): automatically for one query row per
+// sequence (decode) with at least 3 * 2^20 positions in all, where streaming
+// on every SM outweighs its fixed costs (a zeroing memset and a one-CTA
+// selection per row after the last tile).  Measured on GB300, 32768-position
+// rows: 96 rows 154 against 222 us, 160 rows 243 against 446 us (the cluster
+// grid needs a second wave), 256 rows 374 against 470 us; below the
+// threshold the cluster kernel was faster or equal (32 rows 72 against 60 us;
+// 128 rows of 16384 positions 115 against 105 us).  Rows must fit the
+// selection's staging (the query slots and the tile ring) and the row tables
+// its shared memory.
+struct FlatPlan {
+    int ctas, stages, cap_tiles;
+    size_t smem, zero_bytes, ws_bytes;  // workspace bytes past the error block (the first zero_bytes zeroed per call)
+};
+
+bool plan_indexer_flat(int B, int T, int max_len, FlatPlan *f) {
+    const int forced = g_idx_flat.load();
+    if (forced < 0 || T < 1 || T > dsa::indexer_flat_rows_max()) return false;
+    if (forced == 0 && (T > B || g_idx_group.load() > 1 || g_idx_cluster.load() > 0 ||
+                        (long long)T * max_len < (3LL << 20)))
+        return false;
+    const int ctas = sm_count();
+    const long long tiles_max = std::max(1, ceil_div(max_len, 128));
+    const long long cap = ((T * tiles_max + ctas - 1) / ctas + 1 + 3) & ~3LL;
+    if (cap > 1024) return false;
+    const size_t smax = max_smem_optin();
+    const int s_force = g_idx_stages.load();
+    for (int stages = 5; stages >= 3; --stages) {
+        if (s_force && stages != s_force) continue;
+        if (max_len > dsa::indexer_flat_stage_keys(stages)) break;  // fewer stages stage fewer keys
+        const size_t smem = dsa::indexer_flat_smem_bytes(stages, T, (int)cap);
+        if (smem > smax) continue;
+        const size_t ld = (size_t)((max_len + 3) & ~3);
+        const size_t zero = (size_t)T * dsa::indexer_flat_hist_bins() * 4 + (size_t)((T + 3) & ~3) * 4;
+        *f = FlatPlan{ctas, stages, (int)cap, smem, zero, zero + (size_t)T * ld * 4};
+        return true;
+    }
+    return false;
+}
+
 // Launch shape of the MXFP8 indexer: G query rows of one sequence per
 // cluster (2 when a sequence has more query rows than there are sequences,
 // i.e. prefill, if it fits; else 1), C CTAs per cluster, ring depth.
@@ -321,8 +365,9 @@ dsa_status index_common(const void *q_idx, const uint8_t *q_idx_scale, const flo
     if (!q_idx || !head_w || !k_idx_cache || !page_table || !seq_lens || !cu_q || !indices || !workspace)
         return DSA_ERR_INVALID_ARG;
     if (!aligned16(q_idx) || !aligned16(k_idx_cache) || !aligned16(workspace)) return DSA_ERR_INVALID_ARG;
-    if (workspace_bytes < dsa_index_topk_workspace_size(B, T, K, max_pages_per_seq, page_size))
-        return DSA_ERR_INVALID_ARG;
+    // (the error block is the minimum; the flat indexer runs only in a
+    // workspace of the size dsa_index_topk_workspace_size reports)
+    if (workspace_bytes < kErrBytes) return DSA_ERR_INVALID_ARG;
     if (dtype != DSA_IDX_BF16 && dtype != DSA_IDX_MXFP8 && dtype != DSA_IDX_MXFP8_QBF16) return DSA_ERR_UNSUPPORTED;
     if (dtype == DSA_IDX_MXFP8 && (!q_idx_scale || !k_idx_scale || !aligned16(k_idx_scale) ||
                                    (reinterpret_cast<uintptr_t>(q_idx_scale) & 3u)))
@@ -365,8 +410,11 @@ dsa_status index_common(const void *q_idx, const uint8_t *q_idx_scale, const flo
         return cuda_status(dsa::launch_indexer_mxfp8(tk, tq, a, plan.G, plan.C, plan.groups, plan.smem,
                                                      scores != nullptr, quant_q, static_cast<cudaStream_t>(stream)));
     }
-    IdxPlan plan;
-    if (!plan_indexer(B, T, (int)max_len, &plan) || plan.groups > 65535) return DSA_ERR_UNSUPPORTED;
+    FlatPlan flat;
+    const bool use_flat = !scores && plan_indexer_flat(B, T, (int)max_len, &flat) &&
+                          workspace_bytes >= kErrBytes + flat.ws_bytes;
+    IdxPlan plan{};
+    if (!use_flat && (!plan_indexer(B, T, (int)max_len, &plan) || plan.groups > 65535)) return DSA_ERR_UNSUPPORTED;
     CUtensorMap tk, tq;
     if (!encode_rows128_bf16(&tk, k_idx_cache, (uint64_t)num_pages * page_size)) return DSA_ERR_CUDA;
     if (!encode_rows128_bf16(&tq, q_idx, (uint64_t)T * 64)) return DSA_ERR_CUDA;
@@ -385,9 +433,23 @@ dsa_status index_common(const void *q_idx, const uint8_t *q_idx_scale, const flo
     a.T = T;
     a.K = K;
     a.page_size = page_size;
+    a.grid_order = g_idx_order.load() < 0;
+    if (use_flat) {
+        // workspace past the error block: [T][bins] histograms, [T] tile
+        // counters (both zeroed here), [T][ld] keys
+        uint8_t *base = static_cast<uint8_t *>(workspace) + kErrBytes;
+        a.flat_hist = reinterpret_cast<uint32_t *>(base);
+        a.flat_cnt = reinterpret_cast<int32_t *>(base + (size_t)T * dsa::indexer_flat_hist_bins() * 4);
+        a.flat_keys = reinterpret_cast<uint32_t *>(base + flat.zero_bytes);
+        a.ld_flat = (max_len + 3) & ~3LL;
+        a.flat_cap_tiles = flat.cap_tiles;
+        a.stages = flat.stages;
+        cudaError_t e = cudaMemsetAsync(base, 0, flat.zero_bytes, static_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) return cuda_status(e);
+        return cuda_status(dsa::launch_indexer_flat(tk, tq, a, flat.ctas, flat.smem, static_cast<cudaStream_t>(stream)));
+    }
     a.stages = plan.stages;
     a.tiles_cap = plan.tiles_cap;
-    a.grid_order = g_idx_order.load() < 0;
     return cuda_status(dsa::launch_indexer_bf16(tk, tq, a, plan.G, plan.C, plan.groups, plan.smem,
                                                 scores != nullptr, static_cast<cudaStream_t>(stream)));
 }
@@ -432,17 +494,18 @@ int dsa_set_tuning(const char *name, int value) {
     else if (!strcmp(name, "mla_dsplit")) g_mla_ds = value;
     else if (!strcmp(name, "topk_cluster")) g_topk_cluster = value;
     else if (!strcmp(name, "indexer_order")) g_idx_order = value;
+    else if (!strcmp(name, "indexer_flat")) g_idx_flat = value;
     else return -1;
     return 0;
 }
 
 size_t dsa_index_topk_workspace_size(int32_t B, int32_t T, int32_t K, int32_t max_pages_per_seq,
                                      int32_t page_size) {
-    (void)B;
-    (void)T;
     (void)K;
-    (void)max_pages_per_seq;
-    (void)page_size;
+    FlatPlan flat;
+    const long long max_len = (long long)max_pages_per_seq * page_size;
+    if (B >= 1 && T >= 1 && max_len >= 1 && max_len <= (1LL << 30) && plan_indexer_flat(B, T, (int)max_len, &flat))
+        return kErrBytes + flat.ws_bytes;
     return kErrBytes;
 }
 

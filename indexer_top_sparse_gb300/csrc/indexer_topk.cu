@@ -60,10 +60,12 @@ constexpr int kCandCap = 128;   // threshold-bucket keys one CTA may hand to the
 constexpr int kAllCap = 512;    // the same for the whole cluster
 constexpr int kMaxSelThreads = 320;
 
-struct __align__(16) SelectSmem {
+// Shared state of the cluster selection for up to kSegMax threads per CTA.
+template <int kSegMax>
+struct __align__(16) SelectSmemT {
     uint32_t hist[2][kHist];
     uint32_t tot[kHist];
-    int32_t scan[2][16];
+    int32_t scan[2][kSegMax / 32 > 16 ? kSegMax / 32 : 16];  // one word per warp
     int32_t cnt[4];       // this CTA's (n_gt, n_eq) for the cluster exchange; [2] = abort flag
     uint32_t bcast[4];    // digit, count-above
     // bucket selection: published [keys above the bucket, bucket keys kept, overflow, pos0]
@@ -79,8 +81,9 @@ struct __align__(16) SelectSmem {
     int32_t cta_pos0[kMaxCluster];  // first position of each CTA's run
     int32_t cta_gt[kMaxCluster];
     int32_t cta_sel[kMaxCluster];
-    int32_t seg_sel[kMaxSelThreads];
+    int32_t seg_sel[kSegMax];
 };
+using SelectSmem = SelectSmemT<kMaxSelThreads>;
 
 // Exclusive scan of one int per thread across the CTA (kT threads).
 template <int kT>
@@ -115,10 +118,10 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int32_t *warp_tot, in
 // (zero) in place, and write their selected positions in order after those
 // of the lower-ranked CTAs.  Returns false, with every CTA agreeing, when the
 // bucket is too large for this path (the caller continues digit by digit).
-template <int kT>
-__device__ bool select_from_bucket(uint32_t kb, int n_local, int pos0, int K, int32_t *out, SelectSmem &ss,
+template <int kT, class SS>
+__device__ bool select_from_bucket(uint32_t kb, int n_local, int pos0, int K, int32_t *out, SS &ss,
                                    uint32_t prefix, uint32_t mask, int krem) {
-    static_assert(kT <= kMaxSelThreads, "segment counters");
+    static_assert(kT * sizeof(int32_t) <= sizeof(ss.seg_sel), "segment counters");
     cg::cluster_group cluster = cg::this_cluster();
     const int C = (int)cluster.num_blocks(), my = (int)cluster.block_rank();
     const int tid = threadIdx.x;
@@ -250,9 +253,9 @@ __device__ bool select_from_bucket(uint32_t kb, int n_local, int pos0, int K, in
 // Writes min(K, n_valid) positions in ascending order to out[0..] and -1 to
 // the rest of out[0..K).  Every CTA of the cluster must call this with the
 // same n_valid and K (it contains cluster barriers).
-template <int kT>
+template <int kT, class SS>
 __device__ void cluster_topk(const uint32_t *keys, int n_local, int pos0, int n_valid, int K, int32_t *out,
-                             SelectSmem &ss, const uint32_t *hist0 = nullptr) {
+                             SS &ss, const uint32_t *hist0 = nullptr) {
     cg::cluster_group cluster = cg::this_cluster();
     const unsigned C = cluster.num_blocks();
     const unsigned my = cluster.block_rank();
@@ -719,6 +722,601 @@ __global__ void __launch_bounds__(kThreads, 1)
         int32_t *out = a.indices + (size_t)(t0 + gi) * a.K;
         cluster_topk<kThreads>(sKeys + (size_t)gi * key_cap, n_tiles * kTileM, tile0 * kTileM, n_valid, a.K, out,
                                *ss, sHist0 + gi * kHist);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Flat variant (bf16): the 128-position tiles of all query rows, row after
+// row, are split evenly over one CTA per SM.  A cluster launch places only as
+// many clusters as the GPCs hold (with four-CTA clusters, fewer CTAs than
+// SMs), and its rows reach their selection together while memory idles; here
+// every SM streams the same share of the index-key cache whatever the rows'
+// lengths.  Each CTA writes the keys of its positions (the order-preserving
+// form of the scores) to a workspace buffer and adds its counts of their top
+// 11 bits to the row's histogram there, then adds its number of the row's
+// tiles to the row's counter.  The CTA whose addition completes a row selects
+// that row's Top-K after its own scoring: one bulk copy stages the row's keys
+// in its shared memory (the query slots and the tile ring are free by then)
+// and the whole CTA runs a radix select over them.  Warps: 0 TMA, 1 MMA, 2..5
+// epilogue, as in the cluster kernel, and all eight in the selection; the
+// query rows' Q tiles come through two slots.
+constexpr int kFlatThreads = 256;
+constexpr int kFlatWarps = kFlatThreads / 32;
+constexpr int kFlatRowsMax = 512;           // query rows of one launch (row tables in shared memory)
+constexpr int kFlatQSlot = kHI * kDI * 2;   // 16 KB: both 64-column halves of one query row
+constexpr int kFlatBarEpi = 1;              // named barrier of the four epilogue warps
+constexpr int kFlatCandMax = 256;           // threshold-bucket keys the exact ranking takes
+constexpr int kFlatTopBits = 11;            // top digit counted while scoring
+constexpr int kFlatHist = 1 << kFlatTopBits;
+
+struct __align__(16) FlatBars {
+    uint64_t drain;
+    uint64_t full[8], empty[8];
+    uint64_t tfull[2], tempty[2];
+    uint64_t qfull[2], qempty[2];
+    uint64_t staged;  // a selected row's keys have landed in shared memory
+    uint32_t tmem_slot;
+    int abort[2];     // [0] a wait gave up; [1] wait limit in microseconds (0: default)
+    int n_sel;        // rows this CTA selects
+    int first_row;
+    int32_t scan[16];
+};
+
+// Scratch of the one-CTA selection; it overlays the box-row table, which only
+// the TMA producer reads.
+constexpr int kFlatSelMax = 49152;          // keys the selection takes (the query slots and a five-tile ring)
+struct __align__(16) FlatSel {
+    uint32_t hist[2048];                    // counts of the next digit
+    uint32_t gt_mask[kFlatSelMax / 32];     // per row of 32 positions: keys above the threshold bucket
+    uint32_t eq_mask[kFlatSelMax / 32];     // ... and keys in it
+    uint32_t cand_key[kFlatCandMax];
+    int32_t cand_pos[kFlatCandMax];
+    int32_t wscan[16];
+    uint32_t bcast[4];
+    uint32_t ncand;
+    uint32_t pad_[3];
+};
+
+// Byte offsets from the 1024-aligned base of the flat kernel's shared memory.
+struct FlatLayout {
+    size_t k, w, hist, prefix, len, seq, sel, rows, bars, total;
+};
+__host__ __device__ inline FlatLayout flat_layout(int stages, int T, int cap_tiles) {
+    auto r4 = [](size_t x) { return (x + 3) & ~(size_t)3; };
+    FlatLayout L;
+    L.k = 2 * (size_t)kFlatQSlot;                // two query slots, then the tile ring
+    L.w = L.k + (size_t)stages * kTileBytes;     // [2][64] head weights
+    L.hist = L.w + 2 * kHI * 4;                  // [2048] top-digit counts
+    L.prefix = L.hist + kFlatHist * 4;           // [T + 1] tiles before each row
+    L.len = L.prefix + r4(T + 1) * 4;            // [T] positions each row scores
+    L.seq = L.len + r4(T) * 4;                   // [T] sequence of each row
+    L.sel = L.seq + r4(T) * 4;                   // [cap] rows this CTA selects
+    L.rows = L.sel + r4(cap_tiles) * 4;          // [2 cap] cache row of every 64-position box / FlatSel
+    const size_t rows = (size_t)2 * cap_tiles * 4;
+    L.bars = L.rows + (rows > sizeof(FlatSel) ? rows : sizeof(FlatSel));
+    L.total = L.bars + sizeof(FlatBars);
+    return L;
+}
+
+// The row that holds flat tile i (i < prefix[T]): the last row starting at or
+// before it, which has at least one tile.
+__device__ __forceinline__ int flat_row_of(const int32_t *prefix, int T, int i) {
+    int lo = 0, hi = T - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (prefix[mid] <= i) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
+}
+
+// One radix digit, from the top: the digit whose bucket of the nb-bin
+// histogram (nb a multiple of kFlatThreads, at most 2048) at shared address
+// hb holds the krem-th largest counted key, and the number of counted keys
+// above that bucket.  Thread t sums bins nb-1-per*t down to nb-per*(t+1); an
+// exclusive scan over the threads (descending bins) finds the thread whose
+// bins hold the krem-th key, and it walks them.  Every thread returns the
+// result.  (If the counts add up to fewer than krem, digit 0 with nothing
+// above: every thread still takes the same branch.)
+__device__ __forceinline__ void flat_find_digit(uint32_t hb, int nb, int krem, FlatSel &fs, uint32_t *digit,
+                                                int *above) {
+    const int tid = threadIdx.x, per = nb / kFlatThreads;  // 8 or 4 bins
+    const int top = nb - 1 - per * tid;
+    uint32_t c[8];
+    if (per == 8) {
+        const uint4 hi = lds128(hb + 4 * (top - 3)), lo = lds128(hb + 4 * (top - 7));
+        c[0] = hi.w; c[1] = hi.z; c[2] = hi.y; c[3] = hi.x;
+        c[4] = lo.w; c[5] = lo.z; c[6] = lo.y; c[7] = lo.x;
+    } else {
+        const uint4 hi = lds128(hb + 4 * (top - 3));
+        c[0] = hi.w; c[1] = hi.z; c[2] = hi.y; c[3] = hi.x;
+        c[4] = c[5] = c[6] = c[7] = 0u;
+    }
+    const uint32_t part = ((c[0] + c[1]) + (c[2] + c[3])) + ((c[4] + c[5]) + (c[6] + c[7]));
+    if (tid == 0) {
+        fs.bcast[0] = 0u;
+        fs.bcast[1] = 0u;
+    }
+    const uint32_t excl = (uint32_t)block_exclusive_scan<kFlatThreads>((int)part, fs.wscan, nullptr);
+    const uint32_t kr = (uint32_t)krem;
+    if (excl < kr && kr <= excl + part) {
+        uint32_t ab = excl;
+        int i = 0;
+        for (; i < per - 1; ++i) {
+            if (ab + c[i] >= kr) break;
+            ab += c[i];
+        }
+        fs.bcast[0] = (uint32_t)(top - i);
+        fs.bcast[1] = ab;
+    }
+    __syncthreads();
+    *digit = fs.bcast[0];
+    *above = (int)fs.bcast[1];
+    __syncthreads();  // bcast and the scan scratch are rewritten by the next call
+}
+
+// Top-K of one row held in shared memory, by the whole CTA: keys[0..n) (every
+// position valid; n <= kFlatSelMax), hist0 (a shared address) = counts of
+// their top 11 bits.  Writes min(K, n) positions in ascending order to out,
+// then -1 padding.  Radix select from the top: the top 11 bits from hist0,
+// then 11 and 10 more, each digit a pass over the keys still in the
+// threshold bucket, until that bucket is taken whole, holds few enough keys
+// (kFlatCandMax) to rank exactly by (key descending, position ascending), or
+// all 32 bits are fixed (equal keys: lowest positions first).  One more pass
+// stores, per row of 32 positions, the ballot of its keys above the bucket
+// and of its keys in it; the ranked bucket keys are added to the first, and
+// each thread then writes the positions of a contiguous run of rows, in
+// order, at the slot an exclusive scan of the runs' counts gives it.
+// Shared memory is read through shared addresses.
+__device__ void flat_cta_topk(uint32_t *keys, int n, uint32_t hist0, int K, int32_t *out, FlatSel &fs) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (n <= K) {
+        for (int l = tid; l < K; l += kFlatThreads) out[l] = l < n ? l : -1;
+        return;
+    }
+    const uint32_t kb = smem_u32(keys), hb = smem_u32(fs.hist);
+    const int nq = (n + 3) >> 2;  // groups of four keys (the last one may be partial)
+
+    uint32_t digit;
+    int above;
+    flat_find_digit(hist0, kFlatHist, K, fs, &digit, &above);
+    int krem = K - above;
+    int shift = 32 - kFlatTopBits;
+    uint32_t prefix = digit << shift, mask = ~0u << shift, cnt = lds32(hist0 + 4 * digit);
+    while (cnt != (uint32_t)krem && cnt > (uint32_t)kFlatCandMax && shift > 0) {
+        const int width = shift > 10 ? 11 : shift, nshift = shift - width;
+        const uint32_t dm = (1u << width) - 1u;
+        for (int d = tid; d < kFlatHist; d += kFlatThreads) sts32(hb + 4 * d, 0u);
+        __syncthreads();
+        // four groups of four keys per thread per step, all loaded before any count
+        for (int q0 = tid; q0 < nq; q0 += 4 * kFlatThreads) {
+            uint4 v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int q = q0 + u * kFlatThreads;
+                v[u] = q < nq ? lds128(kb + 16 * q) : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int l = 4 * (q0 + u * kFlatThreads);
+                red_shared_add_if(hb + 4 * ((v[u].x >> nshift) & dm), l < n && (v[u].x & mask) == prefix);
+                red_shared_add_if(hb + 4 * ((v[u].y >> nshift) & dm), l + 1 < n && (v[u].y & mask) == prefix);
+                red_shared_add_if(hb + 4 * ((v[u].z >> nshift) & dm), l + 2 < n && (v[u].z & mask) == prefix);
+                red_shared_add_if(hb + 4 * ((v[u].w >> nshift) & dm), l + 3 < n && (v[u].w & mask) == prefix);
+            }
+        }
+        __syncthreads();
+        flat_find_digit(hb, kFlatHist >> (11 - width), krem, fs, &digit, &above);
+        digit &= dm;
+        krem -= above;
+        prefix |= digit << nshift;
+        mask |= dm << nshift;
+        cnt = lds32(hb + 4 * digit);
+        shift = nshift;
+        __syncthreads();  // everyone has read the histogram before it is cleared
+    }
+    // 0: the whole bucket is taken; 1: rank the bucket's keys; 2: equal keys
+    const int mode = cnt == (uint32_t)krem ? 0 : (cnt <= (uint32_t)kFlatCandMax ? 1 : 2);
+    const uint32_t ck = smem_u32(fs.cand_key), cp = smem_u32(fs.cand_pos), nca = smem_u32(&fs.ncand);
+    const uint32_t gm = smem_u32(fs.gt_mask), em = smem_u32(fs.eq_mask);
+    const int nrows = (n + 31) >> 5;
+    if (tid == 0) sts32(nca, 0u);
+    __syncthreads();
+    // ---- per row of 32 positions: keys above the bucket, keys in it (eight
+    // rows per warp per step, all loaded before any ballot)
+    for (int j0 = 8 * warp; j0 < nrows; j0 += 8 * kFlatWarps) {
+        uint32_t k[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int p = 32 * (j0 + u) + lane;
+            k[u] = p < n ? lds32(kb + 4 * p) : 0u;
+        }
+        uint32_t bg[8], be[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const bool in = 32 * (j0 + u) + lane < n;
+            const uint32_t m = k[u] & mask;
+            bg[u] = __ballot_sync(0xffffffffu, in && m > prefix);
+            be[u] = __ballot_sync(0xffffffffu, in && m == prefix);
+        }
+        if (lane < 8) {
+            // lane u stores row j0 + u (rows past the end are not stored)
+            uint32_t g = bg[0], e = be[0];
+#pragma unroll
+            for (int u = 1; u < 8; ++u) {
+                g = lane == u ? bg[u] : g;
+                e = lane == u ? be[u] : e;
+            }
+            if (j0 + lane < nrows) {
+                sts32(gm + 4 * (j0 + lane), g);
+                sts32(em + 4 * (j0 + lane), e);
+            }
+        }
+    }
+    __syncthreads();
+    if (mode == 1) {
+        // the bucket's keys (few): list them from the masks
+        for (int j = tid; j < nrows; j += kFlatThreads) {
+            uint32_t e = lds32(em + 4 * j);
+            while (e != 0u) {
+                const int p = 32 * j + __ffs(e) - 1;
+                e &= e - 1u;
+                const uint32_t c = atom_shared_add(nca, 1u);
+                if (c < (uint32_t)kFlatCandMax) {
+                    sts32(ck + 4 * c, lds32(kb + 4 * p));
+                    sts32(cp + 4 * c, (uint32_t)p);
+                }
+            }
+        }
+        __syncthreads();
+        // rank them; the selected ones join their row's mask
+        const int nc = min((int)lds32(nca), kFlatCandMax);
+        for (int i = tid; i < nc; i += kFlatThreads) {
+            const uint32_t ki = lds32(ck + 4 * i);
+            const int pi = (int)lds32(cp + 4 * i);
+            int r = 0, j = 0;
+            for (; j + 4 <= nc; j += 4) {
+                uint32_t kj[4];
+                int pj[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    kj[u] = lds32(ck + 4 * (j + u));
+                    pj[u] = (int)lds32(cp + 4 * (j + u));
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) r += (kj[u] > ki) || (kj[u] == ki && pj[u] < pi);
+            }
+            for (; j < nc; ++j) {
+                const uint32_t kj = lds32(ck + 4 * j);
+                r += (kj > ki) || (kj == ki && (int)lds32(cp + 4 * j) < pi);
+            }
+            if (r < krem) atomicOr(&fs.gt_mask[pi >> 5], 1u << (pi & 31));
+        }
+        __syncthreads();
+    }
+    // ---- each thread's run of rows: count, scan, write in order
+    const int per = (nrows + kFlatThreads - 1) / kFlatThreads;
+    const int j0 = min(nrows, tid * per), j1 = min(nrows, j0 + per);
+    int c_sel = 0, c_eq = 0;
+    for (int j = j0; j < j1; ++j) {
+        const uint32_t g = lds32(gm + 4 * j), e = lds32(em + 4 * j);
+        c_sel += __popc(mode == 0 ? (g | e) : g);
+        c_eq += __popc(e);
+    }
+    int eq_rank = 0;
+    if (mode == 2) {
+        eq_rank = block_exclusive_scan<kFlatThreads>(c_eq, fs.wscan, nullptr);
+        c_sel += min(max(krem - eq_rank, 0), c_eq);
+    }
+    int slot = block_exclusive_scan<kFlatThreads>(c_sel, fs.wscan, nullptr);
+    for (int j = j0; j < j1; ++j) {
+        uint32_t s = lds32(gm + 4 * j);
+        uint32_t e = lds32(em + 4 * j);
+        if (mode == 0) s |= e;
+        if (mode == 2) {
+            // the bucket's keys in position order: the first krem overall are taken
+            while (e != 0u && eq_rank < krem) {
+                s |= e & (0u - e);
+                e &= e - 1u;
+                ++eq_rank;
+            }
+        }
+        while (s != 0u) {
+            const int b = __ffs(s) - 1;
+            if (slot < K) out[slot] = 32 * j + b;
+            ++slot;
+            s &= s - 1u;
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kFlatThreads, 1)
+    indexer_topk_flat_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
+                             IndexerArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const FlatLayout L = flat_layout(a.stages, a.T, a.flat_cap_tiles);
+    uint8_t *sQ = smem;
+    uint8_t *sK = smem + L.k;
+    float *sW = reinterpret_cast<float *>(smem + L.w);
+    uint32_t *sHist = reinterpret_cast<uint32_t *>(smem + L.hist);
+    int32_t *sPrefix = reinterpret_cast<int32_t *>(smem + L.prefix);
+    int32_t *sLen = reinterpret_cast<int32_t *>(smem + L.len);
+    int32_t *sSeq = reinterpret_cast<int32_t *>(smem + L.seq);
+    int32_t *sSel = reinterpret_cast<int32_t *>(smem + L.sel);
+    int32_t *sRows = reinterpret_cast<int32_t *>(smem + L.rows);
+    FlatBars *bars = reinterpret_cast<FlatBars *>(smem + L.bars);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
+    const int max_len = a.max_pages * a.page_size;
+    grid_dep_wait();  // inputs written by the kernel launched just before are visible
+
+    // ---- every query row's length and sequence, and the tiles before it
+    {
+        const int per = (a.T + kFlatThreads - 1) / kFlatThreads;
+        const int r0 = min(a.T, tid * per), r1 = min(a.T, r0 + per);
+        int sum = 0;
+        for (int r = r0; r < r1; ++r) {
+            const int b = find_seq(a.cu_q, a.B, r);
+            const int c0 = __ldg(a.cu_q + b), nq = __ldg(a.cu_q + b + 1) - c0;
+            const int n = __ldg(a.seq_lens + b) - nq + (r - c0) + 1;  // causal history of row r
+            if (n > max_len && blockIdx.x == 0) report_error(a.err, kErrBadLen);
+            const int nc = max(0, min(n, max_len));
+            sLen[r] = nc;
+            sSeq[r] = b;
+            sum += (nc + kTileM - 1) / kTileM;
+        }
+        int total = 0;
+        int before = block_exclusive_scan<kFlatThreads>(sum, bars->scan, &total);
+        for (int r = r0; r < r1; ++r) {
+            sPrefix[r] = before;
+            before += (sLen[r] + kTileM - 1) / kTileM;
+        }
+        if (tid == 0) sPrefix[a.T] = total;
+    }
+    __syncthreads();
+    const int W = sPrefix[a.T], P = (int)gridDim.x, p = (int)blockIdx.x;
+    const int s0 = (int)((long long)p * W / P);
+    const int n_loc = min((int)((long long)(p + 1) * W / P) - s0, a.flat_cap_tiles);
+    const int s1 = s0 + n_loc;
+    // rows without a position (a sequence shorter than its query rows) select nothing
+    for (int r = p; r < a.T; r += P)
+        if (sPrefix[r + 1] == sPrefix[r])
+            for (int i = tid; i < a.K; i += kFlatThreads) a.indices[(size_t)r * a.K + i] = -1;
+    if (n_loc <= 0) return;  // the whole CTA leaves: it holds no tile and no row
+
+    if (tid == 0) {
+        for (int s = 0; s < a.stages; ++s) {
+            mbar_init(&bars->full[s], 1);
+            mbar_init(&bars->empty[s], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bars->tfull[i], 1);
+            mbar_init(&bars->tempty[i], 4);
+            mbar_init(&bars->qfull[i], 1);
+            mbar_init(&bars->qempty[i], 1);
+        }
+        mbar_init(&bars->staged, 1);
+        mbar_init(&bars->drain, 1);
+        bars->abort[0] = 0;
+        bars->abort[1] = wait_limit_us(a.err);
+        bars->n_sel = 0;
+        bars->first_row = flat_row_of(sPrefix, a.T, s0);
+        fence_mbar_init();
+    }
+    for (int h = tid; h < kFlatHist; h += kFlatThreads) sHist[h] = 0u;
+    // the physical row of every 64-position box of this CTA's tiles, up front
+    for (int j = tid; j < 2 * n_loc; j += kFlatThreads) {
+        const int i = s0 + (j >> 1);
+        const int r = flat_row_of(sPrefix, a.T, i);
+        const int p0 = (i - sPrefix[r]) * kTileM + (j & 1) * kBox;
+        int row = -1;
+        if (p0 < sLen[r]) {
+            const int page = __ldg(a.page_table + (size_t)sSeq[r] * a.max_pages + p0 / a.page_size);
+            if (page < 0 || (int64_t)page >= a.num_pages) report_error(a.err, kErrBadPage);
+            else row = page * a.page_size + p0 % a.page_size;
+        }
+        sRows[j] = row;
+    }
+    if (warp == 1) tmem_alloc(&bars->tmem_slot, 128);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_slot;
+    volatile int *abort = bars->abort;
+    const int wl = abort[1];  // test wait limit in microseconds (0: the default limit)
+    const int first_row = bars->first_row;
+
+    // Every role walks the CTA's tiles in order; a tile at or past row_end
+    // starts this CTA's next row (k counts them).
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- TMA producer
+            tma_prefetch_desc(&tm_k);
+            tma_prefetch_desc(&tm_q);
+            int r = first_row - 1, k = -1, row_end = s0, issued = 0, q_issued = 0;
+            for (int li = 0; li < n_loc; ++li) {
+                const int i = s0 + li;
+                if (i >= row_end) {
+                    do ++r;
+                    while (sPrefix[r + 1] <= i);
+                    row_end = sPrefix[r + 1];
+                    ++k;
+                    const int slot = k & 1;
+                    if (k >= 2 && !mbar_wait(&bars->qempty[slot], ((k - 2) >> 1) & 1, a.err, 0x121, abort, wl)) break;
+                    mbar_arrive_expect_tx(&bars->qfull[slot], 2 * kBoxBytes);
+                    tma_load_2d(sQ + slot * kFlatQSlot, &tm_q, &bars->qfull[slot], 0, r * kHI);
+                    tma_load_2d(sQ + slot * kFlatQSlot + kBoxBytes, &tm_q, &bars->qfull[slot], kBox, r * kHI);
+                    q_issued = k + 1;
+                }
+                const int s = li % a.stages;
+                if (li >= a.stages && !mbar_wait(&bars->empty[s], ((li / a.stages) & 1) ^ 1, a.err, 0x122, abort, wl))
+                    break;
+                issued = li + 1;
+                uint8_t *dst = sK + (size_t)s * kTileBytes;
+                int rows[2];
+                uint32_t bytes = 0;
+                for (int h = 0; h < 2; ++h) {
+                    rows[h] = sRows[2 * li + h];
+                    if (rows[h] >= 0) bytes += 2 * kBoxBytes;
+                }
+                mbar_arrive_expect_tx(&bars->full[s], bytes);
+                for (int h = 0; h < 2; ++h) {
+                    if (rows[h] < 0) continue;
+                    tma_load_2d(dst + h * kBoxBytes, &tm_k, &bars->full[s], 0, rows[h]);
+                    tma_load_2d(dst + kRegionBytes + h * kBoxBytes, &tm_k, &bars->full[s], kBox, rows[h]);
+                }
+            }
+            if (*abort) {
+                // let copies still in flight land before shared memory is reused or released
+                volatile int no_abort[2] = {0, 0};
+                for (int kk = max(0, q_issued - 2); kk < q_issued; ++kk)
+                    mbar_wait(&bars->qfull[kk & 1], (kk >> 1) & 1, nullptr, 0, no_abort);
+                for (int li = max(0, issued - a.stages); li < issued; ++li)
+                    mbar_wait(&bars->full[li % a.stages], (li / a.stages) & 1, nullptr, 0, no_abort);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---------------- tcgen05 issuer: D[128 positions x 64 heads] per tile
+            constexpr uint32_t idesc = idesc_bf16_f32(kTileM, kHI);
+            int r = first_row - 1, k = -1, row_end = s0;
+            for (int li = 0; li < n_loc; ++li) {
+                const int i = s0 + li;
+                if (i >= row_end) {
+                    do ++r;
+                    while (sPrefix[r + 1] <= i);
+                    row_end = sPrefix[r + 1];
+                    ++k;
+                    if (!mbar_wait(&bars->qfull[k & 1], (k >> 1) & 1, a.err, 0x221, abort, wl)) break;
+                }
+                const int s = li % a.stages, buf = li & 1;
+                if (!mbar_wait(&bars->full[s], (li / a.stages) & 1, a.err, 0x222, abort, wl)) break;
+                if (li >= 2 && !mbar_wait(&bars->tempty[buf], ((li >> 1) & 1) ^ 1, a.err, 0x223, abort, wl)) break;
+                tc_fence_after();
+                const uint32_t k_base = smem_u32(sK + (size_t)s * kTileBytes);
+                const uint32_t q_base = smem_u32(sQ + (k & 1) * kFlatQSlot);
+                const uint32_t d = tmem + (uint32_t)(buf * kHI);
+#pragma unroll
+                for (int kk = 0; kk < kDI / 16; ++kk) {
+                    const uint32_t off = (uint32_t)((kk & 3) * 32);
+                    const uint64_t adesc = sdesc_kmajor_sw128(k_base + (kk >> 2) * kRegionBytes + off);
+                    const uint64_t bdesc = sdesc_kmajor_sw128(q_base + (kk >> 2) * kBoxBytes + off);
+                    mma_bf16_ss(d, adesc, bdesc, idesc, kk > 0 ? 1u : 0u);
+                }
+                mma_commit(&bars->empty[s]);
+                mma_commit(&bars->tfull[buf]);
+                if (i + 1 == row_end || li + 1 == n_loc) mma_commit(&bars->qempty[k & 1]);
+            }
+            if (*abort) {
+                // wait for every issued MMA before TMEM is released
+                volatile int no_abort[2] = {0, 0};
+                mma_commit(&bars->drain);
+                mbar_wait(&bars->drain, 0, nullptr, 0, no_abort);
+            }
+        }
+    } else if (warp < 6) {
+        // ---------------- epilogue: warps 2..5, thread = position row of the tile
+        // (warps 6 and 7 wait for the selection)
+        const int quad = warp & 3, te = tid - 64;
+        const int row_t = quad * 32 + lane;
+        int r = first_row - 1, k = -1, row_end = s0, n = 0;
+        bool ok = true;  // equal across each warp; equal across the four warps at row ends
+        for (int li = 0; li < n_loc; ++li) {
+            const int i = s0 + li;
+            if (i >= row_end) {
+                do ++r;
+                while (sPrefix[r + 1] <= i);
+                row_end = sPrefix[r + 1];
+                ++k;
+                n = sLen[r];
+                if (te < kHI) sW[(k & 1) * kHI + te] = __ldg(a.head_w + (size_t)r * kHI + te);
+                bar_sync(kFlatBarEpi, 128);
+            }
+            const int buf = li & 1;
+            if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars->tfull[buf], (li >> 1) & 1, a.err, 0x321, abort, wl));
+            if (ok) {
+                tc_fence_after();
+                const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(buf * kHI);
+                uint32_t r0[32], r1[32];
+                tmem_ld32(taddr, r0);
+                tmem_ld32(taddr + 32, r1);
+                tmem_wait_ld();
+                const float *w = sW + (k & 1) * kHI;
+                float acc = 0.0f;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) acc = fmaf(w[j], fmaxf(__uint_as_float(r0[j]), 0.0f), acc);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) acc = fmaf(w[32 + j], fmaxf(__uint_as_float(r1[j]), 0.0f), acc);
+                const int pos = (i - sPrefix[r]) * kTileM + row_t;
+                if (pos < n) {
+                    const uint32_t key = score_key(acc);
+                    a.flat_keys[(size_t)r * a.ld_flat + pos] = key;
+                    red_shared_add(smem_u32(&sHist[key >> (32 - kFlatTopBits)]), 1u);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->tempty[buf]);
+            }
+            if (i + 1 == row_end || li + 1 == n_loc) {
+                // this CTA's tiles of row r are scored: publish its counts, then its tiles
+                ok = bar_and(kFlatBarEpi, 128, ok);
+                if (ok) {
+                    for (int h = te; h < kFlatHist; h += 128) {
+                        const uint32_t v = sHist[h];
+                        if (v) atomicAdd(a.flat_hist + (size_t)r * kFlatHist + h, v);
+                        sHist[h] = 0u;
+                    }
+                    __threadfence();
+                }
+                bar_sync(kFlatBarEpi, 128);
+                if (ok && te == 0) {
+                    const int mine = min(s1, row_end) - max(s0, sPrefix[r]);
+                    const int old = atomicAdd(a.flat_cnt + r, mine);
+                    if (old + mine == row_end - sPrefix[r]) {
+                        __threadfence();
+                        sSel[bars->n_sel++] = r;
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, 128);
+    if (tid == 0) grid_dep_launch();  // scoring is done: the next kernel may begin launching
+
+    // ---------------- selection of the rows this CTA completed
+    uint32_t *stage = reinterpret_cast<uint32_t *>(smem);  // query slots and tile ring, free now
+    FlatSel &fs = *reinterpret_cast<FlatSel *>(sRows);
+    const int n_sel = bars->n_sel;
+    for (int si = 0; si < n_sel; ++si) {
+        const int r = sSel[si];
+        const int n = sLen[r];
+        if (tid == 0) {
+            // the other CTAs' key stores (ordered before their counter
+            // additions) and this CTA's earlier use of the buffer come before
+            // the bulk copy
+            fence_proxy_async_global();
+            fence_proxy_async_smem();
+            const uint32_t bytes = (uint32_t)((n + 3) & ~3) * 4u;
+            mbar_arrive_expect_tx(&bars->staged, bytes);
+            const uint8_t *src = reinterpret_cast<const uint8_t *>(a.flat_keys + (size_t)r * a.ld_flat);
+            for (uint32_t o = 0; o < bytes; o += 32768u)
+                bulk_load(reinterpret_cast<uint8_t *>(stage) + o, src + o, min(32768u, bytes - o), &bars->staged);
+        }
+        for (int h = tid; h < kFlatHist; h += kFlatThreads) sHist[h] = __ldcg(a.flat_hist + (size_t)r * kFlatHist + h);
+        const bool landed = mbar_wait(&bars->staged, si & 1, a.err, 0x421, abort, wl);
+        if (!__syncthreads_and(landed)) {
+            // the row stays unselected (the error is recorded); the copy lands before the CTA leaves
+            volatile int no_abort[2] = {0, 0};
+            if (tid == 0) mbar_wait(&bars->staged, si & 1, nullptr, 0, no_abort);
+            break;
+        }
+        flat_cta_topk(stage, n, smem_u32(sHist), a.K, a.indices + (size_t)r * a.K, fs);
+        __syncthreads();
     }
 }
 
@@ -1208,6 +1806,42 @@ int indexer_mxfp8_max_active_clusters(int G, int C, size_t smem) {
         return 0;
     }
     return n;
+}
+
+int indexer_flat_rows_max() { return kFlatRowsMax; }
+
+int indexer_flat_hist_bins() { return kFlatHist; }
+
+int indexer_flat_stage_keys(int stages) {
+    const int k = (int)((2 * (size_t)kFlatQSlot + (size_t)stages * kTileBytes) / 4);
+    return k < kFlatSelMax ? k : kFlatSelMax;
+}
+
+size_t indexer_flat_smem_bytes(int stages, int T, int cap_tiles) {
+    return 1024 + flat_layout(stages, T, cap_tiles).total;
+}
+
+cudaError_t launch_indexer_flat(const CUtensorMap &tk, const CUtensorMap &tq, const IndexerArgs &a, int ctas,
+                                size_t smem, cudaStream_t st) {
+    auto kern = indexer_topk_flat_kernel;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)ctas, 1, 1);
+    cfg.blockDim = dim3(kFlatThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    // a cluster of one: the selection's barriers then span this CTA alone
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, kern, tk, tq, a);
 }
 
 size_t topk_smem_bytes(int chunk_cap) { return 16 + (size_t)((chunk_cap + 3) & ~3) * 4 + sizeof(SelectSmem); }

@@ -28,6 +28,12 @@ struct IndexerArgs {
     int32_t stages;             // smem ring depth (<= 8)
     int32_t tiles_cap;          // 128-position tiles one CTA can hold keys for
     int32_t grid_order;         // 1: query rows in grid order instead of longest first (measurement knob)
+    // flat kernel only (workspace buffers; hist and cnt zeroed before the launch)
+    uint32_t *flat_keys;        // [T, ld_flat] order-preserving keys of the scores
+    uint32_t *flat_hist;        // [T, indexer_flat_hist_bins()] top-digit histograms
+    int32_t *flat_cnt;          // [T] tiles of the row scored so far
+    int64_t ld_flat;            // keys per row (multiple of 4, >= max_pages * page_size)
+    int32_t flat_cap_tiles;     // tiles one CTA may be given (multiple of 4)
 };
 
 struct TopkArgs {
@@ -47,6 +53,16 @@ cudaError_t launch_topk_from_scores(const TopkArgs &a, int C, size_t smem, cudaS
 // Clusters of C CTAs of the G-query indexer kernel with `smem` bytes that can
 // be resident at once (0 if the shape cannot launch).
 int indexer_max_active_clusters(int G, int C, size_t smem);
+// Flat bf16 indexer: `ctas` CTAs (one per SM) share the 128-position tiles of
+// all T query rows evenly; the CTA that completes a row selects its Top-K.
+// Needs T <= indexer_flat_rows_max() and rows of at most
+// indexer_flat_stage_keys(stages) positions.
+int indexer_flat_rows_max();
+int indexer_flat_hist_bins();  // per-row histogram words in the workspace
+int indexer_flat_stage_keys(int stages);
+size_t indexer_flat_smem_bytes(int stages, int T, int cap_tiles);
+cudaError_t launch_indexer_flat(const CUtensorMap &tm_k, const CUtensorMap &tm_q, const IndexerArgs &a, int ctas,
+                                size_t smem, cudaStream_t st);
 // MXFP8 variant (G = 1 or 2 query rows of one sequence per cluster).
 size_t indexer_mxfp8_smem_bytes(int G, int stages, int tiles_cap);
 // quant_q: q_idx arrives in bf16 (a.q_bf16) and the kernel quantises it to

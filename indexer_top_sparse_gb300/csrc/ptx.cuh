@@ -246,6 +246,9 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+// The same for global memory: generic-proxy stores (of any thread, acquired
+// before this fence) become visible to this thread's bulk copies.
+__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 
 // ---------------------------------------------------------------- tcgen05
 __device__ __forceinline__ void tmem_alloc(uint32_t *slot_smem, uint32_t ncols) {
@@ -297,6 +300,25 @@ __device__ __forceinline__ void sts32(uint32_t saddr, uint32_t v) {
 }
 __device__ __forceinline__ void red_shared_add(uint32_t saddr, uint32_t v) {
     asm volatile("red.shared.add.u32 [%0], %1;" ::"r"(saddr), "r"(v) : "memory");
+}
+// red.shared.add of 1 under a predicate (no branch around it).
+__device__ __forceinline__ void red_shared_add_if(uint32_t saddr, bool pred) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "@p red.shared.add.u32 [%0], 1;\n\t}" ::"r"(saddr),
+        "r"((uint32_t)pred)
+        : "memory");
+}
+__device__ __forceinline__ uint4 lds128(uint32_t saddr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(saddr));
+    return v;
+}
+__device__ __forceinline__ uint32_t atom_shared_add(uint32_t saddr, uint32_t v) {
+    uint32_t old;
+    asm volatile("atom.shared.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(saddr), "r"(v) : "memory");
+    return old;
 }
 
 // Programmatic dependent launch: wait until the grids this one depends on

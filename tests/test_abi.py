@@ -69,3 +69,13 @@ def test_host_validation_rejects_bad_arguments(lib):
     assert lib.dsa_workspace_init(None, 0, None) == 1
     assert lib.dsa_index_topk_workspace_size(1, 1, 1, 1, 64) >= 16
     assert lib.dsa_sparse_mla_workspace_size(1, 128, 2048) >= 16
+
+
+def test_flat_indexer_is_chosen_for_large_decode_batches(lib):
+    # the workspace size reports whether the flat bf16 indexer applies: one
+    # query row per sequence and at least 3 * 2^20 positions in all, rows of
+    # at most 49152 positions
+    assert lib.dsa_index_topk_workspace_size(96, 96, 2048, 512, 64) > 256       # 96 x 32768
+    assert lib.dsa_index_topk_workspace_size(32, 32, 2048, 512, 64) == 256      # 32 x 32768
+    assert lib.dsa_index_topk_workspace_size(1, 4096, 2048, 512, 64) == 256     # a prefill: rows share a sequence
+    assert lib.dsa_index_topk_workspace_size(96, 96, 2048, 1024, 64) == 256     # rows past the staging limit

@@ -6,7 +6,7 @@ pipeline, lets its own copies and tensor-core work finish, frees its tensor
 memory and returns (the indexer's CTAs still pass every cluster barrier
 together), so the context stays usable.  A test-only wait limit of one
 microsecond (dsa_workspace_set_wait_limit) makes the waits of the fused
-indexer and of the sparse MLA run out on purpose: nothing is left unset,
+indexer (its cluster and flat forms) and of the sparse MLA run out on purpose: nothing is left unset,
 every wait simply gives up early.  The same call with the default limit is
 then correct again, checked against the oracle.  No kernel is made to fault
 or hang."""
@@ -28,19 +28,21 @@ def _expect_timeout(d, ws):
     ws.check()  # the error word was cleared
 
 
-def test_indexer_wait_runs_out_then_recovers(orc):
+@pytest.mark.parametrize("flat", [1, -1], ids=["flat", "cluster"])
+def test_indexer_wait_runs_out_then_recovers(orc, flat):
     import indexer_top_sparse_gb300 as d
     wl = make_workload("timeout_idx", [32768] * 8, [1] * 8, H=16, K=2048, page_size=64, seed=61, with_kv=False)
     t = to_device(wl)
-    ws = d.Workspace(d.index_topk_workspace_size(wl.B, wl.T, wl.K, wl.max_pages, wl.page_size))
-    ws.set_wait_limit(1)
-    d.dsa_index_topk(t["q_idx"], t["head_w"], t["k_idx"], t["page_table"], t["seq_lens"], t["cu_q"], wl.K,
-                     workspace=ws)
-    _expect_timeout(d, ws)
-    ws.set_wait_limit(0)
-    idx = d.dsa_index_topk(t["q_idx"], t["head_w"], t["k_idx"], t["page_table"], t["seq_lens"], t["cu_q"], wl.K,
-                           workspace=ws)
-    ws.check()
+    with tuning(indexer_flat=flat):
+        ws = d.Workspace(d.index_topk_workspace_size(wl.B, wl.T, wl.K, wl.max_pages, wl.page_size))
+        ws.set_wait_limit(1)
+        d.dsa_index_topk(t["q_idx"], t["head_w"], t["k_idx"], t["page_table"], t["seq_lens"], t["cu_q"], wl.K,
+                         workspace=ws)
+        _expect_timeout(d, ws)
+        ws.set_wait_limit(0)
+        idx = d.dsa_index_topk(t["q_idx"], t["head_w"], t["k_idx"], t["page_table"], t["seq_lens"], t["cu_q"],
+                               wl.K, workspace=ws)
+        ws.check()
     idx = idx.cpu().numpy()
     rows = np.array([0, 5], np.int32)
     ref_idx, ref_sc = orc.index_topk(wl.q_idx, wl.head_w, wl.k_idx, wl.page_table, wl.seq_lens, wl.cu_q, wl.K,
