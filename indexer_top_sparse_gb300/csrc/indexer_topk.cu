@@ -727,10 +727,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---------------------------------------------------------------------------
 // Flat variant (bf16): the 128-position tiles of all query rows, row after
-// row, are split evenly over one CTA per SM.  A cluster launch places only as
-// many clusters as the GPCs hold (with four-CTA clusters, fewer CTAs than
-// SMs), and its rows reach their selection together while memory idles; here
-// every SM streams the same share of the index-key cache whatever the rows'
+// row, are split evenly over one CTA per SM.  A cluster grid covers the SMs
+// only where the rows times the cluster size fit them (32 rows on clusters of
+// four take 128 of 152 SMs; 160 rows on one-CTA clusters need a second wave),
+// and its rows reach their selection together while memory idles; here every
+// SM streams the same share of the index-key cache whatever the rows'
 // lengths.  Each CTA writes the keys of its positions (the order-preserving
 // form of the scores) to a workspace buffer and adds its counts of their top
 // 11 bits to the row's histogram there, then adds its number of the row's
