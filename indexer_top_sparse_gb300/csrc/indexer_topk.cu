@@ -109,6 +109,39 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int32_t *warp_tot, in
     return before + x - v;
 }
 
+// Warp 0 (lanes = threads 0..31): the 8-bit digit whose bucket of h[256]
+// holds the krem-th largest counted key, and the count above that bucket,
+// into bcast[0], bcast[1] (left as they are if the counts add up to fewer
+// than krem).
+__device__ __forceinline__ void digit_from_top_warp(const uint32_t *h, int krem, uint32_t *bcast) {
+    const int lane = threadIdx.x & 31;
+    // digits from high to low: lane L owns digits 255-8L .. 248-8L
+    uint32_t part = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) part += h[255 - 8 * lane - i];
+    uint32_t incl = part;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    uint32_t excl = incl - part;
+    bool mine = excl < (uint32_t)krem && (uint32_t)krem <= incl;
+    unsigned ball = __ballot_sync(0xffffffffu, mine);
+    int src = __ffs(ball) - 1;
+    if (lane == src) {
+        uint32_t above = excl;
+        int digit = 255 - 8 * lane;
+        for (int i = 0; i < 8; ++i, --digit) {
+            uint32_t c = h[digit];
+            if (above + c >= (uint32_t)krem) break;
+            above += c;
+        }
+        bcast[0] = (uint32_t)digit;
+        bcast[1] = above;
+    }
+}
+
 // Final step of the selection once two radix digits have fixed the top 16
 // bits of the threshold (prefix under mask) and krem keys are still needed
 // from that 16-bit bucket, which typically holds a few dozen keys: every CTA
@@ -129,23 +162,34 @@ __device__ bool select_from_bucket(uint32_t kb, int n_local, int pos0, int K, in
     ss.seg_sel[tid] = 0;
     if (tid < kMaxCluster) ss.cta_sel[tid] = 0;
     __syncthreads();
-    const int seg = (n_local + kT - 1) / kT;
+    // segments of a multiple of four keys, read 16 bytes at a time (the key
+    // buffers are 16-byte aligned and readable up to n_local rounded up to 4)
+    const int seg = (((n_local + kT - 1) / kT) + 3) & ~3;
     const int l0 = min(n_local, tid * seg), l1 = min(n_local, l0 + seg);
     int n_gt = 0;
-    // loads four at a time, then the tests (keeps several loads in flight)
-    for (int l = l0; l < l1; l += 4) {
-        uint32_t k4[4];
+    for (int l = l0; l < l1; l += 8) {
+        // both 16-byte loads issued before either is used
+        const uint4 va = lds128(kb + 4 * l);
+        const uint4 vb = l + 4 < l1 ? lds128(kb + 4 * (l + 4)) : make_uint4(0u, 0u, 0u, 0u);
+        const uint32_t k8[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
+        uint32_t eqm = 0u;
 #pragma unroll
-        for (int u = 0; u < 4; ++u) k4[u] = l + u < l1 ? lds32(kb + 4 * (l + u)) : 0u;
+        for (int u = 0; u < 8; ++u) {
+            const uint32_t m = k8[u] & mask;
+            const bool in = l + u < l1 && k8[u] != 0u;
+            n_gt += (in && m > prefix) ? 1 : 0;
+            eqm |= (in && m == prefix) ? 1u << u : 0u;
+        }
+        if (eqm != 0u) {
+            // (rare) keys in the bucket
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const uint32_t k = k4[u], m = k & mask;
-            n_gt += k != 0u && m > prefix;
-            if (k != 0u && m == prefix) {
-                const uint32_t c = atomicAdd(&ss.ncand, 1u);
-                if (c < (uint32_t)kCandCap) {
-                    ss.cand_key[c] = k;
-                    ss.cand_loc[c] = l + u;
+            for (int u = 0; u < 8; ++u) {
+                if ((eqm >> u) & 1u) {
+                    const uint32_t c = atomicAdd(&ss.ncand, 1u);
+                    if (c < (uint32_t)kCandCap) {
+                        ss.cand_key[c] = k8[u];
+                        ss.cand_loc[c] = l + u;
+                    }
                 }
             }
         }
@@ -201,30 +245,52 @@ __device__ bool select_from_bucket(uint32_t kb, int n_local, int pos0, int K, in
     }
     __syncthreads();
     cluster_arrive();  // done reading the other CTAs; the matching wait is at the end
+    // Rank the bucket's keys (they share the top 16 bits): one more digit
+    // (bits 15..8) takes the keys above its bucket and leaves the rest out;
+    // the few keys in it are ranked by (key descending, position ascending).
+    // ss.hist[0] is free: the other CTAs read it only before pass 1's barrier.
+    uint32_t *h2 = ss.hist[0];
+    for (int d = tid; d < kHist; d += kT) h2[d] = 0u;
+    if (tid == 0) {
+        ss.bcast[0] = 0u;
+        ss.bcast[1] = 0u;
+    }
+    __syncthreads();
+    for (int i = tid; i < total; i += kT) red_shared_add(smem_u32(&h2[(ss.all_key[i] >> 8) & 0xFFu]), 1u);
+    __syncthreads();
+    if (tid < 32) digit_from_top_warp(h2, krem, ss.bcast);
+    __syncthreads();
+    const uint32_t d2 = ss.bcast[0] & 0xFFu;
+    const int krem2 = krem - (int)ss.bcast[1];
     const uint32_t ak = smem_u32(ss.all_key), ap = smem_u32(ss.all_pos);
     for (int i = tid; i < total; i += kT) {
         const uint32_t ki = ss.all_key[i];
         const int pi = ss.all_pos[i];
-        int r = 0;
-        int j = 0;
-        for (; j + 4 <= total; j += 4) {
-            uint32_t kj[4];
-            int pj[4];
+        bool sel = ((ki >> 8) & 0xFFu) > d2;
+        if (((ki >> 8) & 0xFFu) == d2) {
+            // (the shared loads are issued eight at a time: each volatile load
+            // would otherwise wait for the one before)
+            int r = 0, j = 0;
+            for (; j + 8 <= total; j += 8) {
+                uint32_t kj[8];
+                int pj[8];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                kj[u] = lds32(ak + 4 * (j + u));
-                pj[u] = (int)lds32(ap + 4 * (j + u));
+                for (int u = 0; u < 8; ++u) kj[u] = lds32(ak + 4 * (j + u));
+#pragma unroll
+                for (int u = 0; u < 8; ++u) pj[u] = (int)lds32(ap + 4 * (j + u));
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    r += ((kj[u] >> 8) & 0xFFu) == d2 && ((kj[u] > ki) || (kj[u] == ki && pj[u] < pi));
             }
-#pragma unroll
-            for (int u = 0; u < 4; ++u) r += (kj[u] > ki) || (kj[u] == ki && pj[u] < pi);
+            for (; j < total; ++j) {
+                const uint32_t kj = lds32(ak + 4 * j);
+                const int pj = (int)lds32(ap + 4 * j);
+                r += ((kj >> 8) & 0xFFu) == d2 && ((kj > ki) || (kj == ki && pj < pi));
+            }
+            sel = r < krem2;
         }
-        for (; j < total; ++j) {
-            const uint32_t kj = lds32(ak + 4 * j);
-            r += (kj > ki) || (kj == ki && (int)lds32(ap + 4 * j) < pi);
-        }
-        const bool sel = r < krem;
         const int c = ss.all_cta[i];
-        if (sel) atomicAdd(&ss.cta_sel[c], 1);
+        ss.all_cta[i] = c | (sel ? 0x10000 : 0);  // (no other thread reads entry i)
         if (c == my) {
             const int l = pi - pos0;
             sts32(kb + 4 * l, sel ? 0xFFFFFFFFu : 0u);
@@ -232,16 +298,28 @@ __device__ bool select_from_bucket(uint32_t kb, int n_local, int pos0, int K, in
         }
     }
     __syncthreads();
+    // selected candidates of each CTA (its candidates are one run of the list)
+    {
+        const int warp = tid >> 5, lane = tid & 31;
+        for (int c = warp; c < C; c += kT / 32) {
+            int n = 0;
+            for (int i = ss.cta_off[c] + lane; i < ss.cta_off[c + 1]; i += 32) n += ss.all_cta[i] >> 16;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) n += __shfl_xor_sync(0xffffffffu, n, o);
+            if (lane == 0) ss.cta_sel[c] = n;
+        }
+    }
+    __syncthreads();
     int base = 0;
     for (int c = 0; c < my; ++c) base += ss.cta_gt[c] + ss.cta_sel[c];
     int slot = base + block_exclusive_scan<kT>(n_gt + ss.seg_sel[tid], ss.scan[0], nullptr);
-    for (int l = l0; l < l1; l += 4) {
-        uint32_t k4[4];
+    for (int l = l0; l < l1; l += 8) {
+        const uint4 va = lds128(kb + 4 * l);
+        const uint4 vb = l + 4 < l1 ? lds128(kb + 4 * (l + 4)) : make_uint4(0u, 0u, 0u, 0u);
+        const uint32_t k8[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
 #pragma unroll
-        for (int u = 0; u < 4; ++u) k4[u] = l + u < l1 ? lds32(kb + 4 * (l + u)) : 0u;
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-            if (k4[u] != 0u && (k4[u] & mask) > prefix && slot < K) out[slot++] = pos0 + l + u;
+        for (int u = 0; u < 8; ++u)
+            if (l + u < l1 && k8[u] != 0u && (k8[u] & mask) > prefix && slot < K) out[slot++] = pos0 + l + u;
     }
     cluster_wait();  // nobody leaves while another CTA may still read its candidates
     return true;
@@ -288,30 +366,40 @@ __device__ void cluster_topk(const uint32_t *keys, int n_local, int pos0, int n_
             for (int d = tid; d < kHist; d += kT) h[d] = 0u;
             __syncthreads();
             const uint32_t hb = smem_u32(h);
+            // eight keys per thread loaded before any count; counts predicated
             int l = tid;
-            for (; l + 3 * kT < n_local; l += 4 * kT) {
-                uint32_t k4[4];
+            for (; l + 7 * kT < n_local; l += 8 * kT) {
+                uint32_t k8[8];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) k4[u] = lds32(kb + 4 * (l + u * kT));
+                for (int u = 0; u < 8; ++u) k8[u] = lds32(kb + 4 * (l + u * kT));
 #pragma unroll
-                for (int u = 0; u < 4; ++u)
-                    if (k4[u] != 0u && (k4[u] & mask) == prefix) red_shared_add(hb + 4 * ((k4[u] >> shift) & 0xFFu), 1u);
+                for (int u = 0; u < 8; ++u)
+                    red_shared_add_if(hb + 4 * ((k8[u] >> shift) & 0xFFu), k8[u] != 0u && (k8[u] & mask) == prefix);
             }
             for (; l < n_local; l += kT) {
                 const uint32_t k = lds32(kb + 4 * l);
-                if (k != 0u && (k & mask) == prefix) red_shared_add(hb + 4 * ((k >> shift) & 0xFFu), 1u);
+                red_shared_add_if(hb + 4 * ((k >> shift) & 0xFFu), k != 0u && (k & mask) == prefix);
             }
         }
         cluster.sync();
-        for (int d = tid; d < kHist; d += kT) {
-            // issue every remote load before summing (they are independent)
-            uint32_t v[kMaxCluster];
+        for (int d4 = tid; d4 < kHist / 4; d4 += kT) {
+            // four bins per thread, four CTAs' loads issued before summing
+            uint4 s = make_uint4(0u, 0u, 0u, 0u);
+            for (int c0 = 0; c0 < (int)C; c0 += 4) {
+                uint4 v[4];
 #pragma unroll
-            for (int c = 0; c < kMaxCluster; ++c) v[c] = c < (int)C ? cluster.map_shared_rank(h, c)[d] : 0u;
-            uint32_t s = 0;
+                for (int u = 0; u < 4; ++u)
+                    v[u] = c0 + u < (int)C ? reinterpret_cast<const uint4 *>(cluster.map_shared_rank(h, c0 + u))[d4]
+                                           : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-            for (int c = 0; c < kMaxCluster; ++c) s += v[c];
-            ss.tot[d] = s;
+                for (int u = 0; u < 4; ++u) {
+                    s.x += v[u].x;
+                    s.y += v[u].y;
+                    s.z += v[u].z;
+                    s.w += v[u].w;
+                }
+            }
+            reinterpret_cast<uint4 *>(ss.tot)[d4] = s;
         }
         // digit 0, nothing above it, unless a lane below finds the digit that
         // holds the krem-th key: after an aborted wait the counts may add up
@@ -322,33 +410,7 @@ __device__ void cluster_topk(const uint32_t *keys, int n_local, int pos0, int n_
             ss.bcast[1] = 0u;
         }
         __syncthreads();
-        if (tid < 32) {
-            // digits from high to low: lane L owns digits 255-8L .. 248-8L
-            uint32_t part = 0;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) part += ss.tot[255 - 8 * tid - i];
-            uint32_t incl = part;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-                if (tid >= o) incl += y;
-            }
-            uint32_t excl = incl - part;
-            bool mine = excl < (uint32_t)krem && (uint32_t)krem <= incl;
-            unsigned ball = __ballot_sync(0xffffffffu, mine);
-            int src = __ffs(ball) - 1;
-            if (tid == src) {
-                uint32_t above = excl;
-                int digit = 255 - 8 * tid;
-                for (int i = 0; i < 8; ++i, --digit) {
-                    uint32_t c = ss.tot[digit];
-                    if (above + c >= (uint32_t)krem) break;
-                    above += c;
-                }
-                ss.bcast[0] = (uint32_t)digit;
-                ss.bcast[1] = above;
-            }
-        }
+        if (tid < 32) digit_from_top_warp(ss.tot, krem, ss.bcast);
         __syncthreads();
         // (masked: after an aborted wait the counts may not add up)
         const uint32_t digit = ss.bcast[0] & 0xFFu;
