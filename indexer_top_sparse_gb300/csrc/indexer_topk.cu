@@ -44,7 +44,13 @@ constexpr int kBox = 64;         // rows / columns per TMA box
 constexpr int kBoxBytes = kBox * kBox * 2;           // 8 KB
 constexpr int kTileBytes = kTileM * kDI * 2;         // 32 KB
 constexpr int kRegionBytes = kTileM * 128;           // one 64-column half of a tile: 16 KB
-constexpr int kThreads = 192;
+constexpr int kThreads = 192;    // score-row selection kernel
+// The bf16 indexer: warp 0 TMA, warps 1 and 6 tcgen05 issue (even and odd
+// tiles), warps 2..5 epilogue.  One thread's waits, MMA issues and commits
+// for a tile take longer than the tensor core needs for it, so two threads
+// issue alternate tiles.
+constexpr int kIdxThreads = 224;
+constexpr int kIdxIssuer2 = 6;
 constexpr int kHist = 256;
 constexpr int kMaxCluster = 16;
 
@@ -58,7 +64,7 @@ __device__ __forceinline__ uint32_t score_key(float x) {
 
 constexpr int kCandCap = 128;   // threshold-bucket keys one CTA may hand to the bucket selection
 constexpr int kAllCap = 512;    // the same for the whole cluster
-constexpr int kMaxSelThreads = 320;
+constexpr int kMaxSelThreads = 384;
 
 // Shared state of the cluster selection for up to kSegMax threads per CTA.
 template <int kSegMax>
@@ -486,7 +492,7 @@ struct IdxLayout {
 };
 
 struct __align__(16) IdxBars {
-    uint64_t drain;
+    uint64_t drain[2];  // one per issuing thread
     uint64_t full[8];
     uint64_t empty[8];
     uint64_t tfull[2];
@@ -557,7 +563,7 @@ __device__ int ordered_query(const IndexerArgs &a, int row, int *scratch, int *b
 }
 
 template <int G, bool kWriteScores>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kIdxThreads, 1)
     indexer_topk_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
                              IndexerArgs a) {
     using L = IdxLayout<G>;
@@ -585,7 +591,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     {
         if (G == 1) {
             if ((int)blockIdx.y >= a.T) return;
-            t0 = ordered_query<kThreads>(a, blockIdx.y, reinterpret_cast<int *>(ss), &b);
+            t0 = ordered_query<kIdxThreads>(a, blockIdx.y, reinterpret_cast<int *>(ss), &b);
             gn = 1;
         } else {
             // last (longest, in a causal prefill) groups first
@@ -628,21 +634,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bars->tfull[i], 1);
             mbar_init(&bars->tempty[i], 4);
+            mbar_init(&bars->drain[i], 1);
         }
         mbar_init(&bars->qbar, 1);
-        mbar_init(&bars->drain, 1);
         bars->abort[0] = 0;
         bars->abort[1] = wait_limit_us(a.err);
         fence_mbar_init();
     }
-    for (int i = threadIdx.x; i < G * kHI; i += kThreads) {
+    for (int i = threadIdx.x; i < G * kHI; i += kIdxThreads) {
         int gi = i / kHI;
         sW[i] = gi < gn ? __ldg(a.head_w + (size_t)(t0 + gi) * kHI + (i % kHI)) : 0.0f;
     }
-    for (int i = threadIdx.x; i < G * kHist; i += kThreads) sHist0[i] = 0u;
+    for (int i = threadIdx.x; i < G * kHist; i += kIdxThreads) sHist0[i] = 0u;
     // resolve the physical row of every 64-position box of this CTA's range up
     // front, so that the TMA producer never waits on a page-table load
-    for (int j = threadIdx.x; j < 2 * n_tiles; j += kThreads) {
+    for (int j = threadIdx.x; j < 2 * n_tiles; j += kIdxThreads) {
         const int p0 = tile0 * kTileM + j * kBox;
         int row = -1;
         if (p0 <= pos_last) {
@@ -698,14 +704,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_wait(&bars->full[i % a.stages], (i / a.stages) & 1, nullptr, 0, no_abort);
             }
         }
-    } else if (warp == 1) {
+    } else if (warp == 1 || warp == kIdxIssuer2) {
         if (lane == 0) {
-            // ---------------- tcgen05 issuer
+            // ---------------- tcgen05 issuers: tile i by warp 1 (i even) or kIdxIssuer2 (i odd),
+            // into accumulator i & 1; each commits its own MMAs
+            const int par = warp == 1 ? 0 : 1;
             constexpr uint32_t idesc = idesc_bf16_f32(kTileM, L::kN);
             bool ok = mbar_wait(&bars->qbar, 0, a.err, 0x201, abort, wl);
             const uint32_t q_base = smem_u32(sQ);
-            for (int i = 0; ok && i < n_tiles; ++i) {
-                const int s = i % a.stages, buf = i & 1;
+            for (int i = par; ok && i < n_tiles; i += 2) {
+                const int s = i % a.stages, buf = par;
                 if (!mbar_wait(&bars->full[s], (i / a.stages) & 1, a.err, 0x202, abort, wl)) break;
                 if (i >= 2 && !mbar_wait(&bars->tempty[buf], ((i >> 1) & 1) ^ 1, a.err, 0x203, abort, wl)) break;
                 tc_fence_after();
@@ -724,8 +732,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (*abort) {
                 // wait for every issued MMA before TMEM is released
                 volatile int no_abort[2] = {0, 0};
-                mma_commit(&bars->drain);
-                mbar_wait(&bars->drain, 0, nullptr, 0, no_abort);
+                mma_commit(&bars->drain[par]);
+                mbar_wait(&bars->drain[par], 0, nullptr, 0, no_abort);
             }
         }
     } else {
@@ -782,7 +790,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const int n_valid = pos_first + gi + 1;
         int32_t *out = a.indices + (size_t)(t0 + gi) * a.K;
-        cluster_topk<kThreads>(sKeys + (size_t)gi * key_cap, n_tiles * kTileM, tile0 * kTileM, n_valid, a.K, out,
+        cluster_topk<kIdxThreads>(sKeys + (size_t)gi * key_cap, n_tiles * kTileM, tile0 * kTileM, n_valid, a.K, out,
                                *ss, sHist0 + gi * kHist);
     }
 }
@@ -1399,10 +1407,14 @@ __global__ void __launch_bounds__(kFlatThreads, 1)
 // One cluster serves G query rows of one sequence (G = 1 for decode, 2 in a
 // prefill, where consecutive rows read the same history): the G rows' queries
 // are stacked in the MMA's N dimension (64 G), so each key tile is read once
-// for all of them.  Warps: 0 TMA, 1 MMA, 2..5 epilogue (one per TMEM lane
-// quadrant, thread = position, all 64 heads of every row), 6..9 block scales
-// into TMEM.
-constexpr int kF8Threads = 320;
+// for all of them.  Warps: 0 and 11 TMA, 1 and 10 MMA (even and odd tiles
+// each: one thread's waits, issues and commits for a tile take longer than
+// the copy engine and the tensor core need for it), 2..5 epilogue (one per
+// TMEM lane quadrant, thread = position, all 64 heads of every row), 6..9
+// block scales into TMEM.
+constexpr int kF8Threads = 384;
+constexpr int kF8Issuer2 = 10;
+constexpr int kF8Producer2 = 11;
 constexpr int kF8TileBytes = kTileM * kDI;      // 16 KB of E4M3 keys per tile
 constexpr int kF8BoxBytes = kBox * kDI;         // 8 KB per 64-row box
 
@@ -1413,7 +1425,7 @@ struct __align__(16) F8Bars {
     uint64_t tempty[4];
     uint64_t sf_full[4];  // tile i's key scales are in TMEM scale buffer i % bufs
     uint64_t qbar;
-    uint64_t drain;
+    uint64_t drain[2];  // one per issuing thread
     uint32_t tmem_slot;
     int abort[2];  // [0] a wait gave up; [1] wait limit in microseconds (0: default)
 };
@@ -1505,7 +1517,8 @@ __global__ void __launch_bounds__(kF8Threads, 1)
             mbar_init(&bars->sf_full[i], 4);
         }
         mbar_init(&bars->qbar, 1);
-        mbar_init(&bars->drain, 1);
+        mbar_init(&bars->drain[0], 1);
+        mbar_init(&bars->drain[1], 1);
         bars->abort[0] = 0;
         bars->abort[1] = wait_limit_us(a.err);
         fence_mbar_init();
@@ -1537,16 +1550,21 @@ __global__ void __launch_bounds__(kF8Threads, 1)
     volatile int *abort = bars->abort;
     const int wl = abort[1];  // test wait limit in microseconds (0: the default limit)
 
-    if (warp == 0) {
+    if (warp == 0 || warp == kF8Producer2) {
         if (lane == 0) {
+            // tile i by warp 0 (i even; also the query) or kF8Producer2 (i odd)
+            const int par = warp == 0 ? 0 : 1;
             tma_prefetch_desc(&tm_k);
             if constexpr (!kQuantQ) {
-                tma_prefetch_desc(&tm_q);
-                mbar_arrive_expect_tx(&bars->qbar, (uint32_t)(gn * kHI * kDI));
-                for (int gi = 0; gi < gn; ++gi) tma_load_2d(sQ + gi * kHI * kDI, &tm_q, &bars->qbar, 0, (t0 + gi) * kHI);
+                if (par == 0) {
+                    tma_prefetch_desc(&tm_q);
+                    mbar_arrive_expect_tx(&bars->qbar, (uint32_t)(gn * kHI * kDI));
+                    for (int gi = 0; gi < gn; ++gi)
+                        tma_load_2d(sQ + gi * kHI * kDI, &tm_q, &bars->qbar, 0, (t0 + gi) * kHI);
+                }
             }
-            int issued = 0;
-            for (int i = 0; i < n_tiles; ++i) {
+            int issued = 0;  // one past this thread's last issued tile
+            for (int i = par; i < n_tiles; i += 2) {
                 const int s = i % a.stages;
                 if (i >= a.stages && !mbar_wait(&bars->empty[s], ((i / a.stages) & 1) ^ 1, a.err, 0x121, abort, wl))
                     break;
@@ -1562,17 +1580,20 @@ __global__ void __launch_bounds__(kF8Threads, 1)
                 }
             }
             if (*abort) {
+                // let this thread's copies still in flight land before shared memory is released
                 volatile int no_abort[2] = {0, 0};
-                mbar_wait(&bars->qbar, 0, nullptr, 0, no_abort);
+                if (par == 0) mbar_wait(&bars->qbar, 0, nullptr, 0, no_abort);
                 for (int i = max(0, issued - a.stages); i < issued; ++i)
-                    mbar_wait(&bars->full[i % a.stages], (i / a.stages) & 1, nullptr, 0, no_abort);
+                    if ((i & 1) == par) mbar_wait(&bars->full[i % a.stages], (i / a.stages) & 1, nullptr, 0, no_abort);
             }
         }
-    } else if (warp == 1) {
+    } else if (warp == 1 || warp == kF8Issuer2) {
         if (lane == 0) {
+            // tile i by warp 1 (i even) or kF8Issuer2 (i odd); each commits its own MMAs
+            const int par = warp == 1 ? 0 : 1;
             bool ok = mbar_wait(&bars->qbar, 0, a.err, 0x221, abort, wl);
             const uint32_t q_base = smem_u32(sQ);
-            for (int i = 0; ok && i < n_tiles; ++i) {
+            for (int i = par; ok && i < n_tiles; i += 2) {
                 const int s = i % a.stages, buf = i % kBufs;
                 const uint32_t round = (uint32_t)(i / kBufs) & 1u;
                 if (!mbar_wait(&bars->full[s], (i / a.stages) & 1, a.err, 0x222, abort, wl)) break;
@@ -1590,8 +1611,8 @@ __global__ void __launch_bounds__(kF8Threads, 1)
             }
             if (*abort) {
                 volatile int no_abort[2] = {0, 0};
-                mma_commit(&bars->drain);
-                mbar_wait(&bars->drain, 0, nullptr, 0, no_abort);
+                mma_commit(&bars->drain[par]);
+                mbar_wait(&bars->drain[par], 0, nullptr, 0, no_abort);
             }
         }
     } else if (warp < 6) {
@@ -1618,21 +1639,25 @@ __global__ void __launch_bounds__(kF8Threads, 1)
             const int pos = (tile0 + i) * kTileM + row;
 #pragma unroll
             for (int gi = 0; gi < G; ++gi) {
-                float2 part2 = make_float2(0.0f, 0.0f);
+                // four independent pairs of partial sums (heads 8m + 0,1 / 2,3 / 4,5 / 6,7),
+                // so the additions do not wait on one another
+                float2 p[4] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f),
+                               make_float2(0.0f, 0.0f)};
                 const float4 *w4 = reinterpret_cast<const float4 *>(sW + gi * kHI);
 #pragma unroll
                 for (int k = 0; k < 16; ++k) {
                     const float4 w = w4[k];
-                    part2 = __ffma2_rn(make_float2(w.x, w.y),
-                                       make_float2(fmaxf(__uint_as_float(r[gi][4 * k]), 0.0f),
-                                                   fmaxf(__uint_as_float(r[gi][4 * k + 1]), 0.0f)),
-                                       part2);
-                    part2 = __ffma2_rn(make_float2(w.z, w.w),
-                                       make_float2(fmaxf(__uint_as_float(r[gi][4 * k + 2]), 0.0f),
-                                                   fmaxf(__uint_as_float(r[gi][4 * k + 3]), 0.0f)),
-                                       part2);
+                    const int c = 2 * (k & 1);
+                    p[c] = __ffma2_rn(make_float2(w.x, w.y),
+                                      make_float2(fmaxf(__uint_as_float(r[gi][4 * k]), 0.0f),
+                                                  fmaxf(__uint_as_float(r[gi][4 * k + 1]), 0.0f)),
+                                      p[c]);
+                    p[c + 1] = __ffma2_rn(make_float2(w.z, w.w),
+                                          make_float2(fmaxf(__uint_as_float(r[gi][4 * k + 2]), 0.0f),
+                                                      fmaxf(__uint_as_float(r[gi][4 * k + 3]), 0.0f)),
+                                          p[c + 1]);
                 }
-                const float sc = part2.x + part2.y;
+                const float sc = ((p[0].x + p[1].x) + (p[2].x + p[3].x)) + ((p[0].y + p[1].y) + (p[2].y + p[3].y));
                 const bool valid = gi < gn && pos <= pos_first + gi;
                 const uint32_t key = valid ? score_key(sc) : 0u;
                 sKeys[(size_t)gi * key_cap + i * kTileM + row] = key;
@@ -1921,7 +1946,7 @@ static cudaError_t launch_idx(const CUtensorMap &tk, const CUtensorMap &tq, cons
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)C, (unsigned)groups, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.blockDim = dim3(kIdxThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[2];
@@ -1955,7 +1980,7 @@ static int max_clusters_g(int C, size_t smem) {
         return 0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)C, 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.blockDim = dim3(kIdxThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
