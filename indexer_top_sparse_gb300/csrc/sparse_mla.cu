@@ -65,7 +65,12 @@ constexpr int kQRegion = 64 * 128;           // Q rows padded to the MMA's M = 6
 constexpr int kProd = MLA_PRODUCER_WARPS;
 constexpr int kMmaWarp = kProd;
 constexpr int kSmWarp0 = kProd + 1;          // 4 softmax / epilogue warps
-constexpr int kThreads = (kProd + 1 + 4) * 32;
+// Second tcgen05 issuer (split mode): kMmaWarp issues the logits and P*V of
+// the even tiles, kMmaWarp2 those of the odd tiles, so that the logits of the
+// next tile are issued while this tile's softmax runs (one thread's issues
+// and waits for a tile take longer than the tensor core needs for them).
+constexpr int kMmaWarp2 = kSmWarp0 + 4;
+constexpr int kThreads = (kProd + 1 + 4 + 1) * 32;
 constexpr int kSmThreads = 128;
 constexpr int kBarSm = 1;
 constexpr int kBarProd = 2;
@@ -86,7 +91,9 @@ struct __align__(16) MlaBars {
     // the peer, so the forwarding copies have finished reading it here and
     // the rope region may take P
     uint64_t fwd_done[kStages];
-    uint64_t p_full, o_done, o_full, q_full, drain, table;
+    uint64_t p_full[2];  // P of tile i is in its stage: p_full[i & 1]
+    uint64_t drain[2];   // one per issuing thread
+    uint64_t o_done, o_full, q_full, table;
     uint64_t o_free;  // stream-K: the epilogue of segment 0 has read O
     uint32_t tmem_slot;
     int abort[2];  // [0] a wait gave up; [1] wait limit in microseconds (0: default)
@@ -251,12 +258,14 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
             mbar_init(&bars->fwd_done[i], 1);
         }
         for (int i = 0; i < 2; ++i) mbar_init(&bars->s_full[i], 1);
-        mbar_init(&bars->p_full, kSmThreads / 32);
+        mbar_init(&bars->p_full[0], kSmThreads / 32);
+        mbar_init(&bars->p_full[1], kSmThreads / 32);
         mbar_init(&bars->o_done, 1);
         mbar_init(&bars->o_full, 1);
         mbar_init(&bars->o_free, kSmThreads / 32);
         mbar_init(&bars->q_full, 1);
-        mbar_init(&bars->drain, 1);
+        mbar_init(&bars->drain[0], 1);
+        mbar_init(&bars->drain[1], 1);
         mbar_init(&bars->table, 1);
         bars->abort[0] = 0;
         bars->abort[1] = wait_limit_us(a.err);
@@ -441,16 +450,50 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
             volatile int no_abort[2] = {0, 0};
             mbar_wait(&bars->q_full, 0, nullptr, 0, no_abort);
         }
-    } else if (warp == kMmaWarp) {
-        // ---------------------------------------------------------------- tcgen05 issuer
-        if (lane == 0) {
-            constexpr uint32_t idesc_s = idesc_bf16_f32(64, kKeys);
-            // P*V always runs with N = 64 (all 64 rows of P); columns NH..63
-            // are unused when NH < 64
-            constexpr uint32_t idesc_o = idesc_bf16_f32_amn(128, 64);  // A (V^T) MN-major, B (P) K-major
-            const uint32_t q_base = smem_u32(sQ), kv_base = smem_u32(sKV);
+    } else if (warp == kMmaWarp || warp == kMmaWarp2) {
+        // ---------------------------------------------------------------- tcgen05 issuers
+        constexpr uint32_t idesc_s = idesc_bf16_f32(64, kKeys);
+        // P*V always runs with N = 64 (all 64 rows of P); columns NH..63
+        // are unused when NH < 64
+        constexpr uint32_t idesc_o = idesc_bf16_f32_amn(128, 64);  // A (V^T) MN-major, B (P) K-major
+        const uint32_t q_base = smem_u32(sQ), kv_base = smem_u32(sKV);
+        uint32_t *const err = a.err;
+        if (!kSK && lane == 0) {
+            // split mode: tile i's logits and P*V by kMmaWarp (i even) or
+            // kMmaWarp2 (i odd).  Logits of tile i go to S buffer i & 1, which
+            // the softmax of tile i - 2 has read (p_full) before this thread
+            // issued that tile's P*V; P*V of tile i follows the softmax of tile
+            // i, which waited for P*V of tile i - 1 (o_done), so the additions
+            // into O^T stay in tile order.
+            const int par = warp == kMmaWarp ? 0 : 1;
             bool ok = mbar_wait(&bars->q_full, 0, a.err, 0x502, abort, wl);
-            uint32_t *const err = a.err;
+            for (int i = par; ok && i < n_tiles; i += 2) {
+                if (!(ok = issue_s_tile(i, bars, kv_base, q_base, tmem_s, idesc_s, err, abort, wl))) break;
+                if (!(ok = mbar_wait(&bars->p_full[i & 1], (i >> 1) & 1, a.err, 0x504, abort, wl))) break;
+                tc_fence_after();
+                const int stg = i % kStages;
+                const uint32_t kb = kv_base + stg * kTileBytes;
+                const uint64_t ad0 = sdesc_mnmajor_sw128(kb, kRegionBytes, 1024);
+                const uint64_t bd0 = sdesc_kmajor_sw128(kb + 8 * kRegionBytes);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+#pragma unroll
+                    for (int j = 0; j < kKeys / 16; ++j)
+                        mma_bf16_ss(tmem_o + c * 64, ad0 + (uint64_t)((2 * c * kRegionBytes + j * 2048) >> 4),
+                                    bd0 + (uint64_t)((j * 32) >> 4), idesc_o, (i > 0 || j > 0) ? 1u : 0u);
+                }
+                mma_commit(&bars->kv_empty[stg]);
+                mma_commit(&bars->o_done);
+                // every earlier P*V has completed (o_done of tile i - 1 came before P of tile i)
+                if (i + 1 == n_tiles) mma_commit(&bars->o_full);
+            }
+            if (*abort) {
+                volatile int no_abort[2] = {0, 0};
+                mma_commit(&bars->drain[par]);
+                mbar_wait(&bars->drain[par], 0, nullptr, 0, no_abort);
+            }
+        } else if (kSK && warp == kMmaWarp && lane == 0) {
+            bool ok = mbar_wait(&bars->q_full, 0, a.err, 0x502, abort, wl);
             // Before the logits of segment 1's first tile: the last logits of
             // segment 0 have read Q, so its rows are replaced by segment 1's.
             auto switch_q = [&](int i) -> bool {
@@ -470,7 +513,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
                 if (kStages > 2 && i + 1 < n_tiles &&
                     !(ok = switch_q(i + 1) && issue_s_tile(i + 1, bars, kv_base, q_base, tmem_s, idesc_s, err, abort, wl)))
                     break;
-                if (!(ok = mbar_wait(&bars->p_full, i & 1, a.err, 0x504, abort, wl))) break;
+                if (!(ok = mbar_wait(&bars->p_full[i & 1], (i >> 1) & 1, a.err, 0x504, abort, wl))) break;
                 // segment 1 starts a fresh accumulator once segment 0's epilogue has read O
                 const int first = seg_of(i) ? s1 : 0;
                 if (kSK && i == s1 && !(ok = mbar_wait(&bars->o_free, 0, a.err, 0x50c, abort, wl))) break;
@@ -497,10 +540,10 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
             if (ok && n_tiles > 0) mma_commit(&bars->o_full);
             if (*abort) {
                 volatile int no_abort[2] = {0, 0};
-                mma_commit(&bars->drain);
-                mbar_wait(&bars->drain, 0, nullptr, 0, no_abort);
+                mma_commit(&bars->drain[0]);
+                mbar_wait(&bars->drain[0], 0, nullptr, 0, no_abort);
             }
-        } else if (kPair && lane == 1) {
+        } else if (kPair && warp == kMmaWarp && lane == 1) {
             // Pairs: tell the peer as soon as each tile -- including the half
             // the peer forwarded -- has landed here; the peer then knows that
             // its forwarding copies have read the rows it may overwrite.
@@ -699,7 +742,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
             fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->p_full);
+            if (lane == 0) mbar_arrive(&bars->p_full[i & 1]);
         }
         // ---------------------------------------------------------------- epilogue
         epilogue(n_seg - 1, true);
