@@ -103,8 +103,8 @@ const char *dsa_status_string(dsa_status s);
  * heads, run the two 64-head CTAs of a query as a cluster sharing every
  * gathered row: 1 yes, -1 or 0 no), "mla_stream_k" (64-head CTAs, one per SM, share
  * all (row, head group, key tile) units evenly instead of a split grid: 1 yes
- * where it applies, -1 no, 0 automatic = when the split grid would leave SMs
- * idle with one split per row; it needs the workspace
+ * where it applies, -1 or 0 no (the split grid, whose CTAs issue their even
+ * and odd key tiles from two threads, measured faster); it needs the workspace
  * dsa_sparse_mla_workspace_size reports, and a
  * smaller workspace of the split grid's size keeps it off), "mla_dsplit"
  * (128 heads, bf16 cache: one CTA pair per query row and key split that

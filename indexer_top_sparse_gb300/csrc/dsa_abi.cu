@@ -313,24 +313,19 @@ bool mla_pair(int T, int H, int splits) {
 // Stream-K sparse MLA: CTAs (one per SM) for T rows of H heads with K keys,
 // or 0 for the split grid.  It applies with 64-head CTAs when every CTA gets
 // 2..tpr key tiles (so a CTA's run spans at most two (row, head group) pairs
-// and its row table fits).  Automatically only where it measured faster on
-// GB300: the split grid has fewer CTAs than SMs with one split per (row, head
-// group) (64 x 4k-128k FP8 decode: 137 -> 131 us).  With two or more splits
-// (32 x 32768 decode) the even share of 13.5 instead of 16 tiles per CTA was
-// slower (60 against 57 us, and a larger combine): the two head groups of a
-// row no longer gather the same rows at the same time.
+// and its row table fits).  Only when asked for: the split grid issues each
+// CTA's even and odd tiles from two threads, stream-K from one, and on GB300
+// the split grid measured faster on both decode workloads (64 x 4k-128k FP8
+// decode: 115.7 against 127.3 us; 32 x 32768 bf16 decode: 55.5 against
+// 70.0 us).
 int mla_sk_ctas(int T, int H, int K) {
     const int forced = g_mla_sk.load();
-    if (forced < 0 || mla_heads_per_cta(H) != 64 || g_mla_splits.load() > 0 || g_mla_pair.load() > 0 || T <= 0 ||
+    if (forced <= 0 || mla_heads_per_cta(H) != 64 || g_mla_splits.load() > 0 || g_mla_pair.load() > 0 || T <= 0 ||
         K <= 0)
         return 0;
     const int nsm = sm_count(), tile = dsa::mla_key_tile(), tpr = ceil_div(K, tile);
     const int groups = mla_groups(H), cg = nsm / groups;  // CTAs per head group
     const long long units = (long long)T * tpr;           // per head group
-    if (forced == 0) {
-        const int splits = mla_splits(T, H, K);
-        if (splits > 1 || (long long)T * groups * splits >= nsm) return 0;
-    }
     const long long per = (units + cg - 1) / cg;
     if (cg < 1 || units < 2LL * cg || per > tpr || per * tile > 2048) return 0;
     return cg * groups;

@@ -221,14 +221,14 @@ def test_stream_k_matches(orc, case, fp8):
 
 
 def test_stream_k_off_and_on_agree(orc):
-    # the decode shape where stream-K is the automatic choice, against the
-    # split grid (stream-K off): the same attention up to summation order
+    # a decode shape with one split per row and fewer CTAs than SMs, stream-K
+    # forced on against the split grid: the same attention up to summation order
     import indexer_top_sparse_gb300 as d
     rng = np.random.default_rng(150)
     wl = make_workload("sk2", [4000] * 16, [1] * 16, H=128, K=2048, page_size=64, seed=150, with_idx=False)
     idx = dev(_random_indices(rng, wl, 2048))
     outs = []
-    for mode in (0, -1):
+    for mode in (1, -1):
         d.set_tuning("mla_stream_k", mode)
         d.set_tuning("mla_dsplit", -1)
         try:
