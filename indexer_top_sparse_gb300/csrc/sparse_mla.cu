@@ -86,6 +86,9 @@ struct MlaLayout {
 
 struct __align__(16) MlaBars {
     uint64_t kv_full[kStages], kv_empty[kStages], s_full[2];
+    // bf16 cache, unpaired: the first kEarlyRegions regions of the stage's
+    // tile have landed (the logits start on them while the rest lands)
+    uint64_t kv_early[kStages];
     uint64_t peer_free[kStages];   // pairs: the peer's copy of this stage may be overwritten
     // pairs: every byte of this CTA's half of the stage's tile has landed in
     // the peer, so the forwarding copies have finished reading it here and
@@ -100,6 +103,7 @@ struct __align__(16) MlaBars {
 };
 
 constexpr int kMaxKeysPerSplit = 2048;       // host keeps keys_per_split <= this
+constexpr int kEarlyRegions = 5;             // regions behind kv_early (bf16 cache, unpaired)
 
 struct __align__(16) MlaStats {
     int32_t rows[kMaxKeysPerSplit];             // physical cache row of every key of the split
@@ -153,19 +157,28 @@ __device__ __forceinline__ void dequant16(const uint4 v, const float s, uint32_t
     }
 }
 
-// Issue S = Q . K_tile^T for tile i into S buffer i&1 once the tile landed.
+// Issue S = Q . K_tile^T for tile i into S buffer i&1 once the tile landed
+// (kEarly: the first kEarlyRegions regions' steps once those have landed,
+// the rest once the whole tile has).
+template <bool kEarly>
 __device__ __forceinline__ bool issue_s_tile(int i, MlaBars *bars, uint32_t kv_base, uint32_t q_base, uint32_t tmem_s,
                                              uint32_t idesc_s, uint32_t *err, volatile int *abort, int wl) {
     const int st = i % kStages;
-    if (!mbar_wait(&bars->kv_full[st], (i / kStages) & 1, err, 0x503, abort, wl)) return false;
-    fence_proxy_async_smem();  // the tile was written through the generic proxy
-    tc_fence_after();
     // descriptors advance by (byte offset >> 4) in their start-address field
     const uint64_t ad0 = sdesc_kmajor_sw128(q_base);
     const uint64_t bd0 = sdesc_kmajor_sw128(kv_base + st * kTileBytes);
     const uint32_t d = tmem_s + kKeys * (i & 1);
 #pragma unroll
     for (int r = 0; r < kRegions; ++r) {
+        if (r == (kEarly ? kEarlyRegions : 0)) {
+            if (!mbar_wait(&bars->kv_full[st], (i / kStages) & 1, err, 0x503, abort, wl)) return false;
+            fence_proxy_async_smem();  // the tile was written through the generic proxy
+            tc_fence_after();
+        } else if (kEarly && r == 0) {
+            if (!mbar_wait(&bars->kv_early[st], (i / kStages) & 1, err, 0x515, abort, wl)) return false;
+            fence_proxy_async_smem();
+            tc_fence_after();
+        }
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
             mma_bf16_ss(d, ad0 + (uint64_t)((r * kQRegion + kk * 32) >> 4),
@@ -253,6 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
         constexpr int kFullArrivals = 32 * kProd + (kF8 ? kProd : 0) + (kPair ? 1 : 0);
         for (int i = 0; i < kStages; ++i) {
             mbar_init(&bars->kv_full[i], kFullArrivals);
+            mbar_init(&bars->kv_early[i], 32 * kProd);
             mbar_init(&bars->kv_empty[i], 1);
             mbar_init(&bars->peer_free[i], 1);
             mbar_init(&bars->fwd_done[i], 1);
@@ -380,14 +394,24 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
             const int32_t *rows = st->rows + i * kKeys;
             uint64_t *done = &bars->kv_full[stg];
             if constexpr (!kF8) {
+                // (unpaired: the first kEarlyRegions regions complete kv_early)
+                auto copy_regions = [&](int r0, int r1) {
 #pragma unroll 3
-                for (int r = 0; r < kRegions; ++r) {
+                    for (int r = r0; r < r1; ++r) {
 #pragma unroll
-                    for (int m = 0; m < kKPW * 8 / 32; ++m) {
-                        const int f = m * 32 + lane, key = key0 + (f >> 3), cc = f & 7;
-                        const uint8_t *src = a.kv + (size_t)rows[key] * (kD * 2) + r * 128 + cc * 16;
-                        cp_async16(dst + r * kRegionBytes + key * 128 + ((cc ^ (key & 7)) << 4), src);
+                        for (int m = 0; m < kKPW * 8 / 32; ++m) {
+                            const int f = m * 32 + lane, key = key0 + (f >> 3), cc = f & 7;
+                            const uint8_t *src = a.kv + (size_t)rows[key] * (kD * 2) + r * 128 + cc * 16;
+                            cp_async16(dst + r * kRegionBytes + key * 128 + ((cc ^ (key & 7)) << 4), src);
+                        }
                     }
+                };
+                if constexpr (!kPair) {
+                    copy_regions(0, kEarlyRegions);
+                    cp_async_arrive(&bars->kv_early[stg]);
+                    copy_regions(kEarlyRegions, kRegions);
+                } else {
+                    copy_regions(0, kRegions);
                 }
                 cp_async_arrive(done);
             } else {
@@ -468,7 +492,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
             const int par = warp == kMmaWarp ? 0 : 1;
             bool ok = mbar_wait(&bars->q_full, 0, a.err, 0x502, abort, wl);
             for (int i = par; ok && i < n_tiles; i += 2) {
-                if (!(ok = issue_s_tile(i, bars, kv_base, q_base, tmem_s, idesc_s, err, abort, wl))) break;
+                if (!(ok = issue_s_tile<!kPair && !kF8>(i, bars, kv_base, q_base, tmem_s, idesc_s, err, abort, wl))) break;
                 if (!(ok = mbar_wait(&bars->p_full[i & 1], (i >> 1) & 1, a.err, 0x504, abort, wl))) break;
                 tc_fence_after();
                 const int stg = i % kStages;
@@ -504,14 +528,14 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
                     tma_load_2d(sQ + r * kQRegion, &tm_q, &bars->q_full, 64 * r, seg[1].t * a.H + seg[1].hg * NH);
                 return mbar_wait(&bars->q_full, 1, a.err, 0x50b, abort, wl);
             };
-            if (ok && n_tiles > 0) ok = issue_s_tile(0, bars, kv_base, q_base, tmem_s, idesc_s, err, abort, wl);
+            if (ok && n_tiles > 0) ok = issue_s_tile<!kPair && !kF8>(0, bars, kv_base, q_base, tmem_s, idesc_s, err, abort, wl);
             for (int i = 0; ok && i < n_tiles; ++i) {
                 // With a ring of 3+ tiles the next tile's logits are issued
                 // first, so that they overlap this tile's softmax; with only
                 // 2 buffers the next tile is still loading, so this tile's
                 // P*V goes first (it frees the buffer the tile after needs).
                 if (kStages > 2 && i + 1 < n_tiles &&
-                    !(ok = switch_q(i + 1) && issue_s_tile(i + 1, bars, kv_base, q_base, tmem_s, idesc_s, err, abort, wl)))
+                    !(ok = switch_q(i + 1) && issue_s_tile<!kPair && !kF8>(i + 1, bars, kv_base, q_base, tmem_s, idesc_s, err, abort, wl)))
                     break;
                 if (!(ok = mbar_wait(&bars->p_full[i & 1], (i >> 1) & 1, a.err, 0x504, abort, wl))) break;
                 // segment 1 starts a fresh accumulator once segment 0's epilogue has read O
@@ -534,7 +558,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const __grid
                 mma_commit(&bars->o_done);
                 if (i + 1 == s1 && s1 < n_tiles) mma_commit(&bars->o_full);  // segment 0 is complete
                 if (kStages <= 2 && i + 1 < n_tiles &&
-                    !(ok = switch_q(i + 1) && issue_s_tile(i + 1, bars, kv_base, q_base, tmem_s, idesc_s, err, abort, wl)))
+                    !(ok = switch_q(i + 1) && issue_s_tile<!kPair && !kF8>(i + 1, bars, kv_base, q_base, tmem_s, idesc_s, err, abort, wl)))
                     break;
             }
             if (ok && n_tiles > 0) mma_commit(&bars->o_full);
