@@ -48,8 +48,12 @@ constexpr int kThreads = 192;    // score-row selection kernel
 // The bf16 indexer: warp 0 TMA, warps 1 and 6 tcgen05 issue (even and odd
 // tiles), warps 2..5 epilogue.  One thread's waits, MMA issues and commits
 // for a tile take longer than the tensor core needs for it, so two threads
-// issue alternate tiles.
-constexpr int kIdxThreads = 224;
+// issue alternate tiles.  With one query row per cluster (decode) five more
+// warps join only the selection, whose passes over the keys are bound by
+// latency at two warps per scheduler; the wider epilogue registers of
+// several rows leave no room for them.
+template <int G>
+constexpr int idx_threads() { return G == 1 ? 384 : 224; }
 constexpr int kIdxIssuer2 = 6;
 constexpr int kHist = 256;
 constexpr int kMaxCluster = 16;
@@ -563,10 +567,11 @@ __device__ int ordered_query(const IndexerArgs &a, int row, int *scratch, int *b
 }
 
 template <int G, bool kWriteScores>
-__global__ void __launch_bounds__(kIdxThreads, 1)
+__global__ void __launch_bounds__(idx_threads<G>(), 1)
     indexer_topk_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
                              IndexerArgs a) {
     using L = IdxLayout<G>;
+    constexpr int kIdxThreads = idx_threads<G>();
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int key_cap = a.tiles_cap * kTileM;
@@ -736,7 +741,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
                 mbar_wait(&bars->drain[par], 0, nullptr, 0, no_abort);
             }
         }
-    } else {
+    } else if (warp < 6) {
         // ---------------- epilogue: warps 2..5, thread = position row
         const int quad = warp & 3;
         const int row = quad * 32 + lane;
@@ -1946,7 +1951,7 @@ static cudaError_t launch_idx(const CUtensorMap &tk, const CUtensorMap &tq, cons
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)C, (unsigned)groups, 1);
-    cfg.blockDim = dim3(kIdxThreads, 1, 1);
+    cfg.blockDim = dim3(idx_threads<G>(), 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[2];
@@ -1980,7 +1985,7 @@ static int max_clusters_g(int C, size_t smem) {
         return 0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)C, 1, 1);
-    cfg.blockDim = dim3(kIdxThreads, 1, 1);
+    cfg.blockDim = dim3(idx_threads<G>(), 1, 1);
     cfg.dynamicSmemBytes = smem;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
