@@ -137,14 +137,24 @@ int cached_max_clusters(int G, int C, size_t smem) {
     return n;
 }
 
+// Ring depth a forced "indexer_stages" value stands for in the cluster
+// indexers: even (an odd value is taken one lower), since their two tcgen05
+// issuing threads (and the MXFP8 kernel's two producers) take alternate
+// tiles, and with an even depth every stage belongs to one of each -- each
+// stage's barrier phases are then waited in order by one thread, so a parity
+// wait cannot pass a phase early.
+int even_stages(int forced) { return forced > 0 ? std::max(2, forced & ~1) : 0; }
+
 // Launch shape of the fused indexer: G query rows per cluster, C CTAs per
-// cluster, ring depth.  Preference: the fewest waves (clusters / resident
-// clusters), then the most CTAs in flight, then the deepest ring; a CTA keeps
-// at least 4 tiles of history unless the shape is forced.
+// cluster, ring depth (even, see even_stages).  Preference: the fewest waves
+// (clusters / resident clusters), then the most CTAs in flight, then the
+// deepest ring; a CTA keeps at least 4 tiles of history unless the shape is
+// forced.
 bool plan_indexer(int B, int T, int max_len, IdxPlan *p) {
     const size_t smax = max_smem_optin();
     const int tiles_max = std::max(1, ceil_div(max_len, 128));
-    const int g_force = g_idx_group.load(), c_force = g_idx_cluster.load(), s_force = g_idx_stages.load();
+    const int g_force = g_idx_group.load(), c_force = g_idx_cluster.load(),
+              s_force = even_stages(g_idx_stages.load());
     bool found = false;
     long long best_waves = 0, best_used = 0;
     int best_stages = 0;
@@ -155,7 +165,7 @@ bool plan_indexer(int B, int T, int max_len, IdxPlan *p) {
             if (c_force && C != c_force) continue;
             const int tiles_cap = ceil_div(tiles_max, C);
             if (!c_force && C > 1 && tiles_cap < 4) continue;
-            for (int stages = 6; stages >= 2; --stages) {
+            for (int stages = 6; stages >= 2; stages -= 2) {
                 if (s_force && stages != s_force) continue;
                 size_t smem = dsa::indexer_smem_bytes(G, stages, tiles_cap);
                 // TMEM: 2*64*G columns per CTA; cap the CTAs per SM through
@@ -230,14 +240,15 @@ bool plan_indexer_flat(int B, int T, int max_len, FlatPlan *f) {
 // cluster (2 when a sequence has more query rows than there are sequences,
 // i.e. prefill, if it fits; else 1), C CTAs per cluster, ring depth.
 // Preference as for the bf16 indexer: the fewest waves, then the most CTAs in
-// flight, then the deepest ring.
+// flight, then the deepest ring (even, see even_stages).
 bool plan_indexer_mxfp8(int B, int T, int max_len, IdxPlan *p) {
     static std::mutex mu;
     static std::map<std::tuple<int, int, int, size_t>, int> cache;
     const size_t smax = max_smem_optin();
     const int tiles_max = std::max(1, ceil_div(max_len, 128));
     // (a forced group of 4 takes this kernel's largest, 2)
-    const int g_force = std::min(g_idx_group.load(), 2), c_force = g_idx_cluster.load(), s_force = g_idx_stages.load();
+    const int g_force = std::min(g_idx_group.load(), 2), c_force = g_idx_cluster.load(),
+              s_force = even_stages(g_idx_stages.load());
     bool found = false;
     long long best_waves = 0, best_used = 0;
     int best_stages = 0;
@@ -250,7 +261,7 @@ bool plan_indexer_mxfp8(int B, int T, int max_len, IdxPlan *p) {
             if (c_force && C != c_force) continue;
             const int tiles_cap = ceil_div(tiles_max, C);
             if (!c_force && C > 1 && tiles_cap < 4) continue;
-            for (int stages = 6; stages >= 2; --stages) {
+            for (int stages = 6; stages >= 2; stages -= 2) {
                 if (s_force && stages != s_force) continue;
                 const size_t smem = std::max(dsa::indexer_mxfp8_smem_bytes(G, stages, tiles_cap), (size_t)116 * 1024);
                 if (smem > smax) continue;

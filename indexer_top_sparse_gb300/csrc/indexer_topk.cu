@@ -48,7 +48,9 @@ constexpr int kThreads = 192;    // score-row selection kernel
 // The bf16 indexer: warp 0 TMA, warps 1 and 6 tcgen05 issue (even and odd
 // tiles), warps 2..5 epilogue.  One thread's waits, MMA issues and commits
 // for a tile take longer than the tensor core needs for it, so two threads
-// issue alternate tiles.  With one query row per cluster (decode) five more
+// issue alternate tiles; the ring depth is even, so each stage is always
+// filled for and consumed by the same thread, whose waits on its barriers
+// therefore come in phase order.  With one query row per cluster (decode) five more
 // warps join only the selection, whose passes over the keys are bound by
 // latency at two warps per scheduler; the wider epilogue registers of
 // several rows leave no room for them.
@@ -1414,7 +1416,8 @@ __global__ void __launch_bounds__(kFlatThreads, 1)
 // are stacked in the MMA's N dimension (64 G), so each key tile is read once
 // for all of them.  Warps: 0 and 11 TMA, 1 and 10 MMA (even and odd tiles
 // each: one thread's waits, issues and commits for a tile take longer than
-// the copy engine and the tensor core need for it), 2..5 epilogue (one per
+// the copy engine and the tensor core need for it; with an even ring depth a
+// stage belongs to one producer and one issuer), 2..5 epilogue (one per
 // TMEM lane quadrant, thread = position, all 64 heads of every row), 6..9
 // block scales into TMEM.
 constexpr int kF8Threads = 384;
@@ -1872,6 +1875,8 @@ static cudaError_t launch_f8g(const CUtensorMap &tk, const CUtensorMap &tq, cons
 
 cudaError_t launch_indexer_mxfp8(const CUtensorMap &tm_k, const CUtensorMap &tm_q, const IndexerArgs &a, int G, int C,
                                  int groups, size_t smem, bool write_scores, bool quant_q, cudaStream_t st) {
+    // two producers and two issuers on alternate tiles: every stage must belong to one of each
+    if (a.stages < 2 || (a.stages & 1) || a.stages > 8) return cudaErrorInvalidValue;
     if (G == 2) return launch_f8g<2>(tm_k, tm_q, a, C, groups, smem, write_scores, quant_q, st);
     if (G == 1) return launch_f8g<1>(tm_k, tm_q, a, C, groups, smem, write_scores, quant_q, st);
     return cudaErrorInvalidValue;
@@ -1968,6 +1973,8 @@ static cudaError_t launch_idx(const CUtensorMap &tk, const CUtensorMap &tq, cons
 
 cudaError_t launch_indexer_bf16(const CUtensorMap &tk, const CUtensorMap &tq, const IndexerArgs &a, int G, int C,
                                 int groups, size_t smem, bool write_scores, cudaStream_t st) {
+    // two issuing threads on alternate tiles: every stage must belong to one of them
+    if (a.stages < 2 || (a.stages & 1) || a.stages > 8) return cudaErrorInvalidValue;
     if (G == 1) return write_scores ? launch_idx<1, true>(tk, tq, a, C, groups, smem, st)
                                     : launch_idx<1, false>(tk, tq, a, C, groups, smem, st);
     if (G == 2) return write_scores ? launch_idx<2, true>(tk, tq, a, C, groups, smem, st)

@@ -75,8 +75,9 @@ def test_every_cluster_size(orc, C):
         d.set_tuning("indexer_cluster", 0)
 
 
-@pytest.mark.parametrize("stages", [2, 3])
+@pytest.mark.parametrize("stages", [2, 3, 4])
 def test_ring_depths(orc, stages):
+    # (3 runs as 2: the ring depth is even, two threads issue alternate tiles)
     import indexer_top_sparse_gb300 as d
     wl = make_workload("s", [4100, 2500], [1, 1], H=16, K=300, page_size=64, seed=9, with_kv=False)
     d.set_tuning("indexer_stages", stages)

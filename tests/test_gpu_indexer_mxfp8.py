@@ -84,8 +84,9 @@ def test_mxfp8_cluster_sizes(orc, C):
         d.set_tuning("indexer_cluster", 0)
 
 
-@pytest.mark.parametrize("stages", [2, 4])
+@pytest.mark.parametrize("stages", [2, 4, 5])
 def test_mxfp8_ring_depths(orc, stages):
+    # (5 runs as 4: the ring depth is even, two threads issue alternate tiles)
     import indexer_top_sparse_gb300 as d
     wl = make_workload("s", [4100, 333], [1, 1], H=16, K=256, page_size=64, seed=30 + stages, with_kv=False)
     d.set_tuning("indexer_stages", stages)
