@@ -246,16 +246,16 @@ bool plan_indexer_mxfp8(int B, int T, int max_len, IdxPlan *p) {
     static std::map<std::tuple<int, int, int, size_t>, int> cache;
     const size_t smax = max_smem_optin();
     const int tiles_max = std::max(1, ceil_div(max_len, 128));
-    // (a forced group of 4 takes this kernel's largest, 2)
-    const int g_force = std::min(g_idx_group.load(), 2), c_force = g_idx_cluster.load(),
+    // (a forced group of 4 takes this kernel's largest, 3)
+    const int g_force = std::min(g_idx_group.load(), 3), c_force = g_idx_cluster.load(),
               s_force = even_stages(g_idx_stages.load());
     bool found = false;
     long long best_waves = 0, best_used = 0;
     int best_stages = 0;
     int dev = 0;
     cudaGetDevice(&dev);
-    for (int G : {2, 1}) {
-        if (g_force ? G != g_force : (T <= B && G != 1)) continue;
+    for (int G : {3, 2, 1}) {
+        if (g_force ? G != g_force : ((T <= B && G != 1) || G == 3)) continue;
         const int groups = G == 1 ? T : ceil_div(T, G) + B;
         for (int C = 1; C <= 16; C <<= 1) {
             if (c_force && C != c_force) continue;

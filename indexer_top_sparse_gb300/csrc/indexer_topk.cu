@@ -1444,11 +1444,35 @@ struct __align__(16) F8Bars {
 template <int G>
 struct F8Layout {
     static constexpr int kN = G * kHI;                   // MMA N: the stacked query rows' heads
-    static constexpr int kBufs = G == 1 ? 4 : 3;
-    static constexpr uint32_t kAccCols = kN, kSfQ = kBufs * kN, kSfK = kSfQ + 4;
+    static constexpr int kBufs = G == 1 ? 4 : (G == 2 ? 3 : 2);
+    static constexpr int kSfQCols = kN <= 128 ? 4 : 8;   // query scale columns (N / 32, 4-aligned)
+    static constexpr uint32_t kAccCols = kN, kSfQ = kBufs * kN, kSfK = kSfQ + kSfQCols;
     static_assert(kSfK + 4 * kBufs <= 512, "TMEM");
-    static_assert(kN <= 128, "the query scales fill four TMEM columns at most");
+    static_assert(kN <= 256, "the query scales fill eight TMEM columns at most");
 };
+
+// One position's score for one query row from its 64 head logits (TMEM
+// accumulator columns): sum_h w_h ReLU(logit_h), as four independent pairs of
+// partial sums (heads 8m + 0,1 / 2,3 / 4,5 / 6,7) so that the additions do not
+// wait on one another.
+__device__ __forceinline__ float f8_row_score(const uint32_t (&r)[64], const float *w_row) {
+    float2 p[4] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f),
+                   make_float2(0.0f, 0.0f)};
+    const float4 *w4 = reinterpret_cast<const float4 *>(w_row);
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+        const float4 w = w4[k];
+        const int c = 2 * (k & 1);
+        p[c] = __ffma2_rn(make_float2(w.x, w.y),
+                          make_float2(fmaxf(__uint_as_float(r[4 * k]), 0.0f), fmaxf(__uint_as_float(r[4 * k + 1]), 0.0f)),
+                          p[c]);
+        p[c + 1] = __ffma2_rn(make_float2(w.z, w.w),
+                              make_float2(fmaxf(__uint_as_float(r[4 * k + 2]), 0.0f),
+                                          fmaxf(__uint_as_float(r[4 * k + 3]), 0.0f)),
+                              p[c + 1]);
+    }
+    return ((p[0].x + p[1].x) + (p[2].x + p[3].x)) + ((p[0].y + p[1].y) + (p[2].y + p[3].y));
+}
 
 // kQuantQ: the query arrives in bf16 and is quantised here, by the scale
 // warps, with the standalone quantiser's rule (mxfp8.cuh): codes into the
@@ -1632,45 +1656,50 @@ __global__ void __launch_bounds__(kF8Threads, 1)
             const int buf = i % kBufs;
             if (!mbar_wait(&bars->tfull[buf], (uint32_t)(i / kBufs) & 1u, a.err, 0x321, abort, wl)) break;
             tc_fence_after();
-            uint32_t r[G][64];
-#pragma unroll
-            for (int gi = 0; gi < G; ++gi) {
-                tmem_ld32(tmem + lanes + (uint32_t)(buf * L::kAccCols + gi * kHI),
-                          *reinterpret_cast<uint32_t(*)[32]>(r[gi]));
-                tmem_ld32(tmem + lanes + (uint32_t)(buf * L::kAccCols + gi * kHI + 32),
-                          *reinterpret_cast<uint32_t(*)[32]>(r[gi] + 32));
-            }
-            tmem_wait_ld();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->tempty[buf]);  // the accumulator is in registers
             const int pos = (tile0 + i) * kTileM + row;
-#pragma unroll
-            for (int gi = 0; gi < G; ++gi) {
-                // four independent pairs of partial sums (heads 8m + 0,1 / 2,3 / 4,5 / 6,7),
-                // so the additions do not wait on one another
-                float2 p[4] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f),
-                               make_float2(0.0f, 0.0f)};
-                const float4 *w4 = reinterpret_cast<const float4 *>(sW + gi * kHI);
-#pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    const float4 w = w4[k];
-                    const int c = 2 * (k & 1);
-                    p[c] = __ffma2_rn(make_float2(w.x, w.y),
-                                      make_float2(fmaxf(__uint_as_float(r[gi][4 * k]), 0.0f),
-                                                  fmaxf(__uint_as_float(r[gi][4 * k + 1]), 0.0f)),
-                                      p[c]);
-                    p[c + 1] = __ffma2_rn(make_float2(w.z, w.w),
-                                          make_float2(fmaxf(__uint_as_float(r[gi][4 * k + 2]), 0.0f),
-                                                      fmaxf(__uint_as_float(r[gi][4 * k + 3]), 0.0f)),
-                                          p[c + 1]);
-                }
-                const float sc = ((p[0].x + p[1].x) + (p[2].x + p[3].x)) + ((p[0].y + p[1].y) + (p[2].y + p[3].y));
+            const uint32_t acc = tmem + lanes + (uint32_t)(buf * L::kAccCols);
+            // the score of row gi at this position: key, top-digit count, (score)
+            auto emit = [&](int gi, float sc) {
                 const bool valid = gi < gn && pos <= pos_first + gi;
                 const uint32_t key = valid ? score_key(sc) : 0u;
                 sKeys[(size_t)gi * key_cap + i * kTileM + row] = key;
                 if (valid) red_shared_add(smem_u32(&sHist0[gi * kHist + (key >> 24)]), 1u);
                 if (kWriteScores && valid && pos < a.ld_scores) a.scores[(size_t)(t0 + gi) * a.ld_scores + pos] = sc;
+            };
+            if constexpr (G <= 2) {
+                uint32_t r[G][64];
+#pragma unroll
+                for (int gi = 0; gi < G; ++gi) {
+                    tmem_ld32(acc + gi * kHI, *reinterpret_cast<uint32_t(*)[32]>(r[gi]));
+                    tmem_ld32(acc + gi * kHI + 32, *reinterpret_cast<uint32_t(*)[32]>(r[gi] + 32));
+                }
+                tmem_wait_ld();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->tempty[buf]);  // the accumulator is in registers
+#pragma unroll
+                for (int gi = 0; gi < G; ++gi) emit(gi, f8_row_score(r[gi], sW + gi * kHI));
+            } else {
+                // three rows: 192 columns do not fit in registers at once; row gi + 1
+                // loads while row gi is summed, and the accumulator is handed back
+                // once the last row is in registers
+                static_assert(G == 3, "three stacked rows");
+                uint32_t ra[64], rb[64];
+                tmem_ld32(acc, *reinterpret_cast<uint32_t(*)[32]>(ra));
+                tmem_ld32(acc + 32, *reinterpret_cast<uint32_t(*)[32]>(ra + 32));
+                tmem_wait_ld();
+                tmem_ld32(acc + kHI, *reinterpret_cast<uint32_t(*)[32]>(rb));
+                tmem_ld32(acc + kHI + 32, *reinterpret_cast<uint32_t(*)[32]>(rb + 32));
+                emit(0, f8_row_score(ra, sW));
+                tmem_wait_ld();
+                tmem_ld32(acc + 2 * kHI, *reinterpret_cast<uint32_t(*)[32]>(ra));
+                tmem_ld32(acc + 2 * kHI + 32, *reinterpret_cast<uint32_t(*)[32]>(ra + 32));
+                emit(1, f8_row_score(rb, sW + kHI));
+                tmem_wait_ld();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->tempty[buf]);
+                emit(2, f8_row_score(ra, sW + 2 * kHI));
             }
         }
     } else {
@@ -1727,9 +1756,9 @@ __global__ void __launch_bounds__(kF8Threads, 1)
             if (threadIdx.x == 6 * 32) mbar_arrive(&bars->qbar);
         }
         if (n_tiles > 0) {
-            uint32_t w[4];  // stacked query row r = gi * 64 + head in lane r % 32, column r / 32
+            uint32_t w[L::kSfQCols];  // stacked query row r = gi * 64 + head in lane r % 32, column r / 32
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < L::kSfQCols; ++c) {
                 const int r = lane + 32 * c, gi = r / kHI, h = r % kHI;
                 if (gi >= gn || gi >= G)
                     w[c] = 0x7F7F7F7Fu;
@@ -1738,7 +1767,8 @@ __global__ void __launch_bounds__(kF8Threads, 1)
                 else
                     w[c] = __ldg(reinterpret_cast<const uint32_t *>(a.q_scale + ((size_t)(t0 + gi) * kHI + h) * 4));
             }
-            tmem_st4(tmem + lanes + L::kSfQ, w);
+            if constexpr (L::kSfQCols == 4) tmem_st4(tmem + lanes + L::kSfQ, w);
+            else tmem_st8(tmem + lanes + L::kSfQ, w);
         }
         // The key scales come straight from the cache with plain loads (a
         // warp's 32 rows are 128 contiguous bytes), issued kBufs tiles
@@ -1877,13 +1907,16 @@ cudaError_t launch_indexer_mxfp8(const CUtensorMap &tm_k, const CUtensorMap &tm_
                                  int groups, size_t smem, bool write_scores, bool quant_q, cudaStream_t st) {
     // two producers and two issuers on alternate tiles: every stage must belong to one of each
     if (a.stages < 2 || (a.stages & 1) || a.stages > 8) return cudaErrorInvalidValue;
+    if (G == 3) return launch_f8g<3>(tm_k, tm_q, a, C, groups, smem, write_scores, quant_q, st);
     if (G == 2) return launch_f8g<2>(tm_k, tm_q, a, C, groups, smem, write_scores, quant_q, st);
     if (G == 1) return launch_f8g<1>(tm_k, tm_q, a, C, groups, smem, write_scores, quant_q, st);
     return cudaErrorInvalidValue;
 }
 
 int indexer_mxfp8_max_active_clusters(int G, int C, size_t smem) {
-    auto kern = G == 2 ? indexer_topk_mxfp8_kernel<2, false, false> : indexer_topk_mxfp8_kernel<1, false, false>;
+    auto kern = G == 3   ? indexer_topk_mxfp8_kernel<3, false, false>
+                : G == 2 ? indexer_topk_mxfp8_kernel<2, false, false>
+                         : indexer_topk_mxfp8_kernel<1, false, false>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return 0;
     if (C > 8 && cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
         return 0;

@@ -96,10 +96,12 @@ def test_mxfp8_ring_depths(orc, stages):
         d.set_tuning("indexer_stages", 0)
 
 
-@pytest.mark.parametrize("G", [1, 2])
+@pytest.mark.parametrize("G", [1, 2, 3])
 def test_mxfp8_prefill_causal(orc, G):
     # G query rows of a sequence per cluster share each key tile (their
-    # queries stacked in the MMA's N); 17 rows leave a last group of one
+    # queries stacked in the MMA's N: 192 with three rows, whose query scales
+    # fill six TMEM columns); 17 rows leave a last group of one (G = 2) or two
+    # (G = 3)
     import indexer_top_sparse_gb300 as d
     from _util import tuning
     wl = make_workload("p", [700, 300, 2100], [40, 17, 9], H=16, K=256, page_size=64, seed=41, with_kv=False)
