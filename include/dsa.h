@@ -98,9 +98,11 @@ const char *dsa_status_string(dsa_status s);
 
 /* Launch-shape tuning knobs, read on every call (0 = automatic).  Names:
  * "indexer_cluster" (CTAs per cluster, power of two <= 16), "indexer_stages"
- * (shared-memory ring depth of the cluster indexers: 2, 4 or 6 where it fits; an odd value
- * is taken one lower, since two threads take alternate tiles), "indexer_group" (query rows per cluster:
- * 1, 2 or 4; the MXFP8 indexer takes 1, 2 or 3, a forced 4 as 3, and chooses 3 only when forced), "mla_splits" (key splits per query row), "mla_pair" (with 128
+ * (shared-memory ring depth of the cluster indexers: 2, 4 or 6 where it fits;
+ * an odd value is taken one lower, since two threads take alternate tiles),
+ * "indexer_group" (query rows per cluster: 1, 2 or 4; the MXFP8 indexer takes
+ * 1, 2 or 3, a forced 4 as 3, and chooses 3 only when forced), "mla_splits"
+ * (key splits per query row), "mla_pair" (with 128
  * heads, run the two 64-head CTAs of a query as a cluster sharing every
  * gathered row: 1 yes, -1 or 0 no), "mla_stream_k" (64-head CTAs, one per SM, share
  * all (row, head group, key tile) units evenly instead of a split grid: 1 yes
