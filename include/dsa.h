@@ -304,12 +304,19 @@ dsa_status dsa_cache_append(const void *k_new, const void *kv_new, const int32_t
  *   make it before any stream capture.  Every call on a device shares the
  *   array: calls whose kernels overlap on the GPU race and must not be issued.
  *   Device-side error bits go to the array's own error word, which each call
- *   clears; they cannot be read back (use dsa_sparse_mla for that). */
+ *   clears; dsa_sparse_mla_static_get_error reads them back. */
 dsa_status dsa_sparse_mla_static(const void *q, const void *kv_cache, const void *kv_rope, const float *kv_scale,
                                  int64_t num_pages, const int32_t *page_table, int32_t max_pages_per_seq,
                                  const int32_t *seq_lens, const int32_t *cu_q, const int32_t *indices, int32_t B,
                                  int32_t T, int32_t H, int32_t K, float scale, int32_t page_size, dsa_kv_dtype dtype,
                                  void *out, float *lse, void *stream);
+
+/* The device-side errors of the last dsa_sparse_mla_static call on the current
+ * device, as dsa_get_error reports them for a workspace: synchronises
+ * `stream`, reads the static array's error word, clears it and returns the
+ * first error it records (DSA_OK if none; DSA_ERR_CUDA if the array's address
+ * cannot be looked up).  Not for the hot path. */
+dsa_status dsa_sparse_mla_static_get_error(void *stream);
 
 #ifdef __cplusplus
 }

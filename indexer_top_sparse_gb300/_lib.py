@@ -27,7 +27,8 @@ KV_DTYPES = {"bf16": 0, "fp8_rowscale": 1, "fp8_tile128": 2}
 # Every symbol include/dsa.h declares.
 EXPORTS = ("dsa_status_string", "dsa_set_tuning", "dsa_index_topk_workspace_size", "dsa_sparse_mla_workspace_size",
            "dsa_workspace_init", "dsa_get_error", "dsa_workspace_set_wait_limit", "dsa_index_topk", "dsa_index_scores", "dsa_topk_from_scores",
-           "dsa_sparse_mla", "dsa_sparse_mla_static", "dsa_quant_mxfp8", "dsa_quant_fp8_rows",
+           "dsa_sparse_mla", "dsa_sparse_mla_static", "dsa_sparse_mla_static_get_error", "dsa_quant_mxfp8",
+           "dsa_quant_fp8_rows",
            "dsa_quant_fp8_tiles", "dsa_cache_append")
 
 
@@ -82,6 +83,8 @@ def load(build_if_missing: bool = True):
         lib.dsa_sparse_mla_static.argtypes = [P, P, P, P, i64, P, i32, P, P, P, i32, i32, i32, i32, ctypes.c_float,
                                               i32, c_int, P, P, P]
         lib.dsa_sparse_mla_static.restype = c_int
+        lib.dsa_sparse_mla_static_get_error.argtypes = [P]
+        lib.dsa_sparse_mla_static_get_error.restype = c_int
         lib.dsa_quant_mxfp8.argtypes = [P, i64, P, P, P]
         lib.dsa_quant_mxfp8.restype = c_int
         lib.dsa_quant_fp8_rows.argtypes = [P, i64, P, P, P, P]

@@ -20,7 +20,8 @@
 // array are rejected with DSA_ERR_UNSUPPORTED (and a message on stderr).
 // Every call on a device uses the same array and leaves its contents behind;
 // the call clears the array's error word itself and overwrites every partial
-// it later reads.  Calls whose kernels overlap on the GPU (e.g. on two
+// it later reads; dsa_sparse_mla_static_get_error reads (and clears) the
+// error word of the last call.  Calls whose kernels overlap on the GPU (e.g. on two
 // streams without ordering) race on the array and must be avoided.
 #include <cuda_runtime.h>
 
@@ -91,4 +92,16 @@ extern "C" dsa_status dsa_sparse_mla_static(const void *q, const void *kv_cache,
     return dsa_sparse_mla(q, kv_cache, kv_rope, kv_scale, num_pages, page_table, max_pages_per_seq, seq_lens, cu_q,
                           indices, B, T, H, K, scale, page_size, dtype, out, lse, scratch, kStaticScratchBytes,
                           stream);
+}
+
+extern "C" dsa_status dsa_sparse_mla_static_get_error(void *stream) {
+    void *scratch = nullptr;
+    cudaError_t e = scratch_address(&scratch);
+    if (e != cudaSuccess) {
+        fprintf(stderr, "[dsa] dsa_sparse_mla_static_get_error: cudaGetSymbolAddress failed: %s\n",
+                cudaGetErrorString(e));
+        return DSA_ERR_CUDA;
+    }
+    // the array's first 256 bytes are an ordinary workspace error block
+    return dsa_get_error(scratch, stream);
 }

@@ -131,3 +131,28 @@ def test_static_rejects_requests_beyond_its_scratch():
                                    P(dummy.data_ptr()), P(dummy.data_ptr()), P(dummy.data_ptr()), 1, 100, 128, 8192,
                                    ctypes.c_float(1.0), 64, 0, P(dummy.data_ptr()), None, None)
     assert rc == 2
+
+
+def test_static_errors_are_read_back():
+    # An index past its row's position is reported and its key skipped (the
+    # same rule as dsa_sparse_mla); the allocation-free call keeps the error
+    # bit in its static array, and dsa_sparse_mla_static_get_error reads it
+    # back and clears it, so the next clean call reads DSA_OK.
+    import indexer_top_sparse_gb300 as d
+    lib = d.load()
+    rng = np.random.default_rng(7)
+    wl = make_workload("static_err", [2000, 700], [1, 1], H=64, K=512, page_size=64, seed=7, with_idx=False)
+    t = to_device(wl)
+    idx = _indices(rng, wl)
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    out = torch.empty((wl.T, wl.H, 512), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((wl.T, wl.H), dtype=torch.float32, device="cuda")
+    _call_static(lib, t, dev(idx), wl, out, lse)
+    assert lib.dsa_sparse_mla_static_get_error(stream) == 0
+    bad = idx.copy()
+    bad[1, 3] = int(wl.query_pos()[1]) + 5  # a position row 1 cannot see
+    _call_static(lib, t, dev(bad), wl, out, lse)
+    assert lib.dsa_sparse_mla_static_get_error(stream) == 5  # DSA_ERR_BAD_INDEX
+    assert np.isfinite(out.float().cpu().numpy()).all()
+    _call_static(lib, t, dev(idx), wl, out, lse)
+    assert lib.dsa_sparse_mla_static_get_error(stream) == 0
