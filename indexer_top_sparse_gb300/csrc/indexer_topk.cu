@@ -15,13 +15,14 @@
 //   warp 0      TMA producer: the group's Q rows once, then per tile two
 //               64-row page boxes x two 64-column halves, 128-byte swizzle,
 //               into a STAGES-deep ring.
-//   warp 1      tcgen05 issuer: D[128 pos x 64G] = K_tile[128 x 128] *
-//               Q[64G x 128]^T, eight K=16 steps, fp32 accumulators in TMEM
-//               (double-buffered), commits release the smem stage and hand the
-//               TMEM buffer to the epilogue.
+//   warps 1, 6  tcgen05 issuers (even and odd tiles): D[128 pos x 64G] =
+//               K_tile[128 x 128] * Q[64G x 128]^T, eight K=16 steps, fp32
+//               accumulators in TMEM (one per issuer), commits release the
+//               smem stage and hand the TMEM buffer to the epilogue.
 //   warps 2-5   epilogue: thread = TMEM lane = position; ReLU, weight by w and
 //               sum over the 64 heads in registers; store an order-preserving
 //               32-bit key per (query, position) in shared memory.
+//   warps 7-11  (one query row per cluster) the selection only.
 //   all warps   cluster radix select (8-bit digits, histograms summed across
 //               the cluster through distributed shared memory), ties resolved
 //               to the lowest positions, indices written in ascending order.

@@ -22,11 +22,13 @@
 //               tile ahead), are multiplied by their scale (the row's, or
 //               the one of their 128-dim tile) and stored as
 //               bf16; the rope dims are copied as they are.
-//   warp 8      tcgen05 issuer: S[64 heads x 64 keys] = Q . K_tile^T (M = 64,
+//   warps 8, 13 tcgen05 issuers (split grid: even and odd tiles; stream-K:
+//               warp 8 alone): S[64 heads x 64 keys] = Q . K_tile^T (M = 64,
 //               K-major operands, 36 steps of K = 16, double-buffered in
-//               TMEM), then O^T[512 dims x 64] += V^T . P^T with V^T read
-//               MN-major from the same tile and P^T MN-major (4 chunks of 128
-//               dims, 4 steps of 16 keys).
+//               TMEM; with a bf16 cache the first 20 steps start once regions
+//               0-4 have landed), then O^T[512 dims x 64] += V^T . P^T with V^T
+//               read MN-major from the same tile and P^T MN-major (4 chunks of
+//               128 dims, 4 steps of 16 keys).
 //               With pairs, each gather warp forwards its rows to the peer
 //               (bulk shared-to-shared copies) as soon as they have landed.
 //   warps 9-12  softmax: thread = head (M = 64 places rows 16q..16q+15 in the
