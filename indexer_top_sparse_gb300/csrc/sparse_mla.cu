@@ -25,8 +25,8 @@
 //   warps 8, 13 tcgen05 issuers (split grid: even and odd tiles; stream-K:
 //               warp 8 alone): S[64 heads x 64 keys] = Q . K_tile^T (M = 64,
 //               K-major operands, 36 steps of K = 16, double-buffered in
-//               TMEM; with a bf16 cache the first 20 steps start once regions
-//               0-4 have landed), then O^T[512 dims x 64] += V^T . P^T with V^T
+//               TMEM; with a bf16 cache the first 12 steps start once regions
+//               0-2 have landed), then O^T[512 dims x 64] += V^T . P^T with V^T
 //               read MN-major from the same tile and P^T MN-major (4 chunks of
 //               128 dims, 4 steps of 16 keys).
 //               With pairs, each gather warp forwards its rows to the peer
@@ -105,7 +105,7 @@ struct __align__(16) MlaBars {
 };
 
 constexpr int kMaxKeysPerSplit = 2048;       // host keeps keys_per_split <= this
-constexpr int kEarlyRegions = 5;             // regions behind kv_early (bf16 cache, unpaired)
+constexpr int kEarlyRegions = 3;             // regions behind kv_early (bf16 cache, unpaired)
 
 struct __align__(16) MlaStats {
     int32_t rows[kMaxKeysPerSplit];             // physical cache row of every key of the split
